@@ -1,0 +1,88 @@
+// ftkv_internal.h -- argument blocks and launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ftkv {
+
+struct StoreArgs {
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* slots;
+  int64_t num_tokens;
+  int num_kv_heads;
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  float* k_scales;
+  float* v_scales;
+  int64_t num_rows;
+  int* err;
+};
+
+struct ReconstructArgs {
+  const uint8_t* k_codes;
+  const uint8_t* v_codes;
+  const float* k_scales;
+  const float* v_scales;
+  int64_t num_rows;
+  int num_kv_heads;
+  const int32_t* slots;
+  int64_t num_prefix;
+  uint16_t* ws_k;
+  uint16_t* ws_v;
+  int* err;
+};
+
+struct DecodeArgs {
+  const uint8_t* k_codes;
+  const uint8_t* v_codes;
+  const float* k_scales;
+  const float* v_scales;
+  int64_t num_rows;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;                 // num_q_heads / num_kv_heads (1, 2, 4 or 8)
+  const uint16_t* q;         // [total_q_rows][Hq][128]
+  const int32_t* req_to_slot;
+  int64_t req_stride;
+  const int32_t* seq_lens;
+  const int32_t* q_row_offsets;  // may be null: one row per request
+  int batch;
+  int64_t total_q_rows;
+  int max_q_rows;
+  int64_t max_seq_len;       // host bound used for the split geometry
+  int num_splits;            // key slices per request
+  int64_t chunk;             // keys per slice (multiple of 16)
+  float qk_scale_log2;       // sm_scale * log2(e)
+  float* part_acc;           // [total_q_rows][Hq][num_splits][128]
+  float* part_ml;            // [total_q_rows][Hq][num_splits][2]  (max in log2 units, sum)
+  uint16_t* out;             // [total_q_rows][Hq][128]
+  int* err;
+};
+
+struct PrefillArgs {
+  int num_q_heads;
+  int num_kv_heads;
+  const uint16_t* q;         // [C][Hq][128]
+  const uint16_t* k_chunk;   // [C][Hkv][128]
+  const uint16_t* v_chunk;
+  int64_t chunk_len;
+  const uint16_t* ws_k;      // [P][Hkv][128]
+  const uint16_t* ws_v;
+  int64_t prefix_len;
+  float qk_scale_log2;
+  uint16_t* out;             // [C][Hq][128]
+};
+
+cudaError_t launch_store_quant(const StoreArgs& a, cudaStream_t s);
+cudaError_t launch_reconstruct(const ReconstructArgs& a, cudaStream_t s);
+cudaError_t launch_e4m3_encode(const float* x, uint8_t* c, int64_t n, int num_sms, cudaStream_t s);
+cudaError_t launch_e4m3_decode(const uint8_t* c, float* x, int64_t n, int num_sms, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+int decode_ctas_per_sm(int max_q_rows);
+cudaError_t launch_prefill_mma(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+
+}  // namespace ftkv

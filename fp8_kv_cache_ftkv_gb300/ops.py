@@ -1,0 +1,202 @@
+"""Torch-tensor front end of libftkv.so: argument marshalling only.
+
+Every function checks device/dtype/shape/contiguity, passes raw device pointers and the current CUDA
+stream to the C ABI and returns.  All arithmetic happens in the CUDA kernels behind the ABI; there is no
+CPU or PyTorch fallback.  BF16 tensors are ``torch.bfloat16`` (passed as their 16-bit patterns).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import FtkvPool, check
+
+HEAD_DIM = 128
+
+
+def _stream_ptr(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _req(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+@dataclass
+class KVPool:
+    """One layer's FP8 pool on the GPU: codes uint8 [rows, Hkv, 128], scales float32 [rows, Hkv]."""
+    k_codes: torch.Tensor
+    v_codes: torch.Tensor
+    k_scales: torch.Tensor
+    v_scales: torch.Tensor
+
+    @staticmethod
+    def empty(num_rows: int, num_kv_heads: int, device="cuda", head_dim: int = HEAD_DIM) -> "KVPool":
+        z = dict(device=device)
+        return KVPool(torch.zeros(num_rows, num_kv_heads, head_dim, dtype=torch.uint8, **z),
+                      torch.zeros(num_rows, num_kv_heads, head_dim, dtype=torch.uint8, **z),
+                      torch.zeros(num_rows, num_kv_heads, dtype=torch.float32, **z),
+                      torch.zeros(num_rows, num_kv_heads, dtype=torch.float32, **z))
+
+    @property
+    def num_rows(self) -> int:
+        return self.k_codes.shape[0]
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.k_codes.shape[1]
+
+    def c_struct(self) -> FtkvPool:
+        for n in ("k_codes", "v_codes"):
+            _req(getattr(self, n), torch.uint8, n, 3)
+        for n in ("k_scales", "v_scales"):
+            _req(getattr(self, n), torch.float32, n, 2)
+        return FtkvPool(self.k_codes.data_ptr(), self.v_codes.data_ptr(), self.k_scales.data_ptr(),
+                        self.v_scales.data_ptr(), self.k_codes.shape[0], self.k_codes.shape[1],
+                        self.k_codes.shape[2])
+
+
+def store_quant(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slots: torch.Tensor, stream=None) -> None:
+    """Quantize-on-write of BF16 K/V [T, Hkv, 128] into pool rows ``slots`` (int32 [T])."""
+    _req(k, torch.bfloat16, "k", 3)
+    _req(v, torch.bfloat16, "v", 3)
+    _req(slots, torch.int32, "slots", 1)
+    if k.shape != v.shape or k.shape[0] != slots.shape[0]:
+        raise ValueError("k, v, slots disagree")
+    ps = pool.c_struct()
+    check(_lib.load().ftkv_store_quant(ctypes.byref(ps), _ptr(k), _ptr(v), _ptr(slots), k.shape[0],
+                                       _stream_ptr(stream)), "ftkv_store_quant")
+
+
+def reconstruct_bf16(pool: KVPool, slots: torch.Tensor, ws_k: torch.Tensor = None, ws_v: torch.Tensor = None,
+                     stream=None):
+    """Rebuild rows ``slots`` (logical order) into BF16 workspaces [P, Hkv, 128]; returns (ws_k, ws_v)."""
+    _req(slots, torch.int32, "slots", 1)
+    P = slots.shape[0]
+    shape = (P, pool.num_kv_heads, HEAD_DIM)
+    if ws_k is None:
+        ws_k = torch.empty(shape, dtype=torch.bfloat16, device=slots.device)
+    if ws_v is None:
+        ws_v = torch.empty(shape, dtype=torch.bfloat16, device=slots.device)
+    _req(ws_k, torch.bfloat16, "ws_k", 3)
+    _req(ws_v, torch.bfloat16, "ws_v", 3)
+    if ws_k.shape[0] < P or ws_v.shape[0] < P:
+        raise ValueError("workspace too small")
+    ps = pool.c_struct()
+    check(_lib.load().ftkv_reconstruct_bf16(ctypes.byref(ps), _ptr(slots), P, _ptr(ws_k), _ptr(ws_v),
+                                            _stream_ptr(stream)), "ftkv_reconstruct_bf16")
+    return ws_k, ws_v
+
+
+def decode_workspace_bytes(num_q_heads: int, total_q_rows: int, num_splits: int) -> int:
+    return int(_lib.load().ftkv_decode_workspace_bytes(num_q_heads, HEAD_DIM, total_q_rows, num_splits))
+
+
+def decode_auto_splits(batch: int, num_kv_heads: int, max_seq_len: int, max_q_rows: int = 1) -> int:
+    return int(_lib.load().ftkv_decode_auto_splits(batch, num_kv_heads, max_seq_len, max_q_rows))
+
+
+class DecodePlan:
+    """Host-side decode geometry + the workspace it needs (allocated once, reused by every call)."""
+
+    def __init__(self, num_q_heads: int, num_kv_heads: int, batch: int, total_q_rows: int, max_q_rows: int,
+                 max_seq_len: int, num_splits: int = 0, device="cuda"):
+        self.num_q_heads, self.num_kv_heads = num_q_heads, num_kv_heads
+        self.batch, self.total_q_rows, self.max_q_rows = batch, total_q_rows, max_q_rows
+        self.max_seq_len = max_seq_len
+        self.num_splits = num_splits or decode_auto_splits(batch, num_kv_heads, max_seq_len, max_q_rows)
+        nbytes = decode_workspace_bytes(num_q_heads, total_q_rows, self.num_splits)
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,
+                q_row_offsets: torch.Tensor = None, *, max_seq_len: int, max_q_rows: int = 1,
+                sm_scale: float = HEAD_DIM ** -0.5, num_splits: int = 0, plan: DecodePlan = None,
+                out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, 128]."""
+    _req(q, torch.bfloat16, "q", 3)
+    if req_to_slot.dim() == 1:
+        req_to_slot = req_to_slot.view(1, -1)
+    _req(req_to_slot, torch.int32, "req_to_slot", 2)
+    _req(seq_lens, torch.int32, "seq_lens", 1)
+    if q_row_offsets is not None:
+        _req(q_row_offsets, torch.int32, "q_row_offsets", 1)
+    batch = seq_lens.shape[0]
+    total, hq, _ = q.shape
+    if plan is None:
+        plan = DecodePlan(hq, pool.num_kv_heads, batch, total, max_q_rows, max_seq_len, num_splits, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, torch.bfloat16, "out", 3)
+    ps = pool.c_struct()
+    check(_lib.load().ftkv_decode_attn(
+        ctypes.byref(ps), hq, _ptr(q), _ptr(req_to_slot), req_to_slot.shape[1], _ptr(seq_lens),
+        _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale), plan.num_splits,
+        _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)), "ftkv_decode_attn")
+    return out
+
+
+def prefill_attn(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, ws_k: torch.Tensor = None,
+                 ws_v: torch.Tensor = None, *, sm_scale: float = HEAD_DIM ** -0.5, out: torch.Tensor = None,
+                 impl: str = "tc", stream=None) -> torch.Tensor:
+    """Causal prefill of the chunk over prefix (+) chunk.  ``impl``: "tc" (tcgen05) or "mma" (mma.sync)."""
+    _req(q, torch.bfloat16, "q", 3)
+    _req(k_chunk, torch.bfloat16, "k_chunk", 3)
+    _req(v_chunk, torch.bfloat16, "v_chunk", 3)
+    C, hq, _ = q.shape
+    hkv = k_chunk.shape[1]
+    P = 0 if ws_k is None else ws_k.shape[0]
+    if P:
+        _req(ws_k, torch.bfloat16, "ws_k", 3)
+        _req(ws_v, torch.bfloat16, "ws_v", 3)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, torch.bfloat16, "out", 3)
+    fn = _lib.load().ftkv_prefill_attn if impl == "tc" else _lib.load().ftkv_prefill_attn_mma
+    check(fn(hq, hkv, HEAD_DIM, _ptr(q), _ptr(k_chunk), _ptr(v_chunk), C, _ptr(ws_k) if P else None,
+             _ptr(ws_v) if P else None, P, float(sm_scale), _ptr(out), _stream_ptr(stream)), f"prefill[{impl}]")
+    return out
+
+
+def e4m3_encode(x: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    _req(x, torch.float32, "x")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    check(_lib.load().ftkv_e4m3_encode_f32(_ptr(x), _ptr(out), x.numel(), _stream_ptr(stream)), "e4m3_encode")
+    return out
+
+
+def e4m3_decode(c: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    _req(c, torch.uint8, "codes")
+    if out is None:
+        out = torch.empty(c.shape, dtype=torch.float32, device=c.device)
+    check(_lib.load().ftkv_e4m3_decode_f32(_ptr(c), _ptr(out), c.numel(), _stream_ptr(stream)), "e4m3_decode")
+    return out
+
+
+def pool_bytes(rows: int, layers: int, num_kv_heads: int, head_dim: int = HEAD_DIM) -> dict:
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    check(_lib.load().ftkv_pool_bytes(rows, layers, num_kv_heads, head_dim, ctypes.byref(a), ctypes.byref(b),
+                                      ctypes.byref(c)), "ftkv_pool_bytes")
+    return {"bf16": a.value, "fp8": b.value, "workspace": c.value}
+
+
+def device_errors() -> int:
+    v = ctypes.c_int32()
+    check(_lib.load().ftkv_device_errors(ctypes.byref(v)), "ftkv_device_errors")
+    return v.value

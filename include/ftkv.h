@@ -1,0 +1,192 @@
+/*
+ * ftkv.h -- C ABI of libftkv.so: an FP8 (E4M3FN) per-token/per-head KV cache for BF16 attention on
+ * one GB300 (sm_103a) GPU.
+ *
+ * The operations follow three pages about FreeToken's opt-in FP8 KV cache:
+ *   [#853] FreeToken PR #853 "opt-in FP8 KV cache (R9700)"
+ *   [#897] FreeToken PR #897 "perf(attention): add packed fp8 kv reads on gfx1201"
+ *   [#280] FreeToken issue #280 "Feature Request: opt-in FP8 KV-cache support for long-context MoE
+ *          inference"
+ *
+ * Row format ([#853 "What changes"], [#280 "Proof of concept"]): every physical K/V row (one token,
+ * one KV head) holds head_dim E4M3FN codes, one byte each, plus its own FP32 scale.  The scale is
+ * dynamic: absmax(row) / 448, and code = E4M3FN(x / scale) with round-to-nearest-even, saturating at
+ * +-448 (NaN -> 0x7F).  An all-zero row stores scale 0 and codes +-0.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must be device memory (cudaMalloc or torch CUDA tensors) of
+ *     the current device, 16-byte aligned unless stated otherwise.  BF16 tensors are passed as
+ *     uint16_t bit patterns.  All tensors are dense, row-major, in the layouts stated.
+ *   - The library never allocates or frees device memory; the caller owns every buffer.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous: they
+ *     validate their arguments on the host, enqueue kernels on `stream` and return.
+ *   - Argument errors are reported before anything is enqueued (nothing is launched).  Conditions
+ *     that only the GPU can see (a slot outside the pool, a sequence length above the declared
+ *     maximum) make the kernel skip the offending row and raise a flag in a per-device error word,
+ *     read and cleared with ftkv_device_errors().
+ *   - Supported: head_dim == 128, num_q_heads % num_kv_heads == 0 with group size 1, 2, 4 or 8
+ *     (MHA/GQA), page size 1, one GPU (TP = 1).  Anything else returns FTKV_ERR_UNSUPPORTED, the
+ *     configuration-time rejection of [#853 "What changes"] and [#280 limitations].
+ */
+#ifndef FTKV_H_
+#define FTKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FTKV_ABI_VERSION 1
+#define FTKV_HEAD_DIM 128
+/* Split-K cap of the decode kernel ([#897 "Fresh R9700 stage-1 A/B"]: 64 scratch slots / splits). */
+#define FTKV_MAX_SPLITS 64
+/* Largest number of query rows per request in multi-row decode ([#897] opening description, #900). */
+#define FTKV_MAX_Q_ROWS 8
+
+typedef enum {
+  FTKV_OK = 0,
+  FTKV_ERR_INVALID = -1,      /* null pointer, negative size, inconsistent sizes               */
+  FTKV_ERR_UNSUPPORTED = -2,  /* head_dim, group size or other configuration outside the scope */
+  FTKV_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned                              */
+  FTKV_ERR_WORKSPACE = -4,    /* decode workspace too small                                    */
+  FTKV_ERR_CUDA = -6          /* a CUDA call or launch failed (see ftkv_last_cuda_error)       */
+} ftkv_status;
+
+/* Bits of the per-device error word (ftkv_device_errors). */
+#define FTKV_DEVERR_BAD_SLOT 0x1    /* a slot index was < 0 or >= num_rows; that row was skipped     */
+#define FTKV_DEVERR_SEQ_LEN 0x2     /* a seq_len was < 0 or > max_seq_len / req_stride; clamped        */
+#define FTKV_DEVERR_Q_ROWS 0x4      /* q_row_offsets inconsistent (rows > max_q_rows or past the end);
+                                       that request was skipped                                       */
+
+/* One layer's FP8 pool.  All four arrays are device memory owned by the caller.
+ *   k_codes, v_codes : uint8 [num_rows][num_kv_heads][head_dim]   E4M3FN codes
+ *   k_scales, v_scales: float [num_rows][num_kv_heads]            FP32 per-row scales          */
+typedef struct ftkv_pool {
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  float* k_scales;
+  float* v_scales;
+  int64_t num_rows;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+} ftkv_pool;
+
+/* ---------------------------------------------------------------------------------------------
+ * Quantize-on-write ([#853 "What changes"], [#853 "Follow-up model/workload search"]: every new
+ * K/V row is quantized when it is written to its slot).
+ *   k, v    : device BF16 [num_tokens][num_kv_heads][head_dim]
+ *   slots   : device int32 [num_tokens]; token t is written to pool row slots[t].  Slots must be
+ *             distinct within one call (duplicates leave one of the writers' rows, unspecified which).
+ * Writes codes and scales of rows slots[0..num_tokens) of both K and V.  num_tokens == 0 is a no-op.
+ * --------------------------------------------------------------------------------------------- */
+int ftkv_store_quant(const ftkv_pool* pool, const uint16_t* k, const uint16_t* v,
+                     const int32_t* slots, int64_t num_tokens, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Reconstruct historical rows into the shared BF16 workspace ([#853 "What changes"]: once per
+ * layer, historical FP8 rows are rebuilt into one shared BF16 workspace for prefill).
+ *   slots        : device int32 [num_prefix]; logical token i lives in pool row slots[i]
+ *   ws_k, ws_v   : device BF16 [num_prefix][num_kv_heads][head_dim], written in logical order:
+ *                  ws[i][h][d] = bf16_rne(float(decode(code[slots[i]][h][d])) * scale[slots[i]][h])
+ * Bit-exact: one FP32 product, round-to-nearest-even.  num_prefix == 0 is a no-op.
+ * --------------------------------------------------------------------------------------------- */
+int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t num_prefix,
+                          uint16_t* ws_k, uint16_t* ws_v, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Split-K decode attention over the FP8 pool ([#897 "Fresh R9700 stage-1 A/B"]: a stage-1 kernel
+ * over slices of the keys followed by a merge; [#897] opening description: BF16 query, D128,
+ * GQA 4/8, per-row scales; multi-row decode of up to 8 query rows per request).
+ *
+ *   q              : device BF16 [total_q_rows][num_q_heads][head_dim]
+ *   req_to_slot    : device int32 [batch][req_stride]; key j of request b lives in pool row
+ *                    req_to_slot[b * req_stride + j]
+ *   seq_lens       : device int32 [batch]; request b attends to keys 0 .. seq_lens[b]-1 (the keys of
+ *                    its new rows included; they must already be stored)
+ *   q_row_offsets  : device int32 [batch + 1]; request b owns query rows
+ *                    [q_row_offsets[b], q_row_offsets[b+1]), at most FTKV_MAX_Q_ROWS of them.  Row r
+ *                    of R sees keys 0 .. seq_lens[b] - R + r (causal within the new rows).  NULL means
+ *                    one row per request (total_q_rows == batch).
+ *   max_q_rows     : host upper bound on rows per request (1 .. FTKV_MAX_Q_ROWS)
+ *   max_seq_len    : host upper bound on seq_lens (<= req_stride); it fixes the split geometry
+ *   sm_scale       : softmax scale (1/sqrt(head_dim) for the standard case)
+ *   num_splits     : 0 = automatic (fills the SMs), else 1 .. FTKV_MAX_SPLITS key slices per request
+ *   workspace      : device scratch of at least ftkv_decode_workspace_bytes(...) bytes, 256-byte
+ *                    aligned; overwritten on every call; must not be shared by calls in flight
+ *   out            : device BF16 [total_q_rows][num_q_heads][head_dim]
+ * A query row that sees no key gets zeros.
+ * --------------------------------------------------------------------------------------------- */
+size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t head_dim, int64_t total_q_rows,
+                                   int32_t num_splits);
+
+/* Number of key slices the automatic choice uses for this shape (what num_splits = 0 resolves to). */
+int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max_seq_len,
+                                int32_t max_q_rows);
+
+int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
+                     const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens,
+                     const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
+                     int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
+                     void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Prefill (extend) attention of the current chunk over the reconstructed BF16 prefix plus the BF16
+ * chunk itself ([#853 "What changes"]: current-chunk K/V remains BF16; [#853 "Paired end-to-end
+ * A/B"]: the historical-prefix + new-token operator).
+ *   q                : device BF16 [chunk_len][num_q_heads][head_dim]
+ *   k_chunk, v_chunk : device BF16 [chunk_len][num_kv_heads][head_dim]
+ *   ws_k, ws_v       : device BF16 [prefix_len][num_kv_heads][head_dim] (may be NULL if prefix_len 0)
+ *   out              : device BF16 [chunk_len][num_q_heads][head_dim]
+ * Chunk query t attends to all prefix_len prefix keys and to chunk keys 0..t.  Runs on the tcgen05
+ * tensor cores (BF16 operands, FP32 accumulation in tensor memory).
+ * --------------------------------------------------------------------------------------------- */
+int ftkv_prefill_attn(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
+                      int64_t chunk_len, const uint16_t* ws_k, const uint16_t* ws_v,
+                      int64_t prefix_len, float sm_scale, uint16_t* out, void* stream);
+
+/* Same operation on the legacy warp-level tensor-core path (mma.sync); kept as a comparison point. */
+int ftkv_prefill_attn_mma(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
+                          int64_t chunk_len, const uint16_t* ws_k, const uint16_t* ws_v,
+                          int64_t prefix_len, float sm_scale, uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * E4M3FN codec on the GPU, the same device code the store and attention kernels use.
+ *   ftkv_e4m3_encode_f32: x device float [n] -> codes device uint8 [n]  (RNE, saturating, NaN 0x7F)
+ *   ftkv_e4m3_decode_f32: codes device uint8 [n] -> x device float [n]  (exact)
+ * No alignment requirement.  ([#897 "Regression and CUDA isolation"]: every finite E4M3FN value,
+ * signed zero included, must survive bit-for-bit.)
+ * --------------------------------------------------------------------------------------------- */
+int ftkv_e4m3_encode_f32(const float* x, uint8_t* codes, int64_t n, void* stream);
+int ftkv_e4m3_decode_f32(const uint8_t* codes, float* x, int64_t n, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Byte accounting ([#853 "Validation"], [#853 "Follow-up model/workload search"]), host only.
+ *   bf16_bytes      = rows * layers * num_kv_heads * head_dim * 2 B * 2 (K and V)
+ *   fp8_bytes       = rows * layers * 2 * num_kv_heads * (head_dim + 4)   codes + FP32 scales
+ *   workspace_bytes = rows * num_kv_heads * head_dim * 2 B * 2            one shared BF16 layer
+ * Any output pointer may be NULL.
+ * --------------------------------------------------------------------------------------------- */
+int ftkv_pool_bytes(int64_t rows, int32_t layers, int32_t num_kv_heads, int32_t head_dim,
+                    int64_t* bf16_bytes, int64_t* fp8_bytes, int64_t* workspace_bytes);
+
+/* Read and clear the current device's error word (FTKV_DEVERR_* bits).  Synchronizes the device. */
+int ftkv_device_errors(int32_t* flags);
+
+/* Human-readable name of a status code; never NULL. */
+const char* ftkv_status_str(int status);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if none). */
+const char* ftkv_last_cuda_error(void);
+
+/* ABI version (FTKV_ABI_VERSION). */
+int ftkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FTKV_H_ */

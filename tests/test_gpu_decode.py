@@ -1,0 +1,133 @@
+"""GPU parity: split-K FP8 decode attention against the FP64 oracle.
+
+Covers the 512-token single step, ragged key counts (1, 17, 513), split caps 1/8/64 and automatic,
+GQA group sizes 8/4/2/1, multi-row decode (1..8 rows, rows that see no key), the 32,768- and
+40,000-key batch-1 workloads at full size (sampled layers, every output element), and the batched
+64-request multi-row workload at full size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_kv_cache_ftkv_gb300 import inputs, ops
+from parity import bits_to_cuda_bf16, check_attention
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(wl: inputs.DecodeWorkload, layer: int = 0):
+    """Store one layer of the workload on both sides; return GPU pool, oracle pool, device tensors."""
+    L = wl.layer(layer)
+    gp = ops.KVPool.empty(wl.num_rows, wl.Hkv)
+    if L.slots.size:
+        ops.store_quant(gp, bits_to_cuda_bf16(L.k), bits_to_cuda_bf16(L.v), torch.from_numpy(L.slots).cuda())
+    op = oracle.Pool(wl.num_rows, wl.Hkv, 128)
+    if L.slots.size:
+        oracle.store_quant(op, L.k, L.v, L.slots)
+    dev = dict(q=bits_to_cuda_bf16(L.q), r2s=torch.from_numpy(wl.req_to_slot).cuda(),
+               lens=torch.from_numpy(wl.seq_lens).cuda(), offs=torch.from_numpy(wl.q_row_offsets).cuda())
+    return gp, op, L, dev
+
+
+def _run(wl, gp, dev, num_splits=0, max_q_rows=None):
+    R = np.diff(wl.q_row_offsets)
+    mq = int(max(R.max(), 1)) if max_q_rows is None else max_q_rows
+    return ops.decode_attn(gp, dev["q"], dev["r2s"], dev["lens"], dev["offs"], max_seq_len=int(wl.req_to_slot.shape[1]),
+                           max_q_rows=mq, sm_scale=wl.sm_scale, num_splits=num_splits)
+
+
+def _ref(wl, op, L):
+    return oracle.decode_attn(op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets, wl.sm_scale, wl.Hq)
+
+
+def test_decode_small_step():
+    wl = inputs.decode_small()
+    gp, op, L, dev = _setup(wl)
+    out = _run(wl, gp, dev)
+    stats = check_attention(out, _ref(wl, op, L), "decode_small")
+    assert stats["max_abs"] < 0.05
+    assert ops.device_errors() == 0
+
+
+@pytest.mark.parametrize("n", [1, 17, 513, 4099])
+@pytest.mark.parametrize("splits", [0, 1, 8, 64])
+def test_decode_ragged_lengths_and_split_caps(n, splits):
+    wl = inputs.decode_custom([n], [1], max(2 * n, 64), seed=n)
+    gp, op, L, dev = _setup(wl)
+    out = _run(wl, gp, dev, num_splits=splits)
+    check_attention(out, _ref(wl, op, L), f"n={n} splits={splits}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 4), (16, 4), (8, 4), (4, 4), (64, 8)])
+def test_decode_gqa_groups(Hq, Hkv):
+    wl = inputs.decode_custom([300, 1000], [1, 1], 4000, seed=Hq, Hq=Hq, Hkv=Hkv)
+    gp, op, L, dev = _setup(wl)
+    out = _run(wl, gp, dev)
+    check_attention(out, _ref(wl, op, L), f"Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("rows", [[2], [3, 1, 8], [8, 8], [5, 7, 6, 4]])
+def test_decode_multirow(rows):
+    lens = [200 + 97 * i for i in range(len(rows))]
+    wl = inputs.decode_custom(lens, rows, 5000, sigma=2.0, big_frac=0.01, zero_frac=0.01, seed=len(rows))
+    gp, op, L, dev = _setup(wl)
+    for splits in (0, 1, 5):
+        out = _run(wl, gp, dev, num_splits=splits)
+        check_attention(out, _ref(wl, op, L), f"rows={rows} splits={splits}")
+
+
+def test_decode_rows_that_see_no_key_are_zero():
+    wl = inputs.decode_custom([2, 40], [5, 3], 100, seed=3)
+    gp, op, L, dev = _setup(wl)
+    out = _run(wl, gp, dev)
+    ref = _ref(wl, op, L)
+    assert (ref[:3] == 0).all()
+    check_attention(out, ref, "empty rows")
+    assert (out[:3].float() == 0).all()
+
+
+def test_decode_zero_length_request_and_single_row_path_with_offsets():
+    wl = inputs.decode_custom([0, 33, 1], [1, 1, 1], 64, seed=4)
+    gp, op, L, dev = _setup(wl)
+    out = _run(wl, gp, dev)
+    check_attention(out, _ref(wl, op, L), "zero-length request")
+    assert (out[0].float() == 0).all()
+
+
+@pytest.mark.parametrize("n,R", [(32768, 33059), (40000, 40290)])
+def test_decode_long_context_full_size(n, R):
+    wl = inputs.decode_long(n, R, layers=48)
+    for layer in (0, 47):
+        gp, op, L, dev = _setup(wl, layer)
+        out = _run(wl, gp, dev)
+        stats = check_attention(out, _ref(wl, op, L), f"n={n} layer={layer}")
+        assert stats["rel_l2"] < 2e-3
+    assert ops.device_errors() == 0
+
+
+def test_decode_batched_multirow_full_size():
+    wl = inputs.decode_batched()
+    gp, op, L, dev = _setup(wl)
+    out = _run(wl, gp, dev)
+    # sampled outputs: every query row of 12 requests (all heads, all d)
+    rng = np.random.default_rng(0)
+    for b in sorted(rng.choice(len(wl.seq_lens), size=12, replace=False)):
+        o0, o1 = int(wl.q_row_offsets[b]), int(wl.q_row_offsets[b + 1])
+        ref = oracle.decode_attn(op, L.q[o0:o1], wl.req_to_slot[b:b + 1], wl.seq_lens[b:b + 1],
+                                 np.array([0, o1 - o0], np.int32), wl.sm_scale, wl.Hq)
+        check_attention(out[o0:o1], ref, f"request {b}")
+    assert ops.device_errors() == 0
+
+
+def test_decode_bad_slot_and_seq_len_are_flagged_not_faulted():
+    wl = inputs.decode_custom([50], [1], 128, seed=5)
+    gp, op, L, dev = _setup(wl)
+    bad = dev["r2s"].clone()
+    bad[0, 3] = 10 ** 6
+    ops.decode_attn(gp, dev["q"], bad, dev["lens"], dev["offs"], max_seq_len=50, max_q_rows=1)
+    assert ops.device_errors() & 0x1
+    lens = torch.tensor([60], dtype=torch.int32, device="cuda")
+    ops.decode_attn(gp, dev["q"], dev["r2s"], lens, dev["offs"], max_seq_len=50, max_q_rows=1)
+    assert ops.device_errors() & 0x2
+    assert ops.device_errors() == 0

@@ -1,0 +1,127 @@
+"""GPU parity: E4M3 codec, quantize-on-write and reconstruct -- bit-exact against the oracle.
+
+Quantize-on-write runs the full 8,192-token x 48-layer workload into a 33,059-row pool (the
+configuration the benchmark times); reconstruct runs the chunked-prefill prefix sizes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_kv_cache_ftkv_gb300 import inputs, ops
+from parity import bits_to_cuda_bf16, cuda_bf16_to_bits, pool_to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def test_decode_all_codes_exact():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8).cuda()
+    got = ops.e4m3_decode(codes).cpu().numpy().astype(np.float64)
+    want = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    nan = np.isnan(want)
+    assert (np.isnan(got) == nan).all()
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_encode_every_fp32_bit_pattern():
+    """The store kernel's encoder (same device function) on all 2^32 FP32 inputs."""
+    chunk = 1 << 28
+    base = torch.arange(chunk, dtype=torch.int64, device="cuda")
+    for start in range(0, 1 << 32, chunk):
+        bits = (base + start)
+        bits = torch.where(bits >= (1 << 31), bits - (1 << 32), bits).to(torch.int32)
+        x = bits.view(torch.float32)
+        got = ops.e4m3_encode(x).cpu().numpy()
+        want = oracle.e4m3_encode(x.cpu().numpy())
+        if not np.array_equal(got, want):
+            bad = np.flatnonzero(got != want)[:8]
+            xs = x.cpu().numpy()[bad]
+            pytest.fail(f"chunk {start:#x}: x={xs} gpu={got[bad]} oracle={want[bad]}")
+
+
+def _store_both(T, R, sigma=2.0, big=0.01, zero=0.001, seed=5, slots=None):
+    rng = np.random.default_rng(seed)
+    k, v = inputs.kv_tokens(rng, T, sigma, big, zero)
+    if slots is None:
+        slots = rng.permutation(R)[:T].astype(np.int32)
+    gp = ops.KVPool.empty(R, 4)
+    ops.store_quant(gp, bits_to_cuda_bf16(k), bits_to_cuda_bf16(v), torch.from_numpy(slots).cuda())
+    op = oracle.Pool(R, 4, 128)
+    oracle.store_quant(op, k, v, slots)
+    return gp, op, slots
+
+
+def _assert_pool_equal(gp, op, slots):
+    kc, vc, ks, vs = pool_to_host(gp)
+    assert np.array_equal(kc[slots], op.k_codes[slots])
+    assert np.array_equal(vc[slots], op.v_codes[slots])
+    assert np.array_equal(ks[slots].view(np.uint32), op.k_scales[slots].view(np.uint32))
+    assert np.array_equal(vs[slots].view(np.uint32), op.v_scales[slots].view(np.uint32))
+
+
+def test_store_full_workload_48_layers_bit_exact():
+    wl = inputs.store()
+    slots_d = torch.from_numpy(wl.slots).cuda()
+    gp = ops.KVPool.empty(wl.num_rows, 4)
+    for l in range(wl.layers):
+        k, v = wl.layer(l)
+        ops.store_quant(gp, bits_to_cuda_bf16(k), bits_to_cuda_bf16(v), slots_d)
+        op = oracle.Pool(wl.num_rows, 4, 128)
+        oracle.store_quant(op, k, v, wl.slots)
+        _assert_pool_equal(gp, op, wl.slots)
+    assert ops.device_errors() == 0
+
+
+@pytest.mark.parametrize("T", [1, 7, 33, 1000])
+def test_store_ragged_sizes(T):
+    gp, op, slots = _store_both(T, 2048, seed=T)
+    _assert_pool_equal(gp, op, slots)
+
+
+def test_store_degenerate_rows():
+    x = np.zeros((4, 4, 128), np.float32)
+    x[1, :, ::2] = -0.0
+    x[2, 0, :] = np.linspace(-3, 3, 128)
+    x[2, 0, 5] = np.nan
+    x[2, 1, :] = 1.0
+    x[2, 1, 7] = np.inf
+    x[3] = 1e-40  # BF16 subnormals
+    x[3, 2, 3] = -3e-39
+    bits = inputs.to_bf16_bits(x)
+    slots = np.array([3, 0, 2, 1], np.int32)
+    gp = ops.KVPool.empty(4, 4)
+    ops.store_quant(gp, bits_to_cuda_bf16(bits), bits_to_cuda_bf16(bits), torch.from_numpy(slots).cuda())
+    op = oracle.Pool(4, 4, 128)
+    oracle.store_quant(op, bits, bits, slots)
+    _assert_pool_equal(gp, op, slots)
+
+
+def test_store_empty_is_noop_and_bad_slot_is_flagged():
+    gp = ops.KVPool.empty(16, 4)
+    empty = torch.empty(0, 4, 128, dtype=torch.bfloat16, device="cuda")
+    ops.store_quant(gp, empty, empty, torch.empty(0, dtype=torch.int32, device="cuda"))
+    assert ops.device_errors() == 0
+    k = torch.ones(2, 4, 128, dtype=torch.bfloat16, device="cuda")
+    ops.store_quant(gp, k, k, torch.tensor([3, 99], dtype=torch.int32, device="cuda"))
+    assert ops.device_errors() & 0x1
+    assert ops.device_errors() == 0  # cleared
+    assert (gp.k_codes[3] == 0x7E).all()  # the valid row was written (1.0 / (1/448) = 448)
+
+
+@pytest.mark.parametrize("P", [1, 5, 8192, 14336])
+def test_reconstruct_bit_exact(P):
+    R = 33059
+    gp, op, slots = _store_both(P, R, sigma=1.0, big=0.0, zero=0.0, seed=100 + P)
+    wk, wv = ops.reconstruct_bf16(gp, torch.from_numpy(slots).cuda())
+    ok, ov = oracle.reconstruct(op, slots)
+    assert np.array_equal(cuda_bf16_to_bits(wk), ok)
+    assert np.array_equal(cuda_bf16_to_bits(wv), ov)
+
+
+def test_reconstruct_wide_magnitudes_bit_exact():
+    gp, op, slots = _store_both(3000, 5000, sigma=2.0, big=0.05, zero=0.01, seed=9)
+    wk, wv = ops.reconstruct_bf16(gp, torch.from_numpy(slots).cuda())
+    ok, ov = oracle.reconstruct(op, slots)
+    assert np.array_equal(cuda_bf16_to_bits(wk), ok)
+    assert np.array_equal(cuda_bf16_to_bits(wv), ov)

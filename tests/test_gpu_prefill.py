@@ -1,0 +1,73 @@
+"""GPU parity: prefill attention over the reconstructed prefix plus the BF16 chunk.
+
+The chunked workload runs exactly as the benchmark does (8,192 historical rows, 8,192 new tokens in
+4 chunks of 2,048: reconstruct -> prefill -> quantize-on-write of the chunk) on both sides; every 16th
+query row of each chunk is compared (all heads, all d).  Small cases cover an empty prefix, ragged
+chunk and prefix lengths and GQA group sizes, for both tensor-core paths.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_kv_cache_ftkv_gb300 import inputs, ops
+from parity import bits_to_cuda_bf16, check_attention
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = ["mma"]
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("P,C", [(0, 1), (0, 77), (37, 29), (128, 128), (1000, 300), (257, 513)])
+def test_prefill_small(impl, P, C):
+    rng = np.random.default_rng(P * 1000 + C)
+    wk, wv = inputs.kv_tokens(rng, P, 1.0)
+    kc, vc = inputs.kv_tokens(rng, C, 1.0)
+    q = inputs.queries(rng, C)
+    ref = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE)
+    out = ops.prefill_attn(bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
+                           bits_to_cuda_bf16(wk) if P else None, bits_to_cuda_bf16(wv) if P else None, impl=impl)
+    check_attention(out, ref, f"{impl} P={P} C={C}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (8, 8), (64, 8)])
+def test_prefill_gqa(impl, Hq, Hkv):
+    rng = np.random.default_rng(Hq)
+    P, C = 200, 150
+    wk, wv = inputs.kv_tokens(rng, P, 1.0, Hkv=Hkv)
+    kc, vc = inputs.kv_tokens(rng, C, 1.0, Hkv=Hkv)
+    q = inputs.queries(rng, C, Hq)
+    ref = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE)
+    out = ops.prefill_attn(bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
+                           bits_to_cuda_bf16(wk), bits_to_cuda_bf16(wv), impl=impl)
+    check_attention(out, ref, f"{impl} Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_chunked_prefill_full_workload(impl):
+    wl = inputs.prefill()
+    R = wl.num_rows
+    gp = ops.KVPool.empty(R, 4)
+    op = oracle.Pool(R, 4, 128)
+    hist = torch.from_numpy(wl.hist_slots).cuda()
+    ops.store_quant(gp, bits_to_cuda_bf16(wl.hist_k), bits_to_cuda_bf16(wl.hist_v), hist)
+    oracle.store_quant(op, wl.hist_k, wl.hist_v, wl.hist_slots)
+    slots_all = np.concatenate([wl.hist_slots, wl.new_slots])
+    q_d, k_d, v_d = bits_to_cuda_bf16(wl.q), bits_to_cuda_bf16(wl.k), bits_to_cuda_bf16(wl.v)
+    slots_d = torch.from_numpy(slots_all).cuda()
+    H = wl.hist_slots.shape[0]
+    for c in range(wl.num_chunks):
+        c0, c1 = c * wl.chunk, min((c + 1) * wl.chunk, wl.q.shape[0])
+        P = H + c0
+        wk, wv = ops.reconstruct_bf16(gp, slots_d[:P])
+        out = ops.prefill_attn(q_d[c0:c1], k_d[c0:c1], v_d[c0:c1], wk, wv, impl=impl)
+        ops.store_quant(gp, k_d[c0:c1], v_d[c0:c1], slots_d[P:P + c1 - c0])
+        # oracle: the same pipeline
+        owk, owv = oracle.reconstruct(op, slots_all[:P])
+        rows = np.arange(0, c1 - c0, 16, dtype=np.int64)
+        ref = oracle.prefill_attn(wl.q[c0:c1], wl.k[c0:c1], wl.v[c0:c1], owk, owv, wl.sm_scale, rows)
+        oracle.store_quant(op, wl.k[c0:c1], wl.v[c0:c1], slots_all[P:P + c1 - c0])
+        check_attention(out[torch.from_numpy(rows).cuda()], ref, f"{impl} chunk {c}")
+    assert ops.device_errors() == 0
