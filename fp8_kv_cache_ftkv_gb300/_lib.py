@@ -23,6 +23,7 @@ FTKV_MAX_Q_ROWS = 8
 FTKV_DEVERR_BAD_SLOT = 0x1
 FTKV_DEVERR_SEQ_LEN = 0x2
 FTKV_DEVERR_Q_ROWS = 0x4
+FTKV_DEVERR_TIMEOUT = 0x8
 
 # Every symbol include/ftkv.h declares.
 EXPORTS = (
@@ -68,7 +69,7 @@ def load() -> ctypes.CDLL:
         sig = {
             "ftkv_store_quant": (ctypes.c_int, [PP, P, P, P, I64, P]),
             "ftkv_reconstruct_bf16": (ctypes.c_int, [PP, P, I64, P, P, P]),
-            "ftkv_decode_workspace_bytes": (SZ, [I32, I32, I64, I32]),
+            "ftkv_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I64, I32]),
             "ftkv_decode_auto_splits": (I32, [I32, I32, I64, I32]),
             "ftkv_decode_attn": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P, SZ, P, P]),
             "ftkv_prefill_attn": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),

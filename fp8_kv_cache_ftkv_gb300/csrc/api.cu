@@ -140,14 +140,18 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
   return e == cudaSuccess ? FTKV_OK : cuda_fail(e);
 }
 
-size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t head_dim, int64_t total_q_rows,
-                                   int32_t num_splits) {
-  if (num_q_heads <= 0 || head_dim <= 0 || total_q_rows < 0) return 0;
+// Workspace layout: [partial accumulators | partial (max, sum) | arrival counters], 256-B aligned parts.
+static int64_t ws_acc_bytes(int64_t parts) { return ceil_div(parts * FTKV_HEAD_DIM * 4, 256) * 256; }
+static int64_t ws_ml_bytes(int64_t parts) { return ceil_div(parts * 2 * 4, 256) * 256; }
+
+size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t batch,
+                                   int64_t total_q_rows, int32_t num_splits) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim != FTKV_HEAD_DIM || batch < 0 || total_q_rows < 0)
+    return 0;
   if (num_splits <= 0 || num_splits > FTKV_MAX_SPLITS) num_splits = FTKV_MAX_SPLITS;
   const int64_t parts = total_q_rows * num_q_heads * num_splits;
-  const int64_t acc = ceil_div(parts * head_dim * 4, 256) * 256;
-  const int64_t ml = ceil_div(parts * 2 * 4, 256) * 256;
-  return static_cast<size_t>(acc + ml + 256);
+  const int64_t ctr = ceil_div(int64_t(batch) * num_kv_heads * 4, 256) * 256;
+  return static_cast<size_t>(ws_acc_bytes(parts) + ws_ml_bytes(parts) + ctr);
 }
 
 int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max_seq_len, int32_t max_q_rows) {
@@ -175,6 +179,7 @@ int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t*
   if (max_q_rows < 1 || max_q_rows > FTKV_MAX_Q_ROWS) return FTKV_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > FTKV_MAX_SPLITS) return FTKV_ERR_INVALID;
   if (max_seq_len > req_stride) return FTKV_ERR_INVALID;
+  if (max_seq_len > (int64_t(1) << 31) - 1 - 4096) return FTKV_ERR_UNSUPPORTED;
   if (!q_row_offsets && total_q_rows != batch) return FTKV_ERR_INVALID;
   if (total_q_rows > int64_t(batch) * max_q_rows) return FTKV_ERR_INVALID;
   if (!(sm_scale == sm_scale)) return FTKV_ERR_INVALID;
@@ -188,15 +193,17 @@ int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t*
   int64_t chunk = ceil_div(max_seq_len > 0 ? max_seq_len : 1, num_splits);
   chunk = ceil_div(chunk, 16) * 16;
   const int64_t eff_splits = max_seq_len > 0 ? ceil_div(max_seq_len, chunk) : 1;
-  const size_t need = ftkv_decode_workspace_bytes(num_q_heads, FTKV_HEAD_DIM, total_q_rows,
-                                                  static_cast<int32_t>(eff_splits));
+  const size_t need = ftkv_decode_workspace_bytes(num_q_heads, pool->num_kv_heads, FTKV_HEAD_DIM, batch,
+                                                  total_q_rows, static_cast<int32_t>(eff_splits));
   if (workspace_bytes < need) return FTKV_ERR_WORKSPACE;
 
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FTKV_OK) return st;
   const int64_t parts = total_q_rows * num_q_heads * eff_splits;
   float* part_acc = static_cast<float*>(workspace);
-  float* part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ceil_div(parts * FTKV_HEAD_DIM * 4, 256) * 256);
+  char* ws = static_cast<char*>(workspace);
+  float* part_ml = reinterpret_cast<float*>(ws + ws_acc_bytes(parts));
+  int* counters = reinterpret_cast<int*>(ws + ws_acc_bytes(parts) + ws_ml_bytes(parts));
 
   ftkv::DecodeArgs a{};
   a.k_codes = pool->k_codes;
@@ -221,6 +228,7 @@ int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t*
   a.qk_scale_log2 = sm_scale * 1.4426950408889634f;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
+  a.counters = counters;
   a.out = out;
   a.err = di->err_word;
   cudaError_t e = ftkv::launch_decode(a, static_cast<cudaStream_t>(stream));
@@ -242,9 +250,11 @@ static int prefill_common(int32_t num_q_heads, int32_t num_kv_heads, int32_t hea
   if (!aligned16(q) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(out)) return FTKV_ERR_ALIGN;
   if (prefix_len > 0 && (!aligned16(ws_k) || !aligned16(ws_v))) return FTKV_ERR_ALIGN;
   if (chunk_len > (int64_t(1) << 31) - 1 || prefix_len > (int64_t(1) << 31) - 1) return FTKV_ERR_UNSUPPORTED;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FTKV_OK) return st;
   ftkv::PrefillArgs a{num_q_heads, num_kv_heads, q, k_chunk, v_chunk, chunk_len,
                       prefix_len > 0 ? ws_k : k_chunk, prefix_len > 0 ? ws_v : v_chunk, prefix_len,
-                      sm_scale * 1.4426950408889634f, out};
+                      sm_scale * 1.4426950408889634f, out, di->err_word};
   cudaError_t e = tc ? ftkv::launch_prefill_tc(a, static_cast<cudaStream_t>(stream))
                      : ftkv::launch_prefill_mma(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FTKV_OK : cuda_fail(e);

@@ -1,27 +1,29 @@
-// decode.cu -- split-K decode attention over the FP8 (E4M3FN) pool, plus the split merge.
+// decode.cu -- split-K decode attention over the FP8 (E4M3FN) pool, split merge included.
 //
 // What it computes (FreeToken PR #897, opening description and "Fresh R9700 stage-1 A/B"): for a
 // request with n keys and a BF16 query row, per query head i (KV head h = i / G)
 //     s_j = (q . k^_j) * sm_scale,   k^_j = decode(codeK_j) * scaleK_j,   v^_j likewise,
 //     o   = sum_j softmax(s)_j v^_j,
-// with split-K over the keys: a stage-1 kernel covers one slice of the keys per CTA and writes a
-// partial (max, sum, accumulator); a merge kernel combines the slices.  Multi-row decode: row r of
-// R rows sees keys 0 .. n-R+r.
+// with split-K over the keys: each CTA covers one slice of the keys and writes a partial (max, sum,
+// accumulator); the last slice of a (request, KV head) to finish merges them in the same launch.
+// Multi-row decode: row r of R rows sees keys 0 .. n-R+r.
 //
 // GB300 design:
 //  * CTA = (key slice, KV head, request).  Each warp runs its own software pipeline: cp.async
 //    gathers of 16-key blocks (128 B of K codes + 128 B of V codes + two FP32 scales per key) into a
-//    private 3-4 stage shared-memory ring, so 100+ KB per SM are in flight with no CTA barriers.
-//  * The slot indices of the CTA's slice are staged in shared memory first, so the gathers never
-//    wait on a dependent index load.
-//  * QK^T and PV are warp-level tensor-core MMAs (m16n8k16, FP16 inputs, FP32 accumulation).  The 8
-//    query heads of a GQA group are the MMA's N dimension, so no padding is wasted at G = 8.
-//    E4M3 codes become FP16 exactly with the packed hardware converter; the per-key scales are applied
-//    to the FP32 scores (K) and folded into the probabilities (V) instead of the codes.
-//  * V scales vary over many binades; P*scaleV is kept in FP16 range by tracking the running maximum
-//    binary exponent E of the V scales of a slice (P' = p * scaleV * 2^-E <= 2) and rescaling the
-//    accumulator when E grows -- an exact power-of-two bookkeeping next to the usual running max.
-//  * Queries are scaled by a power of two per head so the FP16 copy of a BF16 query is exact.
+//    private shared-memory ring, so ~150 KB per SM are in flight without CTA-wide barriers.  The slot
+//    indices of the slice are staged in shared memory first, so no gather waits on an index load.
+//  * QK^T runs on the FP8 tensor cores directly on the stored codes (mma m16n8k32, E4M3 x E4M3 ->
+//    FP32): the K codes are the A operand as they sit in memory, no conversion.  The BF16 query is
+//    split per head into two E4M3 pieces q = a (h1 + h2/16), a a power of two: h1 is q rounded to 4
+//    significant bits and the remainder k * 2^(e-7), |k| <= 8, fits h2 exactly, so every element
+//    within 13 binades of the head's largest one is represented without error.  The two partial dot
+//    products are recombined in FP32 with the per-key K scale.
+//  * PV runs on FP16 tensor cores (m16n8k16): V codes are converted exactly with the packed
+//    hardware converter; the V scale is folded into the probabilities.  P' = p * scaleV * 2^-E stays
+//    in FP16 range by tracking the running maximum binary exponent E of the V scales and rescaling
+//    the accumulator when it grows (exact power-of-two bookkeeping next to the usual running max).
+//  * The 8 query heads of a GQA group are the MMA N dimension, so G = 8 wastes nothing.
 #include <cfloat>
 
 #include "ftkv_device.cuh"
@@ -56,16 +58,33 @@ constexpr int smem_bytes() {
   return Cfg<RPW>::WARPS * Cfg<RPW>::NSTAGE * STAGE_BYTES + MAX_SUB * 4;
 }
 static_assert(smem_bytes<1>() <= 227 * 1024, "decode smem");
-static_assert(Cfg<1>::WARPS * 1 * 8 * MERGE_STRIDE * 4 <= Cfg<1>::WARPS * Cfg<1>::NSTAGE * STAGE_BYTES, "merge");
-static_assert(Cfg<2>::WARPS * 2 * 8 * MERGE_STRIDE * 4 <= Cfg<2>::WARPS * Cfg<2>::NSTAGE * STAGE_BYTES, "merge");
+static_assert(Cfg<1>::WARPS * 1 * 8 * MERGE_STRIDE * 4 + 2048 <= Cfg<1>::WARPS * Cfg<1>::NSTAGE * STAGE_BYTES, "merge");
+static_assert(Cfg<2>::WARPS * 2 * 8 * MERGE_STRIDE * 4 + 2048 <= Cfg<2>::WARPS * Cfg<2>::NSTAGE * STAGE_BYTES, "merge");
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// Shared-memory position of 16-byte chunk p of key `key` in a stage (XOR swizzles chosen so the
-// fragment reads below are conflict-free: K rows are read by (key g, chunk t), V rows by (key 2t.., chunk g)).
-__device__ __forceinline__ uint32_t k_chunk_off(int key, int p) { return (key * 8 + (p ^ ((key & 1) << 2))) * 16; }
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D += A(16x32, e4m3, row) * B(32x8, e4m3, col), FP32 accumulate.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Shared-memory position of 16-byte chunk p of key `key` in a stage.  K rows are read as
+// (key g, chunks 2t and 2t+1), V rows as (keys 2t.., chunk g); the XOR swizzles make both reads and
+// the cp.async writes bank-conflict free.
+__device__ __forceinline__ uint32_t k_chunk_off(int key, int p) { return (key * 8 + (p ^ (key & 1))) * 16; }
 __device__ __forceinline__ uint32_t v_chunk_off(int key, int p) { return STAGE_K + (key * 8 + (p ^ (((key >> 1) & 3) << 1))) * 16; }
 
 __device__ __forceinline__ int64_t clamp_seq_len(const DecodeArgs& a, int b, bool report) {
@@ -103,47 +122,51 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     if (threadIdx.x == 0 && split == 0 && h == 0) flag_error(a.err, kDevErrQRows);
     return;  // inconsistent row offsets: skip the request rather than read outside q
   }
-  const int64_t j0 = static_cast<int64_t>(split) * a.chunk;
-  const int64_t j1 = (j0 + a.chunk < n) ? j0 + a.chunk : n;
-  if (j0 >= n || R == 0) return;  // the merge only reads slices that hold keys
+  if (n == 0) {  // no keys: the rows of this KV head's group are zero
+    if (split == 0)
+      for (int i = threadIdx.x; i < R * a.group * kHeadDim; i += blockDim.x)
+        a.out[((row0 + i / (a.group * kHeadDim)) * a.num_q_heads + h * a.group + (i / kHeadDim) % a.group) *
+                  kHeadDim + i % kHeadDim] = 0;
+    return;
+  }
+  // key indices fit in 32 bits (the host rejects max_seq_len >= 2^31)
+  const int j0 = split * static_cast<int>(a.chunk);
+  const int j1 = (static_cast<int64_t>(j0) + a.chunk < n) ? j0 + static_cast<int>(a.chunk) : static_cast<int>(n);
+  if (j0 >= n || R == 0) return;  // slices past the end hold no keys and take no ticket
 
   // ---- warp roles: row group rg (RPW query rows) x key-interleave index kw ----
   const int nrg = (R + RPW - 1) / RPW;
   const int wk = WARPS / nrg;
   const int rg = warp / wk, kw = warp % wk;
   const bool active = rg < nrg;
-  int rabs[RPW];
-  bool rvalid[RPW];
-  int64_t lim[RPW];
+  int lim[RPW];
 #pragma unroll
   for (int i = 0; i < RPW; i++) {
-    rabs[i] = rg * RPW + i;
-    rvalid[i] = active && rabs[i] < R;
-    const int64_t vis = n - R + rabs[i] + 1;  // keys 0 .. vis-1 are visible to this row
-    lim[i] = rvalid[i] ? (vis < j1 ? vis : j1) : j0;
+    const int rabs = rg * RPW + i;
+    const bool valid = active && rabs < R;
+    const int vis = static_cast<int>(n) - R + rabs + 1;  // keys 0 .. vis-1 are visible to this row
+    lim[i] = valid ? (vis < j1 ? vis : j1) : j0;
   }
 
-  // ---- query fragments (B operand of QK^T): head g of the group, d = 64c + 16t + 4sub + {0..3} ----
-  uint32_t qf[RPW][8][2];
-  float fq[RPW][2];  // per-head score multiplier for heads 2t, 2t+1: 2^Eq * sm_scale * log2(e)
+  // ---- query pieces (B operand of QK^T): head g, d = 32t + 8kk + {0..3} (b0) / {4..7} (b1) ----
+  uint32_t qp[RPW][2][4][2];
+  float fq[RPW][2];  // per-head multiplier for heads 2t, 2t+1: a * sm_scale * log2(e)
 #pragma unroll
   for (int i = 0; i < RPW; i++) {
+    const int rabs = rg * RPW + i;
     float qv[32];
     float amax = 0.0f;
-    if (rvalid[i] && g < a.group) {
-      const uint16_t* qp = a.q + ((row0 + rabs[i]) * a.num_q_heads + h * a.group + g) * kHeadDim;
-      const uint4 q0 = __ldg(reinterpret_cast<const uint4*>(qp + 16 * t));
-      const uint4 q1 = __ldg(reinterpret_cast<const uint4*>(qp + 16 * t + 8));
-      const uint4 q2 = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 16 * t));
-      const uint4 q3 = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 16 * t + 8));
-      const uint4 qq[4] = {q0, q1, q2, q3};
+    if (active && rabs < R && g < a.group) {
+      const uint16_t* qptr = a.q + ((row0 + rabs) * a.num_q_heads + h * a.group + g) * kHeadDim + 32 * t;
 #pragma unroll
-      for (int u = 0; u < 4; u++)
+      for (int u = 0; u < 4; u++) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qptr + 8 * u));
 #pragma unroll
         for (int w = 0; w < 4; w++) {
-          qv[u * 8 + 2 * w] = bf16_lo(word(qq[u], w));
-          qv[u * 8 + 2 * w + 1] = bf16_hi(word(qq[u], w));
+          qv[u * 8 + 2 * w] = bf16_lo(word(v, w));
+          qv[u * 8 + 2 * w + 1] = bf16_hi(word(v, w));
         }
+      }
 #pragma unroll
       for (int e = 0; e < 32; e++) amax = fmaxf(amax, fabsf(qv[e]));
     } else {
@@ -153,18 +176,31 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     int ex = (amax > 0.0f) ? ilogbf(amax) : 0;
-    ex = ex < -112 ? -112 : ex;
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + 14 - ex) << 23);       // 2^(14-ex)
-    const float down = __uint_as_float(static_cast<uint32_t>(127 - 14 + ex) << 23) * a.qk_scale_log2;
-    // qv[e]: e in [0,16) -> d = 16t + e ; e in [16,32) -> d = 64 + 16t + (e-16)
+    ex = ex < -120 ? -120 : ex;
+    // x = q * 2^(7-ex) has |x| < 256; pieces: x = h1 + h2/16 (exact unless |q| < 2^-13 max|q|)
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + 7 - ex) << 23);
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * a.qk_scale_log2;
 #pragma unroll
-    for (int c = 0; c < 2; c++)
+    for (int e = 0; e < 32; e += 4) {
+      uint32_t pc[2];
+      float x[4] = {qv[e] * up, qv[e + 1] * up, qv[e + 2] * up, qv[e + 3] * up};
 #pragma unroll
-      for (int sub = 0; sub < 4; sub++) {
-        const int e = c * 16 + 4 * sub;
-        qf[i][4 * c + sub][0] = float2_to_f16x2(qv[e] * up, qv[e + 1] * up);
-        qf[i][4 * c + sub][1] = float2_to_f16x2(qv[e + 2] * up, qv[e + 3] * up);
+      for (int p = 0; p < 2; p++) {
+        const uint32_t c01 = e4m3x2_encode(x[0], x[1]), c23 = e4m3x2_encode(x[2], x[3]);
+        pc[p] = c01 | (c23 << 16);
+        if (p == 0) {
+          const float2 v01 = f16x2_to_float2(e4m3x2_to_f16x2(c01));
+          const float2 v23 = f16x2_to_float2(e4m3x2_to_f16x2(c23));
+          x[0] = (x[0] - v01.x) * 16.0f;
+          x[1] = (x[1] - v01.y) * 16.0f;
+          x[2] = (x[2] - v23.x) * 16.0f;
+          x[3] = (x[3] - v23.y) * 16.0f;
+        }
       }
+      const int kk = e >> 3, half = (e >> 2) & 1;
+#pragma unroll
+      for (int p = 0; p < 2; p++) qp[i][p][kk][half] = pc[p];
+    }
     fq[i][0] = __shfl_sync(0xffffffffu, down, (2 * t) * 4);
     fq[i][1] = __shfl_sync(0xffffffffu, down, (2 * t + 1) * 4);
   }
@@ -183,9 +219,9 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   const uint32_t ring = smem_addr(smem) + warp * NSTAGE * STAGE_BYTES;
   const int64_t hkv = a.num_kv_heads;
 
-  for (int64_t js = j0; js < j1; js += MAX_SUB) {
-    const int64_t je = (js + MAX_SUB < j1) ? js + MAX_SUB : j1;
-    const int nk = static_cast<int>(je - js);
+  for (int js = j0; js < j1; js += MAX_SUB) {
+    const int je = (js + MAX_SUB < j1) ? js + MAX_SUB : j1;
+    const int nk = je - js;
     __syncthreads();  // every warp is done with the previous slot window
     for (int i = threadIdx.x; i < nk; i += blockDim.x) {
       int32_t s = a.req_to_slot[static_cast<int64_t>(b) * a.req_stride + js + i];
@@ -205,14 +241,14 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
       if (i < my_nblk) {
         const int key0 = (kw + i * wk) * KB;
         const uint32_t st = ring + (i % NSTAGE) * STAGE_BYTES;
+        const int p = lane & 7;
 #pragma unroll
         for (int r = 0; r < 4; r++) {
           const int key = (lane >> 3) + 4 * r;
-          const int p = lane & 7;
           if (key0 + key < nk) {
-            const int64_t row = static_cast<int64_t>(sslot[key0 + key]) * hkv + h;
-            cp_async_16(st + k_chunk_off(key, p), a.k_codes + row * kHeadDim + p * 16);
-            cp_async_16(st + v_chunk_off(key, p), a.v_codes + row * kHeadDim + p * 16);
+            const int64_t off = (static_cast<int64_t>(sslot[key0 + key]) * hkv + h) * kHeadDim + p * 16;
+            cp_async_16(st + k_chunk_off(key, p), a.k_codes + off);
+            cp_async_16(st + v_chunk_off(key, p), a.v_codes + off);
           } else {
             st_shared_zero16(st + k_chunk_off(key, p));
             st_shared_zero16(st + v_chunk_off(key, p));
@@ -239,28 +275,29 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
       cp_async_wait<NSTAGE - 1>();
       __syncwarp();
       const uint32_t st = ring + (i % NSTAGE) * STAGE_BYTES;
-      const int64_t jb = js + static_cast<int64_t>(kw + i * wk) * KB;
+      const int jb = js + (kw + i * wk) * KB;
 
-      // ---- S^T = K Q^T : keys as M (rows g, g+8), query heads as N ----
-      const uint4 kA0 = ld_shared_v4(st + k_chunk_off(g, t));
-      const uint4 kA1 = ld_shared_v4(st + k_chunk_off(g, t + 4));
-      const uint4 kB0 = ld_shared_v4(st + k_chunk_off(g + 8, t));
-      const uint4 kB1 = ld_shared_v4(st + k_chunk_off(g + 8, t + 4));
-      float c[RPW][4];
+      // ---- S^T = K Q^T on E4M3 codes: keys as M (rows g, g+8), heads as N, 2 query pieces ----
+      const uint4 kA0 = ld_shared_v4(st + k_chunk_off(g, 2 * t));
+      const uint4 kA1 = ld_shared_v4(st + k_chunk_off(g, 2 * t + 1));
+      const uint4 kB0 = ld_shared_v4(st + k_chunk_off(g + 8, 2 * t));
+      const uint4 kB1 = ld_shared_v4(st + k_chunk_off(g + 8, 2 * t + 1));
+      float c[RPW][2][4];
 #pragma unroll
-      for (int r = 0; r < RPW; r++) c[r][0] = c[r][1] = c[r][2] = c[r][3] = 0.0f;
+      for (int r = 0; r < RPW; r++)
 #pragma unroll
-      for (int cc = 0; cc < 2; cc++)
+        for (int p = 0; p < 2; p++) c[r][p][0] = c[r][p][1] = c[r][p][2] = c[r][p][3] = 0.0f;
 #pragma unroll
-        for (int sub = 0; sub < 4; sub++) {
-          const uint32_t wa = word(cc ? kA1 : kA0, sub);
-          const uint32_t wb = word(cc ? kB1 : kB0, sub);
-          const uint32_t a0 = e4m3_lo2(wa), a2 = e4m3_hi2(wa);
-          const uint32_t a1 = e4m3_lo2(wb), a3 = e4m3_hi2(wb);
+      for (int kk = 0; kk < 4; kk++) {
+        const uint4& A = kk < 2 ? kA0 : kA1;
+        const uint4& B = kk < 2 ? kB0 : kB1;
+        const uint32_t a0 = word(A, 2 * (kk & 1)), a2 = word(A, 2 * (kk & 1) + 1);
+        const uint32_t a1 = word(B, 2 * (kk & 1)), a3 = word(B, 2 * (kk & 1) + 1);
 #pragma unroll
-          for (int r = 0; r < RPW; r++)
-            mma_f16_16816(c[r], a0, a1, a2, a3, qf[r][4 * cc + sub][0], qf[r][4 * cc + sub][1]);
-        }
+        for (int r = 0; r < RPW; r++)
+#pragma unroll
+          for (int p = 0; p < 2; p++) mma_e4m3_16832(c[r][p], a0, a1, a2, a3, qp[r][p][kk][0], qp[r][p][kk][1]);
+      }
 
       // ---- per-key scales; V exponent bookkeeping ----
       const uint32_t ss = st + STAGE_K + STAGE_V;
@@ -274,19 +311,22 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
       const int bnew = max(bexp, be);
       const float inv = __uint_as_float(static_cast<uint32_t>(254 - bnew) << 23);  // 2^(127-bnew)
       const float sv0 = svg * inv, sv8 = svg8 * inv;
-      const float shift = exp2f(static_cast<float>(bexp - bnew));
+      const float shift = (bnew != bexp) ? fast_exp2(static_cast<float>(bexp - bnew)) : 1.0f;
       bexp = bnew;
 
       // ---- online softmax (log2 domain), P' = p * scaleV * 2^-E into B fragments of PV ----
-      const int64_t jg = jb + g, jg8 = jb + g + 8;
+      const int jg = jb + g, jg8 = jb + g + 8;
       uint32_t pb0[RPW], pb1[RPW];
 #pragma unroll
       for (int r = 0; r < RPW; r++) {
-        const int64_t lr = lim[r] < je ? lim[r] : je;
-        const float s0 = (jg < lr) ? c[r][0] * (skg * fq[r][0]) : -INFINITY;
-        const float s1 = (jg < lr) ? c[r][1] * (skg * fq[r][1]) : -INFINITY;
-        const float s2 = (jg8 < lr) ? c[r][2] * (skg8 * fq[r][0]) : -INFINITY;
-        const float s3 = (jg8 < lr) ? c[r][3] * (skg8 * fq[r][1]) : -INFINITY;
+        const int lr = lim[r] < je ? lim[r] : je;
+        float dot[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) dot[e] = fmaf(c[r][1][e], 1.0f / 16.0f, c[r][0][e]);
+        const float s0 = (jg < lr) ? dot[0] * (skg * fq[r][0]) : -INFINITY;
+        const float s1 = (jg < lr) ? dot[1] * (skg * fq[r][1]) : -INFINITY;
+        const float s2 = (jg8 < lr) ? dot[2] * (skg8 * fq[r][0]) : -INFINITY;
+        const float s3 = (jg8 < lr) ? dot[3] * (skg8 * fq[r][1]) : -INFINITY;
         float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -296,20 +336,22 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
         const float mn0 = fmaxf(m[r][0], bm0), mn1 = fmaxf(m[r][1], bm1);
         const float mu0 = (mn0 == -INFINITY) ? 0.0f : mn0;
         const float mu1 = (mn1 == -INFINITY) ? 0.0f : mn1;
-        const float al0 = exp2f(m[r][0] - mu0), al1 = exp2f(m[r][1] - mu1);
-        const float p0 = exp2f(s0 - mu0), p1 = exp2f(s1 - mu1);
-        const float p2 = exp2f(s2 - mu0), p3 = exp2f(s3 - mu1);
+        const float al0 = fast_exp2(m[r][0] - mu0), al1 = fast_exp2(m[r][1] - mu1);
+        const float p0 = fast_exp2(s0 - mu0), p1 = fast_exp2(s1 - mu1);
+        const float p2 = fast_exp2(s2 - mu0), p3 = fast_exp2(s3 - mu1);
         l[r][0] = l[r][0] * al0 + (p0 + p2);
         l[r][1] = l[r][1] * al1 + (p1 + p3);
         m[r][0] = mn0;
         m[r][1] = mn1;
         const float ac0 = al0 * shift, ac1 = al1 * shift;
+        if (__any_sync(0xffffffffu, ac0 != 1.0f || ac1 != 1.0f)) {
 #pragma unroll
-        for (int mt = 0; mt < 8; mt++) {
-          acc[r][mt][0] *= ac0;
-          acc[r][mt][1] *= ac1;
-          acc[r][mt][2] *= ac0;
-          acc[r][mt][3] *= ac1;
+          for (int mt = 0; mt < 8; mt++) {
+            acc[r][mt][0] *= ac0;
+            acc[r][mt][1] *= ac1;
+            acc[r][mt][2] *= ac0;
+            acc[r][mt][3] *= ac1;
+          }
         }
         pb0[r] = movmatrix_trans(float2_to_f16x2(p0 * sv0, p1 * sv0));   // keys 0..7
         pb1[r] = movmatrix_trans(float2_to_f16x2(p2 * sv8, p3 * sv8));   // keys 8..15
@@ -354,6 +396,7 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
 
   __syncthreads();  // the rings are free: reuse them as the merge area
   float* merge = reinterpret_cast<float*>(smem);
+  float* mw = merge + WARPS * RPW * 8 * MERGE_STRIDE;  // per (row, head): wk weights, then M, L
   if (active) {
 #pragma unroll
     for (int r = 0; r < RPW; r++) {
@@ -376,68 +419,108 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   __syncthreads();
 
   // ---- merge the wk warps of each row group; write this slice's partial ----
-  const int items = nrg * RPW * a.group * kHeadDim;
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
-    const int d = it % kHeadDim;
-    const int hh = (it / kHeadDim) % a.group;
-    const int rr = it / (kHeadDim * a.group);      // row index within the request: rg*RPW + r
-    if (rr >= R) continue;
+  // weights first: one thread per (row, head) pair computes M, L and the wk weights 2^(m_k - M)
+  const int npairs = R * a.group;
+  constexpr int WSTRIDE = WARPS + 2;
+  for (int pr = threadIdx.x; pr < npairs; pr += blockDim.x) {
+    const int rr = pr / a.group, hh = pr % a.group;
     const int rgi = rr / RPW, r = rr % RPW;
     float M = -INFINITY;
+    for (int k = 0; k < wk; k++) M = fmaxf(M, merge[(((rgi * wk + k) * RPW + r) * 8 + hh) * MERGE_STRIDE + 128]);
+    float L = 0.0f;
+    float* w = mw + pr * WSTRIDE;
     for (int k = 0; k < wk; k++) {
       const float* src = merge + (((rgi * wk + k) * RPW + r) * 8 + hh) * MERGE_STRIDE;
-      M = fmaxf(M, src[128]);
+      const float wt = (M == -INFINITY) ? 0.0f : exp2f(src[128] - M);
+      w[k] = wt;
+      L += wt * src[129];
     }
-    float A = 0.0f, L = 0.0f;
-    if (M != -INFINITY) {
-      for (int k = 0; k < wk; k++) {
-        const float* src = merge + (((rgi * wk + k) * RPW + r) * 8 + hh) * MERGE_STRIDE;
-        const float w = exp2f(src[128] - M);
-        A += w * src[d];
-        L += w * src[129];
-      }
-    }
+    w[WARPS] = M;
+    w[WARPS + 1] = L;
+  }
+  __syncthreads();
+  for (int it = threadIdx.x; it < npairs * kHeadDim; it += blockDim.x) {
+    const int d = it % kHeadDim, pr = it / kHeadDim;
+    const int rr = pr / a.group, hh = pr % a.group;
+    const int rgi = rr / RPW, r = rr % RPW;
+    const float* w = mw + pr * WSTRIDE;
+    float A = 0.0f;
+    for (int k = 0; k < wk; k++) A += w[k] * merge[(((rgi * wk + k) * RPW + r) * 8 + hh) * MERGE_STRIDE + d];
     const int64_t prow = ((row0 + rr) * a.num_q_heads + h * a.group + hh) * a.num_splits + split;
     a.part_acc[prow * kHeadDim + d] = A;
     if (d == 0) {
-      a.part_ml[prow * 2] = M;
-      a.part_ml[prow * 2 + 1] = L;
+      a.part_ml[prow * 2] = w[WARPS];
+      a.part_ml[prow * 2 + 1] = w[WARPS + 1];
     }
   }
-}
 
-// Merge the slices of one (query row, query head): o = sum_s 2^(M_s-M) A_s / sum_s 2^(M_s-M) L_s.
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
-  const int64_t row = blockIdx.x;
-  const int hq = blockIdx.y;
-  const int d = threadIdx.x;
-  int b;
-  if (a.q_row_offsets) {
-    int lo = 0, hi = a.batch;  // last b with q_row_offsets[b] <= row
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (a.q_row_offsets[mid] <= row) lo = mid; else hi = mid;
-    }
-    b = lo;
-  } else {
-    b = static_cast<int>(row);
+  // ---- split merge, done by the last slice of (request, KV head) to arrive ----
+  // Every slice publishes its partial, then takes a ticket; the CTA that draws the last ticket merges
+  // all slices (o = sum_s 2^(M_s - M) A_s / sum_s 2^(M_s - M) L_s) and resets the counter for the
+  // next call.  Nothing ever waits on another CTA.
+  __shared__ int s_last;
+  const int64_t nsl64 = (n + a.chunk - 1) / a.chunk;
+  const int nslices = static_cast<int>(nsl64 < a.num_splits ? nsl64 : a.num_splits);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int* ctr = a.counters + static_cast<int64_t>(b) * a.num_kv_heads + h;
+    const int prev = atomicAdd(ctr, 1);
+    s_last = (prev == nslices - 1);
+    if (s_last) *ctr = 0;
   }
-  const int64_t n = clamp_seq_len(a, b, false);
-  int64_t S = (n + a.chunk - 1) / a.chunk;
-  if (S > a.num_splits) S = a.num_splits;
-  const int64_t base = (row * a.num_q_heads + hq) * a.num_splits;
-  float M = -INFINITY;
-  for (int64_t s = 0; s < S; s++) M = fmaxf(M, a.part_ml[(base + s) * 2]);
-  float num = 0.0f, den = 0.0f;
-  if (M != -INFINITY) {
-    for (int64_t s = 0; s < S; s++) {
-      const float w = exp2f(a.part_ml[(base + s) * 2] - M);
-      num += w * a.part_acc[(base + s) * kHeadDim + d];
-      den += w * a.part_ml[(base + s) * 2 + 1];
-    }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // merge weights w[(rr*group + hh) * nslices + s] in the (now free) ring memory
+  float* wts = reinterpret_cast<float*>(smem);
+  for (int i = threadIdx.x; i < npairs * nslices; i += blockDim.x) {
+    const int pr = i / nslices, sl = i % nslices;
+    const int64_t prow = ((row0 + pr / a.group) * a.num_q_heads + h * a.group + pr % a.group) * a.num_splits + sl;
+    wts[i] = __ldcg(a.part_ml + prow * 2);
+    wts[npairs * nslices + i] = __ldcg(a.part_ml + prow * 2 + 1);
   }
-  const float o = (den > 0.0f) ? num / den : 0.0f;
-  a.out[(row * a.num_q_heads + hq) * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+  __syncthreads();
+  for (int pr = threadIdx.x; pr < npairs; pr += blockDim.x) {
+    float* wm = wts + pr * nslices;
+    const float* wl = wts + npairs * nslices + pr * nslices;
+    float M = -INFINITY;
+    for (int sl = 0; sl < nslices; sl++) M = fmaxf(M, wm[sl]);
+    float L = 0.0f;
+    if (M != -INFINITY)
+      for (int sl = 0; sl < nslices; sl++) L += exp2f(wm[sl] - M) * wl[sl];
+    const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
+    for (int sl = 0; sl < nslices; sl++) wm[sl] = (invL != 0.0f) ? exp2f(wm[sl] - M) * invL : 0.0f;
+  }
+  __syncthreads();
+  // one float4 of d per thread: 32 threads per (row, head), loads batched 8 deep
+  for (int it = threadIdx.x; it < npairs * (kHeadDim / 4); it += blockDim.x) {
+    const int d4 = it % (kHeadDim / 4), pr = it / (kHeadDim / 4);
+    const int rr = pr / a.group, hh = pr % a.group;
+    const int64_t base = ((row0 + rr) * a.num_q_heads + h * a.group + hh) * a.num_splits;
+    const float* wm = wts + pr * nslices;
+    const float4* src = reinterpret_cast<const float4*>(a.part_acc + base * kHeadDim) + d4;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    int sl = 0;
+    for (; sl + 8 <= nslices; sl += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) v[u] = __ldcg(src + static_cast<int64_t>(sl + u) * (kHeadDim / 4));
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const float wv = wm[sl + u];
+        o.x += wv * v[u].x; o.y += wv * v[u].y; o.z += wv * v[u].z; o.w += wv * v[u].w;
+      }
+    }
+    for (; sl < nslices; sl++) {
+      const float4 v = __ldcg(src + static_cast<int64_t>(sl) * (kHeadDim / 4));
+      const float wv = wm[sl];
+      o.x += wv * v.x; o.y += wv * v.y; o.z += wv * v.z; o.w += wv * v.w;
+    }
+    uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
+    *reinterpret_cast<uint2*>(a.out + ((row0 + rr) * a.num_q_heads + h * a.group + hh) * kHeadDim + 4 * d4) = packed;
+  }
 }
 
 template <int RPW>
@@ -464,14 +547,7 @@ int decode_ctas_per_sm(int max_q_rows) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e = (a.max_q_rows <= 1) ? launch_split<1>(a, s) : launch_split<2>(a, s);
-  if (e != cudaSuccess) return e;
-  if (a.total_q_rows > 0) {
-    dim3 grid(static_cast<unsigned>(a.total_q_rows), a.num_q_heads);
-    decode_combine_kernel<<<grid, 128, 0, s>>>(a);
-    e = cudaGetLastError();
-  }
-  return e;
+  return (a.max_q_rows <= 1) ? launch_split<1>(a, s) : launch_split<2>(a, s);
 }
 
 }  // namespace ftkv

@@ -18,6 +18,7 @@ constexpr int kHeadDim = 128;
 constexpr int kDevErrBadSlot = 0x1;
 constexpr int kDevErrSeqLen = 0x2;
 constexpr int kDevErrQRows = 0x4;
+constexpr int kDevErrTimeout = 0x8;
 
 // ---------------------------------------------------------------------------------------------
 // E4M3FN codec

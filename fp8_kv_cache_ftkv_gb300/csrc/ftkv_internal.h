@@ -58,6 +58,7 @@ struct DecodeArgs {
   float qk_scale_log2;       // sm_scale * log2(e)
   float* part_acc;           // [total_q_rows][Hq][num_splits][128]
   float* part_ml;            // [total_q_rows][Hq][num_splits][2]  (max in log2 units, sum)
+  int* counters;             // [batch][Hkv] arrival tickets; zero between calls
   uint16_t* out;             // [total_q_rows][Hq][128]
   int* err;
 };
@@ -74,6 +75,7 @@ struct PrefillArgs {
   int64_t prefix_len;
   float qk_scale_log2;
   uint16_t* out;             // [C][Hq][128]
+  int* err;
 };
 
 cudaError_t launch_store_quant(const StoreArgs& a, cudaStream_t s);

@@ -1,6 +1,479 @@
-// prefill_tc.cu -- prefill attention on the tcgen05 tensor cores (placeholder until the kernel lands).
+// prefill_tc.cu -- prefill (extend) attention on the sm_100-family tensor cores (tcgen05 + TMA + TMEM).
+//
+// What it computes (FreeToken PR #853, "What changes"): chunk query t attends to every key of the
+// reconstructed BF16 prefix and to chunk keys 0..t; the current chunk's K/V stay BF16.
+//
+// One CTA = 128 query rows of one query head (grid: query tiles x heads, heaviest tiles first).
+// Key tiles of 128 keys come first from the prefix workspace, then from the chunk (causal tiles only).
+//   warp 0      : TMEM allocation; lane 0 issues TMA loads (Q once, then K/V tiles into a 2-stage ring)
+//   warp 1      : lane 0 issues tcgen05.mma: S_j = Q K_j^T into one of two TMEM S buffers, then
+//                 O += P_{j-1} V_{j-1} into the TMEM O accumulator (so QK of the next tile overlaps
+//                 the softmax of the current one)
+//   warps 2..5  : softmax, one query row per thread (= one TMEM lane): reads S_j from TMEM, keeps the
+//                 running max/sum in registers, writes P_j (BF16) to shared memory in the layout the
+//                 MMA reads, and rescales the O row in TMEM only when the running max grew by more than
+//                 8 (log2 units), so the O correction is rare
+// Operands: Q, K, P are K-major with the 128-byte swizzle; V is MN-major (keys x d, d contiguous) with
+// the 128-byte swizzle, read directly by the tensor core.  Every mbarrier wait is bounded in time; on
+// expiry the CTA records an error flag, drains its outstanding operations and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "ftkv_device.cuh"
 #include "ftkv_internal.h"
 
 namespace ftkv {
-cudaError_t launch_prefill_tc(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BM = 128;                    // query rows per CTA (MMA M)
+constexpr int BN = 128;                    // keys per tile (MMA N of QK, MMA K of PV)
+constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 BF16 (128 B)
+constexpr uint32_t TILE_BYTES = 2 * BOX_BYTES;  // 128 rows x 128 BF16
+// shared-memory layout (offsets from a 1024-byte aligned base)
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_KV = OFF_Q + TILE_BYTES;                 // stage s: K at +s*2*TILE, V at +TILE
+constexpr uint32_t OFF_P = OFF_KV + 2 * 2 * TILE_BYTES;         // P buffer b at +b*TILE
+constexpr uint32_t OFF_BAR = OFF_P + 2 * TILE_BYTES;
+constexpr int NBAR = 14;
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;              // TMEM base address, abort flag
+constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;              // slack for the 1024-byte alignment
+static_assert(SMEM_ALLOC <= 232448, "prefill_tc shared memory");
+
+// barrier indices
+constexpr int B_QFULL = 0, B_FULL0 = 1, B_EMPTY0 = 3, B_SFULL0 = 5, B_SFREE0 = 7, B_PFULL0 = 9, B_ODONE = 11,
+              B_OFINAL = 12, B_DRAIN = 13;
+
+constexpr uint32_t TMEM_COLS = 512;        // S0 [0,128) S1 [128,256) O [256,384)
+constexpr uint32_t TMEM_O = 256;
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;   // 4 s
+
+struct TcArgs {
+  int num_q_heads;
+  int group;
+  int chunk_len;
+  int prefix_len;
+  int n_q_tiles;
+  float qk_scale_log2;
+  uint16_t* out;
+  int* err;
+};
+
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Returns false (and raises the CTA abort flag and
+// the device error word) if it does not complete within WAIT_LIMIT_NS or another thread aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      flag_error(err, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: start, leading / stride byte offsets, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(2) << 61;  // swizzle: 128 bytes
+  return d;
+}
+
+// Instruction descriptor, kind::f16: FP32 accumulate, BF16 A and B, M = 128, N = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((128u >> 3) << 17) |
+         ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+      "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
+      "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// K-major SW128 tile of 128 rows x 128 BF16 (two 64-column boxes of 16 KB): descriptor of k-step kk
+// (16 columns) for the MMA.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+  return sw128_desc(tile + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+}
+// MN-major SW128 V tile (128 keys x 128 d, d contiguous; two 64-d boxes): k-step kk covers keys
+// 16kk..16kk+15 (two 8-row swizzle atoms); the two 64-d atoms are BOX_BYTES apart.
+__device__ __forceinline__ uint64_t vtile_desc(uint32_t tile, int kk) {
+  return sw128_desc(tile + kk * 2048, BOX_BYTES, 1024);
+}
+
+__global__ void __launch_bounds__(192, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkc,
+                      const __grid_constant__ CUtensorMap tvc, const __grid_constant__ CUtensorMap twk,
+                      const __grid_constant__ CUtensorMap twv, const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_MISC + 4);
+  const uint32_t tmem_holder = base + OFF_MISC;
+  auto bar = [&](int i) { return base + OFF_BAR + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = a.n_q_tiles - 1 - static_cast<int>(blockIdx.x);  // heaviest (latest) query tiles first
+  const int hq = blockIdx.y;
+  const int hk = hq / a.group;
+  const int t0 = qt * BM;
+  const int nPT = (a.prefix_len + BN - 1) / BN;
+  const int last_q = (t0 + BM - 1 < a.chunk_len - 1) ? t0 + BM - 1 : a.chunk_len - 1;
+  const int nCT = last_q / BN + 1;
+  const int T = nPT + nCT;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(bar(B_FULL0 + s), 1);
+      mbar_init(bar(B_EMPTY0 + s), 1);
+      mbar_init(bar(B_SFULL0 + s), 1);
+      mbar_init(bar(B_SFREE0 + s), 128);
+      mbar_init(bar(B_PFULL0 + s), 128);
+    }
+    mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_OFINAL), 1);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_holder),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + OFF_MISC);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      mbar_expect_tx(bar(B_QFULL), TILE_BYTES);
+      tma_load_3d(base + OFF_Q, &tq, bar(B_QFULL), 0, hq, t0);
+      tma_load_3d(base + OFF_Q + BOX_BYTES, &tq, bar(B_QFULL), 64, hq, t0);
+      int issued = 0;
+      for (int j = 0; j < T; j++) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(bar(B_EMPTY0 + s), ((j >> 1) - 1) & 1, abort_flag, a.err)) break;
+        const bool pre = j < nPT;
+        const CUtensorMap* mk = pre ? &twk : &tkc;
+        const CUtensorMap* mv = pre ? &twv : &tvc;
+        const int row = pre ? j * BN : (j - nPT) * BN;
+        const uint32_t dk = base + OFF_KV + s * 2 * TILE_BYTES, dv = dk + TILE_BYTES;
+        mbar_expect_tx(bar(B_FULL0 + s), 2 * TILE_BYTES);
+        tma_load_3d(dk, mk, bar(B_FULL0 + s), 0, hk, row);
+        tma_load_3d(dk + BOX_BYTES, mk, bar(B_FULL0 + s), 64, hk, row);
+        tma_load_3d(dv, mv, bar(B_FULL0 + s), 0, hk, row);
+        tma_load_3d(dv + BOX_BYTES, mv, bar(B_FULL0 + s), 64, hk, row);
+        issued = j + 1;
+      }
+      // drain: every issued load must land before the CTA may exit
+      mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
+      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; j++) mbar_wait(bar(B_FULL0 + (j & 1)), (j >> 1) & 1, abort_flag, a.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t IDESC_QK = idesc_bf16(false);
+      constexpr uint32_t IDESC_PV = idesc_bf16(true);
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
+      auto issue_pv = [&](int i) -> bool {
+        const int b = i & 1;
+        if (!mbar_wait(bar(B_PFULL0 + b), (i >> 1) & 1, abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t pt = base + OFF_P + b * TILE_BYTES;
+        const uint32_t vt = base + OFF_KV + (i & 1) * 2 * TILE_BYTES + TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++)
+          umma_bf16(tmem + TMEM_O, kmajor_desc(pt, kk), vtile_desc(vt, kk), IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_EMPTY0 + (i & 1)));
+        umma_commit(bar(B_ODONE));
+        return true;
+      };
+      for (int j = 0; ok && j < T; j++) {
+        const int s = j & 1;
+        if (!mbar_wait(bar(B_FULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+        if (j >= 2 && !mbar_wait(bar(B_SFREE0 + s), ((j >> 1) - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kt = base + OFF_KV + s * 2 * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++)
+          umma_bf16(tmem + s * 128, kmajor_desc(base + OFF_Q, kk), kmajor_desc(kt, kk), IDESC_QK, kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_SFULL0 + s));
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && issue_pv(T - 1)) umma_commit(bar(B_OFINAL));
+      // drain every MMA issued by this thread before TMEM is released
+      umma_commit(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0, abort_flag, a.err);
+    }
+  } else {
+    // ---------------- softmax: one query row per thread ----------------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int t = t0 + row;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float m_used = -INFINITY, lsum = 0.0f;
+    bool ok = true;
+    float s[BN];
+    for (int j = 0; j < T && ok; j++) {
+      const int b = j & 1;
+      // wait results are made warp-uniform before any warp-collective tcgen05 access
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL0 + b), (j >> 1) & 1, abort_flag, a.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; c++) tmem_ld32(lane_base + b * 128 + c * 32, s + c * 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_SFREE0 + b));
+
+      const bool pre = j < nPT;
+      const int kbase = pre ? j * BN : (j - nPT) * BN;
+      const int lim = pre ? a.prefix_len - kbase : (t + 1 - kbase);  // columns < lim are visible
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; c++) {
+        s[c] = (c < lim) ? s[c] * a.qk_scale_log2 : -INFINITY;
+        mt = fmaxf(mt, s[c]);
+      }
+      const float m_new = fmaxf(m_used, mt);
+      const bool need = (m_used != -INFINITY) && (m_new > m_used + 8.0f);
+      if (m_used == -INFINITY) m_used = m_new;
+      if (__any_sync(0xffffffffu, need)) {
+        const float f = need ? fast_exp2(m_used - m_new) : 1.0f;
+        if (need) {
+          lsum *= f;
+          m_used = m_new;
+        }
+        if (j >= 1) {  // O holds PV_0..PV_{j-1}: wait for the last of them, then scale the row in place
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (j - 1) & 1, abort_flag, a.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          float o[32];
+#pragma unroll
+          for (int c = 0; c < 4; c++) {
+            tmem_ld32(lane_base + TMEM_O + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; e++) o[e] *= f;
+            tmem_st32(lane_base + TMEM_O + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      const float sub = (m_used == -INFINITY) ? 0.0f : m_used;
+      // P row (BF16) into the K-major SW128 P buffer b
+      const uint32_t pt = base + OFF_P + b * TILE_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+      float ps = 0.0f;
+#pragma unroll
+      for (int k8 = 0; k8 < 16; k8++) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const float p0 = fast_exp2(s[k8 * 8 + 2 * e] - sub);
+          const float p1 = fast_exp2(s[k8 * 8 + 2 * e + 1] - sub);
+          ps += p0 + p1;
+          w[e] = float2_to_bf16x2(p0, p1);
+        }
+        const uint32_t addr = pt + (k8 >> 3) * BOX_BYTES + (((k8 & 7) ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                     "r"(w[3])
+                     : "memory");
+      }
+      lsum += ps;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL0 + b));
+    }
+    // ---- epilogue: O / l -> BF16 ----
+    if (__all_sync(0xffffffffu, ok && mbar_wait(bar(B_OFINAL), 0, abort_flag, a.err))) {
+      tc_fence_after();
+      const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+      uint16_t* dst = a.out + (static_cast<int64_t>(t) * a.num_q_heads + hq) * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        float o[32];
+        tmem_ld32(lane_base + TMEM_O + c * 32, o);
+        tmem_ld_wait();
+        if (t < a.chunk_len) {
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            uint4 v;
+            v.x = float2_to_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+            v.y = float2_to_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+            v.z = float2_to_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+            v.w = float2_to_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [rows][heads][128] BF16 as a 3-D tensor (d, head, row); box = 64 d x 1 head x 128 rows, 128-B swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int heads, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(heads) * 256};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  CUtensorMap tq, tkc, tvc, twk, twv;
+  if (!make_map(&tq, a.q, a.num_q_heads, a.chunk_len) || !make_map(&tkc, a.k_chunk, a.num_kv_heads, a.chunk_len) ||
+      !make_map(&tvc, a.v_chunk, a.num_kv_heads, a.chunk_len))
+    return cudaErrorInvalidValue;
+  if (a.prefix_len > 0) {
+    if (!make_map(&twk, a.ws_k, a.num_kv_heads, a.prefix_len) || !make_map(&twv, a.ws_v, a.num_kv_heads, a.prefix_len))
+      return cudaErrorInvalidValue;
+  } else {
+    twk = tkc;
+    twv = tvc;
+  }
+  TcArgs t{};
+  t.num_q_heads = a.num_q_heads;
+  t.group = a.num_q_heads / a.num_kv_heads;
+  t.chunk_len = static_cast<int>(a.chunk_len);
+  t.prefix_len = static_cast<int>(a.prefix_len);
+  t.n_q_tiles = static_cast<int>((a.chunk_len + BM - 1) / BM);
+  t.qk_scale_log2 = a.qk_scale_log2;
+  t.out = a.out;
+  t.err = a.err;
+  dim3 grid(t.n_q_tiles, a.num_q_heads);
+  prefill_tc_kernel<<<grid, 192, SMEM_ALLOC, s>>>(tq, tkc, tvc, twk, twv, t);
+  return cudaGetLastError();
+}
+
 }  // namespace ftkv

@@ -103,8 +103,10 @@ def reconstruct_bf16(pool: KVPool, slots: torch.Tensor, ws_k: torch.Tensor = Non
     return ws_k, ws_v
 
 
-def decode_workspace_bytes(num_q_heads: int, total_q_rows: int, num_splits: int) -> int:
-    return int(_lib.load().ftkv_decode_workspace_bytes(num_q_heads, HEAD_DIM, total_q_rows, num_splits))
+def decode_workspace_bytes(num_q_heads: int, num_kv_heads: int, batch: int, total_q_rows: int,
+                           num_splits: int) -> int:
+    return int(_lib.load().ftkv_decode_workspace_bytes(num_q_heads, num_kv_heads, HEAD_DIM, batch, total_q_rows,
+                                                       num_splits))
 
 
 def decode_auto_splits(batch: int, num_kv_heads: int, max_seq_len: int, max_q_rows: int = 1) -> int:
@@ -112,7 +114,8 @@ def decode_auto_splits(batch: int, num_kv_heads: int, max_seq_len: int, max_q_ro
 
 
 class DecodePlan:
-    """Host-side decode geometry + the workspace it needs (allocated once, reused by every call)."""
+    """Host-side decode geometry + the zero-filled workspace it needs (allocated once, reused by every call
+    on one stream; the kernels leave its arrival counters at zero)."""
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, batch: int, total_q_rows: int, max_q_rows: int,
                  max_seq_len: int, num_splits: int = 0, device="cuda"):
@@ -120,8 +123,8 @@ class DecodePlan:
         self.batch, self.total_q_rows, self.max_q_rows = batch, total_q_rows, max_q_rows
         self.max_seq_len = max_seq_len
         self.num_splits = num_splits or decode_auto_splits(batch, num_kv_heads, max_seq_len, max_q_rows)
-        nbytes = decode_workspace_bytes(num_q_heads, total_q_rows, self.num_splits)
-        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        nbytes = decode_workspace_bytes(num_q_heads, num_kv_heads, batch, total_q_rows, self.num_splits)
+        self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
 def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,

@@ -59,6 +59,8 @@ typedef enum {
 #define FTKV_DEVERR_SEQ_LEN 0x2     /* a seq_len was < 0 or > max_seq_len / req_stride; clamped        */
 #define FTKV_DEVERR_Q_ROWS 0x4      /* q_row_offsets inconsistent (rows > max_q_rows or past the end);
                                        that request was skipped                                       */
+#define FTKV_DEVERR_TIMEOUT 0x8     /* a bounded wait inside a kernel expired (internal error); the
+                                       affected outputs are unspecified                               */
 
 /* One layer's FP8 pool.  All four arrays are device memory owned by the caller.
  *   k_codes, v_codes : uint8 [num_rows][num_kv_heads][head_dim]   E4M3FN codes
@@ -96,9 +98,10 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
                           uint16_t* ws_k, uint16_t* ws_v, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
- * Split-K decode attention over the FP8 pool ([#897 "Fresh R9700 stage-1 A/B"]: a stage-1 kernel
- * over slices of the keys followed by a merge; [#897] opening description: BF16 query, D128,
- * GQA 4/8, per-row scales; multi-row decode of up to 8 query rows per request).
+ * Split-K decode attention over the FP8 pool ([#897 "Fresh R9700 stage-1 A/B"]: a stage over slices
+ * of the keys followed by a merge; [#897] opening description: BF16 query, D128, GQA 4/8, per-row
+ * scales; multi-row decode of up to 8 query rows per request).  One kernel launch: the last slice
+ * of each (request, KV head) to finish performs the merge.
  *
  *   q              : device BF16 [total_q_rows][num_q_heads][head_dim]
  *   req_to_slot    : device int32 [batch][req_stride]; key j of request b lives in pool row
@@ -114,12 +117,15 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
  *   sm_scale       : softmax scale (1/sqrt(head_dim) for the standard case)
  *   num_splits     : 0 = automatic (fills the SMs), else 1 .. FTKV_MAX_SPLITS key slices per request
  *   workspace      : device scratch of at least ftkv_decode_workspace_bytes(...) bytes, 256-byte
- *                    aligned; overwritten on every call; must not be shared by calls in flight
+ *                    aligned, ZERO-FILLED before its first use (e.g. cudaMemsetAsync).  It holds the
+ *                    per-slice partials and one arrival counter per (request, KV head); every call
+ *                    leaves the counters at zero again, so the zero fill is needed once.  Calls that
+ *                    share a workspace must not overlap on the GPU.
  *   out            : device BF16 [total_q_rows][num_q_heads][head_dim]
  * A query row that sees no key gets zeros.
  * --------------------------------------------------------------------------------------------- */
-size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t head_dim, int64_t total_q_rows,
-                                   int32_t num_splits);
+size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t batch, int64_t total_q_rows, int32_t num_splits);
 
 /* Number of key slices the automatic choice uses for this shape (what num_splits = 0 resolves to). */
 int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max_seq_len,

@@ -66,9 +66,9 @@ def _load():
         lib.ftkv_oracle_reconstruct.argtypes = [P, P, P, P, i64, i32, i32, P, i64, P, P]
         lib.ftkv_oracle_reconstruct.restype = i32
         lib.ftkv_oracle_decode_attn.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, i64, P, P, i32,
-                                                f64, P]
+                                                f64, i32, P]
         lib.ftkv_oracle_decode_attn.restype = i32
-        lib.ftkv_oracle_prefill_attn.argtypes = [i32, i32, i32, P, P, P, i64, P, P, i64, f64, P, i64, P]
+        lib.ftkv_oracle_prefill_attn.argtypes = [i32, i32, i32, P, P, P, i64, P, P, i64, f64, P, i64, i32, P]
         lib.ftkv_oracle_prefill_attn.restype = i32
         lib.ftkv_oracle_pool_bytes.argtypes = [i64, i64, i64, i64, P, P, P]
         lib.ftkv_oracle_set_threads.argtypes = [i32]
@@ -160,8 +160,10 @@ def reconstruct(pool: Pool, slots):
 
 
 def decode_attn(pool: Pool, q_bits, req_to_slot, seq_lens, q_row_offsets, sm_scale: float,
-                num_q_heads: int) -> np.ndarray:
-    """FP64 decode attention over the FP8 pool; returns float64 [total_rows, Hq, D]."""
+                num_q_heads: int, abs_v: bool = False) -> np.ndarray:
+    """FP64 decode attention over the FP8 pool; returns float64 [total_rows, Hq, D].
+
+    ``abs_v=True`` returns sum_j p_j |v_j| / sum_j p_j instead (a test helper that sizes rounding bounds)."""
     q = _c(q_bits, np.uint16)
     r2s = _c(req_to_slot, np.int32)
     if r2s.ndim == 1:
@@ -175,14 +177,14 @@ def decode_attn(pool: Pool, q_bits, req_to_slot, seq_lens, q_row_offsets, sm_sca
     rc = _load().ftkv_oracle_decode_attn(_ptr(pool.k_codes), _ptr(pool.v_codes), _ptr(pool.k_scales),
                                          _ptr(pool.v_scales), pool.num_rows, num_q_heads, pool.Hkv,
                                          pool.D, _ptr(q), _ptr(r2s), r2s.shape[1], _ptr(sl), _ptr(qo), B,
-                                         float(sm_scale), _ptr(out))
+                                         float(sm_scale), int(abs_v), _ptr(out))
     if rc != 0:
         raise ValueError("invalid decode arguments")
     return out
 
 
 def prefill_attn(q_bits, k_chunk_bits, v_chunk_bits, ws_k_bits, ws_v_bits, sm_scale: float,
-                 rows=None) -> np.ndarray:
+                 rows=None, abs_v: bool = False) -> np.ndarray:
     """FP64 causal prefill attention of chunk queries over prefix (+) chunk.
 
     Returns float64 [len(rows), Hq, D] (all C rows when ``rows`` is None)."""
@@ -204,7 +206,7 @@ def prefill_attn(q_bits, k_chunk_bits, v_chunk_bits, ws_k_bits, ws_v_bits, sm_sc
     rc = _load().ftkv_oracle_prefill_attn(Hq, Hkv, D, _ptr(q), _ptr(kc), _ptr(vc), C,
                                           _ptr(wk) if P else None, _ptr(wv) if P else None, P,
                                           float(sm_scale), _ptr(r) if r is not None else None, n,
-                                          _ptr(out))
+                                          int(abs_v), _ptr(out))
     if rc != 0:
         raise ValueError("invalid prefill arguments")
     return out

@@ -62,13 +62,16 @@ double ftkv_oracle_e4m3_decode(uint8_t c) {
   return s ? -mag : mag;
 }
 
-/* The 127 non-negative finite magnitudes, ascending: entry i is the value of code i. */
+/* The 127 non-negative finite magnitudes, ascending: entry i is the value of code i; and the value
+ * of every code (g_dec), both filled from the closed form above. */
 static double g_mag[127];
+static double g_dec[256];
 static int g_mag_ready = 0;
 
 static void init_mag_table(void) {
   if (g_mag_ready) return;
   for (int i = 0; i < 127; i++) g_mag[i] = ftkv_oracle_e4m3_decode((uint8_t)i);
+  for (int i = 0; i < 256; i++) g_dec[i] = ftkv_oracle_e4m3_decode((uint8_t)i);
   g_mag_ready = 1;
 }
 
@@ -181,6 +184,7 @@ int ftkv_oracle_store_quant(const uint16_t* k, const uint16_t* v, const int32_t*
 int ftkv_oracle_reconstruct(const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scales,
                             const float* v_scales, int64_t num_rows, int Hkv, int D,
                             const int32_t* slots, int64_t P, uint16_t* ws_k, uint16_t* ws_v) {
+  init_mag_table();
   for (int64_t i = 0; i < P; i++)
     if (slots[i] < 0 || slots[i] >= num_rows) return -1;
 #pragma omp parallel for schedule(static)
@@ -189,8 +193,8 @@ int ftkv_oracle_reconstruct(const uint8_t* k_codes, const uint8_t* v_codes, cons
     for (int h = 0; h < Hkv; h++) {
       float sk = k_scales[row * Hkv + h], sv = v_scales[row * Hkv + h];
       for (int d = 0; d < D; d++) {
-        float pk = (float)ftkv_oracle_e4m3_decode(k_codes[(row * Hkv + h) * D + d]) * sk;
-        float pv = (float)ftkv_oracle_e4m3_decode(v_codes[(row * Hkv + h) * D + d]) * sv;
+        float pk = (float)g_dec[k_codes[(row * Hkv + h) * D + d]] * sk;
+        float pv = (float)g_dec[v_codes[(row * Hkv + h) * D + d]] * sv;
         ws_k[(i * Hkv + h) * D + d] = f32_to_bf16_rne(pk);
         ws_v[(i * Hkv + h) * D + d] = f32_to_bf16_rne(pv);
       }
@@ -216,7 +220,7 @@ static void pool_row(const pool_ctx* c, int64_t j, double* out) {
   int64_t row = c->slot_of[j];
   const uint8_t* code = c->codes + (row * c->Hkv + c->h) * c->D;
   double s = (double)c->scales[row * c->Hkv + c->h];
-  for (int d = 0; d < c->D; d++) out[d] = ftkv_oracle_e4m3_decode(code[d]) * s; /* exact in double */
+  for (int d = 0; d < c->D; d++) out[d] = g_dec[code[d]] * s; /* exact in double */
 }
 
 /* Decode attention over the FP8 pool.
@@ -225,6 +229,8 @@ static void pool_row(const pool_ctx* c, int64_t j, double* out) {
  *   seq_lens:     int32 [B]; request b has seq_lens[b] keys (the new rows included)
  *   q_row_offsets int32 [B+1]; request b owns query rows [q_row_offsets[b], q_row_offsets[b+1])
  *   out:          double [total_rows][Hq][D]
+ *   abs_v:        if nonzero, accumulate |v^| instead of v^ (the attention-weighted magnitude of the
+ *                 summed terms, used by the tests to size the rounding bound; not part of the method)
  * [#897 "Fresh R9700 stage-1 A/B"]: the reference is CPU FP8 dequantization followed by attention;
  * split-K is an evaluation order and does not appear here.  Multi-row decode (up to 8 rows per
  * request, [#897 opening description]) is causal within the rows; reading: row r of R rows sees
@@ -233,7 +239,8 @@ int ftkv_oracle_decode_attn(const uint8_t* k_codes, const uint8_t* v_codes, cons
                             const float* v_scales, int64_t num_rows, int Hq, int Hkv, int D,
                             const uint16_t* q, const int32_t* req_to_slot, int64_t req_stride,
                             const int32_t* seq_lens, const int32_t* q_row_offsets, int B,
-                            double sm_scale, double* out) {
+                            double sm_scale, int abs_v, double* out) {
+  init_mag_table();
   if (Hkv <= 0 || Hq % Hkv != 0) return -1;
   int G = Hq / Hkv;
   int64_t max_n = 0;
@@ -281,7 +288,7 @@ int ftkv_oracle_decode_attn(const uint8_t* k_codes, const uint8_t* v_codes, cons
           double p = exp(s[j] - m);
           l += p;
           pool_row(&vc, j, kv);
-          for (int d = 0; d < D; d++) o[d] += p * kv[d];
+          for (int d = 0; d < D; d++) o[d] += p * (abs_v ? fabs(kv[d]) : kv[d]);
         }
         for (int d = 0; d < D; d++) o[d] /= l;
       }
@@ -312,12 +319,13 @@ static void cat_row(const cat_ctx* c, int64_t j, double* out) {
  *   q, k_chunk, v_chunk: BF16 [C][Hq|Hkv][D];  ws_k, ws_v: BF16 [P][Hkv][D] (reconstructed prefix)
  *   rows: the chunk query indices to evaluate (n_rows of them; NULL = all C rows in order)
  *   out:  double [n_rows][Hq][D]
+ *   abs_v: if nonzero, accumulate |v| instead of v (test helper, as for decode)
  * [#853 "What changes"]: keys/values are the rebuilt BF16 prefix followed by the BF16 current
  * chunk; chunk query t sees the whole prefix and chunk keys 0..t (causal). */
 int ftkv_oracle_prefill_attn(int Hq, int Hkv, int D, const uint16_t* q, const uint16_t* k_chunk,
                              const uint16_t* v_chunk, int64_t C, const uint16_t* ws_k,
                              const uint16_t* ws_v, int64_t P, double sm_scale, const int64_t* rows,
-                             int64_t n_rows, double* out) {
+                             int64_t n_rows, int abs_v, double* out) {
   if (Hkv <= 0 || Hq % Hkv != 0) return -1;
   int G = Hq / Hkv;
   if (rows)
@@ -353,7 +361,7 @@ int ftkv_oracle_prefill_attn(int Hq, int Hkv, int D, const uint16_t* q, const ui
         double p = exp(s[j] - m);
         l += p;
         cat_row(&vc, j, kv);
-        for (int d = 0; d < D; d++) o[d] += p * kv[d];
+        for (int d = 0; d < D; d++) o[d] += p * (abs_v ? fabs(kv[d]) : kv[d]);
       }
       for (int d = 0; d < D; d++) o[d] /= l;
     }

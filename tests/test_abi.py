@@ -1,0 +1,124 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function include/ftkv.h declares, and
+rejects bad arguments on the host (nothing is enqueued, no device memory is touched).
+
+Fake device pointers below are never dereferenced: every call returns during host validation.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from fp8_kv_cache_ftkv_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ftkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ftkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (ftkv_[a-z0-9_]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.ftkv_abi_version() == 1
+    for code, name in [(0, "FTKV_OK"), (-1, "FTKV_ERR_INVALID"), (-2, "FTKV_ERR_UNSUPPORTED"), (-3, "FTKV_ERR_ALIGN"),
+                       (-4, "FTKV_ERR_WORKSPACE"), (-6, "FTKV_ERR_CUDA"), (-99, "FTKV_ERR_UNKNOWN")]:
+        assert _lib.status_str(code) == name
+
+
+def test_pool_bytes_matches_printed_accounting(lib):
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    assert lib.ftkv_pool_bytes(33059, 48, 4, 128, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)) == 0
+    assert (a.value, b.value, c.value) == (3_249_831_936, 1_675_694_592, 67_704_832)
+    assert lib.ftkv_pool_bytes(-1, 48, 4, 128, None, None, None) == _lib.FTKV_ERR_INVALID
+
+
+def _pool(k=0x10000, v=0x20000, ks=0x30000, vs=0x40000, rows=100, hkv=4, d=128):
+    return _lib.FtkvPool(k, v, ks, vs, rows, hkv, d)
+
+
+def test_store_validation(lib):
+    P = ctypes.byref
+    assert lib.ftkv_store_quant(None, None, None, None, 1, None) == _lib.FTKV_ERR_INVALID
+    assert lib.ftkv_store_quant(P(_pool(d=64)), 0x1000, 0x2000, 0x3000, 1, None) == _lib.FTKV_ERR_UNSUPPORTED
+    assert lib.ftkv_store_quant(P(_pool(k=0x10001)), 0x1000, 0x2000, 0x3000, 1, None) == _lib.FTKV_ERR_ALIGN
+    assert lib.ftkv_store_quant(P(_pool()), 0x1008, 0x2000, 0x3000, 1, None) == _lib.FTKV_ERR_ALIGN
+    assert lib.ftkv_store_quant(P(_pool()), 0x1000, 0x2000, 0x3000, -1, None) == _lib.FTKV_ERR_INVALID
+    assert lib.ftkv_store_quant(P(_pool()), None, 0x2000, 0x3000, 1, None) == _lib.FTKV_ERR_INVALID
+    assert lib.ftkv_store_quant(P(_pool()), None, None, None, 0, None) == _lib.FTKV_OK  # empty: no-op
+    assert lib.ftkv_store_quant(P(_pool(rows=0)), 0x1000, 0x2000, 0x3000, 1, None) == _lib.FTKV_ERR_INVALID
+
+
+def test_reconstruct_validation(lib):
+    P = ctypes.byref
+    assert lib.ftkv_reconstruct_bf16(P(_pool()), 0x3000, 5, 0x5008, 0x6000, None) == _lib.FTKV_ERR_ALIGN
+    assert lib.ftkv_reconstruct_bf16(P(_pool()), None, 5, 0x5000, 0x6000, None) == _lib.FTKV_ERR_INVALID
+    assert lib.ftkv_reconstruct_bf16(P(_pool()), None, 0, None, None, None) == _lib.FTKV_OK
+
+
+def test_decode_validation(lib):
+    P = ctypes.byref
+    ws = lib.ftkv_decode_workspace_bytes(32, 4, 128, 1, 1, 4)
+    assert ws > 0 and ws % 256 == 0
+    assert lib.ftkv_decode_workspace_bytes(32, 4, 64, 1, 1, 8) == 0
+    base = dict(q=0x1000, r2s=0x2000, stride=64, lens=0x3000, offs=None, B=1, total=1, mq=1, maxlen=64,
+                sm=0.0884, splits=4, ws=0x100000, wsb=ws, out=0x4000)
+
+    def call(pool=None, hq=32, **kw):
+        a = dict(base, **kw)
+        return lib.ftkv_decode_attn(P(pool or _pool()), hq, a["q"], a["r2s"], a["stride"], a["lens"], a["offs"],
+                                    a["B"], a["total"], a["mq"], a["maxlen"], a["sm"], a["splits"], a["ws"],
+                                    a["wsb"], a["out"], None)
+
+    assert call(hq=24) == _lib.FTKV_ERR_UNSUPPORTED          # group 6
+    assert call(hq=30) == _lib.FTKV_ERR_UNSUPPORTED          # not a multiple of Hkv
+    assert call(hq=64, pool=_pool(hkv=4)) == _lib.FTKV_ERR_UNSUPPORTED  # group 16
+    assert call(mq=9) == _lib.FTKV_ERR_UNSUPPORTED
+    assert call(splits=65) == _lib.FTKV_ERR_INVALID
+    assert call(maxlen=65) == _lib.FTKV_ERR_INVALID          # above req_stride
+    assert call(total=2) == _lib.FTKV_ERR_INVALID            # no offsets: one row per request
+    assert call(q=0x1002) == _lib.FTKV_ERR_ALIGN
+    assert call(ws=0x100010) == _lib.FTKV_ERR_ALIGN          # workspace must be 256-B aligned
+    assert call(wsb=ws - 1) == _lib.FTKV_ERR_WORKSPACE
+    assert call(sm=float("nan")) == _lib.FTKV_ERR_INVALID
+    assert call(B=0, total=0) == _lib.FTKV_OK                # nothing to do
+
+
+def test_prefill_validation(lib):
+    for fn in (lib.ftkv_prefill_attn, lib.ftkv_prefill_attn_mma):
+        assert fn(32, 4, 64, 0x1000, 0x2000, 0x3000, 16, 0x4000, 0x5000, 16, 0.08, 0x6000, None) == \
+            _lib.FTKV_ERR_UNSUPPORTED
+        assert fn(32, 5, 128, 0x1000, 0x2000, 0x3000, 16, 0x4000, 0x5000, 16, 0.08, 0x6000, None) == \
+            _lib.FTKV_ERR_UNSUPPORTED
+        assert fn(32, 4, 128, 0x1000, 0x2000, 0x3000, 16, None, None, 16, 0.08, 0x6000, None) == \
+            _lib.FTKV_ERR_INVALID
+        assert fn(32, 4, 128, 0x1004, 0x2000, 0x3000, 16, 0x4000, 0x5000, 16, 0.08, 0x6000, None) == \
+            _lib.FTKV_ERR_ALIGN
+        assert fn(32, 4, 128, None, None, None, 0, None, None, 0, 0.08, None, None) == _lib.FTKV_OK
+
+
+def test_codec_validation(lib):
+    assert lib.ftkv_e4m3_encode_f32(None, None, 0, None) == _lib.FTKV_OK
+    assert lib.ftkv_e4m3_encode_f32(None, 0x1000, 4, None) == _lib.FTKV_ERR_INVALID
+    assert lib.ftkv_e4m3_decode_f32(0x1000, 0x2002, 4, None) == _lib.FTKV_ERR_ALIGN

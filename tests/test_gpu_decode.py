@@ -38,14 +38,19 @@ def _run(wl, gp, dev, num_splits=0, max_q_rows=None):
 
 
 def _ref(wl, op, L):
-    return oracle.decode_attn(op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets, wl.sm_scale, wl.Hq)
+    args = (op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets, wl.sm_scale, wl.Hq)
+    return oracle.decode_attn(*args), oracle.decode_attn(*args, abs_v=True)
+
+
+def _check(out, refs, what):
+    return check_attention(out, refs[0], what, refs[1])
 
 
 def test_decode_small_step():
     wl = inputs.decode_small()
     gp, op, L, dev = _setup(wl)
     out = _run(wl, gp, dev)
-    stats = check_attention(out, _ref(wl, op, L), "decode_small")
+    stats = _check(out, _ref(wl, op, L), "decode_small")
     assert stats["max_abs"] < 0.05
     assert ops.device_errors() == 0
 
@@ -56,7 +61,7 @@ def test_decode_ragged_lengths_and_split_caps(n, splits):
     wl = inputs.decode_custom([n], [1], max(2 * n, 64), seed=n)
     gp, op, L, dev = _setup(wl)
     out = _run(wl, gp, dev, num_splits=splits)
-    check_attention(out, _ref(wl, op, L), f"n={n} splits={splits}")
+    _check(out, _ref(wl, op, L), f"n={n} splits={splits}")
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(32, 4), (16, 4), (8, 4), (4, 4), (64, 8)])
@@ -64,7 +69,7 @@ def test_decode_gqa_groups(Hq, Hkv):
     wl = inputs.decode_custom([300, 1000], [1, 1], 4000, seed=Hq, Hq=Hq, Hkv=Hkv)
     gp, op, L, dev = _setup(wl)
     out = _run(wl, gp, dev)
-    check_attention(out, _ref(wl, op, L), f"Hq={Hq} Hkv={Hkv}")
+    _check(out, _ref(wl, op, L), f"Hq={Hq} Hkv={Hkv}")
 
 
 @pytest.mark.parametrize("rows", [[2], [3, 1, 8], [8, 8], [5, 7, 6, 4]])
@@ -74,16 +79,16 @@ def test_decode_multirow(rows):
     gp, op, L, dev = _setup(wl)
     for splits in (0, 1, 5):
         out = _run(wl, gp, dev, num_splits=splits)
-        check_attention(out, _ref(wl, op, L), f"rows={rows} splits={splits}")
+        _check(out, _ref(wl, op, L), f"rows={rows} splits={splits}")
 
 
 def test_decode_rows_that_see_no_key_are_zero():
     wl = inputs.decode_custom([2, 40], [5, 3], 100, seed=3)
     gp, op, L, dev = _setup(wl)
     out = _run(wl, gp, dev)
-    ref = _ref(wl, op, L)
-    assert (ref[:3] == 0).all()
-    check_attention(out, ref, "empty rows")
+    refs = _ref(wl, op, L)
+    assert (refs[0][:3] == 0).all()
+    _check(out, refs, "empty rows")
     assert (out[:3].float() == 0).all()
 
 
@@ -91,7 +96,7 @@ def test_decode_zero_length_request_and_single_row_path_with_offsets():
     wl = inputs.decode_custom([0, 33, 1], [1, 1, 1], 64, seed=4)
     gp, op, L, dev = _setup(wl)
     out = _run(wl, gp, dev)
-    check_attention(out, _ref(wl, op, L), "zero-length request")
+    _check(out, _ref(wl, op, L), "zero-length request")
     assert (out[0].float() == 0).all()
 
 
@@ -101,7 +106,7 @@ def test_decode_long_context_full_size(n, R):
     for layer in (0, 47):
         gp, op, L, dev = _setup(wl, layer)
         out = _run(wl, gp, dev)
-        stats = check_attention(out, _ref(wl, op, L), f"n={n} layer={layer}")
+        stats = _check(out, _ref(wl, op, L), f"n={n} layer={layer}")
         assert stats["rel_l2"] < 2e-3
     assert ops.device_errors() == 0
 
@@ -114,9 +119,9 @@ def test_decode_batched_multirow_full_size():
     rng = np.random.default_rng(0)
     for b in sorted(rng.choice(len(wl.seq_lens), size=12, replace=False)):
         o0, o1 = int(wl.q_row_offsets[b]), int(wl.q_row_offsets[b + 1])
-        ref = oracle.decode_attn(op, L.q[o0:o1], wl.req_to_slot[b:b + 1], wl.seq_lens[b:b + 1],
-                                 np.array([0, o1 - o0], np.int32), wl.sm_scale, wl.Hq)
-        check_attention(out[o0:o1], ref, f"request {b}")
+        args = (op, L.q[o0:o1], wl.req_to_slot[b:b + 1], wl.seq_lens[b:b + 1],
+                np.array([0, o1 - o0], np.int32), wl.sm_scale, wl.Hq)
+        check_attention(out[o0:o1], oracle.decode_attn(*args), f"request {b}", oracle.decode_attn(*args, abs_v=True))
     assert ops.device_errors() == 0
 
 

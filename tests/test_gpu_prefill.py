@@ -15,7 +15,7 @@ from parity import bits_to_cuda_bf16, check_attention
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["mma"]
+IMPLS = ["mma", "tc"]
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -26,9 +26,10 @@ def test_prefill_small(impl, P, C):
     kc, vc = inputs.kv_tokens(rng, C, 1.0)
     q = inputs.queries(rng, C)
     ref = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE)
+    mag = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE, abs_v=True)
     out = ops.prefill_attn(bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
                            bits_to_cuda_bf16(wk) if P else None, bits_to_cuda_bf16(wv) if P else None, impl=impl)
-    check_attention(out, ref, f"{impl} P={P} C={C}")
+    check_attention(out, ref, f"{impl} P={P} C={C}", mag)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -40,9 +41,10 @@ def test_prefill_gqa(impl, Hq, Hkv):
     kc, vc = inputs.kv_tokens(rng, C, 1.0, Hkv=Hkv)
     q = inputs.queries(rng, C, Hq)
     ref = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE)
+    mag = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE, abs_v=True)
     out = ops.prefill_attn(bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
                            bits_to_cuda_bf16(wk), bits_to_cuda_bf16(wv), impl=impl)
-    check_attention(out, ref, f"{impl} Hq={Hq} Hkv={Hkv}")
+    check_attention(out, ref, f"{impl} Hq={Hq} Hkv={Hkv}", mag)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -68,6 +70,7 @@ def test_chunked_prefill_full_workload(impl):
         owk, owv = oracle.reconstruct(op, slots_all[:P])
         rows = np.arange(0, c1 - c0, 16, dtype=np.int64)
         ref = oracle.prefill_attn(wl.q[c0:c1], wl.k[c0:c1], wl.v[c0:c1], owk, owv, wl.sm_scale, rows)
+        mag = oracle.prefill_attn(wl.q[c0:c1], wl.k[c0:c1], wl.v[c0:c1], owk, owv, wl.sm_scale, rows, abs_v=True)
         oracle.store_quant(op, wl.k[c0:c1], wl.v[c0:c1], slots_all[P:P + c1 - c0])
-        check_attention(out[torch.from_numpy(rows).cuda()], ref, f"{impl} chunk {c}")
+        check_attention(out[torch.from_numpy(rows).cuda()], ref, f"{impl} chunk {c}", mag)
     assert ops.device_errors() == 0

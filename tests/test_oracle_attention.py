@@ -173,3 +173,23 @@ def test_prefill_empty_prefix_is_causal_attention():
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
     # first chunk row sees only itself
     np.testing.assert_array_equal(got[0], np.repeat(inputs.bf16_bits_to_f32(vc[0]).astype(np.float64), 8, 0))
+
+
+def test_abs_mode_is_attention_over_absolute_values():
+    """The test helper mode (sum p |v| / sum p) equals torch SDPA with |v| as values."""
+    rng = np.random.default_rng(28)
+    R, n = 80, 50
+    pool, slots = _pool_from(rng, R, n)
+    q = inputs.queries(rng, 1)
+    got = oracle.decode_attn(pool, q, slots[None], [n], [0, 1], SM, 32, abs_v=True)[0]
+    kd = _torch_deq(pool.k_codes[slots], pool.k_scales[slots]).permute(1, 0, 2)
+    vd = _torch_deq(pool.v_codes[slots], pool.v_scales[slots]).permute(1, 0, 2).abs()
+    qd = torch.from_numpy(inputs.bf16_bits_to_f32(q[0])).to(torch.float64)[:, None, :]
+    np.testing.assert_allclose(got, _sdpa(qd, kd, vd)[:, 0, :].numpy(), rtol=1e-12, atol=1e-12)
+    P, C = 20, 15
+    wk, wv = inputs.kv_tokens(rng, P, 1.0)
+    kc, vc = inputs.kv_tokens(rng, C, 1.0)
+    q = inputs.queries(rng, C)
+    absd = lambda b: inputs.to_bf16_bits(np.abs(inputs.bf16_bits_to_f32(b)))
+    np.testing.assert_array_equal(oracle.prefill_attn(q, kc, vc, wk, wv, SM, abs_v=True),
+                                  oracle.prefill_attn(q, kc, absd(vc), wk, absd(wv), SM))
