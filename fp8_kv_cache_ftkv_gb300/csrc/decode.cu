@@ -20,9 +20,12 @@
 //    within 13 binades of the head's largest one is represented without error.  The two partial dot
 //    products are recombined in FP32 with the per-key K scale.
 //  * PV runs on FP16 tensor cores (m16n8k16): V codes are converted exactly with the packed
-//    hardware converter; the V scale is folded into the probabilities.  P' = p * scaleV * 2^-E stays
-//    in FP16 range by tracking the running maximum binary exponent E of the V scales and rescaling
-//    the accumulator when it grows (exact power-of-two bookkeeping next to the usual running max).
+//    hardware converter and the V scale is folded into the probabilities.  FP16 has a narrow exponent
+//    range and the per-row V scales of a slice can span 2^30, so each 16-key block is scaled by its own
+//    maximum W of the value-weighted probabilities w_j = 2^(s_j - m) * scaleV_j (FP32 products, no
+//    logarithms: an added log2(scale) would be rounded to the ulp of a large logit).  With 2^E the power
+//    of two of W, P'_j = w_j * 2^-E < 2 goes through the MMA into a zeroed register tile, which is added
+//    to the FP32 accumulator with the exact factor 2^E.  Only the range within one block fits FP16.
 //  * The 8 query heads of a GQA group are the MMA N dimension, so G = 8 wastes nothing.
 #include <cfloat>
 
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   }
 
   float acc[RPW][8][4];
-  float m[RPW][2], l[RPW][2];
+  float m[RPW][2], l[RPW][2];  // running max of s (log2 units) and running sum of 2^(s - m)
 #pragma unroll
   for (int i = 0; i < RPW; i++) {
 #pragma unroll
@@ -214,7 +217,6 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     m[i][0] = m[i][1] = -INFINITY;
     l[i][0] = l[i][1] = 0.0f;
   }
-  int bexp = 0;  // running max of the biased FP32 exponent of the V scales seen by this warp
 
   const uint32_t ring = smem_addr(smem) + warp * NSTAGE * STAGE_BYTES;
   const int64_t hkv = a.num_kv_heads;
@@ -299,24 +301,15 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
           for (int p = 0; p < 2; p++) mma_e4m3_16832(c[r][p], a0, a1, a2, a3, qp[r][p][kk][0], qp[r][p][kk][1]);
       }
 
-      // ---- per-key scales; V exponent bookkeeping ----
+      // ---- per-key scales ----
       const uint32_t ss = st + STAGE_K + STAGE_V;
       const float skg = ld_shared_f32(ss + g * 4), skg8 = ld_shared_f32(ss + (g + 8) * 4);
       const float svg = ld_shared_f32(ss + 64 + g * 4), svg8 = ld_shared_f32(ss + 64 + (g + 8) * 4);
-      int be = static_cast<int>(max(__float_as_uint(svg) >> 23, __float_as_uint(svg8) >> 23));
-      be = max(be, __shfl_xor_sync(0xffffffffu, be, 4));
-      be = max(be, __shfl_xor_sync(0xffffffffu, be, 8));
-      be = max(be, __shfl_xor_sync(0xffffffffu, be, 16));
-      be = min(be, 253);
-      const int bnew = max(bexp, be);
-      const float inv = __uint_as_float(static_cast<uint32_t>(254 - bnew) << 23);  // 2^(127-bnew)
-      const float sv0 = svg * inv, sv8 = svg8 * inv;
-      const float shift = (bnew != bexp) ? fast_exp2(static_cast<float>(bexp - bnew)) : 1.0f;
-      bexp = bnew;
 
       // ---- online softmax (log2 domain), P' = p * scaleV * 2^-E into B fragments of PV ----
       const int jg = jb + g, jg8 = jb + g + 8;
       uint32_t pb0[RPW], pb1[RPW];
+      float fb[RPW][2];  // FP32 factor that brings the block's PV tile to the accumulator's scale 2^m
 #pragma unroll
       for (int r = 0; r < RPW; r++) {
         const int lr = lim[r] < je ? lim[r] : je;
@@ -343,7 +336,22 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
         l[r][1] = l[r][1] * al1 + (p1 + p3);
         m[r][0] = mn0;
         m[r][1] = mn1;
-        const float ac0 = al0 * shift, ac1 = al1 * shift;
+        // value-weighted probabilities and their block maximum per head
+        const float w0 = p0 * svg, w1 = p1 * svg, w2 = p2 * svg8, w3 = p3 * svg8;
+        float W0 = fmaxf(w0, w2), W1 = fmaxf(w1, w3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          W0 = fmaxf(W0, __shfl_xor_sync(0xffffffffu, W0, off));
+          W1 = fmaxf(W1, __shfl_xor_sync(0xffffffffu, W1, off));
+        }
+        // normalize by the power of two of W (exact, no overflow for tiny or subnormal W): P' in [0, 2)
+        const int e0 = min(max(static_cast<int>(__float_as_uint(W0) >> 23), 1), 253);
+        const int e1 = min(max(static_cast<int>(__float_as_uint(W1) >> 23), 1), 253);
+        fb[r][0] = __uint_as_float(static_cast<uint32_t>(e0) << 23);         // 2^(e0-127)
+        fb[r][1] = __uint_as_float(static_cast<uint32_t>(e1) << 23);
+        const float iw0 = __uint_as_float(static_cast<uint32_t>(254 - e0) << 23);  // 2^(127-e0)
+        const float iw1 = __uint_as_float(static_cast<uint32_t>(254 - e1) << 23);
+        const float ac0 = al0, ac1 = al1;
         if (__any_sync(0xffffffffu, ac0 != 1.0f || ac1 != 1.0f)) {
 #pragma unroll
           for (int mt = 0; mt < 8; mt++) {
@@ -353,8 +361,8 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
             acc[r][mt][3] *= ac1;
           }
         }
-        pb0[r] = movmatrix_trans(float2_to_f16x2(p0 * sv0, p1 * sv0));   // keys 0..7
-        pb1[r] = movmatrix_trans(float2_to_f16x2(p2 * sv8, p3 * sv8));   // keys 8..15
+        pb0[r] = movmatrix_trans(float2_to_f16x2(w0 * iw0, w1 * iw1));   // keys 0..7
+        pb1[r] = movmatrix_trans(float2_to_f16x2(w2 * iw0, w3 * iw1));   // keys 8..15
       }
 
       // ---- O^T += V^T P'^T : d as M (d = 16g + 2mt [+1]), heads as N, keys as K ----
@@ -371,13 +379,23 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
           const uint32_t a0 = e4m3_lo2(lo01), a1 = e4m3_hi2(lo01);
           const uint32_t a2 = e4m3_lo2(lo89), a3 = e4m3_hi2(lo89);
 #pragma unroll
-          for (int r = 0; r < RPW; r++) mma_f16_16816(acc[r][2 * w], a0, a1, a2, a3, pb0[r], pb1[r]);
+          for (int r = 0; r < RPW; r++) {
+            float tile[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            mma_f16_16816(tile, a0, a1, a2, a3, pb0[r], pb1[r]);
+#pragma unroll
+            for (int e = 0; e < 4; e++) acc[r][2 * w][e] = fmaf(tile[e], fb[r][e & 1], acc[r][2 * w][e]);
+          }
         }
         {
           const uint32_t a0 = e4m3_lo2(hi01), a1 = e4m3_hi2(hi01);
           const uint32_t a2 = e4m3_lo2(hi89), a3 = e4m3_hi2(hi89);
 #pragma unroll
-          for (int r = 0; r < RPW; r++) mma_f16_16816(acc[r][2 * w + 1], a0, a1, a2, a3, pb0[r], pb1[r]);
+          for (int r = 0; r < RPW; r++) {
+            float tile[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            mma_f16_16816(tile, a0, a1, a2, a3, pb0[r], pb1[r]);
+#pragma unroll
+            for (int e = 0; e < 4; e++) acc[r][2 * w + 1][e] = fmaf(tile[e], fb[r][e & 1], acc[r][2 * w + 1][e]);
+          }
         }
       }
       __syncwarp();
@@ -385,14 +403,13 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     cp_async_wait<0>();
   }
 
-  // ---- finalize this warp: full row sums, true numerator scale 2^(E-127) ----
+  // ---- finalize this warp: full row sums (the accumulator is already relative to 2^m) ----
 #pragma unroll
   for (int r = 0; r < RPW; r++)
 #pragma unroll
     for (int hh = 0; hh < 2; hh++)
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) l[r][hh] += __shfl_xor_sync(0xffffffffu, l[r][hh], off);
-  const float post = exp2f(static_cast<float>(bexp - 127));
 
   __syncthreads();  // the rings are free: reuse them as the merge area
   float* merge = reinterpret_cast<float*>(smem);
@@ -407,8 +424,8 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
         // head 2t+hh: d = 16g + 2mt -> acc[mt][hh], d = 16g + 2mt + 1 -> acc[mt][2+hh]
 #pragma unroll
         for (int q4 = 0; q4 < 4; q4++)
-          d4[q4] = make_float4(acc[r][2 * q4][hh] * post, acc[r][2 * q4][2 + hh] * post,
-                               acc[r][2 * q4 + 1][hh] * post, acc[r][2 * q4 + 1][2 + hh] * post);
+          d4[q4] = make_float4(acc[r][2 * q4][hh], acc[r][2 * q4][2 + hh], acc[r][2 * q4 + 1][hh],
+                               acc[r][2 * q4 + 1][2 + hh]);
         if (g == 0) {
           dst[128] = m[r][hh];
           dst[129] = l[r][hh];

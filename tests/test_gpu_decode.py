@@ -136,3 +136,64 @@ def test_decode_bad_slot_and_seq_len_are_flagged_not_faulted():
     ops.decode_attn(gp, dev["q"], dev["r2s"], lens, dev["offs"], max_seq_len=50, max_q_rows=1)
     assert ops.device_errors() & 0x2
     assert ops.device_errors() == 0
+
+
+@pytest.mark.parametrize("max_q_rows", [1, 2])
+def test_decode_dominant_key_with_small_v_scale(max_q_rows):
+    """A key holding almost all the probability has a V scale 1e6 x smaller than a key with tiny
+    probability; both terms matter (ratio ~0.1) and the dominant one must keep full precision."""
+    rng = np.random.default_rng(31)
+    n, R = 48, 64
+    k = np.zeros((n, 4, 128), np.float32)
+    v = rng.standard_normal((n, 4, 128)).astype(np.float32)
+    k[:, :, 0] = rng.standard_normal((n, 4)).astype(np.float32)
+    k[7, :, 0] = 181.0          # dominant logit: s = 181 * 0.0884 = 16 above the rest
+    v[7] *= 1.0                 # V scale ~ 1/448 * 3
+    v[23] *= 1.0e6              # e^-16 * 1e6 ~ 0.1 relative contribution
+    q = np.zeros((max_q_rows, 32, 128), np.float32)
+    q[:, :, 0] = 1.0
+    kb, vb, qb = inputs.to_bf16_bits(k), inputs.to_bf16_bits(v), inputs.to_bf16_bits(q)
+    slots = rng.permutation(R)[:n].astype(np.int32)
+    gp = ops.KVPool.empty(R, 4)
+    ops.store_quant(gp, bits_to_cuda_bf16(kb), bits_to_cuda_bf16(vb), torch.from_numpy(slots).cuda())
+    op = oracle.Pool(R, 4, 128)
+    oracle.store_quant(op, kb, vb, slots)
+    offs = np.array([0, max_q_rows], np.int32)
+    lens = np.array([n], np.int32)
+    out = ops.decode_attn(gp, bits_to_cuda_bf16(qb), torch.from_numpy(slots[None]).cuda(),
+                          torch.from_numpy(lens).cuda(), torch.from_numpy(offs).cuda(), max_seq_len=n,
+                          max_q_rows=max_q_rows)
+    args = (op, qb, slots[None], lens, offs, inputs.SM_SCALE, 32)
+    ref, mag = oracle.decode_attn(*args), oracle.decode_attn(*args, abs_v=True)
+    stats = check_attention(out, ref, "dominant small-scale key", mag)
+    assert stats["rel_l2"] < 2e-3
+
+
+def test_decode_one_hot_attention_with_huge_logits():
+    """Logits near 1e5 (a x1e3 key aligned with the query) make the attention one-hot: the output must
+    be that key's dequantized value to BF16 rounding, which fails if the V scale is applied through an
+    addition to the logit (its log would be rounded to the ulp of the logit)."""
+    rng = np.random.default_rng(41)
+    n, R = 40, 64
+    k = rng.standard_normal((n, 4, 128)).astype(np.float32)
+    v = rng.standard_normal((n, 4, 128)).astype(np.float32) * np.float32(0.37)
+    q = rng.standard_normal((1, 32, 128)).astype(np.float32)
+    k[11] = np.repeat(q[0, ::8], 1, axis=0)[:4] * np.float32(3e3)   # kv head h aligned with query head 8h
+    kb, vb, qb = inputs.to_bf16_bits(k), inputs.to_bf16_bits(v), inputs.to_bf16_bits(q)
+    slots = rng.permutation(R)[:n].astype(np.int32)
+    gp = ops.KVPool.empty(R, 4)
+    ops.store_quant(gp, bits_to_cuda_bf16(kb), bits_to_cuda_bf16(vb), torch.from_numpy(slots).cuda())
+    op = oracle.Pool(R, 4, 128)
+    oracle.store_quant(op, kb, vb, slots)
+    lens, offs = np.array([n], np.int32), np.array([0, 1], np.int32)
+    out = ops.decode_attn(gp, bits_to_cuda_bf16(qb), torch.from_numpy(slots[None]).cuda(),
+                          torch.from_numpy(lens).cuda(), torch.from_numpy(offs).cuda(), max_seq_len=n)
+    args = (op, qb, slots[None], lens, offs, inputs.SM_SCALE, 32)
+    ref, mag = oracle.decode_attn(*args), oracle.decode_attn(*args, abs_v=True)
+    vhat = oracle.e4m3_decode(op.v_codes[slots[11]]) * op.v_scales[slots[11]][:, None]
+    for h in range(4):                                   # the aligned heads are one-hot on key 11
+        np.testing.assert_allclose(ref[0, 8 * h], vhat[h], rtol=1e-9, atol=1e-12)
+    o = out.float().cpu().numpy().astype(np.float64)
+    for h in range(4):
+        assert np.abs(o[0, 8 * h] - vhat[h]).max() <= 2.0 ** -8 * np.abs(vhat[h]).max() + 1e-6
+    check_attention(out, ref, "one-hot huge logits", mag)

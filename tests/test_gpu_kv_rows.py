@@ -125,3 +125,25 @@ def test_reconstruct_wide_magnitudes_bit_exact():
     ok, ov = oracle.reconstruct(op, slots)
     assert np.array_equal(cuda_bf16_to_bits(wk), ok)
     assert np.array_equal(cuda_bf16_to_bits(wv), ov)
+
+
+def test_store_random_bit_patterns_bit_exact():
+    """Rows of random finite BF16 bit patterns over the whole exponent range (and rows confined to a
+    few binades at random offsets): codes and scales bit-exact, which checks the per-element division."""
+    rng = np.random.default_rng(77)
+    T, R = 20000, 40000
+    bits = rng.integers(0, 1 << 16, size=(T, 4, 128), dtype=np.uint32).astype(np.uint16)
+    bits[(bits & 0x7F80) == 0x7F80] &= 0xBF7F          # no Inf/NaN
+    narrow = rng.random(T) < 0.5                        # half the tokens: exponents within 3 binades
+    e = rng.integers(1, 250, size=(T, 1, 1)).astype(np.uint16)
+    mant = rng.integers(0, 1 << 7, size=(T, 4, 128)).astype(np.uint16)
+    sign = rng.integers(0, 2, size=(T, 4, 128)).astype(np.uint16) << 15
+    ex = np.clip(e + rng.integers(0, 3, size=(T, 4, 128)).astype(np.uint16), 1, 254)
+    bits[narrow] = (sign | (ex << 7) | mant)[narrow]
+    v = bits[::-1].copy()
+    slots = rng.permutation(R)[:T].astype(np.int32)
+    gp = ops.KVPool.empty(R, 4)
+    ops.store_quant(gp, bits_to_cuda_bf16(bits), bits_to_cuda_bf16(v), torch.from_numpy(slots).cuda())
+    op = oracle.Pool(R, 4, 128)
+    oracle.store_quant(op, bits, v, slots)
+    _assert_pool_equal(gp, op, slots)
