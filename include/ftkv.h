@@ -138,6 +138,30 @@ int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t*
                      void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Decode without any device allocation.  The pages describe no such entry point; it exists for
+ * callers that cannot allocate device memory when they need decode attention (a runtime that forbids
+ * out-of-band device allocations, a plug-in that only receives buffers from its host, code that must
+ * never touch an allocator).  Same arguments and results as ftkv_decode_attn, minus the workspace: the
+ * split partials and arrival counters live in a file-scope device array of FTKV_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) that every GPU which loads this library keeps until the process exits.
+ *   - A call whose partials would not fit (roughly total_q_rows * num_q_heads * splits > 30,000 slices)
+ *     returns FTKV_ERR_WORKSPACE without launching anything.
+ *   - The first call on a device (with that device current) looks up the array's device address; make
+ *     that first call before any stream capture.
+ *   - Every call shares the array, which keeps the previous call's contents; each call clears the
+ *     counters it uses on `stream`.  Calls that overlap on the GPU (other streams, other threads) race
+ *     on the array: serialize them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * --------------------------------------------------------------------------------------------- */
+#define FTKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int ftkv_decode_attn_noalloc(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
+                             const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens,
+                             const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
+                             int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
+                             uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Prefill (extend) attention of the current chunk over the reconstructed BF16 prefix plus the BF16
  * chunk itself ([#853 "What changes"]: current-chunk K/V remains BF16; [#853 "Paired end-to-end
  * A/B"]: the historical-prefix + new-token operator).
