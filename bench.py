@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--pool-rows", type=int, default=33059)
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--num-splits", type=int, default=0)
+    p.add_argument("--decode-impl", choices=["auto", "mma"], default="auto",
+                   help="auto: tcgen05 kernel for the single-row decode; mma: the warp-level mma.sync kernel")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-layers", type=int, default=2)
     return p.parse_args()
@@ -259,7 +261,7 @@ def build_decode(args, torch, ops, inputs, device):
             if events is not None:
                 events[l][0].record()
             ops.decode_attn(pools[l], q[l], slots_d, lens_d, None, max_seq_len=n, max_q_rows=1, plan=plan,
-                            out=outs[l])
+                            out=outs[l], impl=args.decode_impl)
             if events is not None:
                 events[l][1].record()
 
@@ -331,8 +333,12 @@ def run_ours(args, world, rank, local):
                 durs += [a.elapsed_time(b) for a, b in evs]
     dur_ms = statistics.mean(durs)
     achieved = kernel_bytes / (dur_ms * 1e-3) / 1e9
-    traffic = profiled_traffic("decode_split_32k.md", ["fp8_kv_cache_ftkv_gb300/csrc/decode.cu",
-                                                       "fp8_kv_cache_ftkv_gb300/csrc/ftkv_device.cuh"])
+    if args.decode_impl == "auto":
+        kname, prof, ksrc = "decode_tc_kernel", "decode_tc_32k.md", "decode_tc.cu"
+    else:
+        kname, prof, ksrc = "decode_split_kernel<1>", "decode_split_32k.md", "decode.cu"
+    traffic = profiled_traffic(prof, [f"fp8_kv_cache_ftkv_gb300/csrc/{ksrc}",
+                                      "fp8_kv_cache_ftkv_gb300/csrc/ftkv_device.cuh"])
 
     # ---- e2e through the public API with pinned host buffers ----
     e2e = None
@@ -377,6 +383,7 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3-kv/f16-mma/f32-acc", "data": "synthetic",
+            "decode_impl": args.decode_impl,
             "config": {"workload": f"decode_{n}_b1_{args.layers}layers", "context": n, "batch": 1,
                        "layers": args.layers, "Hq": HQ, "Hkv": HKV, "D": D, "pool_rows": args.pool_rows,
                        "num_splits": st["plan"].num_splits, "graph": "one CUDA graph per step",
@@ -384,7 +391,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "decode_split_kernel<1>",
+                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": kname,
                          "bytes_per_launch": kernel_bytes, "mean_launch_us": dur_ms * 1e3,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * args.layers * 2,

@@ -61,6 +61,7 @@ struct DecodeArgs {
   int* counters;             // [batch][Hkv] arrival tickets; zero between calls
   uint16_t* out;             // [total_q_rows][Hq][128]
   int* err;
+  int force_mma;             // 1: the warp-level mma.sync kernel even for single-row batches
 };
 
 struct PrefillArgs {
@@ -83,6 +84,7 @@ cudaError_t launch_reconstruct(const ReconstructArgs& a, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* c, int64_t n, int num_sms, cudaStream_t s);
 cudaError_t launch_e4m3_decode(const uint8_t* c, float* x, int64_t n, int num_sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 int decode_ctas_per_sm(int max_q_rows);
 cudaError_t launch_prefill_mma(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);

@@ -130,8 +130,12 @@ class DecodePlan:
 def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,
                 q_row_offsets: torch.Tensor = None, *, max_seq_len: int, max_q_rows: int = 1,
                 sm_scale: float = HEAD_DIM ** -0.5, num_splits: int = 0, plan: DecodePlan = None,
-                out: torch.Tensor = None, stream=None) -> torch.Tensor:
-    """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, 128]."""
+                out: torch.Tensor = None, impl: str = "auto", stream=None) -> torch.Tensor:
+    """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, 128].
+    ``impl``: "auto" (tcgen05 kernel for single-row batches, warp-level kernel for multi-row ones) or
+    "mma" (the warp-level mma.sync kernel for every batch)."""
+    if impl not in ("auto", "mma"):
+        raise ValueError(f"unknown decode impl {impl!r}")
     _req(q, torch.bfloat16, "q", 3)
     if req_to_slot.dim() == 1:
         req_to_slot = req_to_slot.view(1, -1)
@@ -147,10 +151,11 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
         out = torch.empty_like(q)
     _req(out, torch.bfloat16, "out", 3)
     ps = pool.c_struct()
-    check(_lib.load().ftkv_decode_attn(
+    name = "ftkv_decode_attn" if impl == "auto" else "ftkv_decode_attn_mma"
+    check(getattr(_lib.load(), name)(
         ctypes.byref(ps), hq, _ptr(q), _ptr(req_to_slot), req_to_slot.shape[1], _ptr(seq_lens),
         _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale), plan.num_splits,
-        _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)), "ftkv_decode_attn")
+        _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)), name)
     return out
 
 

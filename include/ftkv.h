@@ -137,6 +137,17 @@ int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t*
                      int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
                      void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
+/* Same operation, arguments, layouts and errors as ftkv_decode_attn, always on the warp-level
+ * mma.sync kernel.  ftkv_decode_attn runs batches with max_q_rows == 1 on the tcgen05 kernel (TMA
+ * gathers of the code rows, E4M3 QK and FP16 PV on the tensor cores with TMEM accumulators) and
+ * multi-row batches on the warp-level kernel; this entry point keeps the warp-level kernel reachable
+ * for single-row batches too, as the comparison point.  Both use the same workspace layout. */
+int ftkv_decode_attn_mma(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
+                         const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens,
+                         const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
+                         int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
+                         void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
+
 /* ---------------------------------------------------------------------------------------------
  * Decode without any device allocation.  The pages describe no such entry point; it exists for
  * callers that cannot allocate device memory when they need decode attention (a runtime that forbids

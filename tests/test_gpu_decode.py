@@ -3,7 +3,8 @@
 Covers the 512-token single step, ragged key counts (1, 17, 513), split caps 1/8/64 and automatic,
 GQA group sizes 8/4/2/1, multi-row decode (1..8 rows, rows that see no key), the 32,768- and
 40,000-key batch-1 workloads at full size (sampled layers, every output element), and the batched
-64-request multi-row workload at full size.
+64-request multi-row workload at full size.  Single-row cases run on both kernels: "auto" (the tcgen05
+kernel for single-row batches) and "mma" (the warp-level mma.sync kernel).
 """
 import numpy as np
 import pytest
@@ -14,6 +15,7 @@ from fp8_kv_cache_ftkv_gb300 import inputs, ops
 from parity import bits_to_cuda_bf16, check_attention
 
 pytestmark = pytest.mark.gpu
+IMPLS = ["auto", "mma"]
 
 
 def _setup(wl: inputs.DecodeWorkload, layer: int = 0):
@@ -30,11 +32,11 @@ def _setup(wl: inputs.DecodeWorkload, layer: int = 0):
     return gp, op, L, dev
 
 
-def _run(wl, gp, dev, num_splits=0, max_q_rows=None):
+def _run(wl, gp, dev, num_splits=0, max_q_rows=None, impl="auto"):
     R = np.diff(wl.q_row_offsets)
     mq = int(max(R.max(), 1)) if max_q_rows is None else max_q_rows
     return ops.decode_attn(gp, dev["q"], dev["r2s"], dev["lens"], dev["offs"], max_seq_len=int(wl.req_to_slot.shape[1]),
-                           max_q_rows=mq, sm_scale=wl.sm_scale, num_splits=num_splits)
+                           max_q_rows=mq, sm_scale=wl.sm_scale, num_splits=num_splits, impl=impl)
 
 
 def _ref(wl, op, L):
@@ -46,29 +48,43 @@ def _check(out, refs, what):
     return check_attention(out, refs[0], what, refs[1])
 
 
-def test_decode_small_step():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_small_step(impl):
     wl = inputs.decode_small()
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev)
+    out = _run(wl, gp, dev, impl=impl)
     stats = _check(out, _ref(wl, op, L), "decode_small")
     assert stats["max_abs"] < 0.05
     assert ops.device_errors() == 0
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("n", [1, 17, 513, 4099])
 @pytest.mark.parametrize("splits", [0, 1, 8, 64])
-def test_decode_ragged_lengths_and_split_caps(n, splits):
+def test_decode_ragged_lengths_and_split_caps(n, splits, impl):
     wl = inputs.decode_custom([n], [1], max(2 * n, 64), seed=n)
+    gp, op, L, dev = _setup(wl)
+    out = _run(wl, gp, dev, num_splits=splits, impl=impl)
+    _check(out, _ref(wl, op, L), f"n={n} splits={splits} impl={impl}")
+
+
+@pytest.mark.parametrize("n,splits", [(9000, 1), (20000, 3), (131, 1), (131, 2)])
+def test_decode_long_slices_cross_slot_windows(n, splits):
+    """Slices of thousands of keys (several 2,048-slot windows of the tcgen05 kernel's producer), a slice
+    whose last 128-key tile holds 3 keys, and slices shorter than one tile."""
+    wl = inputs.decode_custom([n], [1], n + 7, seed=n + splits)
     gp, op, L, dev = _setup(wl)
     out = _run(wl, gp, dev, num_splits=splits)
     _check(out, _ref(wl, op, L), f"n={n} splits={splits}")
+    assert ops.device_errors() == 0
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("Hq,Hkv", [(32, 4), (16, 4), (8, 4), (4, 4), (64, 8)])
-def test_decode_gqa_groups(Hq, Hkv):
+def test_decode_gqa_groups(Hq, Hkv, impl):
     wl = inputs.decode_custom([300, 1000], [1, 1], 4000, seed=Hq, Hq=Hq, Hkv=Hkv)
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev)
+    out = _run(wl, gp, dev, impl=impl)
     _check(out, _ref(wl, op, L), f"Hq={Hq} Hkv={Hkv}")
 
 
@@ -92,21 +108,23 @@ def test_decode_rows_that_see_no_key_are_zero():
     assert (out[:3].float() == 0).all()
 
 
-def test_decode_zero_length_request_and_single_row_path_with_offsets():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_zero_length_request_and_single_row_path_with_offsets(impl):
     wl = inputs.decode_custom([0, 33, 1], [1, 1, 1], 64, seed=4)
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev)
+    out = _run(wl, gp, dev, impl=impl)
     _check(out, _ref(wl, op, L), "zero-length request")
     assert (out[0].float() == 0).all()
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("n,R", [(32768, 33059), (40000, 40290)])
-def test_decode_long_context_full_size(n, R):
+def test_decode_long_context_full_size(n, R, impl):
     wl = inputs.decode_long(n, R, layers=48)
     for layer in (0, 47):
         gp, op, L, dev = _setup(wl, layer)
-        out = _run(wl, gp, dev)
-        stats = _check(out, _ref(wl, op, L), f"n={n} layer={layer}")
+        out = _run(wl, gp, dev, impl=impl)
+        stats = _check(out, _ref(wl, op, L), f"n={n} layer={layer} impl={impl}")
         assert stats["rel_l2"] < 2e-3
     assert ops.device_errors() == 0
 
@@ -125,21 +143,23 @@ def test_decode_batched_multirow_full_size():
     assert ops.device_errors() == 0
 
 
-def test_decode_bad_slot_and_seq_len_are_flagged_not_faulted():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_bad_slot_and_seq_len_are_flagged_not_faulted(impl):
     wl = inputs.decode_custom([50], [1], 128, seed=5)
     gp, op, L, dev = _setup(wl)
     bad = dev["r2s"].clone()
     bad[0, 3] = 10 ** 6
-    ops.decode_attn(gp, dev["q"], bad, dev["lens"], dev["offs"], max_seq_len=50, max_q_rows=1)
+    bad[0, 4] = -7
+    ops.decode_attn(gp, dev["q"], bad, dev["lens"], dev["offs"], max_seq_len=50, max_q_rows=1, impl=impl)
     assert ops.device_errors() & 0x1
     lens = torch.tensor([60], dtype=torch.int32, device="cuda")
-    ops.decode_attn(gp, dev["q"], dev["r2s"], lens, dev["offs"], max_seq_len=50, max_q_rows=1)
+    ops.decode_attn(gp, dev["q"], dev["r2s"], lens, dev["offs"], max_seq_len=50, max_q_rows=1, impl=impl)
     assert ops.device_errors() & 0x2
     assert ops.device_errors() == 0
 
 
-@pytest.mark.parametrize("max_q_rows", [1, 2])
-def test_decode_dominant_key_with_small_v_scale(max_q_rows):
+@pytest.mark.parametrize("max_q_rows,impl", [(1, "auto"), (1, "mma"), (2, "auto")])
+def test_decode_dominant_key_with_small_v_scale(max_q_rows, impl):
     """A key holding almost all the probability has a V scale 1e6 x smaller than a key with tiny
     probability; both terms matter (ratio ~0.1) and the dominant one must keep full precision."""
     rng = np.random.default_rng(31)
@@ -162,14 +182,15 @@ def test_decode_dominant_key_with_small_v_scale(max_q_rows):
     lens = np.array([n], np.int32)
     out = ops.decode_attn(gp, bits_to_cuda_bf16(qb), torch.from_numpy(slots[None]).cuda(),
                           torch.from_numpy(lens).cuda(), torch.from_numpy(offs).cuda(), max_seq_len=n,
-                          max_q_rows=max_q_rows)
+                          max_q_rows=max_q_rows, impl=impl)
     args = (op, qb, slots[None], lens, offs, inputs.SM_SCALE, 32)
     ref, mag = oracle.decode_attn(*args), oracle.decode_attn(*args, abs_v=True)
     stats = check_attention(out, ref, "dominant small-scale key", mag)
     assert stats["rel_l2"] < 2e-3
 
 
-def test_decode_one_hot_attention_with_huge_logits():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_one_hot_attention_with_huge_logits(impl):
     """Logits near 1e5 (a x1e3 key aligned with the query) make the attention one-hot: the output must
     be that key's dequantized value to BF16 rounding, which fails if the V scale is applied through an
     addition to the logit (its log would be rounded to the ulp of the logit)."""
@@ -187,7 +208,8 @@ def test_decode_one_hot_attention_with_huge_logits():
     oracle.store_quant(op, kb, vb, slots)
     lens, offs = np.array([n], np.int32), np.array([0, 1], np.int32)
     out = ops.decode_attn(gp, bits_to_cuda_bf16(qb), torch.from_numpy(slots[None]).cuda(),
-                          torch.from_numpy(lens).cuda(), torch.from_numpy(offs).cuda(), max_seq_len=n)
+                          torch.from_numpy(lens).cuda(), torch.from_numpy(offs).cuda(), max_seq_len=n,
+                          impl=impl)
     args = (op, qb, slots[None], lens, offs, inputs.SM_SCALE, 32)
     ref, mag = oracle.decode_attn(*args), oracle.decode_attn(*args, abs_v=True)
     vhat = oracle.e4m3_decode(op.v_codes[slots[11]]) * op.v_scales[slots[11]][:, None]
