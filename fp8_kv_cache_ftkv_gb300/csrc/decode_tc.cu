@@ -7,31 +7,38 @@
 // partial format and merge as the warp-level kernel in decode.cu).  This kernel serves requests with
 // one query row; the warp-level kernel serves the multi-row (MTP / speculative) case.
 //
-// CTA = (key slice, KV head, request), 320 threads, tiles of 128 keys:
-//   warp 0      TMEM allocation; producer: stages the slice's slot indices in shared memory, then per
-//               tile each lane issues one TMA tile::gather4 for 4 K code rows and one for the same 4 V
-//               code rows (128 B each, 128-byte swizzle) plus cp.async copies of their 8 scales, all
-//               completing on one mbarrier (3-stage ring).  Padding keys past the slice's end gather
-//               the head's row of slot 0 (always in bounds); they get no scales, the softmax gives them
-//               weight 0 by selection and the converter writes their V rows as zeros.
-//   warp 1      lane 0 issues the MMAs:
+// CTA = (key slice, KV head, request), 17 warps, tiles of 128 keys, a 4-stage ring of 33 KB stages:
+//   warps 0-3   producers.  They stage the slice's slot indices in shared memory (the first window is
+//               requested before anything else, so its latency overlaps the set-up); per tile, lanes 0-7
+//               of each warp issue one TMA tile::gather4 for 4 K code rows (128-byte rows, 128-byte
+//               swizzle, box one row high), while every producer thread copies 8 x 16 bytes of V code
+//               rows (8 threads per row, into the same swizzled layout) and the two scales of one key
+//               with cp.async.  All of it completes on the stage's mbarrier (transaction bytes +
+//               cp.async arrivals).  The split keeps both copy engines busy: the SM's TMA unit takes
+//               about 16-20 ns per 4-row gather, so K alone on TMA and V on the LSU path halve the
+//               issue time of a tile.  The K codes stay in the async proxy (TMA writes, tensor cores
+//               read); the V codes stay in the generic proxy (cp.async writes, the converter reads).
+//               Padding keys past the slice's end gather the head's row of slot 0 (in bounds) for K
+//               and copy no V codes and no scales.
+//   warp 4      TMEM owner; lane 0 issues the MMAs:
 //                 S_i = K_i Qp^T    kind::f8f6f4, E4M3 x E4M3 -> FP32, M = 128 keys, N = 16 (8 query
 //                                   heads x 2 exact E4M3 pieces of the BF16 query), K = 128 d; the
-//                                   stored K codes are the A operand exactly as TMA left them.
-//                 D_i = Vh_i^T P'_i kind::f16, M = 128 d, N = 64 (8 heads x 8 blocks of 16 keys),
-//                                   K = 128 keys; V is the MN-major A operand.
+//                                   stored K codes are the A operand as they were gathered.
+//                 D_i = Vh_i^T P'_i kind::f16, M = 128 d, N = 64 ((head half, block of 16 keys, head)
+//                                   rows of P'), K = 128 keys; V is the MN-major A operand.
 //               S and D are double-buffered in TMEM.
-//   warps 2..5  softmax, one thread per key row of S (= TMEM lane): scores, exact per-tile maxima per head
-//               (redux.sync + one shared-memory exchange), p = 2^(s - m), the value-weighted weight
-//               w = p scaleV, and P' = w 2^-E written in FP16 to row (block, head) of P', where 2^E is
-//               the power of two of the block's largest w (each 16-key block keeps FP16's full range).
-//               Then the fold O = O alpha_i + sum_blocks D_i[block] 2^E[block] in FP32 registers, one
-//               thread per d row of D.
-//   warps 6..9  convert the V code tile to FP16 (packed hardware converter) in the MN-major SW128 layout.
+//   warps 5-12  softmax, two warps per TMEM lane quarter, each for 4 of the 8 query heads; a thread is one
+//               key row of S and one d row of D.  Scores, exact per-tile maxima per head (redux.sync and
+//               one shared-memory exchange), p = 2^(s - m), the value-weighted weight w = p scaleV, and
+//               P' = w 2^-E in FP16 where 2^E is the power of two of the largest w of the key's 16-key
+//               block for that head (every block keeps FP16's full range).  Then the fold
+//               O = O alpha_i + sum_blocks D_i[block] 2^E[block] in FP32 registers.
+//   warps 13-16 convert the V code tile to FP16 (packed hardware converter) in the MN-major SW128 layout,
+//               writing zeros for padding keys.
 // Every mbarrier wait is bounded by %globaltimer; on expiry the CTA flags FTKV_DEVERR_TIMEOUT, drains its
-// loads and MMAs, releases TMEM and leaves its outputs unspecified.  Named barriers among the softmax
-// warps are only crossed with a CTA-uniform decision (a flag vote at each barrier), so a timeout cannot
-// leave one warp waiting at a barrier the others skipped.
+// loads and MMAs, releases TMEM and leaves its outputs unspecified.  The named barriers of the producer
+// and softmax groups are crossed only with a group-uniform decision (a reduction or a vote at the
+// barrier), so a timeout cannot strand a warp at a barrier the others skipped.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,43 +49,51 @@ namespace ftkv {
 namespace {
 
 constexpr int TK = 128;                                  // keys per tile
-constexpr int NS = 3;                                    // stages of the gather ring
+constexpr int NS = 4;                                    // stages of the load ring
 constexpr int SLOT_CAP = 2048;                           // slot indices staged per window
+constexpr int NPROD = 4, NSOFT = 8, NCONV = 4;           // warps per role
+constexpr int W_MMA = NPROD, W_SOFT = NPROD + 1, W_CONV = W_SOFT + NSOFT;
+constexpr int NTHREADS = 32 * (W_CONV + NCONV);          // 544
 constexpr uint32_t CODE_TILE = TK * 128;                 // 16 KB of E4M3 codes
 constexpr uint32_t STAGE = 2 * CODE_TILE + 2 * TK * 4;   // K codes, V codes, K scales, V scales
 constexpr uint32_t VH_TILE = TK * 128 * 2;               // 32 KB FP16 V: two 64-d column atoms of 16 KB
 constexpr uint32_t P_ATOM = 64 * 128;                    // 64 rows x 64 keys FP16 (8 KB)
-constexpr uint32_t P_TILE = 2 * P_ATOM;                  // 64 rows (block, head) x 128 keys
+constexpr uint32_t P_TILE = 2 * P_ATOM;                  // 64 rows x 128 keys
 constexpr uint32_t QP_BYTES = 16 * 128;                  // 16 rows x 128 d E4M3
 constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_VH = OFF_STAGE + NS * STAGE;
-constexpr uint32_t OFF_P = OFF_VH + 2 * VH_TILE;
+constexpr uint32_t OFF_P = OFF_VH + VH_TILE;
 constexpr uint32_t OFF_QP = OFF_P + 2 * P_TILE;
 constexpr uint32_t OFF_SLOT = OFF_QP + QP_BYTES;
-constexpr uint32_t OFF_XA = OFF_SLOT + SLOT_CAP * 4;     // int [2][4 warps][8 heads]: tile maxima
-constexpr uint32_t OFF_EB = OFF_XA + 2 * 4 * 8 * 4;      // u32 [2][8 blocks][2]: block exponents, 1 byte/head
-constexpr uint32_t OFF_FLAG = OFF_EB + 2 * 8 * 2 * 4;    // int [2][4] votes, int [4] final vote
-constexpr uint32_t OFF_FQ = OFF_FLAG + 64;               // float [8]: query multipliers
-constexpr uint32_t OFF_LRED = OFF_FQ + 32;               // float [4][8]: row sums
+constexpr uint32_t OFF_XA = OFF_SLOT + SLOT_CAP * 4;     // int [2][4 quarters][8 heads]: tile maxima
+constexpr uint32_t OFF_SCL = OFF_XA + 2 * 4 * 8 * 4;     // float [2][8 blocks][8 heads]: block factors 2^E
+constexpr uint32_t OFF_FLAG = OFF_SCL + 2 * 8 * 8 * 4;   // int [2][8] votes, int [8] final vote
+constexpr uint32_t OFF_FQ = OFF_FLAG + 128;              // float [8]: query multipliers
+constexpr uint32_t OFF_LRED = OFF_FQ + 32;               // float [4 quarters][8 heads]: row sums
 constexpr uint32_t OFF_BAR = OFF_LRED + 128;
-constexpr int NBAR = 2 * NS + 16;
+constexpr int NBAR = 2 * NS + 14;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;        // TMEM base address, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;        // slack to align the base to 1024 B
 static_assert(STAGE % 1024 == 0 && OFF_VH % 1024 == 0 && OFF_P % 1024 == 0 && OFF_QP % 1024 == 0, "alignment");
+static_assert(OFF_SCL % 16 == 0 && OFF_XA % 16 == 0 && OFF_LRED % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 static_assert(SMEM_ALLOC <= 232448, "decode_tc shared memory");
 
-constexpr int B_FULL = 0;              // [NS] 33: expect_tx + one cp.async arrival per producer lane
-constexpr int B_EMPTY = NS;            // [NS] 256: converter + softmax threads
-constexpr int B_QREADY = 2 * NS;       //      128: query pieces written
+constexpr int B_FULL = 0;              // [NS] 4 expect_tx arrivals + 128 cp.async arrivals (producers)
+// Consumer groups arrive once per warp (lane 0, after __syncwarp): counts are in warps.
+constexpr int B_EMPTY = NS;            // [NS] 4 converter + 8 softmax warps
+constexpr int B_QREADY = 2 * NS;       //      8: query pieces written, P' cleared
 constexpr int B_SFULL = 2 * NS + 1;    // [2]  1: QK committed
-constexpr int B_SFREE = 2 * NS + 3;    // [2]  128: S read
-constexpr int B_VHFULL = 2 * NS + 5;   // [2]  128: FP16 V written
-constexpr int B_VHFREE = 2 * NS + 7;   // [2]  1: PV committed (V and P' consumed)
-constexpr int B_PFULL = 2 * NS + 9;    // [2]  128: P' written
-constexpr int B_DFULL = 2 * NS + 11;   // [2]  1: PV committed
-constexpr int B_DFREE = 2 * NS + 13;   // [2]  128: D folded
-constexpr int B_DRAIN = 2 * NS + 15;   //      1: every MMA finished
+constexpr int B_SFREE = 2 * NS + 3;    // [2]  8: S read
+constexpr int B_VHFULL = 2 * NS + 5;   //      4: FP16 V written
+constexpr int B_VHFREE = 2 * NS + 6;   //      1: PV committed (FP16 V consumed)
+constexpr int B_PFULL = 2 * NS + 7;    // [2]  8: P' written
+constexpr int B_DFULL = 2 * NS + 9;    // [2]  1: PV committed
+constexpr int B_DFREE = 2 * NS + 11;   // [2]  8: D folded
+constexpr int B_DRAIN = 2 * NS + 13;   //      1: every MMA finished
+static_assert(B_DRAIN < NBAR, "barrier count");
+constexpr int FULL_COUNT = NPROD + 32 * NPROD;
+constexpr int BAR_SOFT = 1, BAR_PROD = 2;  // named barriers (0 is __syncthreads)
 
 constexpr uint32_t TMEM_COLS = 256;    // S0 [0,16) S1 [16,32) D0 [64,128) D1 [128,192)
 constexpr uint32_t TM_S = 0, TM_D = 64;
@@ -98,19 +113,20 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// try_wait with a suspend-time hint: the warp sleeps in hardware until the phase completes (or the hint
+// runs out), instead of spinning and taking issue slots from the warps that do the work.
+constexpr uint32_t SUSPEND_HINT_NS = 100000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(SUSPEND_HINT_NS)
       : "memory");
   return ok != 0;
 }
-// Bounded wait.  With honor_abort, gives up as soon as another role of the CTA has timed out.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                       bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                            bool honor_abort) {
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -122,8 +138,23 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     }
   }
 }
+// Bounded wait.  With honor_abort, gives up as soon as another role of the CTA has timed out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, honor_abort);
+}
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also returns the AND of v over the participating threads.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool v) {
+  int r;
+  asm volatile("{ .reg .pred p, q; setp.ne.s32 p, %1, 0; bar.red.and.pred q, %2, %3, p; selp.s32 %0, 1, 0, q; }"
+               : "=r"(r)
+               : "r"(static_cast<int>(v)), "r"(id), "r"(count)
+               : "memory");
+  return r != 0;
 }
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar, int r0, int r1,
                                             int r2, int r3) {
@@ -137,6 +168,7 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (start, leading and stride byte offsets >> 4).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -181,20 +213,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,"
-      "%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
         "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]),
-        "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]),
-        "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
-        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
-        "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
 }
@@ -220,9 +247,8 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(320, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                     const DecodeArgs a) {
+__global__ void __launch_bounds__(NTHREADS, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -236,6 +262,17 @@ __global__ void __launch_bounds__(320, 1)
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- the first window of slot indices, requested before the request geometry is known: the table
+  // row holds req_stride entries, so the copy stays in bounds whatever seq_lens says ----
+  if (warp < NPROD) {
+    const int64_t j0p = static_cast<int64_t>(split) * a.chunk;
+    int64_t cnt = a.req_stride - j0p;
+    cnt = cnt < a.chunk ? cnt : a.chunk;
+    cnt = cnt < SLOT_CAP ? cnt : SLOT_CAP;
+    const int32_t* src = a.req_to_slot + static_cast<int64_t>(b) * a.req_stride + j0p;
+    for (int k = threadIdx.x; k < cnt; k += 32 * NPROD) cp_async_4(base + OFF_SLOT + 4 * k, src + k);
+  }
 
   // ---- request geometry (the same checks and conventions as the warp-level kernel) ----
   int64_t n = a.seq_lens[b];
@@ -257,17 +294,25 @@ __global__ void __launch_bounds__(320, 1)
   }
   if (R < 0 || R > 1 || row0 < 0 || row0 + R > a.total_q_rows) {
     if (threadIdx.x == 0 && split == 0 && h == 0) flag_error(a.err, kDevErrQRows);
+    cp_async_wait_all();
     return;
   }
-  if (R == 0) return;
+  if (R == 0) {
+    cp_async_wait_all();
+    return;
+  }
   if (n == 0) {  // nothing to attend to: the output row is zero
     if (split == 0)
       for (int i = threadIdx.x; i < a.group * kHeadDim; i += blockDim.x)
         a.out[(row0 * a.num_q_heads + h * a.group + i / kHeadDim) * kHeadDim + i % kHeadDim] = 0;
+    cp_async_wait_all();
     return;
   }
   const int64_t j0l = static_cast<int64_t>(split) * a.chunk;
-  if (j0l >= n) return;
+  if (j0l >= n) {
+    cp_async_wait_all();
+    return;
+  }
   const int j0 = static_cast<int>(j0l);
   const int j1 = (j0l + a.chunk < n) ? static_cast<int>(j0l + a.chunk) : static_cast<int>(n);
   const int nkeys = j1 - j0;
@@ -277,24 +322,24 @@ __global__ void __launch_bounds__(320, 1)
   // ---- set-up: barriers, TMEM ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; s++) {
-      mbar_init(bar(B_FULL + s), 33);
-      mbar_init(bar(B_EMPTY + s), 256);
+      mbar_init(bar(B_FULL + s), FULL_COUNT);
+      mbar_init(bar(B_EMPTY + s), NCONV + NSOFT);
     }
-    mbar_init(bar(B_QREADY), 128);
+    mbar_init(bar(B_QREADY), NSOFT);
+    mbar_init(bar(B_VHFULL), NCONV);
+    mbar_init(bar(B_VHFREE), 1);
     for (int x = 0; x < 2; x++) {
       mbar_init(bar(B_SFULL + x), 1);
-      mbar_init(bar(B_SFREE + x), 128);
-      mbar_init(bar(B_VHFULL + x), 128);
-      mbar_init(bar(B_VHFREE + x), 1);
-      mbar_init(bar(B_PFULL + x), 128);
+      mbar_init(bar(B_SFREE + x), NSOFT);
+      mbar_init(bar(B_PFULL + x), NSOFT);
       mbar_init(bar(B_DFULL + x), 1);
-      mbar_init(bar(B_DFREE + x), 128);
+      mbar_init(bar(B_DFREE + x), NSOFT);
     }
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {
+  if (warp == W_MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + OFF_MISC),
                  "r"(TMEM_COLS)
                  : "memory");
@@ -305,48 +350,58 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + OFF_MISC);
 
-  if (warp == 0) {
-    // ======================= producer =======================
+  if (warp < NPROD) {
+    // ======================= producers: TMA gathers of K, cp.async of V and the scales =======================
+    const int pt = threadIdx.x;  // 0..127: the key whose scales this thread copies
+    const int vc = pt & 7, vr = pt >> 3;  // V: 16-byte chunk vc of rows vr, vr + 16, ..., vr + 112
     const uint32_t sslot = base + OFF_SLOT;
-    const int32_t* req = a.req_to_slot + static_cast<int64_t>(b) * a.req_stride + j0;
     const int32_t* sslot_p = reinterpret_cast<const int32_t*>(gbase + OFF_SLOT);
+    const int32_t* req = a.req_to_slot + static_cast<int64_t>(b) * a.req_stride + j0;
+    auto row_of = [&](int key) -> int {  // pool row of key (relative to the slice); bad slots read slot 0
+      int32_t slot = sslot_p[key % SLOT_CAP];
+      if (slot < 0 || slot >= a.num_rows) {
+        flag_error(a.err, kDevErrBadSlot);
+        slot = 0;
+      }
+      return static_cast<int>(static_cast<int64_t>(slot) * a.num_kv_heads + h);
+    };
     int issued = 0;
     for (int i = 0; i < nT; i++) {
       const int s = i % NS;
       const int key0 = i * TK;
-      if (key0 % SLOT_CAP == 0) {  // stage the next window of slot indices (the previous one is consumed)
-        const int wn = (nkeys - key0 < SLOT_CAP) ? nkeys - key0 : SLOT_CAP;
-        for (int k = lane; k < wn; k += 32) cp_async_4(sslot + 4 * k, req + key0 + k);
+      bool w = true;
+      if (i >= NS) w = mbar_wait(bar(B_EMPTY + s), ((i / NS) - 1) & 1, abort_flag, a.err);
+      if (!named_bar_and(BAR_PROD, 32 * NPROD, w)) break;  // also: every producer is done with the last tile
+      if (key0 % SLOT_CAP == 0) {  // stage the next window of slot indices (the first is already on its way)
+        if (key0 > 0) {
+          const int wn = (nkeys - key0 < SLOT_CAP) ? nkeys - key0 : SLOT_CAP;
+          for (int k = pt; k < wn; k += 32 * NPROD) cp_async_4(sslot + 4 * k, req + key0 + k);
+        }
         cp_async_wait_all();
-        __syncwarp();
+        named_bar_sync(BAR_PROD, 32 * NPROD);
       }
-      if (i >= NS && !__all_sync(0xffffffffu, mbar_wait(bar(B_EMPTY + s), ((i / NS) - 1) & 1, abort_flag, a.err)))
-        break;
-      int rows[4];
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        const int key = key0 + 4 * lane + e;
-        int r = h;  // padding key: (slot 0, head h)
-        if (key < nkeys) {
-          int32_t slot = sslot_p[key % SLOT_CAP];
-          if (slot < 0 || slot >= a.num_rows) {  // flagged; row 0 keeps the read in bounds
-            flag_error(a.err, kDevErrBadSlot);
-            slot = 0;
-          }
-          r = static_cast<int>(static_cast<int64_t>(slot) * a.num_kv_heads + h);
-        }
-        rows[e] = r;
-      }
-      if (lane == 0) mbar_expect_tx(bar(B_FULL + s), 2 * CODE_TILE);
+      if (lane == 0) mbar_expect_tx(bar(B_FULL + s), CODE_TILE / NPROD);
       __syncwarp();
-      tma_gather4(stage_k(s) + lane * 512, &tmk, bar(B_FULL + s), rows[0], rows[1], rows[2], rows[3]);
-      tma_gather4(stage_v(s) + lane * 512, &tmv, bar(B_FULL + s), rows[0], rows[1], rows[2], rows[3]);
+      if (lane < 32 / NPROD) {  // gather group g: keys 4g .. 4g+3 of the tile
+        const int g = warp * (32 / NPROD) + lane;
+        int rows[4];
 #pragma unroll
-      for (int e = 0; e < 4; e++) {
-        if (key0 + 4 * lane + e < nkeys) {
-          cp_async_4(stage_ks(s) + (4 * lane + e) * 4, a.k_scales + rows[e]);
-          cp_async_4(stage_vs(s) + (4 * lane + e) * 4, a.v_scales + rows[e]);
+        for (int e = 0; e < 4; e++) {
+          const int key = key0 + 4 * g + e;
+          rows[e] = (key < nkeys) ? row_of(key) : h;  // padding key: (slot 0, head h)
         }
+        tma_gather4(stage_k(s) + g * 512, &tmk, bar(B_FULL + s), rows[0], rows[1], rows[2], rows[3]);
+      }
+#pragma unroll
+      for (int j = 0; j < TK / 16; j++) {
+        const int r = vr + 16 * j;
+        if (key0 + r < nkeys)
+          cp_async_16(stage_v(s) + sw128(r, vc), a.v_codes + static_cast<int64_t>(row_of(key0 + r)) * kHeadDim + vc * 16);
+      }
+      if (key0 + pt < nkeys) {
+        const int row = row_of(key0 + pt);
+        cp_async_4(stage_ks(s) + pt * 4, a.k_scales + row);
+        cp_async_4(stage_vs(s) + pt * 4, a.v_scales + row);
       }
       cp_async_arrive_noinc(bar(B_FULL + s));
       issued = i + 1;
@@ -355,7 +410,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = (issued > NS ? issued - NS : 0); i < issued; i++)
       mbar_wait(bar(B_FULL + i % NS), (i / NS) & 1, abort_flag, a.err, false);
     cp_async_wait_all();
-  } else if (warp == 1) {
+  } else if (warp == W_MMA) {
     if (lane == 0) {
       // ======================= MMA issuer =======================
       bool ok = mbar_wait(bar(B_QREADY), 0, abort_flag, a.err);
@@ -363,10 +418,10 @@ __global__ void __launch_bounds__(320, 1)
       auto issue_pv = [&](int i) -> bool {
         const int x = i & 1;
         if (!mbar_wait(bar(B_PFULL + x), (i >> 1) & 1, abort_flag, a.err)) return false;
-        if (!mbar_wait(bar(B_VHFULL + x), (i >> 1) & 1, abort_flag, a.err)) return false;
+        if (!mbar_wait(bar(B_VHFULL), i & 1, abort_flag, a.err)) return false;
         if (i >= 2 && !mbar_wait(bar(B_DFREE + x), ((i >> 1) - 1) & 1, abort_flag, a.err)) return false;
         tc_fence_after();
-        const uint32_t vh = base + OFF_VH + x * VH_TILE, pt = base + OFF_P + x * P_TILE;
+        const uint32_t vh = base + OFF_VH, pt = base + OFF_P + x * P_TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           // A = V^T, MN-major: a k-step is 16 key rows (2 KB); the two 64-d column atoms are 16 KB apart.
@@ -375,7 +430,7 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t bd = sw128_desc(pt + (kk >> 2) * P_ATOM + (kk & 3) * 32, 16, 1024);
           umma_f16(tmem + TM_D + x * 64, ad, bd, IDESC_PV, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(B_VHFREE + x));
+        umma_commit(bar(B_VHFREE));
         umma_commit(bar(B_DFULL + x));
         return true;
       };
@@ -404,14 +459,14 @@ __global__ void __launch_bounds__(320, 1)
       umma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, abort_flag, a.err, false);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= W_CONV) {
     // ======================= V converter: E4M3 codes -> FP16, MN-major SW128 =======================
-    const int t = threadIdx.x - 192;  // key row
+    const int t = threadIdx.x - 32 * W_CONV;  // key row
     for (int i = 0; i < nT; i++) {
-      const int s = i % NS, x = i & 1;
-      if (!mbar_wait(bar(B_FULL + s), (i / NS) & 1, abort_flag, a.err)) break;
-      if (i >= 2 && !mbar_wait(bar(B_VHFREE + x), ((i >> 1) - 1) & 1, abort_flag, a.err)) break;
-      const uint32_t src = stage_v(s), dst = base + OFF_VH + x * VH_TILE;
+      const int s = i % NS;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FULL + s), (i / NS) & 1, abort_flag, a.err))) break;
+      if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar(B_VHFREE), (i - 1) & 1, abort_flag, a.err))) break;
+      const uint32_t src = stage_v(s), dst = base + OFF_VH;
       const uint32_t keep = (i * TK + t < nkeys) ? 0xFFFFFFFFu : 0u;  // padding keys: V row of zeros
 #pragma unroll
       for (int c = 0; c < 8; c++) {
@@ -432,26 +487,32 @@ __global__ void __launch_bounds__(320, 1)
                        : "memory");
         }
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(bar(B_VHFULL + x));
-      mbar_arrive(bar(B_EMPTY + s));
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_VHFULL));
+        mbar_arrive(bar(B_EMPTY + s));
+      }
     }
   } else {
-    // ======================= softmax warps 2..5 =======================
+    // ======================= softmax warps =======================
     // A warp reaches TMEM lanes 32 (warp % 4) .. +31 only: thread t is key row t of S and d row t of D.
-    const int wq = warp & 3;
-    const int t = wq * 32 + lane;
-    const int wi = warp - 2;  // slot in the exchange arrays
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    // Warps W_SOFT .. +3 take heads 0-3, the next four heads 4-7.
+    const int qd = warp & 3;
+    const int wi = warp - W_SOFT;        // 0..7
+    const int hh = wi >> 2;              // head half
+    const int t = qd * 32 + lane;
+    const int st = threadIdx.x - 32 * W_SOFT;  // 0..255
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16);
     int* xa = reinterpret_cast<int*>(gbase + OFF_XA);
-    uint32_t* ebw = reinterpret_cast<uint32_t*>(gbase + OFF_EB);
+    float* scl = reinterpret_cast<float*>(gbase + OFF_SCL);
     volatile int* vote = reinterpret_cast<volatile int*>(gbase + OFF_FLAG);
     float* fqs = reinterpret_cast<float*>(gbase + OFF_FQ);
     float* lred = reinterpret_cast<float*>(gbase + OFF_LRED);
 
-    // --- query pieces: thread -> head g = t / 16, d = 8 (t % 16) .. +7 ---
-    {
-      const int g = t >> 4, d0 = (t & 15) * 8;
+    // --- query pieces (threads st < 128: head g = st / 16, d = 8 (st % 16) .. +7); P' cleared ---
+    if (st < 128) {
+      const int g = st >> 4, d0 = (st & 15) * 8;
       float qv[8];
       float amax = 0.0f;
       if (g < G) {
@@ -493,51 +554,49 @@ __global__ void __launch_bounds__(320, 1)
       asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(qp + sw128(8 + g, d0 >> 4) + (d0 & 15)), "r"(lo[0]),
                    "r"(lo[1])
                    : "memory");
-      if ((t & 15) == 0)
+      if ((st & 15) == 0)
         fqs[g] = (g < G) ? __uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * a.qk_scale_log2 : 0.0f;
-      // P' is zero outside each key's own (block, head) rows: clear both buffers once
-      for (int k = t; k < static_cast<int>(2 * P_TILE / 16); k += 128) st_shared_zero16(base + OFF_P + 16 * k);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      named_bar_sync(1, 128);
-      mbar_arrive(bar(B_QREADY));
     }
-    float fq[8];
-#pragma unroll
-    for (int g = 0; g < 8; g++) fq[g] = fqs[g];
+    // P' is zero outside each key's own (half, block, head) rows: clear both buffers once
+    for (int k = st; k < static_cast<int>(2 * P_TILE / 16); k += 32 * NSOFT) st_shared_zero16(base + OFF_P + 16 * k);
+    fence_proxy_async();
+    named_bar_sync(BAR_SOFT, 32 * NSOFT);
+    if (lane == 0) mbar_arrive(bar(B_QREADY));
 
-    float m[8], lsum[8], O[8], alpha_prev[8];
+    float fq[4], m[4], lsum[4], O[4], alpha_prev[4];
 #pragma unroll
-    for (int g = 0; g < 8; g++) {
-      m[g] = -INFINITY;
-      lsum[g] = 0.0f;
-      O[g] = 0.0f;
-      alpha_prev[g] = 1.0f;
+    for (int gg = 0; gg < 4; gg++) {
+      fq[gg] = fqs[hh * 4 + gg];
+      m[gg] = -INFINITY;
+      lsum[gg] = 0.0f;
+      O[gg] = 0.0f;
+      alpha_prev[gg] = 1.0f;
     }
 
-    // O = O alpha_i + sum over 16-key blocks of D_i[block] 2^(E[block] - 127)
+    // O = O alpha_i + sum over the 8 blocks of D_i[half, block, head] 2^(E[block, head] - 127)
     auto fold = [&](int i) -> bool {
       const int x = i & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_DFULL + x), (i >> 1) & 1, abort_flag, a.err))) return false;
       tc_fence_after();
-      uint32_t dv[64];
-      tmem_ld64(lane_base + TM_D + x * 64, dv);
+      uint32_t dv[32];
+      tmem_ld32(lane_base + TM_D + x * 64 + hh * 32, dv);
       tc_fence_before();
-      mbar_arrive(bar(B_DFREE + x));
-      const uint32_t* eb = ebw + x * 16;
-      float acc[8];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DFREE + x));
+      const float4* sc4 = reinterpret_cast<const float4*>(scl + x * 64 + hh * 4);
+      float acc[4];
 #pragma unroll
-      for (int g = 0; g < 8; g++) acc[g] = O[g] * alpha_prev[g];
+      for (int gg = 0; gg < 4; gg++) acc[gg] = O[gg] * alpha_prev[gg];
 #pragma unroll
       for (int blk = 0; blk < 8; blk++) {
-        const uint32_t e0 = eb[2 * blk], e1 = eb[2 * blk + 1];
-#pragma unroll
-        for (int g = 0; g < 8; g++) {
-          const uint32_t e = ((g < 4 ? e0 : e1) >> (8 * (g & 3))) & 0xFFu;
-          acc[g] = fmaf(__uint_as_float(dv[blk * 8 + g]), __uint_as_float(e << 23), acc[g]);
-        }
+        const float4 f = sc4[blk * 2];  // scl[x][blk][hh*4 .. hh*4+3]
+        acc[0] = fmaf(__uint_as_float(dv[blk * 4 + 0]), f.x, acc[0]);
+        acc[1] = fmaf(__uint_as_float(dv[blk * 4 + 1]), f.y, acc[1]);
+        acc[2] = fmaf(__uint_as_float(dv[blk * 4 + 2]), f.z, acc[2]);
+        acc[3] = fmaf(__uint_as_float(dv[blk * 4 + 3]), f.w, acc[3]);
       }
 #pragma unroll
-      for (int g = 0; g < 8; g++) O[g] = acc[g];
+      for (int gg = 0; gg < 4; gg++) O[gg] = acc[gg];
       return true;
     };
 
@@ -549,107 +608,118 @@ __global__ void __launch_bounds__(320, 1)
       w = w && mbar_wait(bar(B_SFULL + x), (i >> 1) & 1, abort_flag, a.err);
       w = __all_sync(0xffffffffu, w);
       const bool valid = i * TK + t < nkeys;
-      float sg[8], sv = 0.0f;
+      float sg[4], sv = 0.0f;
       if (w) {
         tc_fence_after();
         uint32_t sc[16];
         tmem_ld16(lane_base + TM_S + x * 16, sc);
-        tc_fence_before();
-        mbar_arrive(bar(B_SFREE + x));
         const float sk = ld_shared_f32(stage_ks(s) + t * 4);
         sv = ld_shared_f32(stage_vs(s) + t * 4);
-        mbar_arrive(bar(B_EMPTY + s));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B_SFREE + x));
+          mbar_arrive(bar(B_EMPTY + s));
+        }
 #pragma unroll
-        for (int g = 0; g < 8; g++)
-          sg[g] = valid ? fmaf(__uint_as_float(sc[8 + g]), 1.0f / 16.0f, __uint_as_float(sc[g])) * (sk * fq[g])
-                        : -INFINITY;
+        for (int gg = 0; gg < 4; gg++) {
+          const int g = hh * 4 + gg;
+          sg[gg] = valid ? fmaf(__uint_as_float(sc[8 + g]), 1.0f / 16.0f, __uint_as_float(sc[g])) * (sk * fq[gg])
+                         : -INFINITY;
+        }
       } else {
 #pragma unroll
-        for (int g = 0; g < 8; g++) sg[g] = -INFINITY;
+        for (int gg = 0; gg < 4; gg++) sg[gg] = -INFINITY;
       }
       // exact tile maximum of s per head over the 128 keys; the vote rides on the same barrier
-      int om[8];
+      int om[4];
 #pragma unroll
-      for (int g = 0; g < 8; g++) om[g] = redux_max_s32(f2ord(sg[g]));
+      for (int gg = 0; gg < 4; gg++) om[gg] = redux_max_s32(f2ord(sg[gg]));
       if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < 8; g++) xa[x * 32 + wi * 8 + g] = om[g];
-        vote[x * 4 + wi] = w ? 1 : 0;
+        *reinterpret_cast<int4*>(xa + x * 32 + qd * 8 + hh * 4) = make_int4(om[0], om[1], om[2], om[3]);
+        vote[x * 8 + wi] = w ? 1 : 0;
       }
-      named_bar_sync(1, 128);
-      if (!(vote[x * 4 + 0] && vote[x * 4 + 1] && vote[x * 4 + 2] && vote[x * 4 + 3])) {
+      named_bar_sync(BAR_SOFT, 32 * NSOFT);
+      bool all = true;
+#pragma unroll
+      for (int k = 0; k < NSOFT; k++) all = all && vote[x * 8 + k];
+      if (!all) {
         ok = false;
         break;
       }
-      float alpha[8], wv[8];
-      uint32_t pk0 = 0, pk1 = 0;  // biased exponents of w, one byte per head
+      float alpha[4], wv[4];
+      uint32_t pk = 0;  // biased exponents of w, one byte per head
 #pragma unroll
-      for (int g = 0; g < 8; g++) {
-        const int* xg = xa + x * 32 + g;
+      for (int gg = 0; gg < 4; gg++) {
+        const int* xg = xa + x * 32 + hh * 4 + gg;
         const float mt = ord2f(max(max(xg[0], xg[8]), max(xg[16], xg[24])));
-        const float mn = fmaxf(m[g], mt);
+        const float mn = fmaxf(m[gg], mt);
         const float mu = (mn == -INFINITY) ? 0.0f : mn;
-        alpha[g] = fast_exp2(m[g] - mu);
-        m[g] = mn;
-        const float p = valid ? fast_exp2(sg[g] - mu) : 0.0f;
-        lsum[g] = fmaf(lsum[g], alpha[g], p);
-        wv[g] = valid ? p * sv : 0.0f;
-        const uint32_t eb = __float_as_uint(wv[g]) >> 23;
-        if (g < 4) pk0 |= eb << (8 * g);
-        else pk1 |= eb << (8 * (g - 4));
+        alpha[gg] = fast_exp2(m[gg] - mu);
+        m[gg] = mn;
+        const float p = valid ? fast_exp2(sg[gg] - mu) : 0.0f;
+        lsum[gg] = fmaf(lsum[gg], alpha[gg], p);
+        wv[gg] = valid ? p * sv : 0.0f;
+        pk |= (__float_as_uint(wv[gg]) >> 23) << (8 * gg);
       }
       // block maxima over the 16 keys of this half-warp (bytewise unsigned max), clamped to [1, 253]
 #pragma unroll
-      for (int off = 1; off < 16; off <<= 1) {
-        pk0 = __vmaxu4(pk0, __shfl_xor_sync(0xffffffffu, pk0, off));
-        pk1 = __vmaxu4(pk1, __shfl_xor_sync(0xffffffffu, pk1, off));
-      }
-      pk0 = __vminu4(__vmaxu4(pk0, 0x01010101u), 0xFDFDFDFDu);
-      pk1 = __vminu4(__vmaxu4(pk1, 0x01010101u), 0xFDFDFDFDu);
+      for (int off = 1; off < 16; off <<= 1) pk = __vmaxu4(pk, __shfl_xor_sync(0xffffffffu, pk, off));
+      pk = __vminu4(__vmaxu4(pk, 0x01010101u), 0xFDFDFDFDu);
       const int blk = t >> 4;
       if ((lane & 15) == 0) {
-        ebw[x * 16 + 2 * blk] = pk0;
-        ebw[x * 16 + 2 * blk + 1] = pk1;
+        float4 f;
+        f.x = __uint_as_float((pk & 0xFFu) << 23);
+        f.y = __uint_as_float(((pk >> 8) & 0xFFu) << 23);
+        f.z = __uint_as_float(((pk >> 16) & 0xFFu) << 23);
+        f.w = __uint_as_float((pk >> 24) << 23);
+        *reinterpret_cast<float4*>(scl + x * 64 + blk * 8 + hh * 4) = f;
       }
-      // P'[(blk, g)][t] = w 2^(127 - E) in FP16 (K-major SW128: 64-key atoms, row = 8 blk + g)
+      // P'[(hh, blk, gg)][t] = w 2^(127 - E) in FP16 (K-major SW128: 64-key atoms, row 32 hh + 4 blk + gg)
       const uint32_t pt = base + OFF_P + x * P_TILE + (t >> 6) * P_ATOM;
       const int kc = t & 63;
 #pragma unroll
-      for (int g = 0; g < 8; g++) {
-        const uint32_t e = ((g < 4 ? pk0 : pk1) >> (8 * (g & 3))) & 0xFFu;
-        const __half hv = __float2half_rn(wv[g] * __uint_as_float((254u - e) << 23));
-        const uint32_t addr = pt + sw128(blk * 8 + g, kc >> 3) + (kc & 7) * 2;
+      for (int gg = 0; gg < 4; gg++) {
+        const uint32_t e = (pk >> (8 * gg)) & 0xFFu;
+        const __half hv = __float2half_rn(wv[gg] * __uint_as_float((254u - e) << 23));
+        const uint32_t addr = pt + sw128(hh * 32 + blk * 4 + gg, kc >> 3) + (kc & 7) * 2;
         asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(__half_as_ushort(hv)) : "memory");
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(bar(B_PFULL + x));
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_PFULL + x));
       done = i + 1;
-      // fold the previous tile (its exponents were published before this tile's barrier)
+      // fold the previous tile (its block factors were published before this tile's barrier)
       if (i >= 1) ok = fold(i - 1);
 #pragma unroll
-      for (int g = 0; g < 8; g++) alpha_prev[g] = alpha[g];
+      for (int gg = 0; gg < 4; gg++) alpha_prev[gg] = alpha[gg];
     }
-    // final vote: the last tile's exponents become visible at this barrier too
-    if (lane == 0) vote[8 + wi] = (ok && done == nT) ? 1 : 0;
-    named_bar_sync(1, 128);
-    const bool all_ok = vote[8] && vote[9] && vote[10] && vote[11];
+    // final vote: the last tile's block factors become visible at this barrier too
+    if (lane == 0) vote[16 + wi] = (ok && done == nT) ? 1 : 0;
+    named_bar_sync(BAR_SOFT, 32 * NSOFT);
+    bool all_ok = true;
+#pragma unroll
+    for (int k = 0; k < NSOFT; k++) all_ok = all_ok && vote[16 + k];
     if (all_ok) fold(nT - 1);
 
     // ---- partial (m, l, O) of this slice per query head; thread t = d ----
 #pragma unroll
-    for (int g = 0; g < 8; g++)
+    for (int gg = 0; gg < 4; gg++)
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) lsum[g] += __shfl_xor_sync(0xffffffffu, lsum[g], off);
+      for (int off = 1; off < 32; off <<= 1) lsum[gg] += __shfl_xor_sync(0xffffffffu, lsum[gg], off);
     if (lane == 0)
+      *reinterpret_cast<float4*>(lred + qd * 8 + hh * 4) = make_float4(lsum[0], lsum[1], lsum[2], lsum[3]);
+    named_bar_sync(BAR_SOFT, 32 * NSOFT);
 #pragma unroll
-      for (int g = 0; g < 8; g++) lred[wi * 8 + g] = lsum[g];
-    named_bar_sync(1, 128);
-    for (int g = 0; g < G; g++) {
-      const int64_t prow = ((row0 * a.num_q_heads) + h * G + g) * a.num_splits + split;
-      a.part_acc[prow * kHeadDim + t] = O[g];
-      if (t == 0) {
-        a.part_ml[prow * 2] = m[g];
-        a.part_ml[prow * 2 + 1] = lred[g] + lred[8 + g] + lred[16 + g] + lred[24 + g];
+    for (int gg = 0; gg < 4; gg++) {
+      const int g = hh * 4 + gg;
+      if (g < G) {
+        const int64_t prow = ((row0 * a.num_q_heads) + h * G + g) * a.num_splits + split;
+        a.part_acc[prow * kHeadDim + t] = O[gg];
+        if (t == 0) {
+          a.part_ml[prow * 2] = m[gg];
+          a.part_ml[prow * 2 + 1] = lred[g] + lred[8 + g] + lred[16 + g] + lred[24 + g];
+        }
       }
     }
   }
@@ -657,7 +727,7 @@ __global__ void __launch_bounds__(320, 1)
   // ======================= teardown, then the merge by the last slice to arrive =======================
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == W_MMA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
@@ -675,13 +745,26 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  float* wts = reinterpret_cast<float*>(gbase);  // the gather ring is idle now
+  // The slices' partials of this (request, KV head): weights from (m, l), then O = sum_sl w_sl O_sl.  When
+  // they fit, all partial accumulators are first copied into the idle ring with one round of cp.async.
+  const int64_t pbase = (row0 * a.num_q_heads + h * G) * a.num_splits;  // partial row of (g = 0, slice 0)
+  const bool in_smem = static_cast<uint32_t>(G * nslices) * (kHeadDim * 4 + 8) <= OFF_SLOT;
+  float* pacc = reinterpret_cast<float*>(gbase);  // [G][nslices][128] when in_smem
+  float* wts = in_smem ? pacc + G * nslices * kHeadDim : reinterpret_cast<float*>(gbase);  // [2][G][nslices]
+  if (in_smem) {
+    for (int idx = threadIdx.x; idx < G * nslices * (kHeadDim / 4); idx += blockDim.x) {
+      const int gs = idx / (kHeadDim / 4), d4 = idx % (kHeadDim / 4);  // gs = g * nslices + sl
+      const int g = gs / nslices, sl = gs % nslices;
+      cp_async_16(base + 16u * idx, a.part_acc + (pbase + static_cast<int64_t>(g) * a.num_splits + sl) * kHeadDim + 4 * d4);
+    }
+  }
   for (int i = threadIdx.x; i < G * nslices; i += blockDim.x) {
     const int g = i / nslices, sl = i % nslices;
-    const int64_t prow = ((row0 * a.num_q_heads) + h * G + g) * a.num_splits + sl;
+    const int64_t prow = pbase + static_cast<int64_t>(g) * a.num_splits + sl;
     wts[i] = __ldcg(a.part_ml + prow * 2);
     wts[G * nslices + i] = __ldcg(a.part_ml + prow * 2 + 1);
   }
+  cp_async_wait_all();
   __syncthreads();
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     float* wm = wts + g * nslices;
@@ -697,31 +780,43 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   for (int it = threadIdx.x; it < G * (kHeadDim / 4); it += blockDim.x) {
     const int d4 = it % (kHeadDim / 4), g = it / (kHeadDim / 4);
-    const int64_t basep = ((row0 * a.num_q_heads) + h * G + g) * a.num_splits;
     const float* wm = wts + g * nslices;
-    const float4* src = reinterpret_cast<const float4*>(a.part_acc + basep * kHeadDim) + d4;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    int sl = 0;
-    for (; sl + 8 <= nslices; sl += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; u++) v[u] = __ldcg(src + static_cast<int64_t>(sl + u) * (kHeadDim / 4));
-#pragma unroll
-      for (int u = 0; u < 8; u++) {
-        const float wv = wm[sl + u];
-        o.x += wv * v[u].x;
-        o.y += wv * v[u].y;
-        o.z += wv * v[u].z;
-        o.w += wv * v[u].w;
+    if (in_smem) {
+      const float4* src = reinterpret_cast<const float4*>(pacc + static_cast<int64_t>(g) * nslices * kHeadDim) + d4;
+      for (int sl = 0; sl < nslices; sl++) {
+        const float4 v = src[sl * (kHeadDim / 4)];
+        const float wv = wm[sl];
+        o.x += wv * v.x;
+        o.y += wv * v.y;
+        o.z += wv * v.z;
+        o.w += wv * v.w;
       }
-    }
-    for (; sl < nslices; sl++) {
-      const float4 v = __ldcg(src + static_cast<int64_t>(sl) * (kHeadDim / 4));
-      const float wv = wm[sl];
-      o.x += wv * v.x;
-      o.y += wv * v.y;
-      o.z += wv * v.z;
-      o.w += wv * v.w;
+    } else {
+      const float4* src =
+          reinterpret_cast<const float4*>(a.part_acc + (pbase + static_cast<int64_t>(g) * a.num_splits) * kHeadDim) + d4;
+      int sl = 0;
+      for (; sl + 8 <= nslices; sl += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) v[u] = __ldcg(src + static_cast<int64_t>(sl + u) * (kHeadDim / 4));
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+          const float wv = wm[sl + u];
+          o.x += wv * v[u].x;
+          o.y += wv * v[u].y;
+          o.z += wv * v[u].z;
+          o.w += wv * v[u].w;
+        }
+      }
+      for (; sl < nslices; sl++) {
+        const float4 v = __ldcg(src + static_cast<int64_t>(sl) * (kHeadDim / 4));
+        const float wv = wm[sl];
+        o.x += wv * v.x;
+        o.y += wv * v.y;
+        o.z += wv * v.z;
+        o.w += wv * v.w;
+      }
     }
     const uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
     *reinterpret_cast<uint2*>(a.out + (row0 * a.num_q_heads + h * G + g) * kHeadDim + 4 * d4) = packed;
@@ -769,10 +864,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   }
   const int64_t rows = a.num_rows * a.num_kv_heads;  // gather row coordinates are int32
   if (rows >= (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-  CUtensorMap tmk, tmv;
-  if (!make_row_map(&tmk, a.k_codes, rows) || !make_row_map(&tmv, a.v_codes, rows)) return cudaErrorInvalidValue;
+  CUtensorMap tmk;
+  if (!make_row_map(&tmk, a.k_codes, rows)) return cudaErrorInvalidValue;
   dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-  decode_tc_kernel<<<grid, 320, SMEM_ALLOC, s>>>(tmk, tmv, a);
+  decode_tc_kernel<<<grid, NTHREADS, SMEM_ALLOC, s>>>(tmk, a);
   return cudaGetLastError();
 }
 
