@@ -29,6 +29,7 @@
 //  * The 8 query heads of a GQA group are the MMA N dimension, so G = 8 wastes nothing.
 #include <cfloat>
 
+#include "decode_merge.cuh"
 #include "ftkv_device.cuh"
 #include "ftkv_internal.h"
 
@@ -102,6 +103,7 @@ __device__ __forceinline__ int64_t clamp_seq_len(const DecodeArgs& a, int b, boo
 
 template <int RPW>
 __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(const DecodeArgs a) {
+  pdl_enter();
   constexpr int WARPS = Cfg<RPW>::WARPS;
   constexpr int NSTAGE = Cfg<RPW>::NSTAGE;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -490,54 +492,7 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   if (!s_last) return;
   __threadfence();
 
-  // merge weights w[(rr*group + hh) * nslices + s] in the (now free) ring memory
-  float* wts = reinterpret_cast<float*>(smem);
-  for (int i = threadIdx.x; i < npairs * nslices; i += blockDim.x) {
-    const int pr = i / nslices, sl = i % nslices;
-    const int64_t prow = ((row0 + pr / a.group) * a.num_q_heads + h * a.group + pr % a.group) * a.num_splits + sl;
-    wts[i] = __ldcg(a.part_ml + prow * 2);
-    wts[npairs * nslices + i] = __ldcg(a.part_ml + prow * 2 + 1);
-  }
-  __syncthreads();
-  for (int pr = threadIdx.x; pr < npairs; pr += blockDim.x) {
-    float* wm = wts + pr * nslices;
-    const float* wl = wts + npairs * nslices + pr * nslices;
-    float M = -INFINITY;
-    for (int sl = 0; sl < nslices; sl++) M = fmaxf(M, wm[sl]);
-    float L = 0.0f;
-    if (M != -INFINITY)
-      for (int sl = 0; sl < nslices; sl++) L += exp2f(wm[sl] - M) * wl[sl];
-    const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
-    for (int sl = 0; sl < nslices; sl++) wm[sl] = (invL != 0.0f) ? exp2f(wm[sl] - M) * invL : 0.0f;
-  }
-  __syncthreads();
-  // one float4 of d per thread: 32 threads per (row, head), loads batched 8 deep
-  for (int it = threadIdx.x; it < npairs * (kHeadDim / 4); it += blockDim.x) {
-    const int d4 = it % (kHeadDim / 4), pr = it / (kHeadDim / 4);
-    const int rr = pr / a.group, hh = pr % a.group;
-    const int64_t base = ((row0 + rr) * a.num_q_heads + h * a.group + hh) * a.num_splits;
-    const float* wm = wts + pr * nslices;
-    const float4* src = reinterpret_cast<const float4*>(a.part_acc + base * kHeadDim) + d4;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    int sl = 0;
-    for (; sl + 8 <= nslices; sl += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; u++) v[u] = __ldcg(src + static_cast<int64_t>(sl + u) * (kHeadDim / 4));
-#pragma unroll
-      for (int u = 0; u < 8; u++) {
-        const float wv = wm[sl + u];
-        o.x += wv * v[u].x; o.y += wv * v[u].y; o.z += wv * v[u].z; o.w += wv * v[u].w;
-      }
-    }
-    for (; sl < nslices; sl++) {
-      const float4 v = __ldcg(src + static_cast<int64_t>(sl) * (kHeadDim / 4));
-      const float wv = wm[sl];
-      o.x += wv * v.x; o.y += wv * v.y; o.z += wv * v.z; o.w += wv * v.w;
-    }
-    uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
-    *reinterpret_cast<uint2*>(a.out + ((row0 + rr) * a.num_q_heads + h * a.group + hh) * kHeadDim + 4 * d4) = packed;
-  }
+  merge_split_partials(a, row0, R, h, nslices, smem);  // the ring is idle now
 }
 
 template <int RPW>
@@ -552,8 +507,7 @@ cudaError_t launch_split(const DecodeArgs& a, cudaStream_t s) {
     configured[dev] = true;
   }
   dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-  decode_split_kernel<RPW><<<grid, Cfg<RPW>::WARPS * 32, smem_bytes<RPW>(), s>>>(a);
-  return cudaGetLastError();
+  return launch_k(decode_split_kernel<RPW>, grid, dim3(Cfg<RPW>::WARPS * 32), smem_bytes<RPW>(), s, a);
 }
 
 }  // namespace

@@ -7,19 +7,18 @@
 // partial format and merge as the warp-level kernel in decode.cu).  This kernel serves requests with
 // one query row; the warp-level kernel serves the multi-row (MTP / speculative) case.
 //
-// CTA = (key slice, KV head, request), 17 warps, tiles of 128 keys, a 4-stage ring of 33 KB stages:
-//   warps 0-3   producers.  They stage the slice's slot indices in shared memory (the first window is
-//               requested before anything else, so its latency overlaps the set-up); per tile, lanes 0-7
-//               of each warp issue one TMA tile::gather4 for 4 K code rows (128-byte rows, 128-byte
-//               swizzle, box one row high), while every producer thread copies 8 x 16 bytes of V code
-//               rows (8 threads per row, into the same swizzled layout) and the two scales of one key
-//               with cp.async.  All of it completes on the stage's mbarrier (transaction bytes +
-//               cp.async arrivals).  The split keeps both copy engines busy: the SM's TMA unit takes
-//               about 16-20 ns per 4-row gather, so K alone on TMA and V on the LSU path halve the
-//               issue time of a tile.  The K codes stay in the async proxy (TMA writes, tensor cores
-//               read); the V codes stay in the generic proxy (cp.async writes, the converter reads).
-//               Padding keys past the slice's end gather the head's row of slot 0 (in bounds) for K
-//               and copy no V codes and no scales.
+// CTA = (key slice, KV head, request), 16 warps, tiles of 128 keys, a 4-stage ring of 33 KB stages:
+//   warps 0-3   producers.  They stage the slice's slot indices in shared memory (a double window of 2 x 2048;
+//               the first window is requested before anything else, so its latency overlaps the set-up).
+//               Per tile, each gather group of 4 keys gets one TMA tile::gather4 for its 4 K code rows
+//               and one for its 4 V code rows (128-byte rows, 128-byte swizzle, box one row high); the
+//               32 groups are spread over the producer warps, because a gather4 instruction issues its
+//               lanes' operations one after another.  The scales are read with plain loads one tile
+//               ahead and stored into the stage after the gathers are issued, before the warp's arrival
+//               on the stage's mbarrier (expected bytes announced first, one arrival per warp).  Copies of 4-byte scales through cp.async,
+//               or of the V rows through cp.async, slowed the gathers' issue severalfold when mixed with
+//               them; TMA alone in flight issues at the rate of a pure-load kernel.  Padding keys past
+//               the slice's end gather the head's row of slot 0 (in bounds) and get zero scales.
 //   warp 4      TMEM owner; lane 0 issues the MMAs:
 //                 S_i = K_i Qp^T    kind::f8f6f4, E4M3 x E4M3 -> FP32, M = 128 keys, N = 16 (8 query
 //                                   heads x 2 exact E4M3 pieces of the BF16 query), K = 128 d; the
@@ -33,7 +32,7 @@
 //               P' = w 2^-E in FP16 where 2^E is the power of two of the largest w of the key's 16-key
 //               block for that head (every block keeps FP16's full range).  Then the fold
 //               O = O alpha_i + sum_blocks D_i[block] 2^E[block] in FP32 registers.
-//   warps 13-16 convert the V code tile to FP16 (packed hardware converter) in the MN-major SW128 layout,
+//   warps 13-15 convert the V code tile to FP16 (packed hardware converter) in the MN-major SW128 layout,
 //               writing zeros for padding keys.
 // Every mbarrier wait is bounded by %globaltimer; on expiry the CTA flags FTKV_DEVERR_TIMEOUT, drains its
 // loads and MMAs, releases TMEM and leaves its outputs unspecified.  The named barriers of the producer
@@ -42,6 +41,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "decode_merge.cuh"
 #include "ftkv_device.cuh"
 #include "ftkv_internal.h"
 
@@ -50,10 +50,11 @@ namespace {
 
 constexpr int TK = 128;                                  // keys per tile
 constexpr int NS = 4;                                    // stages of the load ring
-constexpr int SLOT_CAP = 2048;                           // slot indices staged per window
-constexpr int NPROD = 4, NSOFT = 8, NCONV = 4;           // warps per role
+constexpr int SLOT_CAP = 2048;                           // slot indices per window (two windows staged)
+constexpr int NPROD = 4, NSOFT = 8, NCONV = 3;           // warps per role
 constexpr int W_MMA = NPROD, W_SOFT = NPROD + 1, W_CONV = W_SOFT + NSOFT;
-constexpr int NTHREADS = 32 * (W_CONV + NCONV);          // 544
+constexpr int NTHREADS = 32 * (W_CONV + NCONV);          // 512: four warps per scheduler, 128 registers
+constexpr int GATHERS = TK / 4;                          // K gather groups (4 rows) per tile
 constexpr uint32_t CODE_TILE = TK * 128;                 // 16 KB of E4M3 codes
 constexpr uint32_t STAGE = 2 * CODE_TILE + 2 * TK * 4;   // K codes, V codes, K scales, V scales
 constexpr uint32_t VH_TILE = TK * 128 * 2;               // 32 KB FP16 V: two 64-d column atoms of 16 KB
@@ -65,7 +66,7 @@ constexpr uint32_t OFF_VH = OFF_STAGE + NS * STAGE;
 constexpr uint32_t OFF_P = OFF_VH + VH_TILE;
 constexpr uint32_t OFF_QP = OFF_P + 2 * P_TILE;
 constexpr uint32_t OFF_SLOT = OFF_QP + QP_BYTES;
-constexpr uint32_t OFF_XA = OFF_SLOT + SLOT_CAP * 4;     // int [2][4 quarters][8 heads]: tile maxima
+constexpr uint32_t OFF_XA = OFF_SLOT + 2 * SLOT_CAP * 4; // int [2][4 quarters][8 heads]: tile maxima
 constexpr uint32_t OFF_SCL = OFF_XA + 2 * 4 * 8 * 4;     // float [2][8 blocks][8 heads]: block factors 2^E
 constexpr uint32_t OFF_FLAG = OFF_SCL + 2 * 8 * 8 * 4;   // int [2][8] votes, int [8] final vote
 constexpr uint32_t OFF_FQ = OFF_FLAG + 128;              // float [8]: query multipliers
@@ -79,7 +80,7 @@ static_assert(STAGE % 1024 == 0 && OFF_VH % 1024 == 0 && OFF_P % 1024 == 0 && OF
 static_assert(OFF_SCL % 16 == 0 && OFF_XA % 16 == 0 && OFF_LRED % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 static_assert(SMEM_ALLOC <= 232448, "decode_tc shared memory");
 
-constexpr int B_FULL = 0;              // [NS] 4 expect_tx arrivals + 128 cp.async arrivals (producers)
+constexpr int B_FULL = 0;              // [NS] NPROD arrivals + the gathered bytes
 // Consumer groups arrive once per warp (lane 0, after __syncwarp): counts are in warps.
 constexpr int B_EMPTY = NS;            // [NS] 4 converter + 8 softmax warps
 constexpr int B_QREADY = 2 * NS;       //      8: query pieces written, P' cleared
@@ -92,7 +93,7 @@ constexpr int B_DFULL = 2 * NS + 9;    // [2]  1: PV committed
 constexpr int B_DFREE = 2 * NS + 11;   // [2]  8: D folded
 constexpr int B_DRAIN = 2 * NS + 13;   //      1: every MMA finished
 static_assert(B_DRAIN < NBAR, "barrier count");
-constexpr int FULL_COUNT = NPROD + 32 * NPROD;
+constexpr int FULL_COUNT = NPROD;       // one arrival per producer warp (after its scale stores)
 constexpr int BAR_SOFT = 1, BAR_PROD = 2;  // named barriers (0 is __syncthreads)
 
 constexpr uint32_t TMEM_COLS = 256;    // S0 [0,16) S1 [16,32) D0 [64,128) D1 [128,192)
@@ -109,6 +110,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -248,7 +252,9 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const DecodeArgs a) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -351,20 +357,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + OFF_MISC);
 
   if (warp < NPROD) {
-    // ======================= producers: TMA gathers of K, cp.async of V and the scales =======================
-    const int pt = threadIdx.x;  // 0..127: the key whose scales this thread copies
-    const int vc = pt & 7, vr = pt >> 3;  // V: 16-byte chunk vc of rows vr, vr + 16, ..., vr + 112
+    // ======================= producers: TMA gathers of K and V, scales through registers =====================
+    const int pt = threadIdx.x;  // 0 .. 32 NPROD - 1
     const uint32_t sslot = base + OFF_SLOT;
     const int32_t* sslot_p = reinterpret_cast<const int32_t*>(gbase + OFF_SLOT);
     const int32_t* req = a.req_to_slot + static_cast<int64_t>(b) * a.req_stride + j0;
     auto row_of = [&](int key) -> int {  // pool row of key (relative to the slice); bad slots read slot 0
-      int32_t slot = sslot_p[key % SLOT_CAP];
+      int32_t slot = sslot_p[key % (2 * SLOT_CAP)];
       if (slot < 0 || slot >= a.num_rows) {
         flag_error(a.err, kDevErrBadSlot);
         slot = 0;
       }
       return static_cast<int>(static_cast<int64_t>(slot) * a.num_kv_heads + h);
     };
+    // the scales of keys r = pt, pt + 32 NPROD, ... of a tile, loaded one tile ahead into registers
+    constexpr int SPT = (TK + 32 * NPROD - 1) / (32 * NPROD);
+    float ksn[SPT], vsn[SPT];
+    auto load_scales = [&](int i) {
+#pragma unroll
+      for (int u = 0; u < SPT; u++) {
+        const int r = pt + u * 32 * NPROD;
+        ksn[u] = 0.0f;
+        vsn[u] = 0.0f;
+        if (r < TK && i * TK + r < nkeys) {
+          const int row = row_of(i * TK + r);
+          ksn[u] = __ldg(a.k_scales + row);
+          vsn[u] = __ldg(a.v_scales + row);
+        }
+      }
+    };
+    cp_async_wait_all();  // the first window of slot indices, requested at entry
+    named_bar_sync(BAR_PROD, 32 * NPROD);
+    load_scales(0);
     int issued = 0;
     for (int i = 0; i < nT; i++) {
       const int s = i % NS;
@@ -372,18 +396,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool w = true;
       if (i >= NS) w = mbar_wait(bar(B_EMPTY + s), ((i / NS) - 1) & 1, abort_flag, a.err);
       if (!named_bar_and(BAR_PROD, 32 * NPROD, w)) break;  // also: every producer is done with the last tile
-      if (key0 % SLOT_CAP == 0) {  // stage the next window of slot indices (the first is already on its way)
-        if (key0 > 0) {
-          const int wn = (nkeys - key0 < SLOT_CAP) ? nkeys - key0 : SLOT_CAP;
-          for (int k = pt; k < wn; k += 32 * NPROD) cp_async_4(sslot + 4 * k, req + key0 + k);
-        }
+      // The next tile starts a new window of slot indices: stage it in the other half of the double window
+      // (that half's last reads were a whole window ago, before the barriers above).
+      if ((key0 + TK) % SLOT_CAP == 0 && key0 + TK < nkeys) {
+        const int k1 = key0 + TK;
+        const int wn = (nkeys - k1 < SLOT_CAP) ? nkeys - k1 : SLOT_CAP;
+        for (int k = pt; k < wn; k += 32 * NPROD) cp_async_4(sslot + 4 * ((k1 + k) % (2 * SLOT_CAP)), req + k1 + k);
         cp_async_wait_all();
         named_bar_sync(BAR_PROD, 32 * NPROD);
       }
-      if (lane == 0) mbar_expect_tx(bar(B_FULL + s), CODE_TILE / NPROD);
+      // Gather groups g = warp + NPROD * lane (keys 4g .. 4g+3 of the tile), spread over the warps.  The bytes
+      // are announced first and the gathers issued at once; the warp's arrival comes after its scale stores.
+      if (lane == 0) mbar_expect_tx_only(bar(B_FULL + s), 2u * 512u * ((GATHERS - warp + NPROD - 1) / NPROD));
       __syncwarp();
-      if (lane < 32 / NPROD) {  // gather group g: keys 4g .. 4g+3 of the tile
-        const int g = warp * (32 / NPROD) + lane;
+      if (warp + NPROD * lane < GATHERS) {
+        const int g = warp + NPROD * lane;
         int rows[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) {
@@ -391,25 +418,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           rows[e] = (key < nkeys) ? row_of(key) : h;  // padding key: (slot 0, head h)
         }
         tma_gather4(stage_k(s) + g * 512, &tmk, bar(B_FULL + s), rows[0], rows[1], rows[2], rows[3]);
+        tma_gather4(stage_v(s) + g * 512, &tmv, bar(B_FULL + s), rows[0], rows[1], rows[2], rows[3]);
       }
+      // this tile's scales (loaded one iteration ago) into the stage, then the next tile's into registers
 #pragma unroll
-      for (int j = 0; j < TK / 16; j++) {
-        const int r = vr + 16 * j;
-        if (key0 + r < nkeys)
-          cp_async_16(stage_v(s) + sw128(r, vc), a.v_codes + static_cast<int64_t>(row_of(key0 + r)) * kHeadDim + vc * 16);
+      for (int u = 0; u < SPT; u++) {
+        const int r = pt + u * 32 * NPROD;
+        if (r < TK) {
+          st_shared_u32(stage_ks(s) + r * 4, __float_as_uint(ksn[u]));
+          st_shared_u32(stage_vs(s) + r * 4, __float_as_uint(vsn[u]));
+        }
       }
-      if (key0 + pt < nkeys) {
-        const int row = row_of(key0 + pt);
-        cp_async_4(stage_ks(s) + pt * 4, a.k_scales + row);
-        cp_async_4(stage_vs(s) + pt * 4, a.v_scales + row);
-      }
-      cp_async_arrive_noinc(bar(B_FULL + s));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_FULL + s));
+      if (i + 1 < nT) load_scales(i + 1);
       issued = i + 1;
     }
     // every load issued must land before the CTA may exit
     for (int i = (issued > NS ? issued - NS : 0); i < issued; i++)
       mbar_wait(bar(B_FULL + i % NS), (i / NS) & 1, abort_flag, a.err, false);
-    cp_async_wait_all();
   } else if (warp == W_MMA) {
     if (lane == 0) {
       // ======================= MMA issuer =======================
@@ -461,12 +488,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp >= W_CONV) {
     // ======================= V converter: E4M3 codes -> FP16, MN-major SW128 =======================
-    const int t = threadIdx.x - 32 * W_CONV;  // key row
+    const int ct = threadIdx.x - 32 * W_CONV;  // key rows ct, ct + 32 NCONV, ...
     for (int i = 0; i < nT; i++) {
       const int s = i % NS;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FULL + s), (i / NS) & 1, abort_flag, a.err))) break;
       if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar(B_VHFREE), (i - 1) & 1, abort_flag, a.err))) break;
       const uint32_t src = stage_v(s), dst = base + OFF_VH;
+      for (int t = ct; t < TK; t += 32 * NCONV) {
       const uint32_t keep = (i * TK + t < nkeys) ? 0xFFFFFFFFu : 0u;  // padding keys: V row of zeros
 #pragma unroll
       for (int c = 0; c < 8; c++) {
@@ -486,6 +514,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                        "r"(hv[4 * hh + 2]), "r"(hv[4 * hh + 3])
                        : "memory");
         }
+      }
       }
       fence_proxy_async();
       __syncwarp();
@@ -745,82 +774,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // The slices' partials of this (request, KV head): weights from (m, l), then O = sum_sl w_sl O_sl.  When
-  // they fit, all partial accumulators are first copied into the idle ring with one round of cp.async.
-  const int64_t pbase = (row0 * a.num_q_heads + h * G) * a.num_splits;  // partial row of (g = 0, slice 0)
-  const bool in_smem = static_cast<uint32_t>(G * nslices) * (kHeadDim * 4 + 8) <= OFF_SLOT;
-  float* pacc = reinterpret_cast<float*>(gbase);  // [G][nslices][128] when in_smem
-  float* wts = in_smem ? pacc + G * nslices * kHeadDim : reinterpret_cast<float*>(gbase);  // [2][G][nslices]
-  if (in_smem) {
-    for (int idx = threadIdx.x; idx < G * nslices * (kHeadDim / 4); idx += blockDim.x) {
-      const int gs = idx / (kHeadDim / 4), d4 = idx % (kHeadDim / 4);  // gs = g * nslices + sl
-      const int g = gs / nslices, sl = gs % nslices;
-      cp_async_16(base + 16u * idx, a.part_acc + (pbase + static_cast<int64_t>(g) * a.num_splits + sl) * kHeadDim + 4 * d4);
-    }
-  }
-  for (int i = threadIdx.x; i < G * nslices; i += blockDim.x) {
-    const int g = i / nslices, sl = i % nslices;
-    const int64_t prow = pbase + static_cast<int64_t>(g) * a.num_splits + sl;
-    wts[i] = __ldcg(a.part_ml + prow * 2);
-    wts[G * nslices + i] = __ldcg(a.part_ml + prow * 2 + 1);
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  for (int g = threadIdx.x; g < G; g += blockDim.x) {
-    float* wm = wts + g * nslices;
-    const float* wl = wts + G * nslices + g * nslices;
-    float M = -INFINITY;
-    for (int sl = 0; sl < nslices; sl++) M = fmaxf(M, wm[sl]);
-    float L = 0.0f;
-    if (M != -INFINITY)
-      for (int sl = 0; sl < nslices; sl++) L += exp2f(wm[sl] - M) * wl[sl];
-    const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
-    for (int sl = 0; sl < nslices; sl++) wm[sl] = (invL != 0.0f) ? exp2f(wm[sl] - M) * invL : 0.0f;
-  }
-  __syncthreads();
-  for (int it = threadIdx.x; it < G * (kHeadDim / 4); it += blockDim.x) {
-    const int d4 = it % (kHeadDim / 4), g = it / (kHeadDim / 4);
-    const float* wm = wts + g * nslices;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (in_smem) {
-      const float4* src = reinterpret_cast<const float4*>(pacc + static_cast<int64_t>(g) * nslices * kHeadDim) + d4;
-      for (int sl = 0; sl < nslices; sl++) {
-        const float4 v = src[sl * (kHeadDim / 4)];
-        const float wv = wm[sl];
-        o.x += wv * v.x;
-        o.y += wv * v.y;
-        o.z += wv * v.z;
-        o.w += wv * v.w;
-      }
-    } else {
-      const float4* src =
-          reinterpret_cast<const float4*>(a.part_acc + (pbase + static_cast<int64_t>(g) * a.num_splits) * kHeadDim) + d4;
-      int sl = 0;
-      for (; sl + 8 <= nslices; sl += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; u++) v[u] = __ldcg(src + static_cast<int64_t>(sl + u) * (kHeadDim / 4));
-#pragma unroll
-        for (int u = 0; u < 8; u++) {
-          const float wv = wm[sl + u];
-          o.x += wv * v[u].x;
-          o.y += wv * v[u].y;
-          o.z += wv * v[u].z;
-          o.w += wv * v[u].w;
-        }
-      }
-      for (; sl < nslices; sl++) {
-        const float4 v = __ldcg(src + static_cast<int64_t>(sl) * (kHeadDim / 4));
-        const float wv = wm[sl];
-        o.x += wv * v.x;
-        o.y += wv * v.y;
-        o.z += wv * v.z;
-        o.w += wv * v.w;
-      }
-    }
-    const uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
-    *reinterpret_cast<uint2*>(a.out + (row0 * a.num_q_heads + h * G + g) * kHeadDim + 4 * d4) = packed;
-  }
+  merge_split_partials(a, row0, 1, h, nslices, gbase);  // the load ring is idle now
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -864,11 +818,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   }
   const int64_t rows = a.num_rows * a.num_kv_heads;  // gather row coordinates are int32
   if (rows >= (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-  CUtensorMap tmk;
-  if (!make_row_map(&tmk, a.k_codes, rows)) return cudaErrorInvalidValue;
+  CUtensorMap tmk, tmv;
+  if (!make_row_map(&tmk, a.k_codes, rows) || !make_row_map(&tmv, a.v_codes, rows)) return cudaErrorInvalidValue;
   dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-  decode_tc_kernel<<<grid, NTHREADS, SMEM_ALLOC, s>>>(tmk, a);
-  return cudaGetLastError();
+  return launch_k(decode_tc_kernel, grid, dim3(NTHREADS), SMEM_ALLOC, s, tmk, tmv, a);
 }
 
 }  // namespace ftkv

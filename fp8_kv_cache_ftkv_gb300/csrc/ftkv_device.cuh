@@ -145,6 +145,15 @@ __device__ __forceinline__ uint4 ldg_stream16(const void* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 
+// Programmatic dependent launch.  Every kernel of this library is launched with programmatic stream
+// serialization: the next kernel in the stream may be scheduled onto SMs this one has released while it
+// drains.  Each kernel first allows its dependents to launch, then waits for its predecessor's completion
+// and memory before touching global memory, so every result keeps plain stream order.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_error(int* err, int bits) {
   if (err) atomicOr(err, bits);
 }

@@ -79,6 +79,23 @@ struct PrefillArgs {
   int* err;
 };
 
+// Launch with programmatic stream serialization (see pdl_enter in ftkv_device.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_store_quant(const StoreArgs& a, cudaStream_t s);
 cudaError_t launch_reconstruct(const ReconstructArgs& a, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* c, int64_t n, int num_sms, cudaStream_t s);

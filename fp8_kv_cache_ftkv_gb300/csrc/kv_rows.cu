@@ -23,6 +23,7 @@ namespace ftkv {
 constexpr int STORE_UNITS = 2;
 
 __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
+  pdl_enter();
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;   // 0: K, 1: V
@@ -98,6 +99,7 @@ __device__ __forceinline__ void expand16(const uint4& c, float s, uint4& o0, uin
 }
 
 __global__ void __launch_bounds__(256) reconstruct_kernel(ReconstructArgs a) {
+  pdl_enter();
   const int64_t group = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;
   const int l = threadIdx.x & 7;
   const int64_t total = a.num_prefix * a.num_kv_heads;
@@ -141,12 +143,14 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(ReconstructArgs a) {
 // Bare codec (same device conversions as above), one element per thread, no alignment needed.
 // ---------------------------------------------------------------------------------------------
 __global__ void e4m3_encode_kernel(const float* __restrict__ x, uint8_t* __restrict__ c, int64_t n) {
+  pdl_enter();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     c[i] = static_cast<uint8_t>(e4m3x2_encode(x[i], 0.0f) & 0xFFu);
 }
 
 __global__ void e4m3_decode_kernel(const uint8_t* __restrict__ c, float* __restrict__ x, int64_t n) {
+  pdl_enter();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     x[i] = f16x2_to_float2(e4m3x2_to_f16x2(c[i])).x;
@@ -156,29 +160,25 @@ __global__ void e4m3_decode_kernel(const uint8_t* __restrict__ c, float* __restr
 cudaError_t launch_store_quant(const StoreArgs& a, cudaStream_t s) {
   const int64_t warps = (a.num_tokens * a.num_kv_heads + STORE_UNITS - 1) / STORE_UNITS;
   const int64_t blocks = (warps * 32 + 255) / 256;
-  store_quant_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(store_quant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_reconstruct(const ReconstructArgs& a, cudaStream_t s) {
   const int64_t groups = (a.num_prefix * a.num_kv_heads + RECON_UNITS - 1) / RECON_UNITS;
   const int64_t blocks = (groups * 8 + 255) / 256;
-  reconstruct_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(reconstruct_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* c, int64_t n, int num_sms, cudaStream_t s) {
   int64_t blocks = (n + 255) / 256;
   if (blocks > static_cast<int64_t>(num_sms) * 32) blocks = static_cast<int64_t>(num_sms) * 32;
-  e4m3_encode_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(x, c, n);
-  return cudaGetLastError();
+  return launch_k(e4m3_encode_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, x, c, n);
 }
 
 cudaError_t launch_e4m3_decode(const uint8_t* c, float* x, int64_t n, int num_sms, cudaStream_t s) {
   int64_t blocks = (n + 255) / 256;
   if (blocks > static_cast<int64_t>(num_sms) * 32) blocks = static_cast<int64_t>(num_sms) * 32;
-  e4m3_decode_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(c, x, n);
-  return cudaGetLastError();
+  return launch_k(e4m3_decode_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, c, x, n);
 }
 
 }  // namespace ftkv

@@ -49,6 +49,7 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const uint16_t* base, in
 }
 
 __global__ void __launch_bounds__(128) prefill_mma_kernel(const PrefillArgs a) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sQ = smem_addr(smem);
   const uint32_t sKV = sQ + BM * ROWB;  // stage s: K at sKV + s*2*TILE, V at + TILE
@@ -220,8 +221,7 @@ cudaError_t launch_prefill_mma(const PrefillArgs& a, cudaStream_t s) {
     configured[dev] = true;
   }
   dim3 grid(static_cast<unsigned>((a.chunk_len + BM - 1) / BM), a.num_q_heads);
-  prefill_mma_kernel<<<grid, 128, SMEM, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(prefill_mma_kernel, grid, dim3(128), SMEM, s, a);
 }
 
 }  // namespace ftkv

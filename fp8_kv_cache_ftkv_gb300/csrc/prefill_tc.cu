@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(192, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkc,
                       const __grid_constant__ CUtensorMap tvc, const __grid_constant__ CUtensorMap twk,
                       const __grid_constant__ CUtensorMap twv, const TcArgs a) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -472,8 +473,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   t.out = a.out;
   t.err = a.err;
   dim3 grid(t.n_q_tiles, a.num_q_heads);
-  prefill_tc_kernel<<<grid, 192, SMEM_ALLOC, s>>>(tq, tkc, tvc, twk, twv, t);
-  return cudaGetLastError();
+  return launch_k(prefill_tc_kernel, grid, dim3(192), SMEM_ALLOC, s, tq, tkc, tvc, twk, twv, t);
 }
 
 }  // namespace ftkv
