@@ -51,8 +51,8 @@ def parse_args():
     p.add_argument("--pool-rows", type=int, default=33059)
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--num-splits", type=int, default=0)
-    p.add_argument("--decode-impl", choices=["auto", "mma"], default="auto",
-                   help="auto: tcgen05 kernel for the single-row decode; mma: the warp-level mma.sync kernel")
+    p.add_argument("--decode-impl", choices=["mma", "tc"], default="mma",
+                   help="mma: the warp-level kernel (ftkv_decode_attn); tc: the tcgen05 kernel (ftkv_decode_attn_tc)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-layers", type=int, default=2)
     return p.parse_args()
@@ -333,11 +333,12 @@ def run_ours(args, world, rank, local):
                 durs += [a.elapsed_time(b) for a, b in evs]
     dur_ms = statistics.mean(durs)
     achieved = kernel_bytes / (dur_ms * 1e-3) / 1e9
-    if args.decode_impl == "auto":
+    if args.decode_impl == "tc":
         kname, prof, ksrc = "decode_tc_kernel", "decode_tc_32k.md", "decode_tc.cu"
     else:
         kname, prof, ksrc = "decode_split_kernel<1>", "decode_split_32k.md", "decode.cu"
     traffic = profiled_traffic(prof, [f"fp8_kv_cache_ftkv_gb300/csrc/{ksrc}",
+                                      "fp8_kv_cache_ftkv_gb300/csrc/decode_merge.cuh",
                                       "fp8_kv_cache_ftkv_gb300/csrc/ftkv_device.cuh"])
 
     # ---- e2e through the public API with pinned host buffers ----

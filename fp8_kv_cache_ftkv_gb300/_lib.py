@@ -31,7 +31,7 @@ EXPORTS = (
     "ftkv_store_quant", "ftkv_reconstruct_bf16", "ftkv_decode_workspace_bytes", "ftkv_decode_auto_splits",
     "ftkv_decode_attn", "ftkv_prefill_attn", "ftkv_prefill_attn_mma", "ftkv_e4m3_encode_f32",
     "ftkv_e4m3_decode_f32", "ftkv_pool_bytes", "ftkv_device_errors", "ftkv_status_str",
-    "ftkv_last_cuda_error", "ftkv_abi_version", "ftkv_decode_attn_noalloc", "ftkv_decode_attn_mma",
+    "ftkv_last_cuda_error", "ftkv_abi_version", "ftkv_decode_attn_noalloc", "ftkv_decode_attn_tc",
 )
 
 
@@ -73,8 +73,8 @@ def load() -> ctypes.CDLL:
             "ftkv_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I64, I32]),
             "ftkv_decode_auto_splits": (I32, [I32, I32, I64, I32]),
             "ftkv_decode_attn": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P, SZ, P, P]),
-            "ftkv_decode_attn_mma": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P, SZ, P,
-                                                    P]),
+            "ftkv_decode_attn_tc": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P, SZ, P,
+                                                   P]),
             "ftkv_decode_attn_noalloc": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P,
                                                         P]),
             "ftkv_prefill_attn": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),

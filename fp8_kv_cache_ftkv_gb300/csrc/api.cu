@@ -172,7 +172,7 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
                          int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                          int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
                          int32_t num_splits, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream,
-                         bool force_mma) {
+                         bool use_tc) {
   int st = check_pool(pool);
   if (st != FTKV_OK) return st;
   if ((st = check_heads(num_q_heads, pool->num_kv_heads)) != FTKV_OK) return st;
@@ -232,7 +232,7 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   a.counters = counters;
   a.out = out;
   a.err = di->err_word;
-  a.force_mma = force_mma ? 1 : 0;
+  a.use_tc = use_tc ? 1 : 0;
   cudaError_t e = ftkv::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FTKV_OK : cuda_fail(e);
 }
@@ -245,10 +245,11 @@ int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t*
                        max_q_rows, max_seq_len, sm_scale, num_splits, workspace, workspace_bytes, out, stream, false);
 }
 
-int ftkv_decode_attn_mma(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
-                         int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
-                         int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                         int32_t num_splits, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
+int ftkv_decode_attn_tc(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
+                        int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
+                        int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
+                        int32_t num_splits, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
+  if (max_q_rows != 1) return FTKV_ERR_UNSUPPORTED;
   return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
                        max_q_rows, max_seq_len, sm_scale, num_splits, workspace, workspace_bytes, out, stream, true);
 }

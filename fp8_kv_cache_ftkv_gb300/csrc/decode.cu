@@ -517,9 +517,9 @@ int decode_ctas_per_sm(int max_q_rows) {
   return 1;  // both configurations are shared-memory bound at one CTA per SM
 }
 
-// Single-row batches go to the tcgen05 kernel (decode_tc.cu) unless the caller asks for this one.
+// The tcgen05 kernel (decode_tc.cu) when asked for (single-row batches), else this warp-level kernel.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  if (a.max_q_rows <= 1 && !a.force_mma) return launch_decode_tc(a, s);
+  if (a.use_tc && a.max_q_rows <= 1) return launch_decode_tc(a, s);
   return (a.max_q_rows <= 1) ? launch_split<1>(a, s) : launch_split<2>(a, s);
 }
 

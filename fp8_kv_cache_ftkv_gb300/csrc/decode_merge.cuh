@@ -41,6 +41,16 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
     return ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * a.num_splits;
   };
   float* wts = reinterpret_cast<float*>(buf);  // [2][npairs][nslices]: m then l, m replaced by the weights
+  // Output: item (pair, 4 d values) split over 2 adjacent lanes, each summing every other slice with up to 16
+  // loads in flight; the two halves meet through one shuffle.  npairs * 64 and blockDim.x are multiples
+  // of 32, so every warp is either fully inside the range or fully outside it.  (Loading the first batch
+  // before the weights overlapped one round trip but made both kernels spill: slower overall.)
+  constexpr int SPLIT = 2, BATCH = 16;
+  const int total = npairs * (kHeadDim / 4) * SPLIT;
+  auto acc_src = [&](int it) {
+    const int item = it / SPLIT, d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);
+    return reinterpret_cast<const float4*>(a.part_acc + prow0(pr) * kHeadDim) + d4;
+  };
   for (int i = threadIdx.x; i < npairs * nslices; i += blockDim.x) {
     const int pr = i / nslices, sl = i % nslices;
     const int64_t p = prow0(pr) + sl;
@@ -51,15 +61,11 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
   for (int pr = warp; pr < npairs; pr += nwarps)
     merge_weights_warp(wts + pr * nslices, wts + npairs * nslices + pr * nslices, nslices, lane);
   __syncthreads();
-  // Output: item (pair, 4 d values) split over 2 adjacent lanes, each summing every other slice with up to 16
-  // loads in flight; the two halves meet through one shuffle.  npairs * 64 and blockDim.x are multiples
-  // of 32, so every warp is either fully inside the range or fully outside it.
-  constexpr int SPLIT = 2, BATCH = 16;
-  for (int it = threadIdx.x; it < npairs * (kHeadDim / 4) * SPLIT; it += blockDim.x) {
+  for (int it = threadIdx.x; it < total; it += blockDim.x) {
     const int part = it % SPLIT, item = it / SPLIT;
     const int d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);
     const float* wm = wts + pr * nslices;
-    const float4* src = reinterpret_cast<const float4*>(a.part_acc + prow0(pr) * kHeadDim) + d4;
+    const float4* src = acc_src(it);
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = part; s0 < nslices; s0 += SPLIT * BATCH) {
       float4 v[BATCH];

@@ -72,7 +72,7 @@ constexpr uint32_t OFF_FLAG = OFF_SCL + 2 * 8 * 8 * 4;   // int [2][8] votes, in
 constexpr uint32_t OFF_FQ = OFF_FLAG + 128;              // float [8]: query multipliers
 constexpr uint32_t OFF_LRED = OFF_FQ + 32;               // float [4 quarters][8 heads]: row sums
 constexpr uint32_t OFF_BAR = OFF_LRED + 128;
-constexpr int NBAR = 2 * NS + 14;
+constexpr int NBAR = 3 * NS + 14;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;        // TMEM base address, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;        // slack to align the base to 1024 B
@@ -80,7 +80,7 @@ static_assert(STAGE % 1024 == 0 && OFF_VH % 1024 == 0 && OFF_P % 1024 == 0 && OF
 static_assert(OFF_SCL % 16 == 0 && OFF_XA % 16 == 0 && OFF_LRED % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 static_assert(SMEM_ALLOC <= 232448, "decode_tc shared memory");
 
-constexpr int B_FULL = 0;              // [NS] NPROD arrivals + the gathered bytes
+constexpr int B_FULL = 0;              // [NS] K codes and scales: NPROD arrivals + the gathered K bytes
 // Consumer groups arrive once per warp (lane 0, after __syncwarp): counts are in warps.
 constexpr int B_EMPTY = NS;            // [NS] 4 converter + 8 softmax warps
 constexpr int B_QREADY = 2 * NS;       //      8: query pieces written, P' cleared
@@ -92,7 +92,8 @@ constexpr int B_PFULL = 2 * NS + 7;    // [2]  8: P' written
 constexpr int B_DFULL = 2 * NS + 9;    // [2]  1: PV committed
 constexpr int B_DFREE = 2 * NS + 11;   // [2]  8: D folded
 constexpr int B_DRAIN = 2 * NS + 13;   //      1: every MMA finished
-static_assert(B_DRAIN < NBAR, "barrier count");
+constexpr int B_FULLV = 2 * NS + 14;   // [NS] V codes: NPROD arrivals + the gathered V bytes
+static_assert(B_DRAIN < B_FULLV && B_FULLV + NS <= NBAR, "barrier count");
 constexpr int FULL_COUNT = NPROD;       // one arrival per producer warp (after its scale stores)
 constexpr int BAR_SOFT = 1, BAR_PROD = 2;  // named barriers (0 is __syncthreads)
 
@@ -329,6 +330,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; s++) {
       mbar_init(bar(B_FULL + s), FULL_COUNT);
+      mbar_init(bar(B_FULLV + s), FULL_COUNT);
       mbar_init(bar(B_EMPTY + s), NCONV + NSOFT);
     }
     mbar_init(bar(B_QREADY), NSOFT);
@@ -405,21 +407,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         cp_async_wait_all();
         named_bar_sync(BAR_PROD, 32 * NPROD);
       }
-      // Gather groups g = warp + NPROD * lane (keys 4g .. 4g+3 of the tile), spread over the warps.  The bytes
-      // are announced first and the gathers issued at once; the warp's arrival comes after its scale stores.
-      if (lane == 0) mbar_expect_tx_only(bar(B_FULL + s), 2u * 512u * ((GATHERS - warp + NPROD - 1) / NPROD));
-      __syncwarp();
-      if (warp + NPROD * lane < GATHERS) {
-        const int g = warp + NPROD * lane;
-        int rows[4];
+      // Gather groups g = warp + NPROD * lane (keys 4g .. 4g+3 of the tile), spread over the warps.  K first,
+      // on its own barrier, so QK and the softmax can start while the V rows are still on their way; the
+      // bytes are announced before the gathers, and the K barrier's arrival waits for the scale stores.
+      const uint32_t gbytes = 512u * ((GATHERS - warp + NPROD - 1) / NPROD);
+      const bool has_group = warp + NPROD * lane < GATHERS;
+      const int g = warp + NPROD * lane;
+      int rows[4];
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const int key = key0 + 4 * g + e;
-          rows[e] = (key < nkeys) ? row_of(key) : h;  // padding key: (slot 0, head h)
-        }
-        tma_gather4(stage_k(s) + g * 512, &tmk, bar(B_FULL + s), rows[0], rows[1], rows[2], rows[3]);
-        tma_gather4(stage_v(s) + g * 512, &tmv, bar(B_FULL + s), rows[0], rows[1], rows[2], rows[3]);
+      for (int e = 0; e < 4; e++) {
+        const int key = key0 + 4 * g + e;
+        rows[e] = (has_group && key < nkeys) ? row_of(key) : h;  // padding key: (slot 0, head h)
       }
+      if (lane == 0) mbar_expect_tx_only(bar(B_FULL + s), gbytes);
+      __syncwarp();
+      if (has_group) tma_gather4(stage_k(s) + g * 512, &tmk, bar(B_FULL + s), rows[0], rows[1], rows[2], rows[3]);
+      if (lane == 0) mbar_expect_tx(bar(B_FULLV + s), gbytes);
+      __syncwarp();
+      if (has_group) tma_gather4(stage_v(s) + g * 512, &tmv, bar(B_FULLV + s), rows[0], rows[1], rows[2], rows[3]);
       // this tile's scales (loaded one iteration ago) into the stage, then the next tile's into registers
 #pragma unroll
       for (int u = 0; u < SPT; u++) {
@@ -435,8 +440,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       issued = i + 1;
     }
     // every load issued must land before the CTA may exit
-    for (int i = (issued > NS ? issued - NS : 0); i < issued; i++)
+    for (int i = (issued > NS ? issued - NS : 0); i < issued; i++) {
       mbar_wait(bar(B_FULL + i % NS), (i / NS) & 1, abort_flag, a.err, false);
+      mbar_wait(bar(B_FULLV + i % NS), (i / NS) & 1, abort_flag, a.err, false);
+    }
   } else if (warp == W_MMA) {
     if (lane == 0) {
       // ======================= MMA issuer =======================
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int ct = threadIdx.x - 32 * W_CONV;  // key rows ct, ct + 32 NCONV, ...
     for (int i = 0; i < nT; i++) {
       const int s = i % NS;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FULL + s), (i / NS) & 1, abort_flag, a.err))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FULLV + s), (i / NS) & 1, abort_flag, a.err))) break;
       if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar(B_VHFREE), (i - 1) & 1, abort_flag, a.err))) break;
       const uint32_t src = stage_v(s), dst = base + OFF_VH;
       for (int t = ct; t < TK; t += 32 * NCONV) {

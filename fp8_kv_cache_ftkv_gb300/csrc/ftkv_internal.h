@@ -61,7 +61,7 @@ struct DecodeArgs {
   int* counters;             // [batch][Hkv] arrival tickets; zero between calls
   uint16_t* out;             // [total_q_rows][Hq][128]
   int* err;
-  int force_mma;             // 1: the warp-level mma.sync kernel even for single-row batches
+  int use_tc;                // 1: the tcgen05 kernel (single-row batches only)
 };
 
 struct PrefillArgs {

@@ -130,11 +130,10 @@ class DecodePlan:
 def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,
                 q_row_offsets: torch.Tensor = None, *, max_seq_len: int, max_q_rows: int = 1,
                 sm_scale: float = HEAD_DIM ** -0.5, num_splits: int = 0, plan: DecodePlan = None,
-                out: torch.Tensor = None, impl: str = "auto", stream=None) -> torch.Tensor:
+                out: torch.Tensor = None, impl: str = "mma", stream=None) -> torch.Tensor:
     """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, 128].
-    ``impl``: "auto" (tcgen05 kernel for single-row batches, warp-level kernel for multi-row ones) or
-    "mma" (the warp-level mma.sync kernel for every batch)."""
-    if impl not in ("auto", "mma"):
+    ``impl``: "mma" (the warp-level kernel, every batch) or "tc" (the tcgen05 kernel, single-row batches)."""
+    if impl not in ("mma", "tc"):
         raise ValueError(f"unknown decode impl {impl!r}")
     _req(q, torch.bfloat16, "q", 3)
     if req_to_slot.dim() == 1:
@@ -151,7 +150,7 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
         out = torch.empty_like(q)
     _req(out, torch.bfloat16, "out", 3)
     ps = pool.c_struct()
-    name = "ftkv_decode_attn" if impl == "auto" else "ftkv_decode_attn_mma"
+    name = "ftkv_decode_attn" if impl == "mma" else "ftkv_decode_attn_tc"
     check(getattr(_lib.load(), name)(
         ctypes.byref(ps), hq, _ptr(q), _ptr(req_to_slot), req_to_slot.shape[1], _ptr(seq_lens),
         _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale), plan.num_splits,

@@ -137,16 +137,17 @@ int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t*
                      int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
                      void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
-/* Same operation, arguments, layouts and errors as ftkv_decode_attn, always on the warp-level
- * mma.sync kernel.  ftkv_decode_attn runs batches with max_q_rows == 1 on the tcgen05 kernel (TMA
- * gathers of the code rows, E4M3 QK and FP16 PV on the tensor cores with TMEM accumulators) and
- * multi-row batches on the warp-level kernel; this entry point keeps the warp-level kernel reachable
- * for single-row batches too, as the comparison point.  Both use the same workspace layout. */
-int ftkv_decode_attn_mma(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
-                         const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens,
-                         const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
-                         int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
-                         void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
+/* Same operation, arguments, layouts, workspace and errors as ftkv_decode_attn, for single-row
+ * batches (max_q_rows must be 1, else FTKV_ERR_UNSUPPORTED), on the tcgen05 kernel: TMA gathers of
+ * the K and V code rows, QK on the stored E4M3 codes and PV in FP16 on the tensor cores with TMEM
+ * accumulators.  ftkv_decode_attn runs the warp-level mma.sync kernel, measured faster for this
+ * HBM-bound step at the 32K batch-1 shape (the tcgen05 kernel's loads are bound by the rate at which
+ * one SM's TMA unit issues 4-row gathers); this entry point keeps the tcgen05 kernel available. */
+int ftkv_decode_attn_tc(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
+                        const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens,
+                        const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
+                        int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
+                        void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Decode without any device allocation.  The pages describe no such entry point; it exists for

@@ -104,6 +104,16 @@ def test_decode_validation(lib):
     assert call(sm=float("nan")) == _lib.FTKV_ERR_INVALID
     assert call(B=0, total=0) == _lib.FTKV_OK                # nothing to do
 
+    def call_tc(**kw):
+        a = dict(base, **kw)
+        return lib.ftkv_decode_attn_tc(P(_pool()), 32, a["q"], a["r2s"], a["stride"], a["lens"], a["offs"], a["B"],
+                                       a["total"], a["mq"], a["maxlen"], a["sm"], a["splits"], a["ws"], a["wsb"],
+                                       a["out"], None)
+
+    assert call_tc(mq=2) == _lib.FTKV_ERR_UNSUPPORTED        # the tcgen05 kernel serves single-row batches
+    assert call_tc(q=0x1002) == _lib.FTKV_ERR_ALIGN
+    assert call_tc(B=0, total=0) == _lib.FTKV_OK
+
 
 def test_prefill_validation(lib):
     for fn in (lib.ftkv_prefill_attn, lib.ftkv_prefill_attn_mma):

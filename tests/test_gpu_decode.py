@@ -3,8 +3,8 @@
 Covers the 512-token single step, ragged key counts (1, 17, 513), split caps 1/8/64 and automatic,
 GQA group sizes 8/4/2/1, multi-row decode (1..8 rows, rows that see no key), the 32,768- and
 40,000-key batch-1 workloads at full size (sampled layers, every output element), and the batched
-64-request multi-row workload at full size.  Single-row cases run on both kernels: "auto" (the tcgen05
-kernel for single-row batches) and "mma" (the warp-level mma.sync kernel).
+64-request multi-row workload at full size.  Single-row cases run on both kernels: "mma" (the warp-level
+kernel behind ftkv_decode_attn) and "tc" (the tcgen05 kernel behind ftkv_decode_attn_tc).
 """
 import numpy as np
 import pytest
@@ -15,7 +15,7 @@ from fp8_kv_cache_ftkv_gb300 import inputs, ops
 from parity import bits_to_cuda_bf16, check_attention
 
 pytestmark = pytest.mark.gpu
-IMPLS = ["auto", "mma"]
+IMPLS = ["mma", "tc"]
 
 
 def _setup(wl: inputs.DecodeWorkload, layer: int = 0):
@@ -32,7 +32,7 @@ def _setup(wl: inputs.DecodeWorkload, layer: int = 0):
     return gp, op, L, dev
 
 
-def _run(wl, gp, dev, num_splits=0, max_q_rows=None, impl="auto"):
+def _run(wl, gp, dev, num_splits=0, max_q_rows=None, impl="mma"):
     R = np.diff(wl.q_row_offsets)
     mq = int(max(R.max(), 1)) if max_q_rows is None else max_q_rows
     return ops.decode_attn(gp, dev["q"], dev["r2s"], dev["lens"], dev["offs"], max_seq_len=int(wl.req_to_slot.shape[1]),
@@ -68,13 +68,15 @@ def test_decode_ragged_lengths_and_split_caps(n, splits, impl):
     _check(out, _ref(wl, op, L), f"n={n} splits={splits} impl={impl}")
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("n,splits", [(9000, 1), (20000, 3), (131, 1), (131, 2)])
-def test_decode_long_slices_cross_slot_windows(n, splits):
-    """Slices of thousands of keys (several 2,048-slot windows of the tcgen05 kernel's producer), a slice
-    whose last 128-key tile holds 3 keys, and slices shorter than one tile."""
+def test_decode_long_slices_cross_slot_windows(n, splits, impl):
+    """Slices of thousands of keys (several 2,048-slot windows of the tcgen05 kernel's producer; several
+    4,096-slot windows of the warp-level kernel), a slice whose last 128-key tile holds 3 keys, and
+    slices shorter than one tile."""
     wl = inputs.decode_custom([n], [1], n + 7, seed=n + splits)
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev, num_splits=splits)
+    out = _run(wl, gp, dev, num_splits=splits, impl=impl)
     _check(out, _ref(wl, op, L), f"n={n} splits={splits}")
     assert ops.device_errors() == 0
 
@@ -158,7 +160,7 @@ def test_decode_bad_slot_and_seq_len_are_flagged_not_faulted(impl):
     assert ops.device_errors() == 0
 
 
-@pytest.mark.parametrize("max_q_rows,impl", [(1, "auto"), (1, "mma"), (2, "auto")])
+@pytest.mark.parametrize("max_q_rows,impl", [(1, "mma"), (1, "tc"), (2, "mma")])
 def test_decode_dominant_key_with_small_v_scale(max_q_rows, impl):
     """A key holding almost all the probability has a V scale 1e6 x smaller than a key with tiny
     probability; both terms matter (ratio ~0.1) and the dominant one must keep full precision."""
