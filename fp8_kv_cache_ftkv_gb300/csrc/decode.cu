@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   if (!s_last) return;
   __threadfence();
 
-  merge_split_partials(a, row0, R, h, nslices, smem);  // the ring is idle now
+  merge_split_partials(a, row0, R, h, nslices, smem, WARPS * NSTAGE * STAGE_BYTES);  // the ring is idle now
 }
 
 template <int RPW>

@@ -5,14 +5,26 @@
 // sum l_s and unnormalized accumulator O_s,
 //     M = max_s m_s,   L = sum_s 2^(m_s - M) l_s,   o = sum_s (2^(m_s - M) / L) O_s      (o = 0 if L = 0).
 // The weights are computed by one warp per (row, head) with warp reductions (one thread walking all
-// slices three times was a serial tail of microseconds); the accumulators are read from L2 with up to 16
-// loads in flight per thread.  (Copying all partials into shared memory first with cp.async was slower.)
+// slices three times was a serial tail of microseconds).  The accumulators of one (row, head) are
+// contiguous over the slices, and so are their (m, l) pairs: when they fit in the CTA's idle shared
+// memory, both arrive by TMA bulk copies (two per (row, head)) in one round trip; otherwise they are read
+// from L2 with up to 16 loads in flight per thread.  (cp.async of every 16 bytes was slower.)
 #pragma once
 
 #include "ftkv_device.cuh"
 #include "ftkv_internal.h"
 
 namespace ftkv {
+
+__device__ __forceinline__ bool merge_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(100000u)
+      : "memory");
+  return ok != 0;
+}
 
 // w[s] = 2^(m[s] - M) / L for one (row, head), by one warp; wm holds m on entry and the weights on return.
 __device__ __forceinline__ void merge_weights_warp(float* wm, const float* wl, int nslices, int lane) {
@@ -33,24 +45,110 @@ __device__ __forceinline__ void merge_weights_warp(float* wm, const float* wl, i
 // Merge the partials of (request rows row0 .. row0 + nrows - 1, KV head h) into a.out.  buf: the CTA's shared
 // memory that is free at this point, at least 8 bytes per (row, head, slice).  Called by every thread.
 __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_t row0, int nrows, int h,
-                                                     int nslices, uint8_t* buf) {
+                                                     int nslices, uint8_t* buf, uint32_t buf_bytes) {
   const int G = a.group;
   const int npairs = nrows * G;  // pair pr = (row pr / G, head pr % G)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   auto prow0 = [&](int pr) -> int64_t {  // partial row of (pair pr, slice 0)
     return ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * a.num_splits;
   };
+  // Bulk path (even slice counts keep every copy a multiple of 16 bytes and 16-byte aligned): per (row, head), one copy
+  // of its nslices x 128 accumulators and one of its nslices (m, l) pairs, then the weights from shared
+  // memory with one exp2 per slice, then the weighted sums over all threads.
+  const uint32_t acc_bytes = static_cast<uint32_t>(npairs) * nslices * kHeadDim * 4;
+  const uint32_t ml_bytes = static_cast<uint32_t>(npairs) * nslices * 8;
+  // (m, l) copies start at part_ml + 8 prow0 bytes, prow0 a multiple of num_splits: 16-byte aligned when
+  // num_splits is even; the accumulator copies start at 512 prow0 bytes.
+  const bool bulk = (nslices % 2 == 0) && (a.num_splits % 2 == 0) && nslices <= 64 &&
+                    static_cast<uint64_t>(acc_bytes) + 2ull * ml_bytes + 16 <= buf_bytes;
+  if (bulk) {
+    float* pacc = reinterpret_cast<float*>(buf);                    // [npairs][nslices][128]
+    const float* pml = reinterpret_cast<const float*>(buf + acc_bytes);  // [npairs][nslices][2]
+    float* wgt = reinterpret_cast<float*>(buf + acc_bytes + ml_bytes);   // [npairs][nslices]
+    const uint32_t mbar = smem_addr(buf) + acc_bytes + 2 * ml_bytes;
+    // earlier generic accesses to the buffer come before the async proxy overwrites it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      // the other slices' partials were written by generic stores, released through the ticket
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(acc_bytes + ml_bytes)
+                   : "memory");
+      const uint32_t per = static_cast<uint32_t>(nslices) * kHeadDim * 4, per_ml = static_cast<uint32_t>(nslices) * 8;
+      for (int pr = 0; pr < npairs; pr++) {
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                smem_addr(buf) + pr * per),
+            "l"(a.part_acc + prow0(pr) * kHeadDim), "r"(per), "r"(mbar)
+            : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                smem_addr(buf) + acc_bytes + pr * per_ml),
+            "l"(a.part_ml + prow0(pr) * 2), "r"(per_ml), "r"(mbar)
+            : "memory");
+      }
+    }
+    // bounded wait for the copies (they always complete; the bound only guards against a fault)
+    bool ok = merge_try_wait(mbar, 0);
+    if (!ok) {
+      unsigned long long t0, t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+      while (!(ok = merge_try_wait(mbar, 0))) {
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > 4000000000ull) break;
+      }
+    }
+    if (!ok) {
+      flag_error(a.err, kDevErrTimeout);
+      return;
+    }
+    for (int pr = warp; pr < npairs; pr += nwarps) {  // weights: lanes take slices lane and lane + 32
+      const float* ml = pml + pr * nslices * 2;
+      const bool h0 = lane < nslices, h1 = lane + 32 < nslices;
+      const float m0 = h0 ? ml[2 * lane] : -INFINITY, m1 = h1 ? ml[2 * (lane + 32)] : -INFINITY;
+      float M = fmaxf(m0, m1);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float e0 = (h0 && M != -INFINITY) ? exp2f(m0 - M) : 0.0f;
+      const float e1 = (h1 && M != -INFINITY) ? exp2f(m1 - M) : 0.0f;
+      float L = (h0 ? e0 * ml[2 * lane + 1] : 0.0f) + (h1 ? e1 * ml[2 * (lane + 32) + 1] : 0.0f);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+      const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
+      if (h0) wgt[pr * nslices + lane] = e0 * invL;
+      if (h1) wgt[pr * nslices + lane + 32] = e1 * invL;
+    }
+    __syncthreads();
+    // o = sum_s w_s O_s: two adjacent threads per (pair, 4 d values), even and odd slices, one shuffle
+    for (int it = threadIdx.x; it < npairs * (kHeadDim / 4) * 2; it += blockDim.x) {
+      const int part = it & 1, item = it >> 1;
+      const int d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);
+      const float* wm = wgt + pr * nslices;
+      const float4* src = reinterpret_cast<const float4*>(pacc + static_cast<int64_t>(pr) * nslices * kHeadDim) + d4;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sl = part; sl < nslices; sl += 2) {
+        const float4 v = src[sl * (kHeadDim / 4)];
+        const float wv = wm[sl];
+        o.x += wv * v.x;
+        o.y += wv * v.y;
+        o.z += wv * v.z;
+        o.w += wv * v.w;
+      }
+      o.x += __shfl_xor_sync(0xffffffffu, o.x, 1);
+      o.y += __shfl_xor_sync(0xffffffffu, o.y, 1);
+      o.z += __shfl_xor_sync(0xffffffffu, o.z, 1);
+      o.w += __shfl_xor_sync(0xffffffffu, o.w, 1);
+      if (part == 0) {
+        const uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
+        *reinterpret_cast<uint2*>(a.out + ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * kHeadDim + 4 * d4) =
+            packed;
+      }
+    }
+    return;
+  }
   float* wts = reinterpret_cast<float*>(buf);  // [2][npairs][nslices]: m then l, m replaced by the weights
-  // Output: item (pair, 4 d values) split over 2 adjacent lanes, each summing every other slice with up to 16
-  // loads in flight; the two halves meet through one shuffle.  npairs * 64 and blockDim.x are multiples
-  // of 32, so every warp is either fully inside the range or fully outside it.  (Loading the first batch
-  // before the weights overlapped one round trip but made both kernels spill: slower overall.)
-  constexpr int SPLIT = 2, BATCH = 16;
-  const int total = npairs * (kHeadDim / 4) * SPLIT;
-  auto acc_src = [&](int it) {
-    const int item = it / SPLIT, d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);
-    return reinterpret_cast<const float4*>(a.part_acc + prow0(pr) * kHeadDim) + d4;
-  };
   for (int i = threadIdx.x; i < npairs * nslices; i += blockDim.x) {
     const int pr = i / nslices, sl = i % nslices;
     const int64_t p = prow0(pr) + sl;
@@ -61,6 +159,15 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
   for (int pr = warp; pr < npairs; pr += nwarps)
     merge_weights_warp(wts + pr * nslices, wts + npairs * nslices + pr * nslices, nslices, lane);
   __syncthreads();
+  // Output: item (pair, 4 d values) split over 2 adjacent lanes, each summing every other slice with up to 16
+  // loads in flight; the two halves meet through one shuffle.  npairs * 64 and blockDim.x are multiples
+  // of 32, so every warp is either fully inside the range or fully outside it.
+  constexpr int SPLIT = 2, BATCH = 16;
+  const int total = npairs * (kHeadDim / 4) * SPLIT;
+  auto acc_src = [&](int it) {
+    const int item = it / SPLIT, d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);
+    return reinterpret_cast<const float4*>(a.part_acc + prow0(pr) * kHeadDim) + d4;
+  };
   for (int it = threadIdx.x; it < total; it += blockDim.x) {
     const int part = it % SPLIT, item = it / SPLIT;
     const int d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);

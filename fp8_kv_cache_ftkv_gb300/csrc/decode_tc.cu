@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  merge_split_partials(a, row0, 1, h, nslices, gbase);  // the load ring is idle now
+  merge_split_partials(a, row0, 1, h, nslices, gbase, OFF_SLOT);  // everything below the slots is idle now
 }
 
 // ---------------------------------------------------------------------------------------------
