@@ -450,23 +450,27 @@ def run_kernel_workload(args, world, rank, local, torch, ops, inputs, device, hb
         unit_flops = pairs * HQ * D * 2 * 2
         nbytes = None
     with torch.cuda.stream(stream):
+        work()  # eager first call: per-device set-up happens outside capture
+    stream.synchronize()
+    # one iteration = one CUDA graph replay, so host-side launch cost (Python, ctypes) is not timed
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
         work()
-    stream.synchronize()
     for _ in range(args.warmup):
-        with torch.cuda.stream(stream):
-            work()
-    stream.synchronize()
+        graph.replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(args.steps):
-                work()
+                graph.replay()
             e1.record(stream)
         e1.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     rec = {"metric": f"{args.workload} kernel time", "value": ms * 1e3, "unit": "us/iter", "steps": args.steps,
-           "warmup": args.warmup, "higher_is_better": False, "workload": args.workload, "clocks": clk.summary()}
+           "warmup": args.warmup, "higher_is_better": False, "workload": args.workload, "graph": True,
+           "clocks": clk.summary()}
     if nbytes:
         rec["hbm_gbs"] = nbytes / (ms * 1e-3) / 1e9
         rec["hbm_frac"] = rec["hbm_gbs"] / hbm_peak

@@ -10,7 +10,8 @@
 //                 O += P_{j-1} V_{j-1} into the TMEM O accumulator (so QK of the next tile overlaps
 //                 the softmax of the current one)
 //   warps 2..5  : softmax, one query row per thread (= one TMEM lane): reads S_j from TMEM, keeps the
-//                 running max/sum in registers, writes P_j (BF16) to shared memory in the layout the
+//                 running max/sum in registers (the max on raw scores, the scale folded into the exponent's
+//                 FMA; packed f32x2 arithmetic and three-input max), writes P_j (BF16) to shared memory in the layout the
 //                 MMA reads, and rescales the O row in TMEM only when the running max grew by more than
 //                 8 (log2 units), so the O correction is rare
 // Operands: Q, K, P are K-major with the 128-byte swizzle; V is MN-major (keys x d, d contiguous) with
@@ -187,6 +188,28 @@ __device__ __forceinline__ uint64_t vtile_desc(uint32_t tile, int kk) {
   return sw128_desc(tile + kk * 2048, BOX_BYTES, 1024);
 }
 
+// Packed FP32 pairs (one instruction for two lanes of work) and the three-input maximum.
+__device__ __forceinline__ float2 ffma2(float2 x, float2 y, float2 z) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long*>(&x)), "l"(*reinterpret_cast<unsigned long long*>(&y)),
+        "l"(*reinterpret_cast<unsigned long long*>(&z)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 fadd2(float2 x, float2 y) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long*>(&x)), "l"(*reinterpret_cast<unsigned long long*>(&y)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float fmax3(float x, float y, float z) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(x), "f"(y), "f"(z));
+  return d;
+}
+
 __global__ void __launch_bounds__(192, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkc,
                       const __grid_constant__ CUtensorMap tvc, const __grid_constant__ CUtensorMap twk,
@@ -324,12 +347,16 @@ __global__ void __launch_bounds__(192, 1)
       const bool pre = j < nPT;
       const int kbase = pre ? j * BN : (j - nPT) * BN;
       const int lim = pre ? a.prefix_len - kbase : (t + 1 - kbase);  // columns < lim are visible
-      float mt = -INFINITY;
+      // Tile maximum on the raw scores (the scale is positive: same order), masking only boundary tiles;
+      // the scale is applied once, to the maximum, and folded into the exponent's FMA below.
+      if (lim < BN) {
 #pragma unroll
-      for (int c = 0; c < BN; c++) {
-        s[c] = (c < lim) ? s[c] * a.qk_scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[c]);
+        for (int c = 0; c < BN; c++) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
+      float mraw = fmaxf(s[0], s[1]);
+#pragma unroll
+      for (int c = 2; c < BN; c += 2) mraw = fmax3(mraw, s[c], s[c + 1]);
+      const float mt = mraw * a.qk_scale_log2;
       const float m_new = fmaxf(m_used, mt);
       const bool need = (m_used != -INFINITY) && (m_new > m_used + 8.0f);
       if (m_used == -INFINITY) m_used = m_new;
@@ -358,25 +385,26 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       const float sub = (m_used == -INFINITY) ? 0.0f : m_used;
-      // P row (BF16) into the K-major SW128 P buffer b
+      // P row (BF16) into the K-major SW128 P buffer b; p = 2^(s scale - sub), exponents and sums in pairs
       const uint32_t pt = base + OFF_P + b * TILE_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
-      float ps = 0.0f;
+      const float2 scale2 = make_float2(a.qk_scale_log2, a.qk_scale_log2), nsub2 = make_float2(-sub, -sub);
+      float2 ps2 = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int k8 = 0; k8 < 16; k8++) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-          const float p0 = fast_exp2(s[k8 * 8 + 2 * e] - sub);
-          const float p1 = fast_exp2(s[k8 * 8 + 2 * e + 1] - sub);
-          ps += p0 + p1;
-          w[e] = float2_to_bf16x2(p0, p1);
+          const float2 arg = ffma2(make_float2(s[k8 * 8 + 2 * e], s[k8 * 8 + 2 * e + 1]), scale2, nsub2);
+          const float2 pp = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+          ps2 = fadd2(ps2, pp);
+          w[e] = float2_to_bf16x2(pp.x, pp.y);
         }
         const uint32_t addr = pt + (k8 >> 3) * BOX_BYTES + (((k8 & 7) ^ (row & 7)) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                      "r"(w[3])
                      : "memory");
       }
-      lsum += ps;
+      lsum += ps2.x + ps2.y;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(bar(B_PFULL0 + b));
