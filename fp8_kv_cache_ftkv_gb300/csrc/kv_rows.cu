@@ -22,6 +22,23 @@ namespace ftkv {
 // ---------------------------------------------------------------------------------------------
 constexpr int STORE_UNITS = 2;
 
+// (unit / hkv, unit % hkv) without a 64-bit integer division (a long software sequence): a shift for
+// power-of-two head counts, a 32-bit division when the unit fits, the 64-bit one otherwise.
+__device__ __forceinline__ void split_unit(int64_t unit, int hkv, int64_t& t, int& h) {
+  if ((hkv & (hkv - 1)) == 0) {
+    const int sh = __ffs(hkv) - 1;
+    t = unit >> sh;
+    h = static_cast<int>(unit & (hkv - 1));
+  } else if (unit < 0x7FFFFFFF) {
+    const uint32_t u = static_cast<uint32_t>(unit);
+    t = u / static_cast<uint32_t>(hkv);
+    h = static_cast<int>(u % static_cast<uint32_t>(hkv));
+  } else {
+    t = unit / hkv;
+    h = static_cast<int>(unit % hkv);
+  }
+}
+
 __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
   pdl_enter();
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -37,8 +54,9 @@ __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
     slot[u] = -1;
     raw[u] = make_uint4(0, 0, 0, 0);
     if (unit < total) {
-      const int64_t t = unit / a.num_kv_heads;
-      const int h = static_cast<int>(unit % a.num_kv_heads);
+      int64_t t;
+      int h;
+      split_unit(unit, a.num_kv_heads, t, h);
       slot[u] = __ldg(a.slots + t);
       raw[u] = ldg_stream16((half ? a.v : a.k) + (t * a.num_kv_heads + h) * kHeadDim + l * 8);
     }
@@ -47,7 +65,9 @@ __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
   for (int u = 0; u < STORE_UNITS; u++) {
     const int64_t unit = warp_id * STORE_UNITS + u;
     if (unit >= total) break;  // warp-uniform
-    const int h = static_cast<int>(unit % a.num_kv_heads);
+    int64_t t;
+    int h;
+    split_unit(unit, a.num_kv_heads, t, h);
     float x[8];
     x[0] = bf16_lo(raw[u].x); x[1] = bf16_hi(raw[u].x);
     x[2] = bf16_lo(raw[u].y); x[3] = bf16_hi(raw[u].y);
@@ -107,14 +127,19 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(ReconstructArgs a) {
 #pragma unroll
   for (int u = 0; u < RECON_UNITS; u++) {
     const int64_t unit = group * RECON_UNITS + u;
-    slot[u] = (unit < total) ? __ldg(a.slots + unit / a.num_kv_heads) : -1;
+    int64_t t;
+    int h;
+    split_unit(unit, a.num_kv_heads, t, h);
+    slot[u] = (unit < total) ? __ldg(a.slots + t) : -1;
   }
   uint4 kc[RECON_UNITS], vc[RECON_UNITS];
   float ks[RECON_UNITS], vs[RECON_UNITS];
 #pragma unroll
   for (int u = 0; u < RECON_UNITS; u++) {
     const int64_t unit = group * RECON_UNITS + u;
-    const int h = static_cast<int>(unit % a.num_kv_heads);
+    int64_t t;
+    int h;
+    split_unit(unit, a.num_kv_heads, t, h);
     const bool ok = unit < total && slot[u] >= 0 && slot[u] < a.num_rows;
     const int64_t row = ok ? static_cast<int64_t>(slot[u]) * a.num_kv_heads + h : 0;
     kc[u] = ok ? ldg_stream16(a.k_codes + row * kHeadDim + l * 16) : make_uint4(0, 0, 0, 0);

@@ -147,3 +147,28 @@ def test_store_random_bit_patterns_bit_exact():
     op = oracle.Pool(R, 4, 128)
     oracle.store_quant(op, bits, v, slots)
     _assert_pool_equal(gp, op, slots)
+
+
+def test_store_quotients_at_e4m3_midpoints_bit_exact():
+    """Rows whose quotients x / scale land on or within a few ulps of E4M3 rounding midpoints, over scales
+    from 2^-40 to 2^40: the store's reciprocal fast path must fall back to the IEEE quotient exactly where
+    the code could differ.  Element 0 of every row is its absmax, so the scale is known."""
+    rng = np.random.default_rng(123)
+    T, R = 8192, 9000
+    amax = (2.0 ** rng.uniform(-40, 40, size=(T, 4, 1))).astype(np.float32)
+    amax = inputs.to_bf16_bits(amax).astype(np.uint32) << 16
+    amax = amax.view(np.float32)
+    codes = rng.integers(0, 126, size=(T, 4, 128))
+    mids = (oracle.e4m3_decode(codes.astype(np.uint8)) + oracle.e4m3_decode((codes + 1).astype(np.uint8))) / 2
+    wiggle = 1.0 + rng.integers(-4, 5, size=(T, 4, 128)) * 2.0 ** -8  # a few BF16 ulps around the midpoint
+    sign = np.where(rng.random((T, 4, 128)) < 0.5, -1.0, 1.0)
+    x = (sign * mids * wiggle * amax.astype(np.float64) / 448.0).astype(np.float32)
+    x = np.clip(x, -amax, amax)
+    x[:, :, 0] = amax[:, :, 0]
+    bits = inputs.to_bf16_bits(x)
+    slots = rng.permutation(R)[:T].astype(np.int32)
+    gp = ops.KVPool.empty(R, 4)
+    ops.store_quant(gp, bits_to_cuda_bf16(bits), bits_to_cuda_bf16(bits[::-1].copy()), torch.from_numpy(slots).cuda())
+    op = oracle.Pool(R, 4, 128)
+    oracle.store_quant(op, bits, bits[::-1].copy(), slots)
+    _assert_pool_equal(gp, op, slots)
