@@ -62,8 +62,14 @@ constexpr int smem_bytes() {
   return Cfg<RPW>::WARPS * Cfg<RPW>::NSTAGE * STAGE_BYTES + MAX_SUB * 4;
 }
 static_assert(smem_bytes<1>() <= 227 * 1024, "decode smem");
-static_assert(Cfg<1>::WARPS * 1 * 8 * MERGE_STRIDE * 4 + 2048 <= Cfg<1>::WARPS * Cfg<1>::NSTAGE * STAGE_BYTES, "merge");
-static_assert(Cfg<2>::WARPS * 2 * 8 * MERGE_STRIDE * 4 + 2048 <= Cfg<2>::WARPS * Cfg<2>::NSTAGE * STAGE_BYTES, "merge");
+// in-CTA merge area: per (warp, row, head) 128 accumulators + m + l, then per (row, head) pair the
+// warp weights, M and L; rows per request: 1 for RPW = 1, up to 8 (the multi-row cap) for RPW = 2
+template <int RPW>
+constexpr int merge_area_bytes() {
+  return (Cfg<RPW>::WARPS * RPW * 8 * MERGE_STRIDE + (RPW == 1 ? 1 : 8) * 8 * (Cfg<RPW>::WARPS + 2)) * 4;
+}
+static_assert(merge_area_bytes<1>() <= Cfg<1>::WARPS * Cfg<1>::NSTAGE * STAGE_BYTES, "merge");
+static_assert(merge_area_bytes<2>() <= Cfg<2>::WARPS * Cfg<2>::NSTAGE * STAGE_BYTES, "merge");
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -438,24 +444,29 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   __syncthreads();
 
   // ---- merge the wk warps of each row group; write this slice's partial ----
-  // weights first: one thread per (row, head) pair computes M, L and the wk weights 2^(m_k - M)
+  // weights first: one warp per (row, head) pair, lane k holding warp k's maximum and sum; M and L by
+  // warp reductions, weights 2^(m_k - M)
   const int npairs = R * a.group;
   constexpr int WSTRIDE = WARPS + 2;
-  for (int pr = threadIdx.x; pr < npairs; pr += blockDim.x) {
+  for (int pr = warp; pr < npairs; pr += WARPS) {
     const int rr = pr / a.group, hh = pr % a.group;
     const int rgi = rr / RPW, r = rr % RPW;
-    float M = -INFINITY;
-    for (int k = 0; k < wk; k++) M = fmaxf(M, merge[(((rgi * wk + k) * RPW + r) * 8 + hh) * MERGE_STRIDE + 128]);
-    float L = 0.0f;
+    const bool has = lane < wk;
+    const int idx = has ? (((rgi * wk + lane) * RPW + r) * 8 + hh) * MERGE_STRIDE : 0;
+    const float mk = has ? merge[idx + 128] : -INFINITY;
+    float M = mk;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float wt = (has && M != -INFINITY) ? exp2f(mk - M) : 0.0f;
+    float L = has ? wt * merge[idx + 129] : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     float* w = mw + pr * WSTRIDE;
-    for (int k = 0; k < wk; k++) {
-      const float* src = merge + (((rgi * wk + k) * RPW + r) * 8 + hh) * MERGE_STRIDE;
-      const float wt = (M == -INFINITY) ? 0.0f : exp2f(src[128] - M);
-      w[k] = wt;
-      L += wt * src[129];
+    if (has) w[lane] = wt;
+    if (lane == 0) {
+      w[WARPS] = M;
+      w[WARPS + 1] = L;
     }
-    w[WARPS] = M;
-    w[WARPS + 1] = L;
   }
   __syncthreads();
   for (int it = threadIdx.x; it < npairs * kHeadDim; it += blockDim.x) {
@@ -463,8 +474,12 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     const int rr = pr / a.group, hh = pr % a.group;
     const int rgi = rr / RPW, r = rr % RPW;
     const float* w = mw + pr * WSTRIDE;
+    const float* src = merge + ((rgi * wk * RPW + r) * 8 + hh) * MERGE_STRIDE + d;
+    constexpr int KSTEP = RPW * 8 * MERGE_STRIDE;  // floats from warp k to warp k + 1 of the row group
     float A = 0.0f;
-    for (int k = 0; k < wk; k++) A += w[k] * merge[(((rgi * wk + k) * RPW + r) * 8 + hh) * MERGE_STRIDE + d];
+#pragma unroll
+    for (int k = 0; k < WARPS; k++)
+      if (k < wk) A += w[k] * src[k * KSTEP];
     const int64_t prow = ((row0 + rr) * a.num_q_heads + h * a.group + hh) * a.num_splits + split;
     a.part_acc[prow * kHeadDim + d] = A;
     if (d == 0) {

@@ -7,8 +7,9 @@
 // The weights are computed by one warp per (row, head) with warp reductions (one thread walking all
 // slices three times was a serial tail of microseconds).  The accumulators of one (row, head) are
 // contiguous over the slices, and so are their (m, l) pairs: when they fit in the CTA's idle shared
-// memory, both arrive by TMA bulk copies (two per (row, head)) in one round trip; otherwise they are read
-// from L2 with up to 16 loads in flight per thread.  (cp.async of every 16 bytes was slower.)
+// memory, both arrive by TMA bulk copies (two per (row, head), each pair on its own mbarrier, so merging
+// overlaps the copies still in flight); otherwise they are read from L2 with up to 16 loads in flight per
+// thread.  (cp.async of every 16 bytes was slower.)
 #pragma once
 
 #include "ftkv_device.cuh"
@@ -24,6 +25,18 @@ __device__ __forceinline__ bool merge_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity), "r"(100000u)
       : "memory");
   return ok != 0;
+}
+
+// Bounded wait for phase 0 of a copy barrier: the copies always complete; the bound (4 s) only guards
+// against a fault.  Out of line: it is the cold path of every wait.
+static __device__ __noinline__ bool merge_wait_bounded(uint32_t bar) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (!merge_try_wait(bar, 0)) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 4000000000ull) return false;
+  }
+  return true;
 }
 
 // w[s] = 2^(m[s] - M) / L for one (row, head), by one warp; wm holds m on entry and the weights on return.
@@ -52,59 +65,61 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
   auto prow0 = [&](int pr) -> int64_t {  // partial row of (pair pr, slice 0)
     return ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * a.num_splits;
   };
-  // Bulk path (even slice counts keep every copy a multiple of 16 bytes and 16-byte aligned): per (row, head), one copy
-  // of its nslices x 128 accumulators and one of its nslices (m, l) pairs, then the weights from shared
-  // memory with one exp2 per slice, then the weighted sums over all threads.
+  // Bulk path (even slice counts keep every copy a multiple of 16 bytes and 16-byte aligned): per (row, head),
+  // one copy of its nslices x 128 accumulators and one of its nslices (m, l) pairs, completing on that pair's
+  // own mbarrier, so a pair is merged as soon as its data has landed while later pairs are still in flight.
+  // Two warps take one pair: weights from shared memory with one exp2 per slice (each warp its own copy),
+  // then the 32 x 4 outputs, even and odd slices on adjacent lanes.
   const uint32_t acc_bytes = static_cast<uint32_t>(npairs) * nslices * kHeadDim * 4;
   const uint32_t ml_bytes = static_cast<uint32_t>(npairs) * nslices * 8;
+  const uint32_t wgt_bytes = static_cast<uint32_t>(nwarps) * 64 * 4;
   // (m, l) copies start at part_ml + 8 prow0 bytes, prow0 a multiple of num_splits: 16-byte aligned when
   // num_splits is even; the accumulator copies start at 512 prow0 bytes.
-  const bool bulk = (nslices % 2 == 0) && (a.num_splits % 2 == 0) && nslices <= 64 &&
-                    static_cast<uint64_t>(acc_bytes) + 2ull * ml_bytes + 16 <= buf_bytes;
+  const bool bulk = (nslices % 2 == 0) && (a.num_splits % 2 == 0) && nslices <= 64 && (nwarps % 2 == 0) &&
+                    static_cast<uint64_t>(acc_bytes) + ml_bytes + wgt_bytes + 8ull * npairs <= buf_bytes;
   if (bulk) {
-    float* pacc = reinterpret_cast<float*>(buf);                    // [npairs][nslices][128]
-    const float* pml = reinterpret_cast<const float*>(buf + acc_bytes);  // [npairs][nslices][2]
-    float* wgt = reinterpret_cast<float*>(buf + acc_bytes + ml_bytes);   // [npairs][nslices]
-    const uint32_t mbar = smem_addr(buf) + acc_bytes + 2 * ml_bytes;
+    const float* pacc = reinterpret_cast<const float*>(buf);              // [npairs][nslices][128]
+    const float* pml = reinterpret_cast<const float*>(buf + acc_bytes);   // [npairs][nslices][2]
+    float* wgt = reinterpret_cast<float*>(buf + acc_bytes + ml_bytes);    // [nwarps][64]
+    const uint32_t mbar0 = smem_addr(buf) + acc_bytes + ml_bytes + wgt_bytes;  // [npairs] x 8 bytes
+    const uint32_t per = static_cast<uint32_t>(nslices) * kHeadDim * 4, per_ml = static_cast<uint32_t>(nslices) * 8;
     // earlier generic accesses to the buffer come before the async proxy overwrites it
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     if (threadIdx.x == 0) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
+      for (int pr = 0; pr < npairs; pr++)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar0 + 8 * pr) : "memory");
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();  // every barrier is initialised before any thread polls it
+    if (threadIdx.x == 0) {
       // the other slices' partials were written by generic stores, released through the ticket
       asm volatile("fence.proxy.async.global;" ::: "memory");
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(acc_bytes + ml_bytes)
-                   : "memory");
-      const uint32_t per = static_cast<uint32_t>(nslices) * kHeadDim * 4, per_ml = static_cast<uint32_t>(nslices) * 8;
       for (int pr = 0; pr < npairs; pr++) {
+        const uint32_t mb = mbar0 + 8 * pr;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(per + per_ml) : "memory");
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                 smem_addr(buf) + pr * per),
-            "l"(a.part_acc + prow0(pr) * kHeadDim), "r"(per), "r"(mbar)
+            "l"(a.part_acc + prow0(pr) * kHeadDim), "r"(per), "r"(mb)
             : "memory");
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                 smem_addr(buf) + acc_bytes + pr * per_ml),
-            "l"(a.part_ml + prow0(pr) * 2), "r"(per_ml), "r"(mbar)
+            "l"(a.part_ml + prow0(pr) * 2), "r"(per_ml), "r"(mb)
             : "memory");
       }
     }
-    // bounded wait for the copies (they always complete; the bound only guards against a fault)
-    bool ok = merge_try_wait(mbar, 0);
-    if (!ok) {
-      unsigned long long t0, t;
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-      while (!(ok = merge_try_wait(mbar, 0))) {
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-        if (t - t0 > 4000000000ull) break;
+    float* wm = wgt + warp * 64;
+    for (int pr = warp >> 1; pr < npairs; pr += nwarps >> 1) {  // warp-uniform
+      // bounded wait for this pair's copies (they always complete; the bound only guards against a fault)
+      const uint32_t mb = mbar0 + 8 * pr;
+      const bool landed = merge_try_wait(mb, 0) || merge_wait_bounded(mb);
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) flag_error(a.err, kDevErrTimeout);
+        break;
       }
-    }
-    if (!ok) {
-      flag_error(a.err, kDevErrTimeout);
-      return;
-    }
-    for (int pr = warp; pr < npairs; pr += nwarps) {  // weights: lanes take slices lane and lane + 32
+      // weights of this pair: lanes take slices lane and lane + 32
       const float* ml = pml + pr * nslices * 2;
       const bool h0 = lane < nslices, h1 = lane + 32 < nslices;
       const float m0 = h0 ? ml[2 * lane] : -INFINITY, m1 = h1 ? ml[2 * (lane + 32)] : -INFINITY;
@@ -117,17 +132,15 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
       const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
-      if (h0) wgt[pr * nslices + lane] = e0 * invL;
-      if (h1) wgt[pr * nslices + lane + 32] = e1 * invL;
-    }
-    __syncthreads();
-    // o = sum_s w_s O_s: two adjacent threads per (pair, 4 d values), even and odd slices, one shuffle
-    for (int it = threadIdx.x; it < npairs * (kHeadDim / 4) * 2; it += blockDim.x) {
-      const int part = it & 1, item = it >> 1;
-      const int d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);
-      const float* wm = wgt + pr * nslices;
+      if (h0) wm[lane] = e0 * invL;
+      if (h1) wm[lane + 32] = e1 * invL;
+      __syncwarp();
+      // o = sum_s w_s O_s over this lane's slice parity; the two parities meet through one shuffle
+      const int item = (warp & 1) * 32 + lane;  // (4 d values, slice parity) of the pair
+      const int part = item & 1, d4 = item >> 1;
       const float4* src = reinterpret_cast<const float4*>(pacc + static_cast<int64_t>(pr) * nslices * kHeadDim) + d4;
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
       for (int sl = part; sl < nslices; sl += 2) {
         const float4 v = src[sl * (kHeadDim / 4)];
         const float wv = wm[sl];
@@ -145,6 +158,7 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
         *reinterpret_cast<uint2*>(a.out + ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * kHeadDim + 4 * d4) =
             packed;
       }
+      __syncwarp();  // the weights are rewritten for the next pair
     }
     return;
   }
