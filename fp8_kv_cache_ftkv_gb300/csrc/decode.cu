@@ -57,9 +57,15 @@ struct Cfg<2> {                               // multi-row decode: two query row
   static constexpr int NSTAGE = 4;
 };
 
+// query pieces of the CTA's rows, shared by all warps: [row][8 heads][2 pieces][128] E4M3 codes, then
+// [row][8 heads] FP32 multipliers; rows per request: 1 for RPW = 1, up to 8 (the multi-row cap) for RPW = 2
+template <int RPW>
+constexpr int q_rows_max() { return RPW == 1 ? 1 : 8; }
+template <int RPW>
+constexpr int q_area_bytes() { return q_rows_max<RPW>() * 8 * (2 * kHeadDim + 4); }
 template <int RPW>
 constexpr int smem_bytes() {
-  return Cfg<RPW>::WARPS * Cfg<RPW>::NSTAGE * STAGE_BYTES + MAX_SUB * 4;
+  return Cfg<RPW>::WARPS * Cfg<RPW>::NSTAGE * STAGE_BYTES + MAX_SUB * 4 + q_area_bytes<RPW>();
 }
 static_assert(smem_bytes<1>() <= 227 * 1024, "decode smem");
 // in-CTA merge area: per (warp, row, head) 128 accumulators + m + l, then per (row, head) pair the
@@ -114,6 +120,8 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   constexpr int NSTAGE = Cfg<RPW>::NSTAGE;
   extern __shared__ __align__(128) uint8_t smem[];
   int32_t* sslot = reinterpret_cast<int32_t*>(smem + WARPS * NSTAGE * STAGE_BYTES);
+  uint8_t* qsm = smem + WARPS * NSTAGE * STAGE_BYTES + MAX_SUB * 4;              // query piece codes
+  float* qmul = reinterpret_cast<float*>(qsm + q_rows_max<RPW>() * 8 * 2 * kHeadDim);  // their multipliers
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,61 +167,75 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     lim[i] = valid ? (vis < j1 ? vis : j1) : j0;
   }
 
-  // ---- query pieces (B operand of QK^T): head g, d = 32t + 8kk + {0..3} (b0) / {4..7} (b1) ----
+  // The first slot window's indices are requested now and staged after the query pieces, so the two
+  // round trips overlap.
+  constexpr int PRE = 2;  // slot indices per thread read ahead (1,024 keys per CTA)
+  const int nk0 = (j1 - j0 < MAX_SUB) ? j1 - j0 : MAX_SUB;
+  int32_t pre[PRE];
+#pragma unroll
+  for (int u = 0; u < PRE; u++) {
+    const int i = threadIdx.x + u * blockDim.x;
+    pre[u] = (i < nk0) ? a.req_to_slot[static_cast<int64_t>(b) * a.req_stride + j0 + i] : 0;
+  }
+
+  // ---- query pieces, computed once per CTA: one warp per (row, head), 4 d values per lane ----
+  // x = q * 2^(7-ex), ex the exponent of max|q| over the head, has |x| < 256; pieces x = h1 + h2/16, both
+  // E4M3 (exact unless |q| < 2^-13 max|q|); multiplier 2^(ex-7) * sm_scale * log2(e).  Heads past the group
+  // (padding of the 8-wide MMA N dimension) get zero pieces.
+  for (int pr = warp; pr < R * 8; pr += WARPS) {  // warp-uniform
+    const int rr = pr >> 3, hq = pr & 7;
+    float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (hq < a.group) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(
+          a.q + ((row0 + rr) * a.num_q_heads + h * a.group + hq) * kHeadDim + 4 * lane));
+      x[0] = bf16_lo(v.x);
+      x[1] = bf16_hi(v.x);
+      x[2] = bf16_lo(v.y);
+      x[3] = bf16_hi(v.y);
+    }
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    int ex = (amax > 0.0f) ? ilogbf(amax) : 0;
+    ex = ex < -120 ? -120 : ex;
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + 7 - ex) << 23);
+#pragma unroll
+    for (int e = 0; e < 4; e++) x[e] *= up;
+    uint8_t* dst = qsm + (rr * 8 + hq) * 2 * kHeadDim + 4 * lane;
+#pragma unroll
+    for (int p = 0; p < 2; p++) {
+      const uint32_t c01 = e4m3x2_encode(x[0], x[1]), c23 = e4m3x2_encode(x[2], x[3]);
+      *reinterpret_cast<uint32_t*>(dst + p * kHeadDim) = c01 | (c23 << 16);
+      if (p == 0) {
+        const float2 v01 = f16x2_to_float2(e4m3x2_to_f16x2(c01));
+        const float2 v23 = f16x2_to_float2(e4m3x2_to_f16x2(c23));
+        x[0] = (x[0] - v01.x) * 16.0f;
+        x[1] = (x[1] - v01.y) * 16.0f;
+        x[2] = (x[2] - v23.x) * 16.0f;
+        x[3] = (x[3] - v23.y) * 16.0f;
+      }
+    }
+    if (lane == 0) qmul[rr * 8 + hq] = __uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * a.qk_scale_log2;
+  }
+  __syncthreads();
+  // B operand of QK^T for this warp's rows: head g, d = 32t + 8kk + {0..3} (b0) / {4..7} (b1)
   uint32_t qp[RPW][2][4][2];
-  float fq[RPW][2];  // per-head multiplier for heads 2t, 2t+1: a * sm_scale * log2(e)
+  float fq[RPW][2];  // per-head multiplier for heads 2t, 2t+1
 #pragma unroll
   for (int i = 0; i < RPW; i++) {
     const int rabs = rg * RPW + i;
-    float qv[32];
-    float amax = 0.0f;
-    if (active && rabs < R && g < a.group) {
-      const uint16_t* qptr = a.q + ((row0 + rabs) * a.num_q_heads + h * a.group + g) * kHeadDim + 32 * t;
+    const bool valid = active && rabs < R;
+    const int rsafe = valid ? rabs : 0;
+    const uint32_t src = smem_addr(qsm) + (rsafe * 8 + g) * 2 * kHeadDim + 32 * t;
 #pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qptr + 8 * u));
-#pragma unroll
-        for (int w = 0; w < 4; w++) {
-          qv[u * 8 + 2 * w] = bf16_lo(word(v, w));
-          qv[u * 8 + 2 * w + 1] = bf16_hi(word(v, w));
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 32; e++) amax = fmaxf(amax, fabsf(qv[e]));
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; e++) qv[e] = 0.0f;
+    for (int p = 0; p < 2; p++) {
+      const uint4 w0 = valid ? ld_shared_v4(src + p * kHeadDim) : make_uint4(0, 0, 0, 0);
+      const uint4 w1 = valid ? ld_shared_v4(src + p * kHeadDim + 16) : make_uint4(0, 0, 0, 0);
+      qp[i][p][0][0] = w0.x; qp[i][p][0][1] = w0.y; qp[i][p][1][0] = w0.z; qp[i][p][1][1] = w0.w;
+      qp[i][p][2][0] = w1.x; qp[i][p][2][1] = w1.y; qp[i][p][3][0] = w1.z; qp[i][p][3][1] = w1.w;
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    int ex = (amax > 0.0f) ? ilogbf(amax) : 0;
-    ex = ex < -120 ? -120 : ex;
-    // x = q * 2^(7-ex) has |x| < 256; pieces: x = h1 + h2/16 (exact unless |q| < 2^-13 max|q|)
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + 7 - ex) << 23);
-    const float down = __uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * a.qk_scale_log2;
-#pragma unroll
-    for (int e = 0; e < 32; e += 4) {
-      uint32_t pc[2];
-      float x[4] = {qv[e] * up, qv[e + 1] * up, qv[e + 2] * up, qv[e + 3] * up};
-#pragma unroll
-      for (int p = 0; p < 2; p++) {
-        const uint32_t c01 = e4m3x2_encode(x[0], x[1]), c23 = e4m3x2_encode(x[2], x[3]);
-        pc[p] = c01 | (c23 << 16);
-        if (p == 0) {
-          const float2 v01 = f16x2_to_float2(e4m3x2_to_f16x2(c01));
-          const float2 v23 = f16x2_to_float2(e4m3x2_to_f16x2(c23));
-          x[0] = (x[0] - v01.x) * 16.0f;
-          x[1] = (x[1] - v01.y) * 16.0f;
-          x[2] = (x[2] - v23.x) * 16.0f;
-          x[3] = (x[3] - v23.y) * 16.0f;
-        }
-      }
-      const int kk = e >> 3, half = (e >> 2) & 1;
-#pragma unroll
-      for (int p = 0; p < 2; p++) qp[i][p][kk][half] = pc[p];
-    }
-    fq[i][0] = __shfl_sync(0xffffffffu, down, (2 * t) * 4);
-    fq[i][1] = __shfl_sync(0xffffffffu, down, (2 * t + 1) * 4);
+    fq[i][0] = valid ? qmul[rsafe * 8 + 2 * t] : 0.0f;
+    fq[i][1] = valid ? qmul[rsafe * 8 + 2 * t + 1] : 0.0f;
   }
 
   float acc[RPW][8][4];
@@ -233,14 +255,20 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     const int je = (js + MAX_SUB < j1) ? js + MAX_SUB : j1;
     const int nk = je - js;
     __syncthreads();  // every warp is done with the previous slot window
-    for (int i = threadIdx.x; i < nk; i += blockDim.x) {
-      int32_t s = a.req_to_slot[static_cast<int64_t>(b) * a.req_stride + js + i];
-      if (s < 0 || s >= a.num_rows) {
+    auto stage_slot = [&](int i, int32_t sv) {
+      if (sv < 0 || sv >= a.num_rows) {
         flag_error(a.err, kDevErrBadSlot);
-        s = 0;
+        sv = 0;
       }
-      sslot[i] = s;
+      sslot[i] = sv;
+    };
+    int i = threadIdx.x;
+    if (js == j0) {  // the indices read ahead: i < nk0 == nk
+#pragma unroll
+      for (int u = 0; u < PRE; u++, i += blockDim.x)
+        if (i < nk) stage_slot(i, pre[u]);
     }
+    for (; i < nk; i += blockDim.x) stage_slot(i, a.req_to_slot[static_cast<int64_t>(b) * a.req_stride + js + i]);
     __syncthreads();
     if (!active) continue;
 
