@@ -254,18 +254,22 @@ def build_decode(args, torch, ops, inputs, device):
     outs = [out_all[l] for l in range(args.layers)]
     torch.cuda.synchronize()
 
+    fused = args.decode_impl == "mma"  # the warp-level kernel stores the new token itself
+
     def step(decode_only=False, events=None):
         for l in range(args.layers):
-            if not decode_only:
+            if not decode_only and not fused:
                 ops.store_quant(pools[l], newk[l], newv[l], new_slot)
             if events is not None:
                 events[l][0].record()
+            extra = dict(k_new=newk[l], v_new=newv[l]) if fused and not decode_only else {}
             ops.decode_attn(pools[l], q[l], slots_d, lens_d, None, max_seq_len=n, max_q_rows=1, plan=plan,
-                            out=outs[l], impl=args.decode_impl)
+                            out=outs[l], impl=args.decode_impl, **extra)
             if events is not None:
                 events[l][1].record()
 
-    return dict(step=step, q_all=q_all, kv_all=kv_all, out_all=out_all, plan=plan, pools=pools, wl=wl)
+    return dict(step=step, q_all=q_all, kv_all=kv_all, out_all=out_all, plan=plan, pools=pools, wl=wl,
+                launches_per_layer=1 if fused else 2, fused=fused)
 
 
 def decode_bytes_per_layer(n):
@@ -332,6 +336,8 @@ def run_ours(args, world, rank, local):
             if rep > 0:
                 durs += [a.elapsed_time(b) for a, b in evs]
     dur_ms = statistics.mean(durs)
+    if st["fused"]:
+        kernel_bytes += store_bytes  # the decode launch also stores the new token
     achieved = kernel_bytes / (dur_ms * 1e-3) / 1e9
     if args.decode_impl == "tc":
         kname, prof, ksrc = "decode_tc_kernel", "decode_tc_32k.md", "decode_tc.cu"
@@ -385,6 +391,8 @@ def run_ours(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3-kv/f16-mma/f32-acc", "data": "synthetic",
             "decode_impl": args.decode_impl,
+            "step": ("per layer one launch: fused quantize-on-write of the new token + split-K decode"
+                     if st["fused"] else "per layer: store of the new token, then split-K decode"),
             "config": {"workload": f"decode_{n}_b1_{args.layers}layers", "context": n, "batch": 1,
                        "layers": args.layers, "Hq": HQ, "Hkv": HKV, "D": D, "pool_rows": args.pool_rows,
                        "num_splits": st["plan"].num_splits, "graph": "one CUDA graph per step",
@@ -395,7 +403,7 @@ def run_ours(args, world, rank, local):
                          "frac": achieved / hbm_peak, "traffic": traffic, "kernel": kname,
                          "bytes_per_launch": kernel_bytes, "mean_launch_us": dur_ms * 1e3,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * args.layers * 2,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * args.layers * st["launches_per_layer"],
             "clocks": clocks, "device_errors": errors,
         }), flush=True)
     if world > 1:

@@ -32,6 +32,7 @@ EXPORTS = (
     "ftkv_decode_attn", "ftkv_prefill_attn", "ftkv_prefill_attn_mma", "ftkv_e4m3_encode_f32",
     "ftkv_e4m3_decode_f32", "ftkv_pool_bytes", "ftkv_device_errors", "ftkv_status_str",
     "ftkv_last_cuda_error", "ftkv_abi_version", "ftkv_decode_attn_noalloc", "ftkv_decode_attn_tc",
+    "ftkv_decode_attn_store",
 )
 
 
@@ -75,6 +76,8 @@ def load() -> ctypes.CDLL:
             "ftkv_decode_attn": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P, SZ, P, P]),
             "ftkv_decode_attn_tc": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P, SZ, P,
                                                    P]),
+            "ftkv_decode_attn_store": (ctypes.c_int, [PP, I32, P, P, P, P, I64, P, P, I32, I64, I32, I64, F32, I32,
+                                                      P, SZ, P, P]),
             "ftkv_decode_attn_noalloc": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P,
                                                         P]),
             "ftkv_prefill_attn": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),

@@ -172,7 +172,7 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
                          int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                          int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
                          int32_t num_splits, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream,
-                         bool use_tc) {
+                         bool use_tc, const uint16_t* k_new = nullptr, const uint16_t* v_new = nullptr) {
   int st = check_pool(pool);
   if (st != FTKV_OK) return st;
   if ((st = check_heads(num_q_heads, pool->num_kv_heads)) != FTKV_OK) return st;
@@ -233,6 +233,8 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   a.out = out;
   a.err = di->err_word;
   a.use_tc = use_tc ? 1 : 0;
+  a.k_new = k_new;
+  a.v_new = v_new;
   cudaError_t e = ftkv::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FTKV_OK : cuda_fail(e);
 }
@@ -252,6 +254,20 @@ int ftkv_decode_attn_tc(const ftkv_pool* pool, int32_t num_q_heads, const uint16
   if (max_q_rows != 1) return FTKV_ERR_UNSUPPORTED;
   return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
                        max_q_rows, max_seq_len, sm_scale, num_splits, workspace, workspace_bytes, out, stream, true);
+}
+
+int ftkv_decode_attn_store(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const uint16_t* k_new,
+                           const uint16_t* v_new, const int32_t* req_to_slot, int64_t req_stride,
+                           const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
+                           int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
+                           void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
+  if (batch > 0 && total_q_rows > 0) {
+    if (!k_new || !v_new) return FTKV_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new)) return FTKV_ERR_ALIGN;
+  }
+  return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
+                       max_q_rows, max_seq_len, sm_scale, num_splits, workspace, workspace_bytes, out, stream, false,
+                       k_new, v_new);
 }
 
 static int prefill_common(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,

@@ -178,6 +178,37 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     pre[u] = (i < nk0) ? a.req_to_slot[static_cast<int64_t>(b) * a.req_stride + j0 + i] : 0;
   }
 
+  // ---- fused store: the request's new tokens (positions n-R .. n-1) that fall in this slice are
+  // quantized into the pool first, one warp per token (K row on lanes 0-15, V row on 16-31) with the
+  // store kernel's arithmetic, starting from the upper half of the warps while the lower half computes
+  // the query pieces.  The barrier after the pieces orders these writes before every warp's loads, which
+  // then read the new rows like any other key. ----
+  if (a.k_new) {
+    const int nq0 = static_cast<int>(n) - R;  // position of the request's first new token
+    const int first = (nq0 > j0) ? nq0 : j0;
+    if (first < j1) {  // CTA-uniform
+      bool wrote = false;
+      for (int pos = ((first > 0) ? first : 0) + (warp + WARPS / 2) % WARPS; pos < j1; pos += WARPS) {  // warp-uniform
+        const int half = lane >> 4, l = lane & 15;
+        const uint16_t* src =
+            (half ? a.v_new : a.k_new) + ((row0 + pos - nq0) * a.num_kv_heads + h) * kHeadDim + l * 8;
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+        const int32_t sv = a.req_to_slot[static_cast<int64_t>(b) * a.req_stride + pos];
+        float sc;
+        const uint2 packed = quantize_row_lane8(raw, sc);
+        if (sv >= 0 && sv < a.num_rows) {  // a bad slot is flagged when staged; nothing is written
+          const int64_t row = static_cast<int64_t>(sv) * a.num_kv_heads + h;
+          // the pool is the caller's writable memory (ftkv_pool holds non-const pointers)
+          *reinterpret_cast<uint2*>(const_cast<uint8_t*>(half ? a.v_codes : a.k_codes) + row * kHeadDim + l * 8) =
+              packed;
+          if (l == 0) const_cast<float*>(half ? a.v_scales : a.k_scales)[row] = sc;
+        }
+        wrote = true;
+      }
+      if (wrote) __threadfence();  // the rows reach L2 before the barrier below
+    }
+  }
+
   // ---- query pieces, computed once per CTA: one warp per (row, head), 4 d values per lane ----
   // x = q * 2^(7-ex), ex the exponent of max|q| over the head, has |x| < 256; pieces x = h1 + h2/16, both
   // E4M3 (exact unless |q| < 2^-13 max|q|); multiplier 2^(ex-7) * sm_scale * log2(e).  Heads past the group

@@ -59,6 +59,34 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Quantize-on-write of one 128-element BF16 row carried by a 16-lane half warp, lane l holding elements
+// 8l .. 8l+7 in `raw` (FreeToken PR #853, "What changes": each row gets its own FP32 scale).  Row
+// absmax = NaN-ignoring fmaxf from +0, scale = absmax / 448 (IEEE FP32 division), code =
+// E4M3FN_rne_satfinite(x / scale) (IEEE division); an all-zero row keeps scale 0 and divides by 1.
+// Every lane of the warp calls it: the max reduction shuffles within each 16-lane half.  Returns the
+// lane's 8 codes (element 8l in the lowest byte) and sets `scale`.  The store kernel and the decode
+// kernel's fused store both use this one definition.
+__device__ __forceinline__ uint2 quantize_row_lane8(const uint4 raw, float& scale) {
+  float x[8];
+  x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
+  x[2] = bf16_lo(raw.y); x[3] = bf16_hi(raw.y);
+  x[4] = bf16_lo(raw.z); x[5] = bf16_hi(raw.z);
+  x[6] = bf16_lo(raw.w); x[7] = bf16_hi(raw.w);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int off = 1; off < 16; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  scale = __fdiv_rn(amax, 448.0f);
+  const float div = (scale == 0.0f) ? 1.0f : scale;
+  float q[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) q[i] = __fdiv_rn(x[i], div);
+  const uint32_t w0 = e4m3x2_encode(q[0], q[1]), w1 = e4m3x2_encode(q[2], q[3]);
+  const uint32_t w2 = e4m3x2_encode(q[4], q[5]), w3 = e4m3x2_encode(q[6], q[7]);
+  return make_uint2(w0 | (w1 << 16), w2 | (w3 << 16));
+}
+
 // ---------------------------------------------------------------------------------------------
 // Byte permute
 // ---------------------------------------------------------------------------------------------

@@ -62,6 +62,8 @@ struct DecodeArgs {
   uint16_t* out;             // [total_q_rows][Hq][128]
   int* err;
   int use_tc;                // 1: the tcgen05 kernel (single-row batches only)
+  const uint16_t* k_new;     // fused store: [total_q_rows][Hkv][128] K of the new tokens, or null
+  const uint16_t* v_new;     //              V of the new tokens
 };
 
 struct PrefillArgs {

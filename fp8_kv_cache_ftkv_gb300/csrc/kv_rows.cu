@@ -68,28 +68,12 @@ __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
     int64_t t;
     int h;
     split_unit(unit, a.num_kv_heads, t, h);
-    float x[8];
-    x[0] = bf16_lo(raw[u].x); x[1] = bf16_hi(raw[u].x);
-    x[2] = bf16_lo(raw[u].y); x[3] = bf16_hi(raw[u].y);
-    x[4] = bf16_lo(raw[u].z); x[5] = bf16_hi(raw[u].z);
-    x[6] = bf16_lo(raw[u].w); x[7] = bf16_hi(raw[u].w);
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    float scale;
+    const uint2 packed = quantize_row_lane8(raw[u], scale);  // every lane: the reduction shuffles
     if (slot[u] < 0 || slot[u] >= a.num_rows) {
       if (lane == 0) flag_error(a.err, kDevErrBadSlot);
       continue;
     }
-    const float scale = __fdiv_rn(amax, 448.0f);
-    const float div = (scale == 0.0f) ? 1.0f : scale;
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++) q[i] = __fdiv_rn(x[i], div);
-    const uint32_t w0 = e4m3x2_encode(q[0], q[1]), w1 = e4m3x2_encode(q[2], q[3]);
-    const uint32_t w2 = e4m3x2_encode(q[4], q[5]), w3 = e4m3x2_encode(q[6], q[7]);
-    const uint2 packed = make_uint2(w0 | (w1 << 16), w2 | (w3 << 16));
     const int64_t row = static_cast<int64_t>(slot[u]) * a.num_kv_heads + h;
     __stcs(reinterpret_cast<uint2*>((half ? a.v_codes : a.k_codes) + row * kHeadDim + l * 8), packed);
     if (l == 0) __stcs((half ? a.v_scales : a.k_scales) + row, scale);

@@ -130,11 +130,21 @@ class DecodePlan:
 def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,
                 q_row_offsets: torch.Tensor = None, *, max_seq_len: int, max_q_rows: int = 1,
                 sm_scale: float = HEAD_DIM ** -0.5, num_splits: int = 0, plan: DecodePlan = None,
-                out: torch.Tensor = None, impl: str = "mma", stream=None) -> torch.Tensor:
+                out: torch.Tensor = None, impl: str = "mma", k_new: torch.Tensor = None,
+                v_new: torch.Tensor = None, stream=None) -> torch.Tensor:
     """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, 128].
-    ``impl``: "mma" (the warp-level kernel, every batch) or "tc" (the tcgen05 kernel, single-row batches)."""
+    ``impl``: "mma" (the warp-level kernel, every batch) or "tc" (the tcgen05 kernel, single-row batches).
+    ``k_new``/``v_new`` (BF16 [total_q_rows, Hkv, 128], the new tokens' rows, one per query row): quantize them
+    into the pool at their positions' slots first, in the same launch (``ftkv_decode_attn_store``)."""
     if impl not in ("mma", "tc"):
         raise ValueError(f"unknown decode impl {impl!r}")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        if impl != "mma":
+            raise ValueError("the fused store runs on the warp-level kernel (impl='mma')")
+        _req(k_new, torch.bfloat16, "k_new", 3)
+        _req(v_new, torch.bfloat16, "v_new", 3)
     _req(q, torch.bfloat16, "q", 3)
     if req_to_slot.dim() == 1:
         req_to_slot = req_to_slot.view(1, -1)
@@ -150,6 +160,15 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
         out = torch.empty_like(q)
     _req(out, torch.bfloat16, "out", 3)
     ps = pool.c_struct()
+    if k_new is not None:
+        if k_new.shape != (total, pool.num_kv_heads, HEAD_DIM) or v_new.shape != k_new.shape:
+            raise ValueError(f"k_new/v_new must be [{total}, {pool.num_kv_heads}, {HEAD_DIM}]")
+        check(_lib.load().ftkv_decode_attn_store(
+            ctypes.byref(ps), hq, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(req_to_slot), req_to_slot.shape[1],
+            _ptr(seq_lens), _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale),
+            plan.num_splits, _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)),
+            "ftkv_decode_attn_store")
+        return out
     name = "ftkv_decode_attn" if impl == "mma" else "ftkv_decode_attn_tc"
     check(getattr(_lib.load(), name)(
         ctypes.byref(ps), hq, _ptr(q), _ptr(req_to_slot), req_to_slot.shape[1], _ptr(seq_lens),

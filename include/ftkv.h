@@ -150,6 +150,29 @@ int ftkv_decode_attn_tc(const ftkv_pool* pool, int32_t num_q_heads, const uint16
                         void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Quantize-on-write of the new tokens fused into decode: what ftkv_store_quant followed by
+ * ftkv_decode_attn computes, in one launch.  The pages quantize each new K/V row when it is written
+ * ([#853 "What changes"]) and then attend over the stored rows ([#897 "Fresh R9700 stage-1 A/B"]);
+ * here the decode CTA whose key slice holds a new token writes that token's rows first, so a decode
+ * step needs no separate store launch.
+ *   k_new, v_new : device BF16 [total_q_rows][num_kv_heads][head_dim], 16-byte aligned: the K and V
+ *                  rows of the new tokens, one per query row.  Query row r of request b (R rows) is
+ *                  the token at position seq_lens[b] - R + r; its rows are quantized exactly as
+ *                  ftkv_store_quant does and written to pool row req_to_slot[b * req_stride + that
+ *                  position] before any key is read.  A position below 0 is not stored; a slot outside
+ *                  the pool is flagged (ftkv_device_errors) and not written.
+ * Every other argument, layout, the workspace rules and the errors are those of ftkv_decode_attn
+ * (warp-level kernel); k_new or v_new NULL with work to do -> FTKV_ERR_INVALID, misaligned ->
+ * FTKV_ERR_ALIGN.
+ * --------------------------------------------------------------------------------------------- */
+int ftkv_decode_attn_store(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
+                           const uint16_t* k_new, const uint16_t* v_new, const int32_t* req_to_slot,
+                           int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets,
+                           int32_t batch, int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len,
+                           float sm_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Decode without any device allocation.  The pages describe no such entry point; it exists for
  * callers that cannot allocate device memory when they need decode attention (a runtime that forbids
  * out-of-band device allocations, a plug-in that only receives buffers from its host, code that must

@@ -114,6 +114,19 @@ def test_decode_validation(lib):
     assert call_tc(q=0x1002) == _lib.FTKV_ERR_ALIGN
     assert call_tc(B=0, total=0) == _lib.FTKV_OK
 
+    def call_store(kn=0x7000, vn=0x8000, **kw):
+        a = dict(base, **kw)
+        return lib.ftkv_decode_attn_store(P(_pool()), 32, a["q"], kn, vn, a["r2s"], a["stride"], a["lens"],
+                                          a["offs"], a["B"], a["total"], a["mq"], a["maxlen"], a["sm"],
+                                          a["splits"], a["ws"], a["wsb"], a["out"], None)
+
+    assert call_store(kn=None) == _lib.FTKV_ERR_INVALID       # the fused store needs the new rows
+    assert call_store(vn=None) == _lib.FTKV_ERR_INVALID
+    assert call_store(kn=0x7008) == _lib.FTKV_ERR_ALIGN
+    assert call_store(vn=0x8004) == _lib.FTKV_ERR_ALIGN
+    assert call_store(mq=9) == _lib.FTKV_ERR_UNSUPPORTED       # the decode checks still apply
+    assert call_store(kn=None, vn=None, B=0, total=0) == _lib.FTKV_OK
+
 
 def test_prefill_validation(lib):
     for fn in (lib.ftkv_prefill_attn, lib.ftkv_prefill_attn_mma):

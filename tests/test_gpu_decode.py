@@ -221,3 +221,79 @@ def test_decode_one_hot_attention_with_huge_logits(impl):
     for h in range(4):
         assert np.abs(o[0, 8 * h] - vhat[h]).max() <= 2.0 ** -8 * np.abs(vhat[h]).max() + 1e-6
     check_attention(out, ref, "one-hot huge logits", mag)
+
+
+# ---- fused store + decode (ftkv_decode_attn_store) ----
+
+def _new_tokens(wl, L):
+    """K/V rows of each request's new tokens (its last R_b positions, one per query row; zeros for a
+    position below 0) and a mask of those tokens among the workload's tokens."""
+    R = np.diff(wl.q_row_offsets)
+    starts = np.concatenate([[0], np.cumsum(wl.seq_lens)[:-1]]).astype(np.int64)
+    total = int(wl.q_row_offsets[-1])
+    k_new = np.zeros((total, wl.Hkv, wl.head_dim), np.uint16)
+    v_new = np.zeros_like(k_new)
+    new = np.zeros(L.slots.shape[0], bool)
+    for b in range(len(wl.seq_lens)):
+        n = int(wl.seq_lens[b])
+        for r in range(int(R[b])):
+            pos = n - int(R[b]) + r
+            if pos < 0:
+                continue
+            t = starts[b] + pos
+            k_new[wl.q_row_offsets[b] + r] = L.k[t]
+            v_new[wl.q_row_offsets[b] + r] = L.v[t]
+            new[t] = True
+    return k_new, v_new, new
+
+
+@pytest.mark.parametrize("lens,rows,splits", [
+    ([512], [1], 0), ([33], [1], 1), ([4099], [1], 8), ([9000], [1], 1), ([1], [1], 0),
+    ([200, 297, 394], [3, 1, 8], 0), ([200, 297, 394], [3, 1, 8], 5), ([2, 40], [5, 3], 0), ([0, 33, 1], [1, 1, 1], 0),
+])
+def test_decode_fused_store_equals_store_then_decode(lens, rows, splits):
+    """The new tokens' rows land in the pool bit-exactly as the store kernel writes them (oracle store),
+    and the attention over them matches the oracle; new tokens split across slices and windows, rows
+    past the start of the sequence, and an empty request included."""
+    wl = inputs.decode_custom(lens, rows, max(2 * sum(lens), 64), sigma=2.0, big_frac=0.01, zero_frac=0.01,
+                              seed=sum(lens) + len(rows))
+    L = wl.layer(0)
+    k_new, v_new, new = _new_tokens(wl, L)
+    gp = ops.KVPool.empty(wl.num_rows, wl.Hkv)
+    old = ~new
+    if old.any():
+        ops.store_quant(gp, bits_to_cuda_bf16(L.k[old]), bits_to_cuda_bf16(L.v[old]),
+                        torch.from_numpy(L.slots[old]).cuda())
+    op = oracle.Pool(wl.num_rows, wl.Hkv, 128)
+    if L.slots.size:
+        oracle.store_quant(op, L.k, L.v, L.slots)
+    R = np.diff(wl.q_row_offsets)
+    out = ops.decode_attn(gp, bits_to_cuda_bf16(L.q), torch.from_numpy(wl.req_to_slot).cuda(),
+                          torch.from_numpy(wl.seq_lens).cuda(), torch.from_numpy(wl.q_row_offsets).cuda(),
+                          max_seq_len=int(wl.req_to_slot.shape[1]), max_q_rows=int(max(R.max(), 1)),
+                          sm_scale=wl.sm_scale, num_splits=splits, k_new=bits_to_cuda_bf16(k_new),
+                          v_new=bits_to_cuda_bf16(v_new))
+    s = L.slots
+    assert np.array_equal(gp.k_codes.cpu().numpy()[s], op.k_codes[s])
+    assert np.array_equal(gp.v_codes.cpu().numpy()[s], op.v_codes[s])
+    assert np.array_equal(gp.k_scales.cpu().numpy()[s].view(np.uint32), op.k_scales[s].view(np.uint32))
+    assert np.array_equal(gp.v_scales.cpu().numpy()[s].view(np.uint32), op.v_scales[s].view(np.uint32))
+    _check(out, _ref(wl, op, L), f"fused lens={lens} rows={rows} splits={splits}")
+    assert ops.device_errors() == 0
+
+
+def test_decode_fused_store_bad_slot_is_flagged_and_not_written():
+    wl = inputs.decode_custom([50], [1], 128, seed=6)
+    L = wl.layer(0)
+    k_new, v_new, new = _new_tokens(wl, L)
+    gp = ops.KVPool.empty(wl.num_rows, wl.Hkv)
+    ops.store_quant(gp, bits_to_cuda_bf16(L.k[~new]), bits_to_cuda_bf16(L.v[~new]),
+                    torch.from_numpy(L.slots[~new]).cuda())
+    before = (gp.k_codes.cpu().clone(), gp.k_scales.cpu().clone())
+    bad = torch.from_numpy(wl.req_to_slot).cuda().clone()
+    bad[0, 49] = 10 ** 6  # the new token's slot
+    ops.decode_attn(gp, bits_to_cuda_bf16(L.q), bad, torch.from_numpy(wl.seq_lens).cuda(), None, max_seq_len=50,
+                    k_new=bits_to_cuda_bf16(k_new), v_new=bits_to_cuda_bf16(v_new))
+    assert ops.device_errors() & 0x1
+    assert torch.equal(gp.k_codes.cpu(), before[0]) and torch.equal(gp.k_scales.cpu(), before[1])
+    assert ops.device_errors() == 0
