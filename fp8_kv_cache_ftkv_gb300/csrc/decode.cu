@@ -42,7 +42,6 @@ constexpr int STAGE_V = KB * kHeadDim;       // 2048 B of V codes
 constexpr int STAGE_S = KB * 4 * 2;          // 16 K scales + 16 V scales
 constexpr int STAGE_BYTES = STAGE_K + STAGE_V + STAGE_S;
 constexpr int MAX_SUB = 4096;                // slot indices staged in shared memory at a time
-constexpr int MERGE_STRIDE = 132;            // floats per (warp, row, head) in the merge area
 
 template <int RPW>
 struct Cfg;
@@ -68,11 +67,12 @@ constexpr int smem_bytes() {
   return Cfg<RPW>::WARPS * Cfg<RPW>::NSTAGE * STAGE_BYTES + MAX_SUB * 4 + q_area_bytes<RPW>();
 }
 static_assert(smem_bytes<1>() <= 227 * 1024, "decode smem");
-// in-CTA merge area: per (warp, row, head) 128 accumulators + m + l, then per (row, head) pair the
-// warp weights, M and L; rows per request: 1 for RPW = 1, up to 8 (the multi-row cap) for RPW = 2
+// in-CTA merge area: per (warp, row, head) 128 accumulators, then per (warp, row, head) m and l, then per
+// (row, head) pair the warp weights, M and L; rows per request: 1 for RPW = 1, up to 8 (the multi-row
+// cap) for RPW = 2
 template <int RPW>
 constexpr int merge_area_bytes() {
-  return (Cfg<RPW>::WARPS * RPW * 8 * MERGE_STRIDE + (RPW == 1 ? 1 : 8) * 8 * (Cfg<RPW>::WARPS + 2)) * 4;
+  return (Cfg<RPW>::WARPS * RPW * 8 * (kHeadDim + 2) + (RPW == 1 ? 1 : 8) * 8 * (Cfg<RPW>::WARPS + 2)) * 4;
 }
 static_assert(merge_area_bytes<1>() <= Cfg<1>::WARPS * Cfg<1>::NSTAGE * STAGE_BYTES, "merge");
 static_assert(merge_area_bytes<2>() <= Cfg<2>::WARPS * Cfg<2>::NSTAGE * STAGE_BYTES, "merge");
@@ -479,45 +479,49 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
       for (int off = 4; off < 32; off <<= 1) l[r][hh] += __shfl_xor_sync(0xffffffffu, l[r][hh], off);
 
   __syncthreads();  // the rings are free: reuse them as the merge area
-  float* merge = reinterpret_cast<float*>(smem);
-  float* mw = merge + WARPS * RPW * 8 * MERGE_STRIDE;  // per (row, head): wk weights, then M, L
+  // ---- merge the wk warps of each row group into this slice's partial ----
+  // Accumulator rows hold 32 float4 chunks; chunk c of head hd sits at c ^ ((hd >> 1) & 3), which makes
+  // the stores (lanes g, t write chunk 4g + q of heads 2t, 2t+1) and the loads of the sums (consecutive
+  // chunks of one head) free of bank conflicts.
+  float* macc = reinterpret_cast<float*>(smem);              // [warp][row][head][128]
+  float* wml = macc + WARPS * RPW * 8 * kHeadDim;             // [warp][row][head][2]: m, l
+  float* mw = wml + WARPS * RPW * 8 * 2;                      // per (row, head) pair: wk weights, then M, L
   if (active) {
 #pragma unroll
     for (int r = 0; r < RPW; r++) {
 #pragma unroll
       for (int hh = 0; hh < 2; hh++) {
-        float* dst = merge + ((warp * RPW + r) * 8 + 2 * t + hh) * MERGE_STRIDE;
-        float4* d4 = reinterpret_cast<float4*>(dst + 16 * g);
-        // head 2t+hh: d = 16g + 2mt -> acc[mt][hh], d = 16g + 2mt + 1 -> acc[mt][2+hh]
+        const int hd = 2 * t + hh;
+        float4* dst = reinterpret_cast<float4*>(macc + ((warp * RPW + r) * 8 + hd) * kHeadDim);
+        // head hd: d = 16g + 2mt -> acc[mt][hh], d = 16g + 2mt + 1 -> acc[mt][2+hh]; chunk 4g + q4 holds
+        // d = 16g + 4q4 .. 16g + 4q4 + 3
 #pragma unroll
         for (int q4 = 0; q4 < 4; q4++)
-          d4[q4] = make_float4(acc[r][2 * q4][hh], acc[r][2 * q4][2 + hh], acc[r][2 * q4 + 1][hh],
-                               acc[r][2 * q4 + 1][2 + hh]);
+          dst[(4 * g + q4) ^ t] = make_float4(acc[r][2 * q4][hh], acc[r][2 * q4][2 + hh], acc[r][2 * q4 + 1][hh],
+                                               acc[r][2 * q4 + 1][2 + hh]);
         if (g == 0) {
-          dst[128] = m[r][hh];
-          dst[129] = l[r][hh];
+          wml[((warp * RPW + r) * 8 + hd) * 2] = m[r][hh];
+          wml[((warp * RPW + r) * 8 + hd) * 2 + 1] = l[r][hh];
         }
       }
     }
   }
   __syncthreads();
-
-  // ---- merge the wk warps of each row group; write this slice's partial ----
-  // weights first: one warp per (row, head) pair, lane k holding warp k's maximum and sum; M and L by
-  // warp reductions, weights 2^(m_k - M)
+  // weights: one warp per (row, head) pair, lane k holding warp k's maximum and sum; M and L by warp
+  // reductions, weights 2^(m_k - M)
   const int npairs = R * a.group;
   constexpr int WSTRIDE = WARPS + 2;
   for (int pr = warp; pr < npairs; pr += WARPS) {
     const int rr = pr / a.group, hh = pr % a.group;
     const int rgi = rr / RPW, r = rr % RPW;
     const bool has = lane < wk;
-    const int idx = has ? (((rgi * wk + lane) * RPW + r) * 8 + hh) * MERGE_STRIDE : 0;
-    const float mk = has ? merge[idx + 128] : -INFINITY;
+    const int idx = has ? (((rgi * wk + lane) * RPW + r) * 8 + hh) * 2 : 0;
+    const float mk = has ? wml[idx] : -INFINITY;
     float M = mk;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float wt = (has && M != -INFINITY) ? exp2f(mk - M) : 0.0f;
-    float L = has ? wt * merge[idx + 129] : 0.0f;
+    float L = has ? wt * wml[idx + 1] : 0.0f;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     float* w = mw + pr * WSTRIDE;
@@ -528,22 +532,39 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     }
   }
   __syncthreads();
-  for (int it = threadIdx.x; it < npairs * kHeadDim; it += blockDim.x) {
-    const int d = it % kHeadDim, pr = it / kHeadDim;
-    const int rr = pr / a.group, hh = pr % a.group;
-    const int rgi = rr / RPW, r = rr % RPW;
+  // sums: item (pair, chunk) split over two adjacent lanes, even and odd warps, joined by one shuffle;
+  // npairs * 64 and blockDim.x are multiples of 32, so a warp is either fully inside the range or outside
+  constexpr int KSTEP4 = RPW * 8 * kHeadDim / 4;  // float4s from warp k to warp k + 1 of the row group
+  for (int it = threadIdx.x; it < npairs * 64; it += blockDim.x) {
+    const int half = it & 1, c = (it >> 1) & 31, pr = it >> 6;
+    const int rr = pr / a.group, hh = pr - rr * a.group;
+    const int rgi = rr / RPW, r = rr - rgi * RPW;
     const float* w = mw + pr * WSTRIDE;
-    const float* src = merge + ((rgi * wk * RPW + r) * 8 + hh) * MERGE_STRIDE + d;
-    constexpr int KSTEP = RPW * 8 * MERGE_STRIDE;  // floats from warp k to warp k + 1 of the row group
-    float A = 0.0f;
+    const float4* src = reinterpret_cast<const float4*>(macc + ((rgi * wk * RPW + r) * 8 + hh) * kHeadDim) +
+                        (c ^ ((hh >> 1) & 3));
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < WARPS; k++)
-      if (k < wk) A += w[k] * src[k * KSTEP];
-    const int64_t prow = ((row0 + rr) * a.num_q_heads + h * a.group + hh) * a.num_splits + split;
-    a.part_acc[prow * kHeadDim + d] = A;
-    if (d == 0) {
-      a.part_ml[prow * 2] = w[WARPS];
-      a.part_ml[prow * 2 + 1] = w[WARPS + 1];
+    for (int k = 0; k < WARPS; k += 2) {
+      if (k + half < wk) {
+        const float4 v = src[(k + half) * KSTEP4];
+        const float wv = w[k + half];
+        A.x = fmaf(wv, v.x, A.x);
+        A.y = fmaf(wv, v.y, A.y);
+        A.z = fmaf(wv, v.z, A.z);
+        A.w = fmaf(wv, v.w, A.w);
+      }
+    }
+    A.x += __shfl_xor_sync(0xffffffffu, A.x, 1);
+    A.y += __shfl_xor_sync(0xffffffffu, A.y, 1);
+    A.z += __shfl_xor_sync(0xffffffffu, A.z, 1);
+    A.w += __shfl_xor_sync(0xffffffffu, A.w, 1);
+    if (half == 0) {
+      const int64_t prow = ((row0 + rr) * a.num_q_heads + h * a.group + hh) * a.num_splits + split;
+      reinterpret_cast<float4*>(a.part_acc + prow * kHeadDim)[c] = A;
+      if (c == 0) {
+        a.part_ml[prow * 2] = w[WARPS];
+        a.part_ml[prow * 2 + 1] = w[WARPS + 1];
+      }
     }
   }
 
