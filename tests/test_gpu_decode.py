@@ -297,3 +297,27 @@ def test_decode_fused_store_bad_slot_is_flagged_and_not_written():
     assert ops.device_errors() & 0x1
     assert torch.equal(gp.k_codes.cpu(), before[0]) and torch.equal(gp.k_scales.cpu(), before[1])
     assert ops.device_errors() == 0
+
+
+@pytest.mark.parametrize("lens,rows", [([4099], [1]), ([3000, 70, 1], [1, 1, 1]), ([900, 2000], [4, 2])])
+def test_decode_shared_merge_state_resets_between_calls(lens, rows):
+    """Consecutive calls on one workspace: the arrival tickets left by one call must be clean for the next;
+    groups with different slice counts in one batch."""
+    wl = inputs.decode_custom(lens, rows, 2 * sum(lens) + 64, seed=len(lens) + 40)
+    gp, op, L, dev = _setup(wl)
+    R = np.diff(wl.q_row_offsets)
+    mq = int(max(R.max(), 1))
+    plan = ops.DecodePlan(wl.Hq, wl.Hkv, len(lens), int(wl.q_row_offsets[-1]), mq, int(wl.req_to_slot.shape[1]), 0,
+                          "cuda")
+    refs = _ref(wl, op, L)
+    first = None
+    for it in range(4):
+        out = ops.decode_attn(gp, dev["q"], dev["r2s"], dev["lens"], dev["offs"],
+                              max_seq_len=int(wl.req_to_slot.shape[1]), max_q_rows=mq, sm_scale=wl.sm_scale,
+                              plan=plan)
+        _check(out, refs, f"call {it}")
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out, first)
+    assert ops.device_errors() == 0
