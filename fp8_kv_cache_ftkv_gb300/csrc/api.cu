@@ -150,7 +150,7 @@ size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, in
     return 0;
   if (num_splits <= 0 || num_splits > FTKV_MAX_SPLITS) num_splits = FTKV_MAX_SPLITS;
   const int64_t parts = total_q_rows * num_q_heads * num_splits;
-  const int64_t ctr = ceil_div(int64_t(batch) * num_kv_heads * 4, 256) * 256;
+  const int64_t ctr = ceil_div((int64_t(batch) * num_kv_heads + 2) * 4, 256) * 256;  // + the grid barrier
   return static_cast<size_t>(ws_acc_bytes(parts) + ws_ml_bytes(parts) + ctr);
 }
 
@@ -230,6 +230,7 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   a.part_acc = part_acc;
   a.part_ml = part_ml;
   a.counters = counters;
+  a.gbar = counters + int64_t(batch) * pool->num_kv_heads;
   a.out = out;
   a.err = di->err_word;
   a.use_tc = use_tc ? 1 : 0;

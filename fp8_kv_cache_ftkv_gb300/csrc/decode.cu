@@ -113,6 +113,133 @@ __device__ __forceinline__ int64_t clamp_seq_len(const DecodeArgs& a, int b, boo
   return n;
 }
 
+// ---- cooperative finish: the split merge after a grid barrier, spread over every warp of the grid ----
+// Used when the whole grid is resident at once (cooperative launch).  Every CTA calls it exactly once,
+// after publishing its partials (or instead of doing anything, if its slice holds no keys).  The barrier
+// waits until every CTA has arrived; then output item (query row, query head, quarter of d) i goes to warp
+// i / ncta of CTA i % ncta and merges that (row, head)'s slices (same arithmetic as the ticket merge:
+// M = max m_s, L = sum 2^(m_s - M) l_s, o = sum 2^(m_s - M) A_s / L).  The CTA that finishes last resets
+// the barrier for the next call.  All waits are bounded (a timeout is flagged).
+template <int WARPS>
+__device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ncta = gridDim.x * gridDim.y * gridDim.z;
+  const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  __threadfence();  // this CTA's partials before its arrival
+  __syncthreads();
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    atomicAdd(a.gbar, 1);
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    int v = 0;
+    bool ok = false;
+    for (;;) {
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.gbar) : "memory");
+      if (v >= ncta) {
+        ok = true;
+        break;
+      }
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > 2000000000ull) break;
+      __nanosleep(32);
+    }
+    if (!ok) flag_error(a.err, kDevErrTimeout);
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (s_ok) {
+    const int64_t items = a.total_q_rows * a.num_q_heads * 4;
+    const int d4 = lane & 7, sg = lane >> 3;  // 4 d values, slice group (slices sg, sg + 4, ...)
+    for (int64_t it = cta + static_cast<int64_t>(ncta) * warp; it < items; it += static_cast<int64_t>(ncta) * WARPS) {
+      const int64_t t = it / (a.num_q_heads * 4);  // query row
+      const int rem = static_cast<int>(it - t * a.num_q_heads * 4);
+      const int qh = rem >> 2, qd = rem & 3;
+      int b = static_cast<int>(t), R = 1;
+      if (a.q_row_offsets) {  // request of row t
+        int lo = 0, hi = a.batch;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (a.q_row_offsets[mid + 1] <= t) lo = mid + 1; else hi = mid;
+        }
+        b = lo;
+        if (b >= a.batch) continue;
+        const int64_t r0 = a.q_row_offsets[b];
+        R = a.q_row_offsets[b + 1] - a.q_row_offsets[b];
+        if (R < 0 || R > a.max_q_rows || r0 < 0 || r0 + R > a.total_q_rows) continue;  // skipped request
+      }
+      int64_t n = a.seq_lens[b];
+      const int64_t nmax = a.max_seq_len < a.req_stride ? a.max_seq_len : a.req_stride;
+      n = n < 0 ? 0 : (n > nmax ? nmax : n);
+      const int64_t nsl64 = (n + a.chunk - 1) / a.chunk;
+      const int nslices = static_cast<int>(nsl64 < a.num_splits ? nsl64 : a.num_splits);
+      uint16_t* dst = a.out + (t * a.num_q_heads + qh) * kHeadDim + qd * 32;
+      if (nslices == 0) {  // no keys: zeros
+        dst[lane] = 0;
+        continue;
+      }
+      const int64_t prow0 = (t * a.num_q_heads + qh) * a.num_splits;
+      const bool h0 = lane < nslices, h1 = lane + 32 < nslices;
+      const float2 ml0 = h0 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml) + prow0 + lane) : make_float2(-INFINITY, 0.f);
+      const float2 ml1 = h1 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml) + prow0 + lane + 32) : make_float2(-INFINITY, 0.f);
+      float4 v[8];
+      auto load8 = [&](int k0) {  // slices sg + 4k, k = k0 .. k0 + 7
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          const int sl = sg + 4 * (k0 + k);
+          v[k] = (sl < nslices)
+                     ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (prow0 + sl) * kHeadDim + qd * 32) + d4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      };
+      load8(0);
+      float M = fmaxf(ml0.x, ml1.x);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float e0 = (h0 && M != -INFINITY) ? exp2f(ml0.x - M) : 0.0f;
+      const float e1 = (h1 && M != -INFINITY) ? exp2f(ml1.x - M) : 0.0f;
+      float L = (h0 ? e0 * ml0.y : 0.0f) + (h1 ? e1 * ml1.y : 0.0f);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+      const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
+      const float w0 = e0 * invL, w1 = e1 * invL;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      auto fold8 = [&](int k0) {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          const int sl = sg + 4 * (k0 + k);
+          const float wa = __shfl_sync(0xffffffffu, w0, sl & 31), wb = __shfl_sync(0xffffffffu, w1, sl & 31);
+          const float wv = (sl < nslices) ? (sl < 32 ? wa : wb) : 0.0f;
+          o.x = fmaf(wv, v[k].x, o.x);
+          o.y = fmaf(wv, v[k].y, o.y);
+          o.z = fmaf(wv, v[k].z, o.z);
+          o.w = fmaf(wv, v[k].w, o.w);
+        }
+      };
+      fold8(0);
+      if (nslices > 32) {  // warp-uniform
+        load8(8);
+        fold8(8);
+      }
+#pragma unroll
+      for (int off = 8; off < 32; off <<= 1) {
+        o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
+        o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
+        o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
+        o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
+      }
+      if (sg == 0)
+        *reinterpret_cast<uint2*>(dst + 4 * d4) = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(a.gbar + 1, 1) == ncta - 1) {  // every CTA is past the barrier
+    a.gbar[0] = 0;
+    a.gbar[1] = 0;
+  }
+}
+
 template <int RPW>
 __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(const DecodeArgs a) {
   pdl_enter();
@@ -139,6 +266,7 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   }
   if (R < 0 || R > a.max_q_rows || row0 < 0 || row0 + R > a.total_q_rows) {
     if (threadIdx.x == 0 && split == 0 && h == 0) flag_error(a.err, kDevErrQRows);
+    if (a.coop) coop_finish<WARPS>(a);
     return;  // inconsistent row offsets: skip the request rather than read outside q
   }
   if (n == 0) {  // no keys: the rows of this KV head's group are zero
@@ -146,12 +274,16 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
       for (int i = threadIdx.x; i < R * a.group * kHeadDim; i += blockDim.x)
         a.out[((row0 + i / (a.group * kHeadDim)) * a.num_q_heads + h * a.group + (i / kHeadDim) % a.group) *
                   kHeadDim + i % kHeadDim] = 0;
+    if (a.coop) coop_finish<WARPS>(a);
     return;
   }
   // key indices fit in 32 bits (the host rejects max_seq_len >= 2^31)
   const int j0 = split * static_cast<int>(a.chunk);
   const int j1 = (static_cast<int64_t>(j0) + a.chunk < n) ? j0 + static_cast<int>(a.chunk) : static_cast<int>(n);
-  if (j0 >= n || R == 0) return;  // slices past the end hold no keys and take no ticket
+  if (j0 >= n || R == 0) {  // slices past the end hold no keys and take no ticket
+    if (a.coop) coop_finish<WARPS>(a);
+    return;
+  }
 
   // ---- warp roles: row group rg (RPW query rows) x key-interleave index kw ----
   const int nrg = (R + RPW - 1) / RPW;
@@ -568,6 +700,10 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     }
   }
 
+  if (a.coop) {
+    coop_finish<WARPS>(a);
+    return;
+  }
   // ---- split merge, done by the last slice of (request, KV head) to arrive ----
   // Every slice publishes its partial, then takes a ticket; the CTA that draws the last ticket merges
   // all slices (o = sum_s 2^(M_s - M) A_s / sum_s 2^(M_s - M) L_s) and resets the counter for the
@@ -602,7 +738,22 @@ cudaError_t launch_split(const DecodeArgs& a, cudaStream_t s) {
     configured[dev] = true;
   }
   dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-  return launch_k(decode_split_kernel<RPW>, grid, dim3(Cfg<RPW>::WARPS * 32), smem_bytes<RPW>(), s, a);
+  // a grid that fits on the GPU at once is launched cooperatively and merges after a grid barrier
+  static int resident[64] = {};  // co-resident CTAs per device (0: not known yet, -1: no cooperative launch)
+  if (dev >= 0 && dev < 64 && resident[dev] == 0) {
+    int coop_ok = 0, sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&coop_ok, cudaDevAttrCooperativeLaunch, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<RPW>, Cfg<RPW>::WARPS * 32,
+                                                      smem_bytes<RPW>()) != cudaSuccess)
+      per_sm = 0;
+    resident[dev] = (coop_ok && per_sm > 0 && sms > 0) ? per_sm * sms : -1;
+  }
+  DecodeArgs c = a;
+  const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
+  c.coop = (dev >= 0 && dev < 64 && resident[dev] > 0 && ctas <= resident[dev]) ? 1 : 0;
+  if (c.coop) return launch_k_coop(decode_split_kernel<RPW>, grid, dim3(Cfg<RPW>::WARPS * 32), smem_bytes<RPW>(), s, c);
+  return launch_k(decode_split_kernel<RPW>, grid, dim3(Cfg<RPW>::WARPS * 32), smem_bytes<RPW>(), s, c);
 }
 
 }  // namespace

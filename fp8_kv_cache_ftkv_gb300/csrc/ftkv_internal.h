@@ -62,6 +62,8 @@ struct DecodeArgs {
   uint16_t* out;             // [total_q_rows][Hq][128]
   int* err;
   int use_tc;                // 1: the tcgen05 kernel (single-row batches only)
+  int coop;                  // set by the launcher: cooperative launch, merge after a grid barrier
+  int* gbar;                 // [2] grid-barrier arrivals and finished CTAs; zero between calls
   const uint16_t* k_new;     // fused store: [total_q_rows][Hkv][128] K of the new tokens, or null
   const uint16_t* v_new;     //              V of the new tokens
 };
@@ -95,6 +97,25 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// Same, as a cooperative launch: every CTA of the grid is resident at once (the launch fails otherwise).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2]{};
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
