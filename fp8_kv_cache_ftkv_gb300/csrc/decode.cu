@@ -116,8 +116,8 @@ __device__ __forceinline__ int64_t clamp_seq_len(const DecodeArgs& a, int b, boo
 // ---- cooperative finish: the split merge after a grid barrier, spread over every warp of the grid ----
 // Used when the whole grid is resident at once (cooperative launch).  Every CTA calls it exactly once,
 // after publishing its partials (or instead of doing anything, if its slice holds no keys).  The barrier
-// waits until every CTA has arrived; then output item (query row, query head, quarter of d) i goes to warp
-// i / ncta of CTA i % ncta and merges that (row, head)'s slices (same arithmetic as the ticket merge:
+// waits until every CTA has arrived; then output item (query row, query head, 16 of the 128 d) i goes to
+// warp i / ncta of CTA i % ncta and merges that (row, head)'s slices (same arithmetic as the ticket merge:
 // M = max m_s, L = sum 2^(m_s - M) l_s, o = sum 2^(m_s - M) A_s / L).  The CTA that finishes last resets
 // the barrier for the next call.  All waits are bounded (a timeout is flagged).
 template <int WARPS>
@@ -150,12 +150,12 @@ __device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
   }
   __syncthreads();
   if (s_ok) {
-    const int64_t items = a.total_q_rows * a.num_q_heads * 4;
-    const int d4 = lane & 7, sg = lane >> 3;  // 4 d values, slice group (slices sg, sg + 4, ...)
+    const int64_t items = a.total_q_rows * a.num_q_heads * 8;
+    const int d4 = lane & 3, sg = lane >> 2;  // 4 d values, slice group (slices sg, sg + 8, ...)
     for (int64_t it = cta + static_cast<int64_t>(ncta) * warp; it < items; it += static_cast<int64_t>(ncta) * WARPS) {
-      const int64_t t = it / (a.num_q_heads * 4);  // query row
-      const int rem = static_cast<int>(it - t * a.num_q_heads * 4);
-      const int qh = rem >> 2, qd = rem & 3;
+      const int64_t t = it / (a.num_q_heads * 8);  // query row
+      const int rem = static_cast<int>(it - t * a.num_q_heads * 8);
+      const int qh = rem >> 3, qd = rem & 7;
       int b = static_cast<int>(t), R = 1;
       if (a.q_row_offsets) {  // request of row t
         int lo = 0, hi = a.batch;
@@ -174,26 +174,22 @@ __device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
       n = n < 0 ? 0 : (n > nmax ? nmax : n);
       const int64_t nsl64 = (n + a.chunk - 1) / a.chunk;
       const int nslices = static_cast<int>(nsl64 < a.num_splits ? nsl64 : a.num_splits);
-      uint16_t* dst = a.out + (t * a.num_q_heads + qh) * kHeadDim + qd * 32;
+      uint16_t* dst = a.out + (t * a.num_q_heads + qh) * kHeadDim + qd * 16;
       if (nslices == 0) {  // no keys: zeros
-        dst[lane] = 0;
+        if (lane < 16) dst[lane] = 0;
         continue;
       }
       const int64_t prow0 = (t * a.num_q_heads + qh) * a.num_splits;
       const bool h0 = lane < nslices, h1 = lane + 32 < nslices;
       const float2 ml0 = h0 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml) + prow0 + lane) : make_float2(-INFINITY, 0.f);
       const float2 ml1 = h1 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml) + prow0 + lane + 32) : make_float2(-INFINITY, 0.f);
-      float4 v[8];
-      auto load8 = [&](int k0) {  // slices sg + 4k, k = k0 .. k0 + 7
+      float4 v[8];  // slices sg + 8k (all 64 slices at most), every load in flight at once
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-          const int sl = sg + 4 * (k0 + k);
-          v[k] = (sl < nslices)
-                     ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (prow0 + sl) * kHeadDim + qd * 32) + d4)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      };
-      load8(0);
+      for (int k = 0; k < 8; k++) {
+        const int sl = sg + 8 * k;
+        v[k] = (sl < nslices) ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (prow0 + sl) * kHeadDim + qd * 16) + d4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       float M = fmaxf(ml0.x, ml1.x);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -205,25 +201,18 @@ __device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
       const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
       const float w0 = e0 * invL, w1 = e1 * invL;
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      auto fold8 = [&](int k0) {
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-          const int sl = sg + 4 * (k0 + k);
-          const float wa = __shfl_sync(0xffffffffu, w0, sl & 31), wb = __shfl_sync(0xffffffffu, w1, sl & 31);
-          const float wv = (sl < nslices) ? (sl < 32 ? wa : wb) : 0.0f;
-          o.x = fmaf(wv, v[k].x, o.x);
-          o.y = fmaf(wv, v[k].y, o.y);
-          o.z = fmaf(wv, v[k].z, o.z);
-          o.w = fmaf(wv, v[k].w, o.w);
-        }
-      };
-      fold8(0);
-      if (nslices > 32) {  // warp-uniform
-        load8(8);
-        fold8(8);
+      for (int k = 0; k < 8; k++) {
+        const int sl = sg + 8 * k;
+        const float wa = __shfl_sync(0xffffffffu, w0, sl & 31), wb = __shfl_sync(0xffffffffu, w1, sl & 31);
+        const float wv = (sl < nslices) ? (sl < 32 ? wa : wb) : 0.0f;
+        o.x = fmaf(wv, v[k].x, o.x);
+        o.y = fmaf(wv, v[k].y, o.y);
+        o.z = fmaf(wv, v[k].z, o.z);
+        o.w = fmaf(wv, v[k].w, o.w);
       }
 #pragma unroll
-      for (int off = 8; off < 32; off <<= 1) {
+      for (int off = 4; off < 32; off <<= 1) {
         o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
         o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
         o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
