@@ -45,7 +45,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["decode", "store", "reconstruct", "prefill", "prefill_mma"],
+    p.add_argument("--workload", choices=["decode", "store", "reconstruct", "prefill", "prefill_mma",
+                                          "decode_batched"],
                    default="decode")
     p.add_argument("--context", type=int, default=32768)
     p.add_argument("--pool-rows", type=int, default=33059)
@@ -426,6 +427,30 @@ def run_kernel_workload(args, world, rank, local, torch, ops, inputs, device, hb
                 ops.store_quant(pool, k, v, slots)
         T = wl.slots.shape[0]
         nbytes = wl.layers * (T * HKV * D * 2 * 2 + T * (HKV * D + HKV * 4) * 2 + T * 4)
+        unit_flops = None
+    elif args.workload == "decode_batched":
+        # 64 requests, context ~ U[1,024, 40,000], 1-8 query rows each, one layer of a 2,000,000-row pool;
+        # 4 launches per iteration over the same pool (1.4 GB of rows: far beyond L2)
+        wl = inputs.decode_batched()
+        L = wl.layer(0)
+        pool = ops.KVPool.empty(wl.num_rows, HKV, device=device)
+        ops.store_quant(pool, to_dev(L.k), to_dev(L.v), torch.from_numpy(L.slots).to(device))
+        del L.k, L.v
+        q_d = to_dev(L.q)
+        r2s = torch.from_numpy(wl.req_to_slot).to(device)
+        lens = torch.from_numpy(wl.seq_lens).to(device)
+        offs = torch.from_numpy(wl.q_row_offsets).to(device)
+        mq = int(np.diff(wl.q_row_offsets).max())
+        stride = int(wl.req_to_slot.shape[1])
+        plan = ops.DecodePlan(HQ, HKV, len(wl.seq_lens), int(wl.q_row_offsets[-1]), mq, stride, 0, device)
+        out = torch.empty_like(q_d)
+
+        def work():
+            for _ in range(4):
+                ops.decode_attn(pool, q_d, r2s, lens, offs, max_seq_len=stride, max_q_rows=mq, plan=plan, out=out)
+        keys = int(wl.seq_lens.sum())
+        rows = int(wl.q_row_offsets[-1])
+        nbytes = 4 * (keys * (HKV * D * 2 + HKV * 4 * 2 + 4) + rows * HQ * D * 2 * 2)
         unit_flops = None
     elif args.workload == "reconstruct":
         wl = inputs.prefill()
