@@ -165,7 +165,8 @@ def reduce_max(value: float, world: int):
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    on_gpu = dist.get_backend() == "nccl"
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
