@@ -127,7 +127,10 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
 size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                    int32_t batch, int64_t total_q_rows, int32_t num_splits);
 
-/* Number of key slices the automatic choice uses for this shape (what num_splits = 0 resolves to). */
+/* Number of key slices the automatic choice uses for this shape (what num_splits = 0 resolves to):
+ * with few (request, KV head) groups, as many as fill the GPU in one wave of CTAs; with many, enough for
+ * about eight waves, so that long requests are cut into balanced pieces; at least ~128 keys per slice,
+ * at most FTKV_MAX_SPLITS. */
 int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max_seq_len,
                                 int32_t max_q_rows);
 
