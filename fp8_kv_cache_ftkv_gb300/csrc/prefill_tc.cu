@@ -5,7 +5,10 @@
 //
 // One CTA = 128 query rows of one query head (grid: query tiles x heads, heaviest tiles first).
 // Key tiles of 128 keys come first from the prefix workspace, then from the chunk (causal tiles only).
-//   warp 0      : TMEM allocation; lane 0 issues TMA loads (Q once, then K/V tiles into a 2-stage ring)
+//   warp 0      : TMEM allocation; lane 0 issues the TMA loads of Q and of the K tiles into a 2-stage K ring
+//   warp 6      : lane 0 issues the TMA loads of the V tiles into a 2-stage V ring.  A K stage is refilled as
+//                 soon as its QK product is done, a V stage once its PV product is done (one shared K+V
+//                 stage waited for the PV product, which exposed the tile load latency in every tile)
 //   warp 1      : lane 0 issues tcgen05.mma: S_j = Q K_j^T into one of two TMEM S buffers, then
 //                 O += P_{j-1} V_{j-1} into the TMEM O accumulator (so QK of the next tile overlaps
 //                 the softmax of the current one)
@@ -35,7 +38,7 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_KV = OFF_Q + TILE_BYTES;                 // stage s: K at +s*2*TILE, V at +TILE
 constexpr uint32_t OFF_P = OFF_KV + 2 * 2 * TILE_BYTES;         // P buffer b at +b*TILE
 constexpr uint32_t OFF_BAR = OFF_P + 2 * TILE_BYTES;
-constexpr int NBAR = 14;
+constexpr int NBAR = 18;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;              // TMEM base address, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;              // slack for the 1024-byte alignment
@@ -43,7 +46,7 @@ static_assert(SMEM_ALLOC <= 232448, "prefill_tc shared memory");
 
 // barrier indices
 constexpr int B_QFULL = 0, B_FULL0 = 1, B_EMPTY0 = 3, B_SFULL0 = 5, B_SFREE0 = 7, B_PFULL0 = 9, B_ODONE = 11,
-              B_OFINAL = 12, B_DRAIN = 13;
+              B_OFINAL = 12, B_DRAIN = 13, B_FULLV0 = 14, B_EMPTYV0 = 16;  // FULL/EMPTY: K tiles; FULLV/EMPTYV: V
 
 constexpr uint32_t TMEM_COLS = 512;        // S0 [0,128) S1 [128,256) O [256,384)
 constexpr uint32_t TMEM_O = 256;
@@ -210,7 +213,9 @@ __device__ __forceinline__ float fmax3(float x, float y, float z) {
   return d;
 }
 
-__global__ void __launch_bounds__(192, 1)
+constexpr int NTHREADS = 224;  // K producer, MMA issuer, 4 softmax warps, V producer
+
+__global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkc,
                       const __grid_constant__ CUtensorMap tvc, const __grid_constant__ CUtensorMap twk,
                       const __grid_constant__ CUtensorMap twv, const TcArgs a) {
@@ -238,6 +243,8 @@ __global__ void __launch_bounds__(192, 1)
     for (int s = 0; s < 2; s++) {
       mbar_init(bar(B_FULL0 + s), 1);
       mbar_init(bar(B_EMPTY0 + s), 1);
+      mbar_init(bar(B_FULLV0 + s), 1);
+      mbar_init(bar(B_EMPTYV0 + s), 1);
       mbar_init(bar(B_SFULL0 + s), 1);
       mbar_init(bar(B_SFREE0 + s), 128);
       mbar_init(bar(B_PFULL0 + s), 128);
@@ -259,31 +266,32 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + OFF_MISC);
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      mbar_expect_tx(bar(B_QFULL), TILE_BYTES);
-      tma_load_3d(base + OFF_Q, &tq, bar(B_QFULL), 0, hq, t0);
-      tma_load_3d(base + OFF_Q + BOX_BYTES, &tq, bar(B_QFULL), 64, hq, t0);
+      // ---------------- TMA producers: warp 0 Q and the K tiles, warp 6 the V tiles ----------------
+      const bool is_k = warp == 0;
+      if (is_k) {
+        mbar_expect_tx(bar(B_QFULL), TILE_BYTES);
+        tma_load_3d(base + OFF_Q, &tq, bar(B_QFULL), 0, hq, t0);
+        tma_load_3d(base + OFF_Q + BOX_BYTES, &tq, bar(B_QFULL), 64, hq, t0);
+      }
+      const int FULL = is_k ? B_FULL0 : B_FULLV0, EMPTY = is_k ? B_EMPTY0 : B_EMPTYV0;
       int issued = 0;
       for (int j = 0; j < T; j++) {
         const int s = j & 1;
-        if (j >= 2 && !mbar_wait(bar(B_EMPTY0 + s), ((j >> 1) - 1) & 1, abort_flag, a.err)) break;
+        if (j >= 2 && !mbar_wait(bar(EMPTY + s), ((j >> 1) - 1) & 1, abort_flag, a.err)) break;
         const bool pre = j < nPT;
-        const CUtensorMap* mk = pre ? &twk : &tkc;
-        const CUtensorMap* mv = pre ? &twv : &tvc;
+        const CUtensorMap* m = is_k ? (pre ? &twk : &tkc) : (pre ? &twv : &tvc);
         const int row = pre ? j * BN : (j - nPT) * BN;
-        const uint32_t dk = base + OFF_KV + s * 2 * TILE_BYTES, dv = dk + TILE_BYTES;
-        mbar_expect_tx(bar(B_FULL0 + s), 2 * TILE_BYTES);
-        tma_load_3d(dk, mk, bar(B_FULL0 + s), 0, hk, row);
-        tma_load_3d(dk + BOX_BYTES, mk, bar(B_FULL0 + s), 64, hk, row);
-        tma_load_3d(dv, mv, bar(B_FULL0 + s), 0, hk, row);
-        tma_load_3d(dv + BOX_BYTES, mv, bar(B_FULL0 + s), 64, hk, row);
+        const uint32_t d = base + OFF_KV + s * 2 * TILE_BYTES + (is_k ? 0 : TILE_BYTES);
+        mbar_expect_tx(bar(FULL + s), TILE_BYTES);
+        tma_load_3d(d, m, bar(FULL + s), 0, hk, row);
+        tma_load_3d(d + BOX_BYTES, m, bar(FULL + s), 64, hk, row);
         issued = j + 1;
       }
       // drain: every issued load must land before the CTA may exit
-      mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; j++) mbar_wait(bar(B_FULL0 + (j & 1)), (j >> 1) & 1, abort_flag, a.err);
+      if (is_k) mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
+      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; j++) mbar_wait(bar(FULL + (j & 1)), (j >> 1) & 1, abort_flag, a.err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -294,13 +302,14 @@ __global__ void __launch_bounds__(192, 1)
       auto issue_pv = [&](int i) -> bool {
         const int b = i & 1;
         if (!mbar_wait(bar(B_PFULL0 + b), (i >> 1) & 1, abort_flag, a.err)) return false;
+        if (!mbar_wait(bar(B_FULLV0 + b), (i >> 1) & 1, abort_flag, a.err)) return false;
         tc_fence_after();
         const uint32_t pt = base + OFF_P + b * TILE_BYTES;
         const uint32_t vt = base + OFF_KV + (i & 1) * 2 * TILE_BYTES + TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++)
           umma_bf16(tmem + TMEM_O, kmajor_desc(pt, kk), vtile_desc(vt, kk), IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_EMPTY0 + (i & 1)));
+        umma_commit(bar(B_EMPTYV0 + (i & 1)));
         umma_commit(bar(B_ODONE));
         return true;
       };
@@ -314,6 +323,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int kk = 0; kk < 8; kk++)
           umma_bf16(tmem + s * 128, kmajor_desc(base + OFF_Q, kk), kmajor_desc(kt, kk), IDESC_QK, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL0 + s));
+        umma_commit(bar(B_EMPTY0 + s));  // K tile j is consumed once its QK product is done
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok && issue_pv(T - 1)) umma_commit(bar(B_OFINAL));
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(192, 1)
       umma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, abort_flag, a.err);
     }
-  } else {
+  } else {  // warps 2..5
     // ---------------- softmax: one query row per thread ----------------
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -501,7 +511,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   t.out = a.out;
   t.err = a.err;
   dim3 grid(t.n_q_tiles, a.num_q_heads);
-  return launch_k(prefill_tc_kernel, grid, dim3(192), SMEM_ALLOC, s, tq, tkc, tvc, twk, twv, t);
+  return launch_k(prefill_tc_kernel, grid, dim3(NTHREADS), SMEM_ALLOC, s, tq, tkc, tvc, twk, twv, t);
 }
 
 }  // namespace ftkv
