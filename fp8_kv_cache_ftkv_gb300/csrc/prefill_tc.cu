@@ -5,19 +5,20 @@
 //
 // One CTA = 128 query rows of one query head (grid: query tiles x heads, heaviest tiles first).
 // Key tiles of 128 keys come first from the prefix workspace, then from the chunk (causal tiles only).
-//   warp 0      : TMEM allocation; lane 0 issues the TMA loads of Q and of the K tiles into a 2-stage K ring
-//   warp 6      : lane 0 issues the TMA loads of the V tiles into a 2-stage V ring.  A K stage is refilled as
+//   warp 0      : TMEM allocation; lane 0 issues the TMA loads of Q and of the K tiles into a 3-stage K ring
+//   warp 6      : lane 0 issues the TMA loads of the V tiles into a 3-stage V ring.  A K stage is refilled as
 //                 soon as its QK product is done, a V stage once its PV product is done (one shared K+V
 //                 stage waited for the PV product, which exposed the tile load latency in every tile)
 //   warp 1      : lane 0 issues tcgen05.mma: S_j = Q K_j^T into one of two TMEM S buffers, then
-//                 O += P_{j-1} V_{j-1} into the TMEM O accumulator (so QK of the next tile overlaps
-//                 the softmax of the current one)
+//                 O += P_{j-1} V_{j-1} into the TMEM O accumulator, P read from TMEM (so QK of the next
+//                 tile overlaps the softmax of the current one)
 //   warps 2..5  : softmax, one query row per thread (= one TMEM lane): reads S_j from TMEM, keeps the
 //                 running max/sum in registers (the max on raw scores, the scale folded into the exponent's
-//                 FMA; packed f32x2 arithmetic and three-input max), writes P_j (BF16) to shared memory in the layout the
-//                 MMA reads, and rescales the O row in TMEM only when the running max grew by more than
-//                 8 (log2 units), so the O correction is rare
-// Operands: Q, K, P are K-major with the 128-byte swizzle; V is MN-major (keys x d, d contiguous) with
+//                 FMA; packed f32x2 arithmetic and three-input max), writes P_j (BF16 pairs) into one of
+//                 two TMEM P buffers (its own lane), and rescales the O row in TMEM only when the running
+//                 max grew by more than 8 (log2 units), so the O correction is rare.  Keeping P in TMEM
+//                 leaves the shared memory to the Q tile and the two 3-stage rings
+// Operands: Q, K are K-major with the 128-byte swizzle; P is the TMEM A operand of the PV product; V is MN-major (keys x d, d contiguous) with
 // the 128-byte swizzle, read directly by the tensor core.  Every mbarrier wait is bounded in time; on
 // expiry the CTA records an error flag, drains its outstanding operations and exits.
 #include <cuda.h>
@@ -35,21 +36,23 @@ constexpr uint32_t BOX_BYTES = 128 * 128;  // one TMA box: 128 rows x 64 BF16 (1
 constexpr uint32_t TILE_BYTES = 2 * BOX_BYTES;  // 128 rows x 128 BF16
 // shared-memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = OFF_Q + TILE_BYTES;                 // stage s: K at +s*2*TILE, V at +TILE
-constexpr uint32_t OFF_P = OFF_KV + 2 * 2 * TILE_BYTES;         // P buffer b at +b*TILE
-constexpr uint32_t OFF_BAR = OFF_P + 2 * TILE_BYTES;
-constexpr int NBAR = 18;
+constexpr int NS = 3;                                            // stages of the K ring and of the V ring
+constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;                   // K stage s at +s*TILE
+constexpr uint32_t OFF_V = OFF_K + NS * TILE_BYTES;              // V stage s at +s*TILE
+constexpr uint32_t OFF_BAR = OFF_V + NS * TILE_BYTES;
+constexpr int NBAR = 22;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;              // TMEM base address, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;              // slack for the 1024-byte alignment
 static_assert(SMEM_ALLOC <= 232448, "prefill_tc shared memory");
 
 // barrier indices
-constexpr int B_QFULL = 0, B_FULL0 = 1, B_EMPTY0 = 3, B_SFULL0 = 5, B_SFREE0 = 7, B_PFULL0 = 9, B_ODONE = 11,
-              B_OFINAL = 12, B_DRAIN = 13, B_FULLV0 = 14, B_EMPTYV0 = 16;  // FULL/EMPTY: K tiles; FULLV/EMPTYV: V
+constexpr int B_QFULL = 0, B_FULL0 = 1, B_EMPTY0 = 4, B_FULLV0 = 7, B_EMPTYV0 = 10,  // K ring, V ring (NS each)
+              B_SFULL0 = 13, B_SFREE0 = 15, B_PFULL0 = 17, B_ODONE = 19, B_OFINAL = 20, B_DRAIN = 21;
 
-constexpr uint32_t TMEM_COLS = 512;        // S0 [0,128) S1 [128,256) O [256,384)
+constexpr uint32_t TMEM_COLS = 512;        // S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512)
 constexpr uint32_t TMEM_O = 256;
+constexpr uint32_t TMEM_P = 384;           // P buffer b: 128 keys as 64 columns of packed BF16 pairs
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;   // 4 s
 
 struct TcArgs {
@@ -136,6 +139,15 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
   asm volatile(
       "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D += A B with A read from tensor memory (128 lanes = rows, 8 columns = 16 BF16 of K) and B from shared memory
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -240,11 +252,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
-    for (int s = 0; s < 2; s++) {
+    for (int s = 0; s < NS; s++) {
       mbar_init(bar(B_FULL0 + s), 1);
       mbar_init(bar(B_EMPTY0 + s), 1);
       mbar_init(bar(B_FULLV0 + s), 1);
       mbar_init(bar(B_EMPTYV0 + s), 1);
+    }
+    for (int s = 0; s < 2; s++) {
       mbar_init(bar(B_SFULL0 + s), 1);
       mbar_init(bar(B_SFREE0 + s), 128);
       mbar_init(bar(B_PFULL0 + s), 128);
@@ -278,12 +292,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int FULL = is_k ? B_FULL0 : B_FULLV0, EMPTY = is_k ? B_EMPTY0 : B_EMPTYV0;
       int issued = 0;
       for (int j = 0; j < T; j++) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(bar(EMPTY + s), ((j >> 1) - 1) & 1, abort_flag, a.err)) break;
+        const int s = j % NS, use = j / NS;  // stage, and how often it was filled before
+        if (use >= 1 && !mbar_wait(bar(EMPTY + s), (use - 1) & 1, abort_flag, a.err)) break;
         const bool pre = j < nPT;
         const CUtensorMap* m = is_k ? (pre ? &twk : &tkc) : (pre ? &twv : &tvc);
         const int row = pre ? j * BN : (j - nPT) * BN;
-        const uint32_t d = base + OFF_KV + s * 2 * TILE_BYTES + (is_k ? 0 : TILE_BYTES);
+        const uint32_t d = base + (is_k ? OFF_K : OFF_V) + s * TILE_BYTES;
         mbar_expect_tx(bar(FULL + s), TILE_BYTES);
         tma_load_3d(d, m, bar(FULL + s), 0, hk, row);
         tma_load_3d(d + BOX_BYTES, m, bar(FULL + s), 64, hk, row);
@@ -291,7 +305,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // drain: every issued load must land before the CTA may exit
       if (is_k) mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; j++) mbar_wait(bar(FULL + (j & 1)), (j >> 1) & 1, abort_flag, a.err);
+      for (int j = (issued > NS ? issued - NS : 0); j < issued; j++) mbar_wait(bar(FULL + j % NS), (j / NS) & 1, abort_flag, a.err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -300,30 +314,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t IDESC_PV = idesc_bf16(true);
       bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
       auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1;
+        const int b = i & 1, sv = i % NS;
         if (!mbar_wait(bar(B_PFULL0 + b), (i >> 1) & 1, abort_flag, a.err)) return false;
-        if (!mbar_wait(bar(B_FULLV0 + b), (i >> 1) & 1, abort_flag, a.err)) return false;
+        if (!mbar_wait(bar(B_FULLV0 + sv), (i / NS) & 1, abort_flag, a.err)) return false;
         tc_fence_after();
-        const uint32_t pt = base + OFF_P + b * TILE_BYTES;
-        const uint32_t vt = base + OFF_KV + (i & 1) * 2 * TILE_BYTES + TILE_BYTES;
+        const uint32_t vt = base + OFF_V + sv * TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++)
-          umma_bf16(tmem + TMEM_O, kmajor_desc(pt, kk), vtile_desc(vt, kk), IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_EMPTYV0 + (i & 1)));
+          umma_bf16_ta(tmem + TMEM_O, tmem + TMEM_P + b * 64 + kk * 8, vtile_desc(vt, kk), IDESC_PV,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_EMPTYV0 + sv));
         umma_commit(bar(B_ODONE));
         return true;
       };
       for (int j = 0; ok && j < T; j++) {
         const int s = j & 1;
-        if (!mbar_wait(bar(B_FULL0 + s), (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+        if (!mbar_wait(bar(B_FULL0 + j % NS), (j / NS) & 1, abort_flag, a.err)) { ok = false; break; }
         if (j >= 2 && !mbar_wait(bar(B_SFREE0 + s), ((j >> 1) - 1) & 1, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kt = base + OFF_KV + s * 2 * TILE_BYTES;
+        const uint32_t kt = base + OFF_K + (j % NS) * TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++)
           umma_bf16(tmem + s * 128, kmajor_desc(base + OFF_Q, kk), kmajor_desc(kt, kk), IDESC_QK, kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL0 + s));
-        umma_commit(bar(B_EMPTY0 + s));  // K tile j is consumed once its QK product is done
+        umma_commit(bar(B_EMPTY0 + j % NS));  // K tile j is consumed once its QK product is done
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok && issue_pv(T - 1)) umma_commit(bar(B_OFINAL));
@@ -395,27 +409,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       const float sub = (m_used == -INFINITY) ? 0.0f : m_used;
-      // P row (BF16) into the K-major SW128 P buffer b; p = 2^(s scale - sub), exponents and sums in pairs
-      const uint32_t pt = base + OFF_P + b * TILE_BYTES + (row >> 3) * 1024 + (row & 7) * 128;
+      // P row (BF16 pairs) into TMEM P buffer b, this thread's lane, columns 0..63; p = 2^(s scale - sub),
+      // exponents and sums in pairs
       const float2 scale2 = make_float2(a.qk_scale_log2, a.qk_scale_log2), nsub2 = make_float2(-sub, -sub);
       float2 ps2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int k8 = 0; k8 < 16; k8++) {
-        uint32_t w[4];
+      for (int half = 0; half < 2; half++) {
+        float w[32];  // 32 packed BF16 pairs, as raw 32-bit words
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const float2 arg = ffma2(make_float2(s[k8 * 8 + 2 * e], s[k8 * 8 + 2 * e + 1]), scale2, nsub2);
+        for (int e = 0; e < 32; e++) {
+          const int c = half * 64 + 2 * e;
+          const float2 arg = ffma2(make_float2(s[c], s[c + 1]), scale2, nsub2);
           const float2 pp = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
           ps2 = fadd2(ps2, pp);
-          w[e] = float2_to_bf16x2(pp.x, pp.y);
+          w[e] = __uint_as_float(float2_to_bf16x2(pp.x, pp.y));
         }
-        const uint32_t addr = pt + (k8 >> 3) * BOX_BYTES + (((k8 & 7) ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                     "r"(w[3])
-                     : "memory");
+        tmem_st32(lane_base + TMEM_P + b * 64 + half * 32, w);
       }
       lsum += ps2.x + ps2.y;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL0 + b));
     }
