@@ -18,8 +18,8 @@
 //                 two TMEM P buffers (its own lane), and rescales the O row in TMEM only when the running
 //                 max grew by more than 8 (log2 units), so the O correction is rare.  Keeping P in TMEM
 //                 leaves the shared memory to the Q tile and the two 3-stage rings
-// Operands: Q, K are K-major with the 128-byte swizzle; P is the TMEM A operand of the PV product; V is MN-major (keys x d, d contiguous) with
-// the 128-byte swizzle, read directly by the tensor core.  Every mbarrier wait is bounded in time; on
+// Operands: Q, K are K-major with the 128-byte swizzle; P is the TMEM A operand of the PV product; V is
+// MN-major (keys x d, d contiguous) with the 128-byte swizzle, read directly by the tensor core.  Every mbarrier wait is bounded in time; on
 // expiry the CTA records an error flag, drains its outstanding operations and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
