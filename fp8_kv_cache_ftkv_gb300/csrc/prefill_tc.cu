@@ -465,6 +465,289 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
+// Two query heads per CTA (even GQA groups).  Query heads 2y and 2y+1 share a KV head, so one K/V stream
+// feeds both: each K/V tile is fetched once for two heads, which halves the tile bytes per unit of work
+// (what bounds the one-head kernel).  The softmax warpgroup alternates between the heads, and each
+// head's tensor-core work overlaps the other head's softmax.  TMEM: S_h at columns [128h, 128h + 128),
+// P_h written over the first 64 of them (BF16 pairs) once S_h is in registers; O_h at [256 + 128h, ...).
+// The QK product of the next tile into S_h is issued after PV_h, so the in-order tensor pipe never
+// overwrites a P it has not read.  Issue order: QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) ...
+namespace tc2 {
+constexpr int NSK = 3, NSV = 2;                                   // K and V ring stages
+constexpr uint32_t OFF_Q = 0;                                     // head h at +h*TILE
+constexpr uint32_t OFF_K = 2 * TILE_BYTES;                        // K stage s at +s*TILE
+constexpr uint32_t OFF_V = OFF_K + NSK * TILE_BYTES;              // V stage s at +s*TILE
+constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE_BYTES;
+constexpr int B_QFULL = 0, B_FULL0 = 1, B_EMPTY0 = 4, B_FULLV0 = 7, B_EMPTYV0 = 9, B_SFULL0 = 11, B_PFULL0 = 13,
+              B_ODONE0 = 15, B_OFINAL = 17, B_DRAIN = 18, NBAR = 20;
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;                 // TMEM base address, abort flag
+constexpr uint32_t SMEM_ALLOC = OFF_MISC + 16 + 1024;             // + slack for the 1024-byte alignment
+static_assert(SMEM_ALLOC <= 232448, "prefill_tc2 shared memory");
+}  // namespace tc2
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_tc2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkc,
+                       const __grid_constant__ CUtensorMap tvc, const __grid_constant__ CUtensorMap twk,
+                       const __grid_constant__ CUtensorMap twv, const TcArgs a) {
+  using tc2::NSK, tc2::NSV, tc2::OFF_Q, tc2::OFF_K, tc2::OFF_V, tc2::OFF_BAR, tc2::OFF_MISC;
+  using tc2::B_QFULL, tc2::B_FULL0, tc2::B_EMPTY0, tc2::B_FULLV0, tc2::B_EMPTYV0, tc2::B_SFULL0, tc2::B_PFULL0,
+      tc2::B_ODONE0, tc2::B_OFINAL, tc2::B_DRAIN;
+  pdl_enter();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_MISC + 4);
+  const uint32_t tmem_holder = base + OFF_MISC;
+  auto bar = [&](int i) { return base + OFF_BAR + 8u * i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = a.n_q_tiles - 1 - static_cast<int>(blockIdx.x);  // heaviest (latest) query tiles first
+  const int hq0 = 2 * static_cast<int>(blockIdx.y);
+  const int hk = hq0 / a.group;
+  const int t0 = qt * BM;
+  const int nPT = (a.prefix_len + BN - 1) / BN;
+  const int last_q = (t0 + BM - 1 < a.chunk_len - 1) ? t0 + BM - 1 : a.chunk_len - 1;
+  const int nCT = last_q / BN + 1;
+  const int T = nPT + nCT;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_QFULL), 1);
+    for (int s = 0; s < NSK; s++) {
+      mbar_init(bar(B_FULL0 + s), 1);
+      mbar_init(bar(B_EMPTY0 + s), 1);
+    }
+    for (int s = 0; s < NSV; s++) {
+      mbar_init(bar(B_FULLV0 + s), 1);
+      mbar_init(bar(B_EMPTYV0 + s), 1);
+    }
+    for (int h = 0; h < 2; h++) {
+      mbar_init(bar(B_SFULL0 + h), 1);
+      mbar_init(bar(B_PFULL0 + h), 128);
+      mbar_init(bar(B_ODONE0 + h), 1);
+    }
+    mbar_init(bar(B_OFINAL), 1);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_holder),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + OFF_MISC);
+
+  if (warp == 0 || warp == 6) {
+    if (lane == 0) {
+      // ---------------- TMA producers: warp 0 the two Q tiles and the K tiles, warp 6 the V tiles ----------------
+      const bool is_k = warp == 0;
+      if (is_k) {
+        mbar_expect_tx(bar(B_QFULL), 2 * TILE_BYTES);
+        for (int h = 0; h < 2; h++) {
+          tma_load_3d(base + OFF_Q + h * TILE_BYTES, &tq, bar(B_QFULL), 0, hq0 + h, t0);
+          tma_load_3d(base + OFF_Q + h * TILE_BYTES + BOX_BYTES, &tq, bar(B_QFULL), 64, hq0 + h, t0);
+        }
+      }
+      const int FULL = is_k ? B_FULL0 : B_FULLV0, EMPTY = is_k ? B_EMPTY0 : B_EMPTYV0;
+      const int NS = is_k ? NSK : NSV;
+      int issued = 0;
+      for (int j = 0; j < T; j++) {
+        const int s = j % NS, use = j / NS;  // stage, and how often it was filled before
+        if (use >= 1 && !mbar_wait(bar(EMPTY + s), (use - 1) & 1, abort_flag, a.err)) break;
+        const bool pre = j < nPT;
+        const CUtensorMap* m = is_k ? (pre ? &twk : &tkc) : (pre ? &twv : &tvc);
+        const int row = pre ? j * BN : (j - nPT) * BN;
+        const uint32_t d = base + (is_k ? OFF_K : OFF_V) + s * TILE_BYTES;
+        mbar_expect_tx(bar(FULL + s), TILE_BYTES);
+        tma_load_3d(d, m, bar(FULL + s), 0, hk, row);
+        tma_load_3d(d + BOX_BYTES, m, bar(FULL + s), 64, hk, row);
+        issued = j + 1;
+      }
+      // drain: every issued load must land before the CTA may exit
+      if (is_k) mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
+      for (int j = (issued > NS ? issued - NS : 0); j < issued; j++) mbar_wait(bar(FULL + j % NS), (j / NS) & 1, abort_flag, a.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t IDESC_QK = idesc_bf16(false);
+      constexpr uint32_t IDESC_PV = idesc_bf16(true);
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
+      auto qk = [&](int j, int h) {  // S_h = Q_h K_j^T
+        const uint32_t kt = base + OFF_K + (j % NSK) * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++)
+          umma_bf16(tmem + h * 128, kmajor_desc(base + OFF_Q + h * TILE_BYTES, kk), kmajor_desc(kt, kk), IDESC_QK,
+                    kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_SFULL0 + h));
+      };
+      auto wait_k = [&](int j) -> bool {
+        if (!mbar_wait(bar(B_FULL0 + j % NSK), (j / NSK) & 1, abort_flag, a.err)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto pv = [&](int j, int h) -> bool {  // O_h += P_h V_j, P_h from TMEM
+        if (!mbar_wait(bar(B_PFULL0 + h), j & 1, abort_flag, a.err)) return false;
+        if (h == 0 && !mbar_wait(bar(B_FULLV0 + j % NSV), (j / NSV) & 1, abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t vt = base + OFF_V + (j % NSV) * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++)
+          umma_bf16_ta(tmem + TMEM_O + h * 128, tmem + h * 128 + kk * 8, vtile_desc(vt, kk), IDESC_PV,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_ODONE0 + h));
+        if (h == 1) umma_commit(bar(B_EMPTYV0 + j % NSV));  // both PV products of tile j read its V stage
+        return true;
+      };
+      if (ok && wait_k(0)) {
+        qk(0, 0);
+        qk(0, 1);
+        umma_commit(bar(B_EMPTY0));
+      } else {
+        ok = false;
+      }
+      for (int j = 0; ok && j < T; j++) {
+        if (!pv(j, 0)) { ok = false; break; }
+        const bool more = j + 1 < T;
+        if (more) {
+          if (!wait_k(j + 1)) { ok = false; break; }
+          qk(j + 1, 0);
+        }
+        if (!pv(j, 1)) { ok = false; break; }
+        if (more) {
+          qk(j + 1, 1);
+          umma_commit(bar(B_EMPTY0 + (j + 1) % NSK));  // both QK products of tile j+1 read its K stage
+        }
+      }
+      if (ok) umma_commit(bar(B_OFINAL));
+      // drain every MMA issued by this thread before TMEM is released
+      umma_commit(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0, abort_flag, a.err);
+    }
+  } else {  // warps 2..5
+    // ---------------- softmax: one query row per thread, the two heads in turn ----------------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int t = t0 + row;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float m_used[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
+    bool ok = true;
+    float s[BN];
+    for (int j = 0; j < T && ok; j++) {
+      const bool pre = j < nPT;
+      const int kbase = pre ? j * BN : (j - nPT) * BN;
+      const int lim = pre ? a.prefix_len - kbase : (t + 1 - kbase);  // columns < lim are visible
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        // wait results are made warp-uniform before any warp-collective tcgen05 access
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL0 + h), j & 1, abort_flag, a.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; c++) tmem_ld32(lane_base + h * 128 + c * 32, s + c * 32);
+        tmem_ld_wait();
+        if (lim < BN) {
+#pragma unroll
+          for (int c = 0; c < BN; c++) s[c] = (c < lim) ? s[c] : -INFINITY;
+        }
+        float mraw = fmaxf(s[0], s[1]);
+#pragma unroll
+        for (int c = 2; c < BN; c += 2) mraw = fmax3(mraw, s[c], s[c + 1]);
+        const float mt = mraw * a.qk_scale_log2;
+        const float m_new = fmaxf(m_used[h], mt);
+        const bool need = (m_used[h] != -INFINITY) && (m_new > m_used[h] + 8.0f);
+        if (m_used[h] == -INFINITY) m_used[h] = m_new;
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? fast_exp2(m_used[h] - m_new) : 1.0f;
+          if (need) {
+            lsum[h] *= f;
+            m_used[h] = m_new;
+          }
+          if (j >= 1) {  // O_h holds PV_h(0..j-1): wait for the last of them, then scale the row in place
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ODONE0 + h), (j - 1) & 1, abort_flag, a.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            float o[32];
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+              tmem_ld32(lane_base + TMEM_O + h * 128 + c * 32, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; e++) o[e] *= f;
+              tmem_st32(lane_base + TMEM_O + h * 128 + c * 32, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        const float sub = (m_used[h] == -INFINITY) ? 0.0f : m_used[h];
+        // P_h row (BF16 pairs) over the first 64 columns of S_h; p = 2^(s scale - sub), in pairs
+        const float2 scale2 = make_float2(a.qk_scale_log2, a.qk_scale_log2), nsub2 = make_float2(-sub, -sub);
+        float2 ps2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+          float w[32];  // 32 packed BF16 pairs, as raw 32-bit words
+#pragma unroll
+          for (int e = 0; e < 32; e++) {
+            const int c = half * 64 + 2 * e;
+            const float2 arg = ffma2(make_float2(s[c], s[c + 1]), scale2, nsub2);
+            const float2 pp = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+            ps2 = fadd2(ps2, pp);
+            w[e] = __uint_as_float(float2_to_bf16x2(pp.x, pp.y));
+          }
+          tmem_st32(lane_base + h * 128 + half * 32, w);
+        }
+        lsum[h] += ps2.x + ps2.y;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_PFULL0 + h));
+      }
+    }
+    // ---- epilogue: O_h / l_h -> BF16 ----
+    if (__all_sync(0xffffffffu, ok && mbar_wait(bar(B_OFINAL), 0, abort_flag, a.err))) {
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        const float inv = lsum[h] > 0.0f ? 1.0f / lsum[h] : 0.0f;
+        uint16_t* dst = a.out + (static_cast<int64_t>(t) * a.num_q_heads + hq0 + h) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          float o[32];
+          tmem_ld32(lane_base + TMEM_O + h * 128 + c * 32, o);
+          tmem_ld_wait();
+          if (t < a.chunk_len) {
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+              uint4 v;
+              v.x = float2_to_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+              v.y = float2_to_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+              v.z = float2_to_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+              v.w = float2_to_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+              *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -500,6 +783,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (dev >= 0 && dev < 64 && !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc2::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   CUtensorMap tq, tkc, tvc, twk, twv;
@@ -522,6 +807,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   t.qk_scale_log2 = a.qk_scale_log2;
   t.out = a.out;
   t.err = a.err;
+  if (t.group % 2 == 0) {  // query heads 2y and 2y+1 share a KV head: one CTA, one K/V stream for both
+    dim3 grid(t.n_q_tiles, a.num_q_heads / 2);
+    return launch_k(prefill_tc2_kernel, grid, dim3(NTHREADS), tc2::SMEM_ALLOC, s, tq, tkc, tvc, twk, twv, t);
+  }
   dim3 grid(t.n_q_tiles, a.num_q_heads);
   return launch_k(prefill_tc_kernel, grid, dim3(NTHREADS), SMEM_ALLOC, s, tq, tkc, tvc, twk, twv, t);
 }

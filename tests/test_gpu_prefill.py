@@ -33,7 +33,7 @@ def test_prefill_small(impl, P, C):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (8, 8), (64, 8)])
+@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (8, 8), (64, 8), (8, 4)])
 def test_prefill_gqa(impl, Hq, Hkv):
     rng = np.random.default_rng(Hq)
     P, C = 200, 150
