@@ -477,9 +477,11 @@ def run_kernel_workload(args, world, rank, local, torch, ops, inputs, device, hb
         wk_d, wv_d = to_dev(wk), to_dev(wv)
         out = torch.empty_like(q_d)
         impl = "mma" if args.workload == "prefill_mma" else "tc"
+        # the tcgen05 kernel runs stream-K over a zero-filled workspace (one persistent CTA per SM)
+        pplan = ops.PrefillPlan(0, device) if impl == "tc" else None
 
         def work():
-            ops.prefill_attn(q_d, k_d, v_d, wk_d, wv_d, out=out, impl=impl)
+            ops.prefill_attn(q_d, k_d, v_d, wk_d, wv_d, out=out, impl=impl, plan=pplan)
         pairs = C * P + C * (C + 1) // 2
         unit_flops = pairs * HQ * D * 2 * 2
         nbytes = None

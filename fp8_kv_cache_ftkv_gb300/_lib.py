@@ -29,7 +29,8 @@ FTKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 # Every symbol include/ftkv.h declares.
 EXPORTS = (
     "ftkv_store_quant", "ftkv_reconstruct_bf16", "ftkv_decode_workspace_bytes", "ftkv_decode_auto_splits",
-    "ftkv_decode_attn", "ftkv_prefill_attn", "ftkv_prefill_attn_mma", "ftkv_e4m3_encode_f32",
+    "ftkv_decode_attn", "ftkv_prefill_attn", "ftkv_prefill_attn_ws", "ftkv_prefill_workspace_bytes",
+    "ftkv_prefill_attn_mma", "ftkv_e4m3_encode_f32",
     "ftkv_e4m3_decode_f32", "ftkv_pool_bytes", "ftkv_device_errors", "ftkv_status_str",
     "ftkv_last_cuda_error", "ftkv_abi_version", "ftkv_decode_attn_noalloc", "ftkv_decode_attn_tc",
     "ftkv_decode_attn_store",
@@ -82,6 +83,8 @@ def load() -> ctypes.CDLL:
                                                         P]),
             "ftkv_prefill_attn": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),
             "ftkv_prefill_attn_mma": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),
+            "ftkv_prefill_attn_ws": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, I32, P, I64, P, P]),
+            "ftkv_prefill_workspace_bytes": (I64, [I32]),
             "ftkv_e4m3_encode_f32": (ctypes.c_int, [P, P, I64, P]),
             "ftkv_e4m3_decode_f32": (ctypes.c_int, [P, P, I64, P]),
             "ftkv_pool_bytes": (ctypes.c_int, [I64, I32, I32, I32, P, P, P]),

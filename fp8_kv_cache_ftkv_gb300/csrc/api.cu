@@ -277,7 +277,8 @@ int ftkv_decode_attn_store(const ftkv_pool* pool, int32_t num_q_heads, const uin
 static int prefill_common(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,
                           const uint16_t* k_chunk, const uint16_t* v_chunk, int64_t chunk_len,
                           const uint16_t* ws_k, const uint16_t* ws_v, int64_t prefix_len, float sm_scale,
-                          uint16_t* out, void* stream, bool tc) {
+                          uint16_t* out, void* stream, bool tc, int32_t max_ctas = 0, void* workspace = nullptr,
+                          int64_t workspace_bytes = 0) {
   int st = check_heads(num_q_heads, num_kv_heads);
   if (st != FTKV_OK) return st;
   if (head_dim != FTKV_HEAD_DIM) return FTKV_ERR_UNSUPPORTED;
@@ -291,9 +292,15 @@ static int prefill_common(int32_t num_q_heads, int32_t num_kv_heads, int32_t hea
   if (chunk_len > (int64_t(1) << 31) - 1 || prefix_len > (int64_t(1) << 31) - 1) return FTKV_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FTKV_OK) return st;
+  if (workspace) {
+    if (!aligned16(workspace)) return FTKV_ERR_ALIGN;
+    if (workspace_bytes < ftkv::prefill_workspace_bytes(max_ctas > 0 ? max_ctas : di->num_sms))
+      return FTKV_ERR_WORKSPACE;
+  }
   ftkv::PrefillArgs a{num_q_heads, num_kv_heads, q, k_chunk, v_chunk, chunk_len,
                       prefix_len > 0 ? ws_k : k_chunk, prefix_len > 0 ? ws_v : v_chunk, prefix_len,
-                      sm_scale * 1.4426950408889634f, out, di->err_word};
+                      sm_scale * 1.4426950408889634f, out, di->err_word, workspace, workspace_bytes,
+                      max_ctas};
   cudaError_t e = tc ? ftkv::launch_prefill_tc(a, static_cast<cudaStream_t>(stream))
                      : ftkv::launch_prefill_mma(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FTKV_OK : cuda_fail(e);
@@ -304,6 +311,24 @@ int ftkv_prefill_attn(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_di
                       const uint16_t* ws_v, int64_t prefix_len, float sm_scale, uint16_t* out, void* stream) {
   return prefill_common(num_q_heads, num_kv_heads, head_dim, q, k_chunk, v_chunk, chunk_len, ws_k, ws_v,
                         prefix_len, sm_scale, out, stream, true);
+}
+
+int ftkv_prefill_attn_ws(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,
+                         const uint16_t* k_chunk, const uint16_t* v_chunk, int64_t chunk_len, const uint16_t* ws_k,
+                         const uint16_t* ws_v, int64_t prefix_len, float sm_scale, int32_t max_ctas,
+                         void* workspace, int64_t workspace_bytes, uint16_t* out, void* stream) {
+  if (!workspace || workspace_bytes < 0) return FTKV_ERR_INVALID;
+  return prefill_common(num_q_heads, num_kv_heads, head_dim, q, k_chunk, v_chunk, chunk_len, ws_k, ws_v,
+                        prefix_len, sm_scale, out, stream, true, max_ctas, workspace, workspace_bytes);
+}
+
+int64_t ftkv_prefill_workspace_bytes(int32_t max_ctas) {
+  if (max_ctas <= 0) {
+    DeviceInfo* di = nullptr;
+    if (device_info(&di) != FTKV_OK) return -1;
+    max_ctas = di->num_sms;
+  }
+  return ftkv::prefill_workspace_bytes(max_ctas);
 }
 
 int ftkv_prefill_attn_mma(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,

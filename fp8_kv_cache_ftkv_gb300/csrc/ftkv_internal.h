@@ -81,7 +81,15 @@ struct PrefillArgs {
   float qk_scale_log2;
   uint16_t* out;             // [C][Hq][128]
   int* err;
+  // stream-K scheduling of the two-heads-per-CTA kernel (tcgen05 path): workspace, or null for one CTA
+  // per work item; max_ctas <= 0 means the SM count
+  void* workspace;
+  int64_t workspace_bytes;
+  int max_ctas;
 };
+
+// Bytes of the stream-K prefill workspace for up to max_ctas persistent CTAs (see launch_prefill_tc).
+int64_t prefill_workspace_bytes(int max_ctas);
 
 // Launch with programmatic stream serialization (see pdl_enter in ftkv_device.cuh).
 template <typename... KArgs, typename... Args>

@@ -64,6 +64,12 @@ struct TcArgs {
   float qk_scale_log2;
   uint16_t* out;
   int* err;
+  // two-heads-per-CTA kernel: key tiles per head pair (all its query tiles), and stream-K scheduling
+  long long sk_wpair;
+  long long sk_units;   // sk_wpair x head pairs
+  int sk_ctas;          // persistent CTAs (0: one CTA per item)
+  float* sk_part;       // [sk_ctas + 1 boundaries][2 pieces][piece floats]
+  int* sk_ticket;       // [sk_ctas + 1 boundaries][4 softmax warps], zero between calls
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -472,6 +478,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // P_h written over the first 64 of them (BF16 pairs) once S_h is in registers; O_h at [256 + 128h, ...).
 // The QK product of the next tile into S_h is issued after PV_h, so the in-order tensor pipe never
 // overwrites a P it has not read.  Issue order: QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) ...
+//
+// Work items are (head pair y, query tile qt), T = nPT + qt + 1 key tiles each.  Either one CTA per item
+// (sk_ctas == 0), or stream-K: the items' tiles, laid end to end (pair-major, qt ascending), are cut into
+// sk_ctas equal ranges, one per persistent CTA, so every SM gets the same number of tiles whatever the
+// mix of item sizes.  A CTA runs the segments (item, tile range) of its range in order.  An item cut by a
+// range boundary has two pieces, in CTAs c and c+1: each writes its unnormalised O, its running max and
+// its sum to the boundary's slot and takes a ticket (one per softmax warp and its 32 rows); the second
+// to arrive merges the two
+// (o = (2^(m0-m) O0 + 2^(m1-m) O1) / (2^(m0-m) l0 + 2^(m1-m) l1), m = max) and resets the ticket.
+// Ranges are at least as long as the largest item, so no item has more than two pieces.
 namespace tc2 {
 constexpr int NSK = 3, NSV = 2;                                   // K and V ring stages
 constexpr uint32_t OFF_Q = 0;                                     // head h at +h*TILE
@@ -479,19 +495,47 @@ constexpr uint32_t OFF_K = 2 * TILE_BYTES;                        // K stage s a
 constexpr uint32_t OFF_V = OFF_K + NSK * TILE_BYTES;              // V stage s at +s*TILE
 constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE_BYTES;
 constexpr int B_QFULL = 0, B_FULL0 = 1, B_EMPTY0 = 4, B_FULLV0 = 7, B_EMPTYV0 = 9, B_SFULL0 = 11, B_PFULL0 = 13,
-              B_ODONE0 = 15, B_OFINAL = 17, B_DRAIN = 18, NBAR = 20;
+              B_ODONE0 = 15, B_OFREE0 = 17, B_QEMPTY = 19, B_DRAIN = 20, NBAR = 21;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;                 // TMEM base address, abort flag
 constexpr uint32_t SMEM_ALLOC = OFF_MISC + 16 + 1024;             // + slack for the 1024-byte alignment
 static_assert(SMEM_ALLOC <= 232448, "prefill_tc2 shared memory");
+// One piece of a cut item: O [head][d/4][row][4] FP32 (a warp's rows read and write 512 contiguous bytes),
+// then m [head][row] and l [head][row].
+constexpr int PIECE_FLOATS = 2 * BM * kHeadDim + 4 * BM;
 }  // namespace tc2
+
+// A segment: head pair p, query tile qt, key tiles [ja, jb) of the item's T.
+struct Seg {
+  int p, qt, ja, jb, T;
+};
+
+// The next segment of the unit range [u, u1), advancing u; false when the range is used up.
+__device__ __forceinline__ bool next_segment(long long& u, long long u1, const TcArgs& a, int nPT, Seg& sg) {
+  if (u >= u1) return false;
+  sg.p = static_cast<int>(u / a.sk_wpair);
+  const long long rem = u - static_cast<long long>(sg.p) * a.sk_wpair;
+  int qt = 0;
+  long long base = 0;
+  while (qt + 1 < a.n_q_tiles && base + nPT + qt + 1 <= rem) {
+    base += nPT + qt + 1;
+    qt++;
+  }
+  sg.qt = qt;
+  sg.T = nPT + qt + 1;
+  sg.ja = static_cast<int>(rem - base);
+  const long long left = u1 - u;
+  sg.jb = (sg.ja + left < sg.T) ? sg.ja + static_cast<int>(left) : sg.T;
+  u += sg.jb - sg.ja;
+  return true;
+}
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkc,
                        const __grid_constant__ CUtensorMap tvc, const __grid_constant__ CUtensorMap twk,
                        const __grid_constant__ CUtensorMap twv, const TcArgs a) {
-  using tc2::NSK, tc2::NSV, tc2::OFF_Q, tc2::OFF_K, tc2::OFF_V, tc2::OFF_BAR, tc2::OFF_MISC;
+  using tc2::NSK, tc2::NSV, tc2::OFF_Q, tc2::OFF_K, tc2::OFF_V, tc2::OFF_BAR, tc2::OFF_MISC, tc2::PIECE_FLOATS;
   using tc2::B_QFULL, tc2::B_FULL0, tc2::B_EMPTY0, tc2::B_FULLV0, tc2::B_EMPTYV0, tc2::B_SFULL0, tc2::B_PFULL0,
-      tc2::B_ODONE0, tc2::B_OFINAL, tc2::B_DRAIN;
+      tc2::B_ODONE0, tc2::B_OFREE0, tc2::B_QEMPTY, tc2::B_DRAIN;
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -502,17 +546,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto bar = [&](int i) { return base + OFF_BAR + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = a.n_q_tiles - 1 - static_cast<int>(blockIdx.x);  // heaviest (latest) query tiles first
-  const int hq0 = 2 * static_cast<int>(blockIdx.y);
-  const int hk = hq0 / a.group;
-  const int t0 = qt * BM;
   const int nPT = (a.prefix_len + BN - 1) / BN;
-  const int last_q = (t0 + BM - 1 < a.chunk_len - 1) ? t0 + BM - 1 : a.chunk_len - 1;
-  const int nCT = last_q / BN + 1;
-  const int T = nPT + nCT;
+  // this CTA's unit range: stream-K, or the one item of (blockIdx.x, blockIdx.y) (heaviest first)
+  long long u_begin, u_end;
+  if (a.sk_ctas > 0) {
+    u_begin = static_cast<long long>(blockIdx.x) * a.sk_units / a.sk_ctas;
+    u_end = static_cast<long long>(blockIdx.x + 1) * a.sk_units / a.sk_ctas;
+  } else {
+    const int qt = a.n_q_tiles - 1 - static_cast<int>(blockIdx.x);
+    u_begin = static_cast<long long>(blockIdx.y) * a.sk_wpair + static_cast<long long>(qt) * nPT +
+              static_cast<long long>(qt) * (qt + 1) / 2;
+    u_end = u_begin + nPT + qt + 1;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QEMPTY), 1);
     for (int s = 0; s < NSK; s++) {
       mbar_init(bar(B_FULL0 + s), 1);
       mbar_init(bar(B_EMPTY0 + s), 1);
@@ -525,8 +574,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_SFULL0 + h), 1);
       mbar_init(bar(B_PFULL0 + h), 128);
       mbar_init(bar(B_ODONE0 + h), 1);
+      mbar_init(bar(B_OFREE0 + h), 128);
     }
-    mbar_init(bar(B_OFINAL), 1);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -546,30 +595,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       // ---------------- TMA producers: warp 0 the two Q tiles and the K tiles, warp 6 the V tiles ----------------
       const bool is_k = warp == 0;
-      if (is_k) {
-        mbar_expect_tx(bar(B_QFULL), 2 * TILE_BYTES);
-        for (int h = 0; h < 2; h++) {
-          tma_load_3d(base + OFF_Q + h * TILE_BYTES, &tq, bar(B_QFULL), 0, hq0 + h, t0);
-          tma_load_3d(base + OFF_Q + h * TILE_BYTES + BOX_BYTES, &tq, bar(B_QFULL), 64, hq0 + h, t0);
-        }
-      }
       const int FULL = is_k ? B_FULL0 : B_FULLV0, EMPTY = is_k ? B_EMPTY0 : B_EMPTYV0;
       const int NS = is_k ? NSK : NSV;
-      int issued = 0;
-      for (int j = 0; j < T; j++) {
-        const int s = j % NS, use = j / NS;  // stage, and how often it was filled before
-        if (use >= 1 && !mbar_wait(bar(EMPTY + s), (use - 1) & 1, abort_flag, a.err)) break;
-        const bool pre = j < nPT;
-        const CUtensorMap* m = is_k ? (pre ? &twk : &tkc) : (pre ? &twv : &tvc);
-        const int row = pre ? j * BN : (j - nPT) * BN;
-        const uint32_t d = base + (is_k ? OFF_K : OFF_V) + s * TILE_BYTES;
-        mbar_expect_tx(bar(FULL + s), TILE_BYTES);
-        tma_load_3d(d, m, bar(FULL + s), 0, hk, row);
-        tma_load_3d(d + BOX_BYTES, m, bar(FULL + s), 64, hk, row);
-        issued = j + 1;
+      int issued = 0, nseg = 0;  // tiles issued (all segments), segments started
+      bool ok = true;
+      long long u = u_begin;
+      Seg sg;
+      while (ok && next_segment(u, u_end, a, nPT, sg)) {
+        const int hq0 = 2 * sg.p, hk = hq0 / a.group, t0 = sg.qt * BM;
+        if (is_k) {  // the segment's Q tiles, once the previous segment's QK products are done with Q
+          if (nseg >= 1 && !mbar_wait(bar(B_QEMPTY), (nseg - 1) & 1, abort_flag, a.err)) break;
+          mbar_expect_tx(bar(B_QFULL), 2 * TILE_BYTES);
+          for (int h = 0; h < 2; h++) {
+            tma_load_3d(base + OFF_Q + h * TILE_BYTES, &tq, bar(B_QFULL), 0, hq0 + h, t0);
+            tma_load_3d(base + OFF_Q + h * TILE_BYTES + BOX_BYTES, &tq, bar(B_QFULL), 64, hq0 + h, t0);
+          }
+        }
+        nseg++;
+        for (int j = sg.ja; j < sg.jb; j++) {
+          const int s = issued % NS, use = issued / NS;  // stage, and how often it was filled before
+          if (use >= 1 && !mbar_wait(bar(EMPTY + s), (use - 1) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          const bool pre = j < nPT;
+          const CUtensorMap* m = is_k ? (pre ? &twk : &tkc) : (pre ? &twv : &tvc);
+          const int row = pre ? j * BN : (j - nPT) * BN;
+          const uint32_t d = base + (is_k ? OFF_K : OFF_V) + s * TILE_BYTES;
+          mbar_expect_tx(bar(FULL + s), TILE_BYTES);
+          tma_load_3d(d, m, bar(FULL + s), 0, hk, row);
+          tma_load_3d(d + BOX_BYTES, m, bar(FULL + s), 64, hk, row);
+          issued++;
+        }
       }
       // drain: every issued load must land before the CTA may exit
-      if (is_k) mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
+      if (is_k && nseg >= 1) mbar_wait(bar(B_QFULL), (nseg - 1) & 1, abort_flag, a.err);
       for (int j = (issued > NS ? issued - NS : 0); j < issued; j++) mbar_wait(bar(FULL + j % NS), (j / NS) & 1, abort_flag, a.err);
     }
   } else if (warp == 1) {
@@ -577,54 +637,65 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---------------- MMA issuer ----------------
       constexpr uint32_t IDESC_QK = idesc_bf16(false);
       constexpr uint32_t IDESC_PV = idesc_bf16(true);
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, a.err);
-      auto qk = [&](int j, int h) {  // S_h = Q_h K_j^T
-        const uint32_t kt = base + OFF_K + (j % NSK) * TILE_BYTES;
+      bool ok = true;
+      int nseg = 0, g0 = 0;  // segments done, global index of the segment's first tile
+      long long u = u_begin;
+      Seg sg;
+      auto qk = [&](int g, int h) {  // S_h = Q_h K_g^T
+        const uint32_t kt = base + OFF_K + (g % NSK) * TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++)
           umma_bf16(tmem + h * 128, kmajor_desc(base + OFF_Q + h * TILE_BYTES, kk), kmajor_desc(kt, kk), IDESC_QK,
                     kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL0 + h));
       };
-      auto wait_k = [&](int j) -> bool {
-        if (!mbar_wait(bar(B_FULL0 + j % NSK), (j / NSK) & 1, abort_flag, a.err)) return false;
+      auto wait_k = [&](int g) -> bool {
+        if (!mbar_wait(bar(B_FULL0 + g % NSK), (g / NSK) & 1, abort_flag, a.err)) return false;
         tc_fence_after();
         return true;
       };
-      auto pv = [&](int j, int h) -> bool {  // O_h += P_h V_j, P_h from TMEM
-        if (!mbar_wait(bar(B_PFULL0 + h), j & 1, abort_flag, a.err)) return false;
-        if (h == 0 && !mbar_wait(bar(B_FULLV0 + j % NSV), (j / NSV) & 1, abort_flag, a.err)) return false;
-        tc_fence_after();
-        const uint32_t vt = base + OFF_V + (j % NSV) * TILE_BYTES;
+      while (ok && next_segment(u, u_end, a, nPT, sg)) {
+        const int n = sg.jb - sg.ja, glast = g0 + n - 1;
+        if (!mbar_wait(bar(B_QFULL), nseg & 1, abort_flag, a.err) || !wait_k(g0)) {
+          ok = false;
+          break;
+        }
+        qk(g0, 0);
+        qk(g0, 1);
+        umma_commit(bar(B_EMPTY0 + g0 % NSK));
+        if (n == 1) umma_commit(bar(B_QEMPTY));
+        auto pv = [&](int g, int h) -> bool {  // O_h += P_h V_g, P_h from TMEM
+          if (!mbar_wait(bar(B_PFULL0 + h), g & 1, abort_flag, a.err)) return false;
+          if (h == 0 && !mbar_wait(bar(B_FULLV0 + g % NSV), (g / NSV) & 1, abort_flag, a.err)) return false;
+          // the first PV of a segment overwrites O_h: the previous segment's epilogue must have read it
+          if (g == g0 && nseg >= 1 && !mbar_wait(bar(B_OFREE0 + h), (nseg - 1) & 1, abort_flag, a.err)) return false;
+          tc_fence_after();
+          const uint32_t vt = base + OFF_V + (g % NSV) * TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < 8; kk++)
-          umma_bf16_ta(tmem + TMEM_O + h * 128, tmem + h * 128 + kk * 8, vtile_desc(vt, kk), IDESC_PV,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_ODONE0 + h));
-        if (h == 1) umma_commit(bar(B_EMPTYV0 + j % NSV));  // both PV products of tile j read its V stage
-        return true;
-      };
-      if (ok && wait_k(0)) {
-        qk(0, 0);
-        qk(0, 1);
-        umma_commit(bar(B_EMPTY0));
-      } else {
-        ok = false;
-      }
-      for (int j = 0; ok && j < T; j++) {
-        if (!pv(j, 0)) { ok = false; break; }
-        const bool more = j + 1 < T;
-        if (more) {
-          if (!wait_k(j + 1)) { ok = false; break; }
-          qk(j + 1, 0);
+          for (int kk = 0; kk < 8; kk++)
+            umma_bf16_ta(tmem + TMEM_O + h * 128, tmem + h * 128 + kk * 8, vtile_desc(vt, kk), IDESC_PV,
+                         (g > g0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(B_ODONE0 + h));
+          if (h == 1) umma_commit(bar(B_EMPTYV0 + g % NSV));  // both PV products of tile g read its V stage
+          return true;
+        };
+        for (int g = g0; g <= glast; g++) {
+          if (!pv(g, 0)) { ok = false; break; }
+          const bool more = g < glast;
+          if (more) {
+            if (!wait_k(g + 1)) { ok = false; break; }
+            qk(g + 1, 0);
+          }
+          if (!pv(g, 1)) { ok = false; break; }
+          if (more) {
+            qk(g + 1, 1);
+            umma_commit(bar(B_EMPTY0 + (g + 1) % NSK));  // both QK products of tile g+1 read its K stage
+            if (g + 1 == glast) umma_commit(bar(B_QEMPTY));  // the segment's last QK products read Q
+          }
         }
-        if (!pv(j, 1)) { ok = false; break; }
-        if (more) {
-          qk(j + 1, 1);
-          umma_commit(bar(B_EMPTY0 + (j + 1) % NSK));  // both QK products of tile j+1 read its K stage
-        }
+        nseg++;
+        g0 += n;
       }
-      if (ok) umma_commit(bar(B_OFINAL));
       // drain every MMA issued by this thread before TMEM is released
       umma_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, abort_flag, a.err);
@@ -633,89 +704,104 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ---------------- softmax: one query row per thread, the two heads in turn ----------------
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int t = t0 + row;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float m_used[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
     bool ok = true;
     float s[BN];
-    for (int j = 0; j < T && ok; j++) {
-      const bool pre = j < nPT;
-      const int kbase = pre ? j * BN : (j - nPT) * BN;
-      const int lim = pre ? a.prefix_len - kbase : (t + 1 - kbase);  // columns < lim are visible
+    int g0 = 0;
+    long long u = u_begin;
+    Seg sg;
+    while (ok && next_segment(u, u_end, a, nPT, sg)) {
+      const int hq0 = 2 * sg.p, t = sg.qt * BM + row;
+      const int n = sg.jb - sg.ja, glast = g0 + n - 1;
+      float m_used[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
+      for (int j = sg.ja; j < sg.jb && ok; j++) {
+        const int g = g0 + (j - sg.ja);
+        const bool pre = j < nPT;
+        const int kbase = pre ? j * BN : (j - nPT) * BN;
+        const int lim = pre ? a.prefix_len - kbase : (t + 1 - kbase);  // columns < lim are visible
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          // wait results are made warp-uniform before any warp-collective tcgen05 access
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL0 + h), g & 1, abort_flag, a.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; c++) tmem_ld32(lane_base + h * 128 + c * 32, s + c * 32);
+          tmem_ld_wait();
+          if (lim < BN) {
+#pragma unroll
+            for (int c = 0; c < BN; c++) s[c] = (c < lim) ? s[c] : -INFINITY;
+          }
+          float mraw = fmaxf(s[0], s[1]);
+#pragma unroll
+          for (int c = 2; c < BN; c += 2) mraw = fmax3(mraw, s[c], s[c + 1]);
+          const float mt = mraw * a.qk_scale_log2;
+          const float m_new = fmaxf(m_used[h], mt);
+          const bool need = (m_used[h] != -INFINITY) && (m_new > m_used[h] + 8.0f);
+          if (m_used[h] == -INFINITY) m_used[h] = m_new;
+          if (__any_sync(0xffffffffu, need)) {
+            const float f = need ? fast_exp2(m_used[h] - m_new) : 1.0f;
+            if (need) {
+              lsum[h] *= f;
+              m_used[h] = m_new;
+            }
+            if (g > g0) {  // O_h holds PV_h of the segment's earlier tiles: wait for the last, scale in place
+              if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ODONE0 + h), (g - 1) & 1, abort_flag, a.err))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              float o[32];
+#pragma unroll
+              for (int c = 0; c < 4; c++) {
+                tmem_ld32(lane_base + TMEM_O + h * 128 + c * 32, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; e++) o[e] *= f;
+                tmem_st32(lane_base + TMEM_O + h * 128 + c * 32, o);
+              }
+              tmem_st_wait();
+            }
+          }
+          const float sub = (m_used[h] == -INFINITY) ? 0.0f : m_used[h];
+          // P_h row (BF16 pairs) over the first 64 columns of S_h; p = 2^(s scale - sub), in pairs
+          const float2 scale2 = make_float2(a.qk_scale_log2, a.qk_scale_log2), nsub2 = make_float2(-sub, -sub);
+          float2 ps2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int half = 0; half < 2; half++) {
+            float w[32];  // 32 packed BF16 pairs, as raw 32-bit words
+#pragma unroll
+            for (int e = 0; e < 32; e++) {
+              const int c = half * 64 + 2 * e;
+              const float2 arg = ffma2(make_float2(s[c], s[c + 1]), scale2, nsub2);
+              const float2 pp = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+              ps2 = fadd2(ps2, pp);
+              w[e] = __uint_as_float(float2_to_bf16x2(pp.x, pp.y));
+            }
+            tmem_st32(lane_base + h * 128 + half * 32, w);
+          }
+          lsum[h] += ps2.x + ps2.y;
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(B_PFULL0 + h));
+        }
+      }
+      if (!ok) break;
+      // ---- segment epilogue: a whole item writes O_h / l_h as BF16; a piece of a cut item writes its
+      // partial (O_h, m_h, l_h) to the boundary's slot, and the second piece to arrive merges ----
+      const bool whole = sg.ja == 0 && sg.jb == sg.T;
+      const int bnd = (sg.ja > 0) ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) + 1;  // boundary
+      float* piece = whole ? nullptr
+                           : a.sk_part + (static_cast<long long>(bnd) * 2 + (sg.ja > 0 ? 1 : 0)) * PIECE_FLOATS;
 #pragma unroll
       for (int h = 0; h < 2; h++) {
-        // wait results are made warp-uniform before any warp-collective tcgen05 access
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL0 + h), j & 1, abort_flag, a.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ODONE0 + h), glast & 1, abort_flag, a.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; c++) tmem_ld32(lane_base + h * 128 + c * 32, s + c * 32);
-        tmem_ld_wait();
-        if (lim < BN) {
-#pragma unroll
-          for (int c = 0; c < BN; c++) s[c] = (c < lim) ? s[c] : -INFINITY;
-        }
-        float mraw = fmaxf(s[0], s[1]);
-#pragma unroll
-        for (int c = 2; c < BN; c += 2) mraw = fmax3(mraw, s[c], s[c + 1]);
-        const float mt = mraw * a.qk_scale_log2;
-        const float m_new = fmaxf(m_used[h], mt);
-        const bool need = (m_used[h] != -INFINITY) && (m_new > m_used[h] + 8.0f);
-        if (m_used[h] == -INFINITY) m_used[h] = m_new;
-        if (__any_sync(0xffffffffu, need)) {
-          const float f = need ? fast_exp2(m_used[h] - m_new) : 1.0f;
-          if (need) {
-            lsum[h] *= f;
-            m_used[h] = m_new;
-          }
-          if (j >= 1) {  // O_h holds PV_h(0..j-1): wait for the last of them, then scale the row in place
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ODONE0 + h), (j - 1) & 1, abort_flag, a.err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            float o[32];
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-              tmem_ld32(lane_base + TMEM_O + h * 128 + c * 32, o);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 32; e++) o[e] *= f;
-              tmem_st32(lane_base + TMEM_O + h * 128 + c * 32, o);
-            }
-            tmem_st_wait();
-          }
-        }
-        const float sub = (m_used[h] == -INFINITY) ? 0.0f : m_used[h];
-        // P_h row (BF16 pairs) over the first 64 columns of S_h; p = 2^(s scale - sub), in pairs
-        const float2 scale2 = make_float2(a.qk_scale_log2, a.qk_scale_log2), nsub2 = make_float2(-sub, -sub);
-        float2 ps2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int half = 0; half < 2; half++) {
-          float w[32];  // 32 packed BF16 pairs, as raw 32-bit words
-#pragma unroll
-          for (int e = 0; e < 32; e++) {
-            const int c = half * 64 + 2 * e;
-            const float2 arg = ffma2(make_float2(s[c], s[c + 1]), scale2, nsub2);
-            const float2 pp = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
-            ps2 = fadd2(ps2, pp);
-            w[e] = __uint_as_float(float2_to_bf16x2(pp.x, pp.y));
-          }
-          tmem_st32(lane_base + h * 128 + half * 32, w);
-        }
-        lsum[h] += ps2.x + ps2.y;
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(B_PFULL0 + h));
-      }
-    }
-    // ---- epilogue: O_h / l_h -> BF16 ----
-    if (__all_sync(0xffffffffu, ok && mbar_wait(bar(B_OFINAL), 0, abort_flag, a.err))) {
-      tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < 2; h++) {
         const float inv = lsum[h] > 0.0f ? 1.0f / lsum[h] : 0.0f;
         uint16_t* dst = a.out + (static_cast<int64_t>(t) * a.num_q_heads + hq0 + h) * kHeadDim;
 #pragma unroll
@@ -723,19 +809,80 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           float o[32];
           tmem_ld32(lane_base + TMEM_O + h * 128 + c * 32, o);
           tmem_ld_wait();
-          if (t < a.chunk_len) {
+          if (whole) {
+            if (t < a.chunk_len) {
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-              uint4 v;
-              v.x = float2_to_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
-              v.y = float2_to_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
-              v.z = float2_to_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
-              v.w = float2_to_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
-              *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+              for (int q = 0; q < 4; q++) {
+                uint4 v;
+                v.x = float2_to_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+                v.y = float2_to_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+                v.z = float2_to_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+                v.w = float2_to_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+                *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; q++)
+              *reinterpret_cast<float4*>(piece + ((h * 32 + c * 8 + q) * BM + row) * 4) =
+                  make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
+          }
+        }
+        if (!whole) {
+          piece[2 * BM * kHeadDim + h * BM + row] = m_used[h];
+          piece[2 * BM * kHeadDim + 2 * BM + h * BM + row] = lsum[h];
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_OFREE0 + h));  // O_h is read: the next segment's first PV_h may overwrite it
+      }
+      if (!ok) break;
+      if (!whole) {
+        // one ticket per (boundary, warp): each softmax warp hands over its own 32 rows, so no barrier
+        // joins the warps (a warp that gave up on a timeout cannot hold the others)
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) {
+          prev = atomicAdd(a.sk_ticket + bnd * 4 + quarter, 1);
+          if (prev == 1) a.sk_ticket[bnd * 4 + quarter] = 0;  // both pieces are in: ready for the next call
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == 1) {
+          __threadfence();
+          const float* p0 = a.sk_part + static_cast<long long>(bnd) * 2 * PIECE_FLOATS;
+          const float* p1 = p0 + PIECE_FLOATS;
+#pragma unroll 1
+          for (int h = 0; h < 2; h++) {
+            const float m0 = __ldcg(p0 + 2 * BM * kHeadDim + h * BM + row);
+            const float m1 = __ldcg(p1 + 2 * BM * kHeadDim + h * BM + row);
+            const float l0 = __ldcg(p0 + 2 * BM * kHeadDim + 2 * BM + h * BM + row);
+            const float l1 = __ldcg(p1 + 2 * BM * kHeadDim + 2 * BM + h * BM + row);
+            const float mm = fmaxf(m0, m1);
+            const float f0 = (mm == -INFINITY) ? 0.0f : exp2f(m0 - mm);
+            const float f1 = (mm == -INFINITY) ? 0.0f : exp2f(m1 - mm);
+            const float L = l0 * f0 + l1 * f1;
+            const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+            const float w0 = f0 * inv, w1 = f1 * inv;
+            uint16_t* dst = a.out + (static_cast<int64_t>(t) * a.num_q_heads + hq0 + h) * kHeadDim;
+#pragma unroll 4
+            for (int c4 = 0; c4 < 32; c4 += 2) {
+              const float4 x0 = __ldcg(reinterpret_cast<const float4*>(p0 + ((h * 32 + c4) * BM + row) * 4));
+              const float4 y0 = __ldcg(reinterpret_cast<const float4*>(p0 + ((h * 32 + c4 + 1) * BM + row) * 4));
+              const float4 x1 = __ldcg(reinterpret_cast<const float4*>(p1 + ((h * 32 + c4) * BM + row) * 4));
+              const float4 y1 = __ldcg(reinterpret_cast<const float4*>(p1 + ((h * 32 + c4 + 1) * BM + row) * 4));
+              if (t < a.chunk_len) {
+                uint4 v;
+                v.x = float2_to_bf16x2(x0.x * w0 + x1.x * w1, x0.y * w0 + x1.y * w1);
+                v.y = float2_to_bf16x2(x0.z * w0 + x1.z * w1, x0.w * w0 + x1.w * w1);
+                v.z = float2_to_bf16x2(y0.x * w0 + y1.x * w1, y0.y * w0 + y1.y * w1);
+                v.w = float2_to_bf16x2(y0.z * w0 + y1.z * w1, y0.w * w0 + y1.w * w1);
+                *reinterpret_cast<uint4*>(dst + c4 * 4) = v;
+              }
             }
           }
         }
       }
+      g0 += n;
     }
   }
 
@@ -776,6 +923,13 @@ bool make_map(CUtensorMap* m, const void* ptr, int heads, int64_t rows) {
 
 }  // namespace
 
+// Stream-K workspace: tickets [max_ctas + 1][4] (rounded up to 256 bytes), then the pieces
+// [max_ctas + 1][2][PIECE_FLOATS].
+int64_t prefill_workspace_bytes(int max_ctas) {
+  const int64_t n = max_ctas + 1;
+  return (n * 4 * 4 + 255) / 256 * 256 + n * 2 * tc2::PIECE_FLOATS * 4;
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   static bool configured[64] = {};
   int dev = 0;
@@ -808,6 +962,26 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   t.out = a.out;
   t.err = a.err;
   if (t.group % 2 == 0) {  // query heads 2y and 2y+1 share a KV head: one CTA, one K/V stream for both
+    const long long nPT = (a.prefix_len + BN - 1) / BN, nQT = t.n_q_tiles, pairs = a.num_q_heads / 2;
+    t.sk_wpair = nQT * nPT + nQT * (nQT + 1) / 2;
+    t.sk_units = pairs * t.sk_wpair;
+    if (a.workspace) {
+      // stream-K when there are more items than CTAs and every CTA's range holds a whole largest item
+      // (so no item is cut twice); otherwise one CTA per item
+      int cap = a.max_ctas;
+      if (cap <= 0) {
+        cudaError_t e = cudaDeviceGetAttribute(&cap, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+      }
+      if (prefill_workspace_bytes(cap) > a.workspace_bytes) return cudaErrorInvalidValue;
+      if (nQT * pairs > cap && t.sk_units / cap >= nPT + nQT) {
+        t.sk_ctas = cap;
+        t.sk_ticket = static_cast<int*>(a.workspace);
+        t.sk_part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) +
+                                             ((static_cast<int64_t>(cap + 1) * 4 * 4 + 255) / 256) * 256);
+        return launch_k(prefill_tc2_kernel, dim3(cap), dim3(NTHREADS), tc2::SMEM_ALLOC, s, tq, tkc, tvc, twk, twv, t);
+      }
+    }
     dim3 grid(t.n_q_tiles, a.num_q_heads / 2);
     return launch_k(prefill_tc2_kernel, grid, dim3(NTHREADS), tc2::SMEM_ALLOC, s, tq, tkc, tvc, twk, twv, t);
   }

@@ -177,10 +177,28 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
     return out
 
 
+def prefill_workspace_bytes(max_ctas: int = 0) -> int:
+    n = int(_lib.load().ftkv_prefill_workspace_bytes(max_ctas))
+    if n < 0:
+        raise RuntimeError("ftkv_prefill_workspace_bytes: the current device could not be queried")
+    return n
+
+
+class PrefillPlan:
+    """Zero-filled stream-K workspace for ``prefill_attn`` (allocated once; calls that share it must be
+    ordered on one stream; the kernel leaves its tickets at zero)."""
+
+    def __init__(self, max_ctas: int = 0, device="cuda"):
+        self.max_ctas = max_ctas
+        self.workspace = torch.zeros(prefill_workspace_bytes(max_ctas), dtype=torch.uint8, device=device)
+
+
 def prefill_attn(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, ws_k: torch.Tensor = None,
                  ws_v: torch.Tensor = None, *, sm_scale: float = HEAD_DIM ** -0.5, out: torch.Tensor = None,
-                 impl: str = "tc", stream=None) -> torch.Tensor:
-    """Causal prefill of the chunk over prefix (+) chunk.  ``impl``: "tc" (tcgen05) or "mma" (mma.sync)."""
+                 impl: str = "tc", plan: PrefillPlan = None, stream=None) -> torch.Tensor:
+    """Causal prefill of the chunk over prefix (+) chunk.  ``impl``: "tc" (tcgen05) or "mma" (mma.sync).
+    With ``plan`` (tcgen05 only) the launch is scheduled stream-K over the plan's workspace
+    (``ftkv_prefill_attn_ws``)."""
     _req(q, torch.bfloat16, "q", 3)
     _req(k_chunk, torch.bfloat16, "k_chunk", 3)
     _req(v_chunk, torch.bfloat16, "v_chunk", 3)
@@ -193,9 +211,16 @@ def prefill_attn(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, 
     if out is None:
         out = torch.empty_like(q)
     _req(out, torch.bfloat16, "out", 3)
+    args = (hq, hkv, HEAD_DIM, _ptr(q), _ptr(k_chunk), _ptr(v_chunk), C, _ptr(ws_k) if P else None,
+            _ptr(ws_v) if P else None, P, float(sm_scale))
+    if plan is not None:
+        if impl != "tc":
+            raise ValueError("the stream-K plan is for the tcgen05 kernel (impl='tc')")
+        check(_lib.load().ftkv_prefill_attn_ws(*args, plan.max_ctas, _ptr(plan.workspace), plan.workspace.numel(),
+                                                _ptr(out), _stream_ptr(stream)), "prefill[tc, stream-K]")
+        return out
     fn = _lib.load().ftkv_prefill_attn if impl == "tc" else _lib.load().ftkv_prefill_attn_mma
-    check(fn(hq, hkv, HEAD_DIM, _ptr(q), _ptr(k_chunk), _ptr(v_chunk), C, _ptr(ws_k) if P else None,
-             _ptr(ws_v) if P else None, P, float(sm_scale), _ptr(out), _stream_ptr(stream)), f"prefill[{impl}]")
+    check(fn(*args, _ptr(out), _stream_ptr(stream)), f"prefill[{impl}]")
     return out
 
 

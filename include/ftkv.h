@@ -50,7 +50,7 @@ typedef enum {
   FTKV_ERR_INVALID = -1,      /* null pointer, negative size, inconsistent sizes               */
   FTKV_ERR_UNSUPPORTED = -2,  /* head_dim, group size or other configuration outside the scope */
   FTKV_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned                              */
-  FTKV_ERR_WORKSPACE = -4,    /* decode workspace too small                                    */
+  FTKV_ERR_WORKSPACE = -4,    /* decode or prefill workspace too small                         */
   FTKV_ERR_CUDA = -6          /* a CUDA call or launch failed (see ftkv_last_cuda_error)       */
 } ftkv_status;
 
@@ -214,6 +214,29 @@ int ftkv_prefill_attn(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_di
                       const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
                       int64_t chunk_len, const uint16_t* ws_k, const uint16_t* ws_v,
                       int64_t prefix_len, float sm_scale, uint16_t* out, void* stream);
+
+/* Same operation with stream-K scheduling over a caller-provided workspace (the faster entry point
+ * for large chunks).  With even GQA groups the kernel takes two query heads per CTA; the work items
+ * (head pair, 128-query tile) hold T = ceil(prefix_len/128) + tile + 1 key tiles.  When there are more
+ * items than CTAs and each CTA's share holds a whole largest item, max_ctas persistent CTAs (<= 0: the
+ * SM count) take equal ranges of all items' key tiles laid end to end; an item cut by a range boundary
+ * is finished by whichever of its two pieces arrives second (partials of both in the workspace).
+ * Otherwise the launch is the same as ftkv_prefill_attn.
+ *   workspace       : device memory, 16-byte aligned, at least ftkv_prefill_workspace_bytes(max_ctas)
+ *                     bytes, ZERO-FILLED before its first use; every call leaves its tickets at zero
+ *                     again.  Calls that share a workspace must be ordered (one stream).
+ * Errors: as ftkv_prefill_attn; NULL workspace -> FTKV_ERR_INVALID; too small -> FTKV_ERR_WORKSPACE;
+ * unaligned -> FTKV_ERR_ALIGN.  The result is the same attention as ftkv_prefill_attn up to FP32
+ * summation order (the two pieces of a cut item are combined in FP32). */
+int ftkv_prefill_attn_ws(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
+                         int64_t chunk_len, const uint16_t* ws_k, const uint16_t* ws_v,
+                         int64_t prefix_len, float sm_scale, int32_t max_ctas, void* workspace,
+                         int64_t workspace_bytes, uint16_t* out, void* stream);
+
+/* Workspace bytes for ftkv_prefill_attn_ws with up to max_ctas CTAs (<= 0: the current device's SM
+ * count); -1 if the device cannot be queried. */
+int64_t ftkv_prefill_workspace_bytes(int32_t max_ctas);
 
 /* Same operation on the legacy warp-level tensor-core path (mma.sync); kept as a comparison point. */
 int ftkv_prefill_attn_mma(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

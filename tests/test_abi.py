@@ -141,6 +141,23 @@ def test_prefill_validation(lib):
         assert fn(32, 4, 128, None, None, None, 0, None, None, 0, 0.08, None, None) == _lib.FTKV_OK
 
 
+def test_prefill_stream_k_validation(lib):
+    def call(ws=0x7000, nbytes=1 << 30, **kw):
+        a = dict(hq=32, hkv=4, d=128, q=0x1000, k=0x2000, v=0x3000, C=16, wk=0x4000, wv=0x5000, P=16, ctas=4)
+        a.update(kw)
+        return lib.ftkv_prefill_attn_ws(a["hq"], a["hkv"], a["d"], a["q"], a["k"], a["v"], a["C"], a["wk"], a["wv"],
+                                        a["P"], 0.08, a["ctas"], ws, nbytes, 0x6000, None)
+    assert call(ws=None) == _lib.FTKV_ERR_INVALID          # the workspace is required
+    assert call(nbytes=-1) == _lib.FTKV_ERR_INVALID
+    assert call(d=64) == _lib.FTKV_ERR_UNSUPPORTED         # the prefill checks still apply
+    assert call(q=0x1004) == _lib.FTKV_ERR_ALIGN
+    # workspace size: tickets [ctas + 1][4] rounded up to 256 B, then two FP32 pieces per boundary
+    piece = (2 * 128 * 128 + 4 * 128) * 4
+    for ctas in (1, 5, 152):
+        n = ctas + 1
+        assert lib.ftkv_prefill_workspace_bytes(ctas) == (n * 16 + 255) // 256 * 256 + n * 2 * piece
+
+
 def test_codec_validation(lib):
     assert lib.ftkv_e4m3_encode_f32(None, None, 0, None) == _lib.FTKV_OK
     assert lib.ftkv_e4m3_encode_f32(None, 0x1000, 4, None) == _lib.FTKV_ERR_INVALID

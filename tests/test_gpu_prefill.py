@@ -15,7 +15,20 @@ from parity import bits_to_cuda_bf16, check_attention
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["mma", "tc"]
+IMPLS = ["mma", "tc", "tc_sk"]
+_PLANS = {}
+
+
+def _prefill(impl, q, kc, vc, wk, wv, ctas=5):
+    """impl "tc_sk": the tcgen05 kernel scheduled stream-K over `ctas` persistent CTAs (0: the SM count;
+    a small count on small inputs makes every CTA run several items and cuts items between CTAs).  The
+    plans are shared by all tests, so each test also checks that the previous calls left the tickets at
+    zero."""
+    if impl == "tc_sk":
+        if ctas not in _PLANS:
+            _PLANS[ctas] = ops.PrefillPlan(ctas)
+        return ops.prefill_attn(q, kc, vc, wk, wv, impl="tc", plan=_PLANS[ctas])
+    return ops.prefill_attn(q, kc, vc, wk, wv, impl=impl)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -27,8 +40,8 @@ def test_prefill_small(impl, P, C):
     q = inputs.queries(rng, C)
     ref = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE)
     mag = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE, abs_v=True)
-    out = ops.prefill_attn(bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
-                           bits_to_cuda_bf16(wk) if P else None, bits_to_cuda_bf16(wv) if P else None, impl=impl)
+    out = _prefill(impl, bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
+                   bits_to_cuda_bf16(wk) if P else None, bits_to_cuda_bf16(wv) if P else None)
     check_attention(out, ref, f"{impl} P={P} C={C}", mag)
 
 
@@ -42,8 +55,8 @@ def test_prefill_gqa(impl, Hq, Hkv):
     q = inputs.queries(rng, C, Hq)
     ref = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE)
     mag = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE, abs_v=True)
-    out = ops.prefill_attn(bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
-                           bits_to_cuda_bf16(wk), bits_to_cuda_bf16(wv), impl=impl)
+    out = _prefill(impl, bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
+                   bits_to_cuda_bf16(wk), bits_to_cuda_bf16(wv))
     check_attention(out, ref, f"{impl} Hq={Hq} Hkv={Hkv}", mag)
 
 
@@ -64,7 +77,7 @@ def test_chunked_prefill_full_workload(impl):
         c0, c1 = c * wl.chunk, min((c + 1) * wl.chunk, wl.q.shape[0])
         P = H + c0
         wk, wv = ops.reconstruct_bf16(gp, slots_d[:P])
-        out = ops.prefill_attn(q_d[c0:c1], k_d[c0:c1], v_d[c0:c1], wk, wv, impl=impl)
+        out = _prefill(impl, q_d[c0:c1], k_d[c0:c1], v_d[c0:c1], wk, wv, ctas=0)
         ops.store_quant(gp, k_d[c0:c1], v_d[c0:c1], slots_d[P:P + c1 - c0])
         # oracle: the same pipeline
         owk, owv = oracle.reconstruct(op, slots_all[:P])
@@ -73,4 +86,30 @@ def test_chunked_prefill_full_workload(impl):
         mag = oracle.prefill_attn(wl.q[c0:c1], wl.k[c0:c1], wl.v[c0:c1], owk, owv, wl.sm_scale, rows, abs_v=True)
         oracle.store_quant(op, wl.k[c0:c1], wl.v[c0:c1], slots_all[P:P + c1 - c0])
         check_attention(out[torch.from_numpy(rows).cuda()], ref, f"{impl} chunk {c}", mag)
+    assert ops.device_errors() == 0
+
+
+@pytest.mark.parametrize("ctas", [2, 3, 7, 19])
+def test_prefill_stream_k_cuts(ctas):
+    """Stream-K with CTA counts that cut items at many different tiles (prefix and chunk tiles, first
+    and last query tiles): same attention as the oracle, bit-identical on a repeated call (the tickets
+    were reset), and within FP32 summation order of the one-CTA-per-item launch."""
+    rng = np.random.default_rng(100 + ctas)
+    P, C = 700, 390  # 6 prefix tiles (the last one ragged), 4 query tiles (the last one ragged)
+    wk, wv = inputs.kv_tokens(rng, P, 1.0)
+    kc, vc = inputs.kv_tokens(rng, C, 1.0)
+    q = inputs.queries(rng, C)
+    ref = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE)
+    mag = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE, abs_v=True)
+    args = [bits_to_cuda_bf16(x) for x in (q, kc, vc, wk, wv)]
+    plan = ops.PrefillPlan(ctas)
+    out1 = ops.prefill_attn(*args, impl="tc", plan=plan)
+    out2 = ops.prefill_attn(*args, impl="tc", plan=plan)
+    whole = ops.prefill_attn(*args, impl="tc")
+    check_attention(out1, ref, f"stream-K ctas={ctas}", mag)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    tickets = ((ctas + 1) * 16 + 255) // 256 * 256
+    assert torch.count_nonzero(plan.workspace[:tickets]).item() == 0  # every ticket back at zero
+    d = (out1.float() - whole.float()).abs().max().item()
+    assert d <= 2.0 ** -6 * max(1.0, whole.float().abs().max().item()), d
     assert ops.device_errors() == 0
