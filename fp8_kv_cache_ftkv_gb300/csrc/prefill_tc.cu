@@ -231,6 +231,19 @@ __device__ __forceinline__ float fmax3(float x, float y, float z) {
   return d;
 }
 
+// Row maximum of 128 scores as four independent chains (a single chain is 64 dependent fmax3 deep).
+__device__ __forceinline__ float row_max(const float (&s)[BN]) {
+  float m0 = fmaxf(s[0], s[1]), m1 = fmaxf(s[2], s[3]), m2 = fmaxf(s[4], s[5]), m3 = fmaxf(s[6], s[7]);
+#pragma unroll
+  for (int c = 8; c < BN; c += 8) {
+    m0 = fmax3(m0, s[c], s[c + 1]);
+    m1 = fmax3(m1, s[c + 2], s[c + 3]);
+    m2 = fmax3(m2, s[c + 4], s[c + 5]);
+    m3 = fmax3(m3, s[c + 6], s[c + 7]);
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
 constexpr int NTHREADS = 224;  // K producer, MMA issuer, 4 softmax warps, V producer
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -383,9 +396,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < BN; c++) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
-      float mraw = fmaxf(s[0], s[1]);
-#pragma unroll
-      for (int c = 2; c < BN; c += 2) mraw = fmax3(mraw, s[c], s[c + 1]);
+      const float mraw = row_max(s);
       const float mt = mraw * a.qk_scale_log2;
       const float m_new = fmaxf(m_used, mt);
       const bool need = (m_used != -INFINITY) && (m_new > m_used + 8.0f);
@@ -418,7 +429,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // P row (BF16 pairs) into TMEM P buffer b, this thread's lane, columns 0..63; p = 2^(s scale - sub),
       // exponents and sums in pairs
       const float2 scale2 = make_float2(a.qk_scale_log2, a.qk_scale_log2), nsub2 = make_float2(-sub, -sub);
-      float2 ps2 = make_float2(0.0f, 0.0f);
+      float2 ps2[4] = {};  // four independent partial sums
 #pragma unroll
       for (int half = 0; half < 2; half++) {
         float w[32];  // 32 packed BF16 pairs, as raw 32-bit words
@@ -427,12 +438,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int c = half * 64 + 2 * e;
           const float2 arg = ffma2(make_float2(s[c], s[c + 1]), scale2, nsub2);
           const float2 pp = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
-          ps2 = fadd2(ps2, pp);
+          ps2[e & 3] = fadd2(ps2[e & 3], pp);
           w[e] = __uint_as_float(float2_to_bf16x2(pp.x, pp.y));
         }
         tmem_st32(lane_base + TMEM_P + b * 64 + half * 32, w);
       }
-      lsum += ps2.x + ps2.y;
+      lsum += ((ps2[0].x + ps2[1].x) + (ps2[2].x + ps2[3].x)) + ((ps2[0].y + ps2[1].y) + (ps2[2].y + ps2[3].y));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL0 + b));
@@ -734,9 +745,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int c = 0; c < BN; c++) s[c] = (c < lim) ? s[c] : -INFINITY;
           }
-          float mraw = fmaxf(s[0], s[1]);
-#pragma unroll
-          for (int c = 2; c < BN; c += 2) mraw = fmax3(mraw, s[c], s[c + 1]);
+          const float mraw = row_max(s);
           const float mt = mraw * a.qk_scale_log2;
           const float m_new = fmaxf(m_used[h], mt);
           const bool need = (m_used[h] != -INFINITY) && (m_new > m_used[h] + 8.0f);
@@ -768,7 +777,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const float sub = (m_used[h] == -INFINITY) ? 0.0f : m_used[h];
           // P_h row (BF16 pairs) over the first 64 columns of S_h; p = 2^(s scale - sub), in pairs
           const float2 scale2 = make_float2(a.qk_scale_log2, a.qk_scale_log2), nsub2 = make_float2(-sub, -sub);
-          float2 ps2 = make_float2(0.0f, 0.0f);
+          float2 ps2[4] = {};  // four independent partial sums
 #pragma unroll
           for (int half = 0; half < 2; half++) {
             float w[32];  // 32 packed BF16 pairs, as raw 32-bit words
@@ -777,12 +786,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const int c = half * 64 + 2 * e;
               const float2 arg = ffma2(make_float2(s[c], s[c + 1]), scale2, nsub2);
               const float2 pp = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
-              ps2 = fadd2(ps2, pp);
+              ps2[e & 3] = fadd2(ps2[e & 3], pp);
               w[e] = __uint_as_float(float2_to_bf16x2(pp.x, pp.y));
             }
             tmem_st32(lane_base + h * 128 + half * 32, w);
           }
-          lsum[h] += ps2.x + ps2.y;
+          lsum[h] += ((ps2[0].x + ps2[1].x) + (ps2[2].x + ps2[3].x)) + ((ps2[0].y + ps2[1].y) + (ps2[2].y + ps2[3].y));
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bar(B_PFULL0 + h));
