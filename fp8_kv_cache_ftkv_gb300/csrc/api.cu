@@ -162,8 +162,11 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
   const int64_t resident = int64_t(sms) * ftkv::decode_ctas_per_sm(max_q_rows);
   const int64_t groups = int64_t(batch) * num_kv_heads;
   // Few (request, KV head) groups: one wave of CTAs (the grid is resident at once and merges cooperatively).
-  // Many: about 8 waves of slices, so that long requests are cut into pieces and the waves stay balanced.
-  int64_t s = (2 * groups <= resident) ? resident / groups : ceil_div(8 * resident, groups);
+  // Many: about 8 waves of slices, so that long requests are cut into pieces and the waves stay balanced;
+  // 16 for multi-row batches, whose CTAs are issue-bound and balance better in finer pieces (64 requests
+  // of 1-8 rows: 5 splits 1,326 us, 10 splits 1,247 us).
+  const int64_t waves = max_q_rows > 1 ? 16 : 8;
+  int64_t s = (2 * groups <= resident) ? resident / groups : ceil_div(waves * resident, groups);
   const int64_t by_len = ceil_div(max_seq_len, 128);  // at least ~128 keys per slice
   if (s > by_len) s = by_len;
   if (s > FTKV_MAX_SPLITS) s = FTKV_MAX_SPLITS;

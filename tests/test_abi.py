@@ -9,6 +9,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 from fp8_kv_cache_ftkv_gb300 import _lib, build
 
@@ -126,6 +127,19 @@ def test_decode_validation(lib):
     assert call_store(vn=0x8004) == _lib.FTKV_ERR_ALIGN
     assert call_store(mq=9) == _lib.FTKV_ERR_UNSUPPORTED       # the decode checks still apply
     assert call_store(kn=None, vn=None, B=0, total=0) == _lib.FTKV_OK
+
+
+def test_decode_auto_splits_host_logic(lib):
+    """The automatic split count (host only; without a GPU the SM count defaults to 152, one CTA each)."""
+    if torch.cuda.is_available():
+        pytest.skip("the expected values assume the 152-SM default")
+    f = lib.ftkv_decode_auto_splits
+    assert f(1, 4, 32768, 1) == 38            # few groups: one wave, 152 // 4
+    assert f(1, 4, 1000, 1) == 8              # at least ~128 keys per slice
+    assert f(64, 4, 40000, 1) == 5            # many groups: ~8 waves, ceil(8 * 152 / 256)
+    assert f(64, 4, 40000, 8) == 10           # multi-row: ~16 waves, ceil(16 * 152 / 256)
+    assert f(1, 1, 10 ** 9, 1) == 64          # capped at FTKV_MAX_SPLITS
+    assert f(0, 4, 100, 1) == 1
 
 
 def test_prefill_validation(lib):
