@@ -224,7 +224,9 @@ int ftkv_prefill_attn(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_di
  * Otherwise the launch is the same as ftkv_prefill_attn.
  *   workspace       : device memory, 16-byte aligned, at least ftkv_prefill_workspace_bytes(max_ctas)
  *                     bytes, ZERO-FILLED before its first use; every call leaves its tickets at zero
- *                     again.  Calls that share a workspace must be ordered (one stream).
+ *                     again.  Calls that share a workspace must be ordered (one stream).  After a call
+ *                     that raised FTKV_DEVERR_TIMEOUT the tickets may be left set: zero-fill the
+ *                     workspace again before reusing it.
  * Errors: as ftkv_prefill_attn; NULL workspace -> FTKV_ERR_INVALID; too small -> FTKV_ERR_WORKSPACE;
  * unaligned -> FTKV_ERR_ALIGN.  The result is the same attention as ftkv_prefill_attn up to FP32
  * summation order (the two pieces of a cut item are combined in FP32). */
