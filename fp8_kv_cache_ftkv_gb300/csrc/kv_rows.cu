@@ -13,14 +13,15 @@ namespace ftkv {
 
 // ---------------------------------------------------------------------------------------------
 // Quantize-on-write.  Half a warp carries one row (token, KV head, tensor): 16 lanes x 8 BF16 elements.
-// A warp handles UNITS (token, head) pairs -- K and V rows of each -- and issues all its loads before
-// any arithmetic, so every lane has 2*UNITS 16-byte loads in flight.
+// A warp handles STORE_UNITS (token, head) pairs -- K and V rows of each -- and issues all its loads
+// before any arithmetic.  One pair per warp: more warps in flight hide the division's latency better
+// than longer load batches per warp (48-layer store: 1 pair 431 us, 2 pairs 468 us, 4 pairs 618 us).
 // Per row: NaN-ignoring absmax (fmaxf from +0), a 16-lane max reduction, scale = absmax / 448 (IEEE
 // division), then x / scale for every element (IEEE division: a reciprocal-times-correction shortcut
 // is not bit-identical to the quotient for every scale, e.g. subnormal ones).
 // Bytes per (token, head): 2 x 256 B read, 2 x (128 B + 4 B) written, + the slot.
 // ---------------------------------------------------------------------------------------------
-constexpr int STORE_UNITS = 2;
+constexpr int STORE_UNITS = 1;  // the loop form is kept so the batch size stays a one-line choice
 
 // (unit / hkv, unit % hkv) without a 64-bit integer division (a long software sequence): a shift for
 // power-of-two head counts, a 32-bit division when the unit fits, the 64-bit one otherwise.
@@ -82,11 +83,13 @@ __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
 
 // ---------------------------------------------------------------------------------------------
 // Reconstruct: 8 lanes per (logical row i, KV head h), 16 codes per lane for K and for V; each lane
-// handles RECON_UNITS such units with every load issued before any conversion.
+// handles RECON_UNITS such units with every load issued before any conversion.  One unit per lane: the
+// scattered code rows are latency-bound, and more warps in flight beat longer batches (8 launches over
+// 14,336 rows: 1 unit 51.0 us, 2 units 61.0 us, 4 units 66.3 us).
 //   ws[i][h][d] = bf16_rne(float(decode(code)) * scale)   -- one FP32 product, no FMA contraction.
 // Bytes per (row, head): 2 x (128 B + 4 B) read (scattered rows), 2 x 256 B written (dense).
 // ---------------------------------------------------------------------------------------------
-constexpr int RECON_UNITS = 2;
+constexpr int RECON_UNITS = 1;
 
 __device__ __forceinline__ void expand16(const uint4& c, float s, uint4& o0, uint4& o1) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
