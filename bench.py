@@ -1,26 +1,29 @@
 #!/usr/bin/env python
 """Benchmark: FP8-KV decode attention, 32K context, batch 1, 48 layers, on one GB300.
 
-One step = one decode step of a 48-layer model's attention over an FP8 KV cache: for every layer,
-quantize-on-write of the new token's K/V into its slot (ftkv_store_quant) and split-K decode attention
-of the BF16 query over all 32,768 keys of that layer's 33,059-row pool (ftkv_decode_attn).  The 48
-layers' pools are distinct (1.67 GB), so every layer streams from HBM (inputs larger than L2).  The step
-is replayed as one CUDA graph.
+One step = one decode step of a 48-layer model's attention over an FP8 KV cache: per layer one launch of
+ftkv_decode_attn_store, which quantizes the new token's K/V into its slot and runs split-K decode attention
+of the BF16 query over all 32,768 keys of that layer's 33,059-row pool (FTKV_DECODE_STABLE_HISTORY: the
+history of a layer is not written by the launches before it, so each launch may start loading while the
+previous one finishes).  The 48 layers' pools are distinct (1.67 GB, far beyond L2), so every step streams
+from HBM.  The step is replayed as one CUDA graph.
 
-Printed (rank 0, one JSON line): value = microseconds per step (lower is better) plus
-  roofline     -- the decode kernel alone: algorithmic bytes per launch / mean launch duration (CUDA
-                  events around each launch on its stream), against the measured HBM copy bandwidth;
-  cpu_baseline -- the FP64 C oracle on the host cores, timed on a bounded sample of layers;
+Printed (rank 0): ONE JSON line on stdout, value = microseconds per step (lower is better), plus
+  roofline     -- algorithmic bytes of the step / graph-timed step time (step level: the launches of a
+                  step overlap, so a per-launch time is the step time / 48), against the measured HBM copy
+                  bandwidth of MEASURED_PEAKS.json;
+  cpu_baseline -- the FP64 C oracle on the host cores (all cores and one thread), timed on a stated
+                  bounded sample and scaled to one step;
   e2e          -- the same step through the Python API with pinned host buffers: H2D of the queries
                   and new K/V, the step, D2H of the outputs, synchronized every step;
   clocks       -- nvidia-smi samples taken during the timed region.
-``--impl reference`` times the oracle alone (the CPU reference arm).
-Other ``--workload`` values time single kernels for profiling; they are not the headline metric.
+Then one "detail" JSON line per other workload on stderr (configs 0, 1, 3, 4, the 40,000-key decode, cold
+reconstruct, and the BF16-KV comparison), each with its own roofline and cpu_baseline; --no-details skips
+them.  ``--impl reference`` times the oracle alone (the CPU reference arm).
 """
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
 import statistics
@@ -42,20 +45,19 @@ HQ, HKV, D = 32, 4, 128
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["decode", "store", "reconstruct", "prefill", "prefill_mma",
-                                          "decode_batched"],
-                   default="decode")
     p.add_argument("--context", type=int, default=32768)
     p.add_argument("--pool-rows", type=int, default=33059)
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--num-splits", type=int, default=0)
-    p.add_argument("--decode-impl", choices=["mma", "tc"], default="mma",
-                   help="mma: the warp-level kernel (ftkv_decode_attn); tc: the tcgen05 kernel (ftkv_decode_attn_tc)")
+    p.add_argument("--no-stable-history", action="store_true",
+                   help="do not pass FTKV_DECODE_STABLE_HISTORY (every decode launch waits for the previous one)")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--cpu-sample-layers", type=int, default=2)
+    p.add_argument("--no-details", action="store_true", help="headline line only")
+    p.add_argument("--details-only", action="store_true", help="detail lines only (no headline)")
+    p.add_argument("--cpu-budget-s", type=float, default=20.0, help="bound on the oracle time of a sample")
     return p.parse_args()
 
 
@@ -65,9 +67,8 @@ def peaks():
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained", 1700.0), \
-            "measured"
-    return 6800.0, 1900.0, 1700.0, "fallback"
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -85,7 +86,7 @@ class ClockSampler:
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -93,7 +94,7 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        time.sleep(0.2)
+        time.sleep(0.1)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -124,36 +125,8 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def source_hash(*files):
-    h = hashlib.sha256()
-    for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()[:16]
-
-
-def profiled_traffic(profile_name: str, kernel_files):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", profile_name)
-    if not os.path.exists(path):
-        return None
-    want = source_hash(*kernel_files)
-    vals = {}
-    with open(path) as f:
-        for line in f:
-            if ":" in line and line.strip().startswith("- "):
-                k, v = line.strip()[2:].split(":", 1)
-                vals[k.strip()] = v.strip()
-    if vals.get("source_hash") != want:
-        return None
-    try:
-        return int(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
-
-
 # ------------------------------------------------------------------------------------------------
-def dist_setup(args):
+def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -177,110 +150,176 @@ def barrier(world):
         dist.barrier()
 
 
+def decode_bytes_per_layer(n):
+    """Algorithmic bytes of one decode launch at n keys (batch 1): K and V codes and scales of every key,
+    the slot table, the query and the output, plus the fused store of the new token (its BF16 K/V read,
+    its codes and scales written)."""
+    codes = n * HKV * D * 2
+    scales = n * HKV * 4 * 2
+    slots = n * 4
+    qo = HQ * D * 2 * 2
+    store = HKV * D * 2 * 2 + (HKV * D + HKV * 4) * 2
+    return codes + scales + slots + qo + store
+
+
 # ------------------------------------------------------------------------------------------------
-def cpu_oracle_decode(args, layers_sample: int):
-    """FP64 oracle: store the new token + decode at the full context, on a sample of layers."""
+# CPU oracle (the reported baseline and the reference arm): bounded samples, stated, scaled to the metric
+def timed_min(fn, reps=2):
+    best = None
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    return best
+
+
+def oracle_threads(n):
+    import oracle
+    oracle.set_threads(n)
+    return oracle.get_threads()
+
+
+def cpu_decode_layer_fn(context, pool_rows, layer=0):
+    """One layer of the batch-1 decode step on the oracle: store of the new token + FP64 decode."""
     import oracle
     from fp8_kv_cache_ftkv_gb300 import inputs
+    wl = inputs.decode_long(context, pool_rows, layers=48)
+    L = wl.layer(layer)
+    op = oracle.Pool(wl.num_rows, HKV, D)
+    oracle.store_quant(op, L.k, L.v, L.slots)
+    n = context
+
+    def run():
+        oracle.store_quant(op, L.k[n - 1:n], L.v[n - 1:n], L.slots[n - 1:n])
+        oracle.decode_attn(op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets, wl.sm_scale, HQ)
+    return run
+
+
+def cpu_baseline_scaled(fn, units_in_sample, units_in_metric, unit, sample, budget_s, to_unit=1e6):
+    """Time fn (one sample) on all host cores and on one thread (if that takes at most budget_s); scale the
+    seconds to the metric's unit (to_unit: 1e6 for microseconds) and from the sample to the metric."""
     ncores = os.cpu_count() or 1
-    oracle.set_threads(ncores)
-    wl = inputs.decode_long(args.context, args.pool_rows, layers=args.layers)
-    n = args.context
-    pools, layers = [], []
-    for l in range(layers_sample):
-        L = wl.layer(l)
-        op = oracle.Pool(wl.num_rows, HKV, D)
-        oracle.store_quant(op, L.k, L.v, L.slots)
-        pools.append(op)
-        layers.append(L)
-
-    def one_sample():
-        t0 = time.perf_counter()
-        for op, L in zip(pools, layers):
-            oracle.store_quant(op, L.k[n - 1:n], L.v[n - 1:n], L.slots[n - 1:n])
-            oracle.decode_attn(op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets, wl.sm_scale, HQ)
-        return time.perf_counter() - t0
-
-    return one_sample, oracle.get_threads(), \
-        f"{layers_sample} of {args.layers} layers (store of the new token + FP64 decode over {n} keys), " \
-        f"scaled x{args.layers / layers_sample:g} to one step"
+    cores = oracle_threads(ncores)
+    t_all = timed_min(fn)
+    single = None
+    oracle_threads(1)
+    t0 = time.perf_counter()
+    fn()  # one single-thread sample only if it is cheap enough
+    t1 = time.perf_counter() - t0
+    if t1 <= budget_s:
+        single = {"value": t1 * to_unit * units_in_metric / units_in_sample, "unit": unit, "cores": 1}
+    oracle_threads(ncores)
+    return {"value": t_all * to_unit * units_in_metric / units_in_sample, "unit": unit, "cores": cores,
+            "kind": "oracle", "sample": sample, "single_thread": single}
 
 
 def run_reference(args, world, rank):
+    """The CPU reference arm: the FP64 oracle's decode step.  Each timed step runs L of the 48 layers in
+    full (L = 48 when the whole run fits in ~150 s of oracle time) and is scaled to 48 layers."""
     if rank != 0:
         return
-    one_sample, cores, sample = cpu_oracle_decode(args, args.cpu_sample_layers)
+    cores = oracle_threads(os.cpu_count() or 1)
+    fns = [cpu_decode_layer_fn(args.context, args.pool_rows, layer=l) for l in range(2)]
+    t_layer = timed_min(fns[0], reps=1)
+    L = int(max(1, min(args.layers, 150.0 / max(t_layer, 1e-6) / max(args.steps + args.warmup, 1))))
+    fns += [cpu_decode_layer_fn(args.context, args.pool_rows, layer=l) for l in range(2, min(L, 48))]
+    layer_fns = [fns[l % len(fns)] for l in range(L)]
+
+    def one_step():
+        t0 = time.perf_counter()
+        for f in layer_fns:
+            f()
+        return time.perf_counter() - t0
     for _ in range(args.warmup):
-        one_sample()
-    times = [one_sample() for _ in range(args.steps)]
-    us = statistics.median(times) * 1e6 * args.layers / args.cpu_sample_layers
+        one_step()
+    t0 = time.perf_counter()
+    times = [one_step() for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    us = statistics.median(times) * 1e6 * args.layers / L
+    sample = (f"{L} of {args.layers} layers per timed step (store of the new token + FP64 decode over "
+              f"{args.context} keys each, {min(L, 48)} distinct layers), scaled x{args.layers / L:g} to one step")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"decode_{args.context}_b1_{args.layers}layers", "context": args.context,
                    "batch": 1, "layers": args.layers, "Hq": HQ, "Hkv": HKV, "D": D, "pool_rows": args.pool_rows},
+        "timed_region_s": wall,
         "cpu_baseline": {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
 # ------------------------------------------------------------------------------------------------
-def build_decode(args, torch, ops, inputs, device):
-    wl = inputs.decode_long(args.context, args.pool_rows, layers=args.layers)
-    n = args.context
+def to_dev_fn(torch, device):
+    return lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def build_decode(args, torch, ops, inputs, device, context=None, pool_rows=None):
+    n = context or args.context
+    wl = inputs.decode_long(n, pool_rows or args.pool_rows, layers=args.layers)
     slots_d = torch.from_numpy(wl.req_to_slot).to(device)
     lens_d = torch.from_numpy(wl.seq_lens).to(device)
-    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(device)
-    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
-        layers = list(ex.map(wl.layer, range(args.layers)))
+    to_dev = to_dev_fn(torch, device)
     # contiguous per-step inputs/outputs (views per layer), so a step's host<->device traffic is 3 copies
     q_all = torch.empty(args.layers, 1, HQ, D, dtype=torch.bfloat16, device=device)
     kv_all = torch.empty(args.layers, 2, 1, HKV, D, dtype=torch.bfloat16, device=device)
     out_all = torch.empty(args.layers, 1, HQ, D, dtype=torch.bfloat16, device=device)
     pools = []
     all_slots = torch.from_numpy(wl.token_slots.astype(np.int32)).to(device)
-    for l, L in enumerate(layers):
-        pool = ops.KVPool.empty(wl.num_rows, HKV, device=device)
-        ops.store_quant(pool, to_dev(L.k), to_dev(L.v), all_slots)
-        pools.append(pool)
-        q_all[l].copy_(to_dev(L.q))
-        kv_all[l, 0].copy_(to_dev(L.k[n - 1:n]))
-        kv_all[l, 1].copy_(to_dev(L.v[n - 1:n]))
-    del layers
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
+        for l, L in enumerate(ex.map(wl.layer, range(args.layers))):
+            pool = ops.KVPool.empty(wl.num_rows, HKV, device=device)
+            ops.store_quant(pool, to_dev(L.k[:n - 1]), to_dev(L.v[:n - 1]), all_slots[:n - 1])
+            pools.append(pool)
+            q_all[l].copy_(to_dev(L.q))
+            kv_all[l, 0].copy_(to_dev(L.k[n - 1:n]))
+            kv_all[l, 1].copy_(to_dev(L.v[n - 1:n]))
     q = [q_all[l] for l in range(args.layers)]
     newk = [kv_all[l, 0] for l in range(args.layers)]
     newv = [kv_all[l, 1] for l in range(args.layers)]
-    new_slot = all_slots[n - 1:n].clone()
     plan = ops.DecodePlan(HQ, HKV, 1, 1, 1, n, args.num_splits, device)
     outs = [out_all[l] for l in range(args.layers)]
     torch.cuda.synchronize()
 
-    fused = args.decode_impl == "mma"  # the warp-level kernel stores the new token itself
-
-    def step(decode_only=False, events=None):
+    def step():
         for l in range(args.layers):
-            if not decode_only and not fused:
-                ops.store_quant(pools[l], newk[l], newv[l], new_slot)
-            if events is not None:
-                events[l][0].record()
-            extra = dict(k_new=newk[l], v_new=newv[l]) if fused and not decode_only else {}
             ops.decode_attn(pools[l], q[l], slots_d, lens_d, None, max_seq_len=n, max_q_rows=1, plan=plan,
-                            out=outs[l], impl=args.decode_impl, **extra)
-            if events is not None:
-                events[l][1].record()
+                            out=outs[l], k_new=newk[l], v_new=newv[l], stable_history=not args.no_stable_history)
 
-    return dict(step=step, q_all=q_all, kv_all=kv_all, out_all=out_all, plan=plan, pools=pools, wl=wl,
-                launches_per_layer=1 if fused else 2, fused=fused)
+    return dict(step=step, q_all=q_all, kv_all=kv_all, out_all=out_all, plan=plan, pools=pools, n=n)
 
 
-def decode_bytes_per_layer(n):
-    codes = n * HKV * D * 2
-    scales = n * HKV * 4 * 2
-    slots = n * 4
-    qo = HQ * D * 2 * 2
-    store = HKV * D * 2 * 2 + (HKV * D + HKV * 4) * 2 + 4
-    return codes + scales + slots + qo, store, codes + scales + slots + HQ * D * 2
+def graph_of(torch, stream, work):
+    """Run `work` once eagerly (per-device set-up outside capture), then capture it as a CUDA graph."""
+    with torch.cuda.stream(stream):
+        work()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        work()
+    return g
+
+
+def time_graph(torch, stream, g, steps, warmup, clocks_gpu=None):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(clocks_gpu) if clocks_gpu is not None else None
+    if clk:
+        clk.__enter__()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    if clk:
+        clk.__exit__(None, None, None)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, (clk.summary() if clk else None)
 
 
 def run_ours(args, world, rank, local):
@@ -293,61 +332,28 @@ def run_ours(args, world, rank, local):
     from fp8_kv_cache_ftkv_gb300 import build as fbuild
     fbuild.build()
     from fp8_kv_cache_ftkv_gb300 import inputs, ops
-    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks()
-
-    if args.workload != "decode":
-        return run_kernel_workload(args, world, rank, local, torch, ops, inputs, device, hbm_peak, bf16_peak,
-                                   peak_src)
-
-    st = build_decode(args, torch, ops, inputs, device)
+    hbm_peak, bf16_peak, peak_src = peaks()
     stream = torch.cuda.Stream(device)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        st["step"]()  # eager warm-up (per-device set-up happens outside capture)
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        st["step"]()
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps):
-                graph.replay()
-            e1.record(stream)
-        e1.synchronize()
-    torch.cuda.synchronize()
-    ms_step = e0.elapsed_time(e1) / args.steps
-    ms_step = reduce_max(ms_step, world)
-    clocks = clk.summary()
 
-    # ---- roofline: per-launch durations of the decode kernel (events around each launch) ----
+    if not args.details_only:
+        run_headline(args, world, rank, local, torch, ops, inputs, device, stream, hbm_peak, peak_src)
+    if not args.no_details and rank == 0 and world == 1:
+        run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, peak_src)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_headline(args, world, rank, local, torch, ops, inputs, device, stream, hbm_peak, peak_src):
+    st = build_decode(args, torch, ops, inputs, device)
+    graph = graph_of(torch, stream, st["step"])
+    barrier(world)
+    ms_step, clocks = time_graph(torch, stream, graph, args.steps, args.warmup, clocks_gpu=local)
+    ms_step = reduce_max(ms_step, world)
     n = args.context
-    per_layer, store_bytes, kernel_bytes = decode_bytes_per_layer(n)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.layers)]
-    durs = []
-    with torch.cuda.stream(stream):
-        for rep in range(max(3, min(args.steps, 10))):
-            torch.cuda._sleep(20_000_000)  # back up the queue so the launches run back to back
-            st["step"](decode_only=False, events=evs)
-            stream.synchronize()
-            if rep > 0:
-                durs += [a.elapsed_time(b) for a, b in evs]
-    dur_ms = statistics.mean(durs)
-    if st["fused"]:
-        kernel_bytes += store_bytes  # the decode launch also stores the new token
-    achieved = kernel_bytes / (dur_ms * 1e-3) / 1e9
-    if args.decode_impl == "tc":
-        kname, prof, ksrc = "decode_tc_kernel", "decode_tc_32k.md", "decode_tc.cu"
-    else:
-        kname, prof, ksrc = "decode_split_kernel<1>", "decode_split_32k.md", "decode.cu"
-    traffic = profiled_traffic(prof, [f"fp8_kv_cache_ftkv_gb300/csrc/{ksrc}",
-                                      "fp8_kv_cache_ftkv_gb300/csrc/decode_merge.cuh",
-                                      "fp8_kv_cache_ftkv_gb300/csrc/ftkv_device.cuh"])
+    layer_bytes = decode_bytes_per_layer(n)
+    step_bytes = args.layers * layer_bytes
+    achieved = step_bytes / (ms_step * 1e-3) / 1e9
 
     # ---- e2e through the public API with pinned host buffers ----
     e2e = None
@@ -377,149 +383,241 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1:
-        one_sample, cores, sample = cpu_oracle_decode(args, args.cpu_sample_layers)
-        one_sample()
-        t = min(one_sample() for _ in range(2))
-        cpu = {"value": t * 1e6 * args.layers / args.cpu_sample_layers, "unit": "us/step", "cores": cores,
-               "kind": "oracle", "sample": sample}
+        fn = cpu_decode_layer_fn(n, args.pool_rows)
+        cpu = cpu_baseline_scaled(fn, 1, args.layers, "us/step",
+                                  f"1 of {args.layers} layers (store of the new token + FP64 decode over {n} keys), "
+                                  f"scaled x{args.layers} to one step", args.cpu_budget_s)
 
     errors = ops.device_errors()
     if rank == 0:
-        step_bytes = args.layers * (per_layer + store_bytes)
         us = ms_step * 1e3
-        gbs = step_bytes / (ms_step * 1e-3) / 1e9
         print(json.dumps({
             "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3-kv/f16-mma/f32-acc", "data": "synthetic",
-            "decode_impl": args.decode_impl,
-            "step": ("per layer one launch: fused quantize-on-write of the new token + split-K decode"
-                     if st["fused"] else "per layer: store of the new token, then split-K decode"),
+            "stable_history": not args.no_stable_history,
+            "step": "per layer one launch: fused quantize-on-write of the new token + split-K decode + split merge",
             "config": {"workload": f"decode_{n}_b1_{args.layers}layers", "context": n, "batch": 1,
                        "layers": args.layers, "Hq": HQ, "Hkv": HKV, "D": D, "pool_rows": args.pool_rows,
                        "num_splits": st["plan"].num_splits, "graph": "one CUDA graph per step",
                        "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of distinct pools per step)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+            "hbm_gbs": achieved, "hbm_frac": achieved / hbm_peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": kname,
-                         "bytes_per_launch": kernel_bytes, "mean_launch_us": dur_ms * 1e3,
-                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * args.layers * st["launches_per_layer"],
+                         "frac": achieved / hbm_peak, "traffic": None, "kernel": "decode_tok_kernel<4>",
+                         "bytes_per_launch": layer_bytes, "per_launch_us": ms_step * 1e3 / args.layers,
+                         "basis": "step level: algorithmic bytes of 48 launches / graph-timed step",
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * args.layers,
             "clocks": clocks, "device_errors": errors,
         }), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    del st, graph
+    torch.cuda.empty_cache()
 
 
-def run_kernel_workload(args, world, rank, local, torch, ops, inputs, device, hbm_peak, bf16_peak, peak_src):
-    """Single-kernel timing of the other hot-path steps (for profiling; not the headline metric)."""
-    to_dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(device)
-    stream = torch.cuda.Stream(device)
-    if args.workload == "store":
-        wl = inputs.store(layers=min(args.layers, 48))
-        slots = torch.from_numpy(wl.slots).to(device)
-        pool = ops.KVPool.empty(wl.num_rows, HKV, device=device)
-        kv = [tuple(to_dev(x) for x in wl.layer(l)) for l in range(wl.layers)]
+# ------------------------------------------------------------------------------------------------
+def detail_line(name, value, unit, roofline, cpu, extra=None):
+    rec = {"detail": name, "value": value, "unit": unit, "higher_is_better": False, "roofline": roofline,
+           "cpu_baseline": cpu}
+    if extra:
+        rec.update(extra)
+    print(json.dumps(rec), file=sys.stderr, flush=True)
 
-        def work():
-            for k, v in kv:
-                ops.store_quant(pool, k, v, slots)
-        T = wl.slots.shape[0]
-        nbytes = wl.layers * (T * HKV * D * 2 * 2 + T * (HKV * D + HKV * 4) * 2 + T * 4)
-        unit_flops = None
-    elif args.workload == "decode_batched":
-        # 64 requests, context ~ U[1,024, 40,000], 1-8 query rows each, one layer of a 2,000,000-row pool;
-        # 4 launches per iteration over the same pool (1.4 GB of rows: far beyond L2)
-        wl = inputs.decode_batched()
-        L = wl.layer(0)
-        pool = ops.KVPool.empty(wl.num_rows, HKV, device=device)
-        ops.store_quant(pool, to_dev(L.k), to_dev(L.v), torch.from_numpy(L.slots).to(device))
-        del L.k, L.v
-        q_d = to_dev(L.q)
-        r2s = torch.from_numpy(wl.req_to_slot).to(device)
-        lens = torch.from_numpy(wl.seq_lens).to(device)
-        offs = torch.from_numpy(wl.q_row_offsets).to(device)
-        mq = int(np.diff(wl.q_row_offsets).max())
-        stride = int(wl.req_to_slot.shape[1])
-        plan = ops.DecodePlan(HQ, HKV, len(wl.seq_lens), int(wl.q_row_offsets[-1]), mq, stride, 0, device)
-        out = torch.empty_like(q_d)
 
-        def work():
-            for _ in range(4):
-                ops.decode_attn(pool, q_d, r2s, lens, offs, max_seq_len=stride, max_q_rows=mq, plan=plan, out=out)
-        keys = int(wl.seq_lens.sum())
-        rows = int(wl.q_row_offsets[-1])
-        nbytes = 4 * (keys * (HKV * D * 2 + HKV * 4 * 2 + 4) + rows * HQ * D * 2 * 2)
-        unit_flops = None
-    elif args.workload == "reconstruct":
-        wl = inputs.prefill()
-        pool = ops.KVPool.empty(wl.num_rows, HKV, device=device)
-        hist = torch.from_numpy(wl.hist_slots).to(device)
-        ops.store_quant(pool, to_dev(wl.hist_k), to_dev(wl.hist_v), hist)
-        ws_k = torch.empty(hist.shape[0], HKV, D, dtype=torch.bfloat16, device=device)
-        ws_v = torch.empty_like(ws_k)
+def hbm_roof(nbytes, ms, peak, src, kernel):
+    a = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": a, "peak": peak, "unit": "GB/s", "frac": a / peak, "traffic": None,
+            "kernel": kernel, "bytes": nbytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"}
 
-        def work():
-            for _ in range(8):
-                ops.reconstruct_bf16(pool, hist, ws_k, ws_v)
-        P = hist.shape[0]
-        nbytes = 8 * (P * (HKV * D + HKV * 4) * 2 + P * 4 + P * HKV * D * 2 * 2)
-        unit_flops = None
-    else:
-        wl = inputs.prefill()
-        C = wl.chunk
-        P = wl.hist_slots.shape[0] + 3 * C  # the last chunk of the workload
-        rng = np.random.default_rng(1)
-        wk, wv = inputs.kv_tokens(rng, P, 1.0)
-        q_d, k_d, v_d = to_dev(wl.q[:C]), to_dev(wl.k[:C]), to_dev(wl.v[:C])
-        wk_d, wv_d = to_dev(wk), to_dev(wv)
-        out = torch.empty_like(q_d)
-        impl = "mma" if args.workload == "prefill_mma" else "tc"
-        # the tcgen05 kernel runs stream-K over a zero-filled workspace (one persistent CTA per SM)
-        pplan = ops.PrefillPlan(0, device) if impl == "tc" else None
 
-        def work():
-            ops.prefill_attn(q_d, k_d, v_d, wk_d, wv_d, out=out, impl=impl, plan=pplan)
-        pairs = C * P + C * (C + 1) // 2
-        unit_flops = pairs * HQ * D * 2 * 2
-        nbytes = None
-    with torch.cuda.stream(stream):
-        work()  # eager first call: per-device set-up happens outside capture
-    stream.synchronize()
-    # one iteration = one CUDA graph replay, so host-side launch cost (Python, ctypes) is not timed
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        work()
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps):
-                graph.replay()
-            e1.record(stream)
-        e1.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    rec = {"metric": f"{args.workload} kernel time", "value": ms * 1e3, "unit": "us/iter", "steps": args.steps,
-           "warmup": args.warmup, "higher_is_better": False, "workload": args.workload, "graph": True,
-           "clocks": clk.summary()}
-    if nbytes:
-        rec["hbm_gbs"] = nbytes / (ms * 1e-3) / 1e9
-        rec["hbm_frac"] = rec["hbm_gbs"] / hbm_peak
-    if unit_flops:
-        rec["tflops"] = unit_flops / (ms * 1e-3) / 1e12
-        rec["tensor_frac_of_bf16_peak"] = rec["tflops"] / bf16_peak
-    if rank == 0:
-        print(json.dumps(rec), flush=True)
+def run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, peak_src):
+    import oracle
+    to_dev = to_dev_fn(torch, device)
+    budget = args.cpu_budget_s
+    steps, warm = max(20, args.steps // 4), 5
+
+    # ---- config 0: one decode step, one layer, 512 keys in a 1,024-row pool (latency-dominated) ----
+    wl = inputs.decode_small()
+    L = wl.layer(0)
+    n = int(wl.seq_lens[0])
+    pool = ops.KVPool.empty(wl.num_rows, wl.Hkv, device=device)
+    ops.store_quant(pool, to_dev(L.k[:n - 1]), to_dev(L.v[:n - 1]), torch.from_numpy(L.slots[:n - 1]).to(device))
+    qd, kn, vn = to_dev(L.q), to_dev(L.k[n - 1:n]), to_dev(L.v[n - 1:n])
+    r2s, lens = torch.from_numpy(wl.req_to_slot).to(device), torch.from_numpy(wl.seq_lens).to(device)
+    plan = ops.DecodePlan(HQ, HKV, 1, 1, 1, n, 0, device)
+    out = torch.empty_like(qd)
+    g = graph_of(torch, stream, lambda: ops.decode_attn(pool, qd, r2s, lens, None, max_seq_len=n, plan=plan, out=out,
+                                                         k_new=kn, v_new=vn))
+    ms, clk = time_graph(torch, stream, g, steps, warm)
+    op = oracle.Pool(wl.num_rows, wl.Hkv, D)
+    oracle.store_quant(op, L.k, L.v, L.slots)
+    cpu = cpu_baseline_scaled(lambda: oracle.decode_attn(op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets,
+                                                         wl.sm_scale, HQ), 1, 1, "us/call", "the whole call", budget)
+    detail_line("config0_decode_512_b1", ms * 1e3, "us/call",
+                hbm_roof(decode_bytes_per_layer(n), ms, hbm_peak, peak_src, "decode_tok_kernel<4>"), cpu,
+                {"note": "one launch of 0.56 MB: latency-bound and L2-warm across replays"})
+    del pool, g
+
+    # ---- config 1: quantize-on-write, 8,192 tokens x 48 layers into 48 distinct 33,059-row pools ----
+    sw = inputs.store(layers=48)
+    slots = torch.from_numpy(sw.slots).to(device)
+    kv = []
+    for l in range(sw.layers):
+        k, v = sw.layer(l)
+        kv.append((to_dev(k), to_dev(v)))
+    pools = [ops.KVPool.empty(sw.num_rows, HKV, device=device) for _ in range(sw.layers)]
+
+    def store_all():
+        for (k, v), p in zip(kv, pools):
+            ops.store_quant(p, k, v, slots)
+    g = graph_of(torch, stream, store_all)
+    ms, _ = time_graph(torch, stream, g, steps, warm)
+    T = sw.slots.shape[0]
+    nbytes = sw.layers * (T * HKV * D * 2 * 2 + T * (HKV * D + HKV * 4) * 2 + T * 4)
+    k0, v0 = sw.layer(0)
+    op = oracle.Pool(sw.num_rows, HKV, D)
+    cpu = cpu_baseline_scaled(lambda: oracle.store_quant(op, k0, v0, sw.slots), 1, sw.layers, "us/step",
+                              f"1 of {sw.layers} layers (8,192 tokens), scaled x{sw.layers}", budget)
+    detail_line("config1_store_8192x48", ms * 1e3, "us/step", hbm_roof(nbytes, ms, hbm_peak, peak_src, "store_quant_kernel"),
+                cpu, {"note": "48 distinct destination pools (1.67 GB): the written rows leave L2"})
+    del kv, pools, g
+    torch.cuda.empty_cache()
+
+    # ---- config 2 at 40,000 keys in 40,290-row pools, 48 layers ----
+    st = build_decode(args, torch, ops, inputs, device, context=40000, pool_rows=40290)
+    g = graph_of(torch, stream, st["step"])
+    ms, _ = time_graph(torch, stream, g, steps, warm)
+    fn = cpu_decode_layer_fn(40000, 40290)
+    cpu = cpu_baseline_scaled(fn, 1, args.layers, "us/step",
+                              f"1 of {args.layers} layers (store + FP64 decode over 40000 keys), scaled x{args.layers}",
+                              budget)
+    detail_line("config2_decode_40000_b1_48layers", ms * 1e3, "us/step",
+                hbm_roof(args.layers * decode_bytes_per_layer(40000), ms, hbm_peak, peak_src, "decode_tok_kernel<4>"),
+                cpu, {"num_splits": st["plan"].num_splits})
+    del st, g
+    torch.cuda.empty_cache()
+
+    # ---- config 3: chunked prefill pipeline, one layer: for each of 4 chunks of 2,048 new tokens,
+    # reconstruct the FP8 prefix into the BF16 workspace, prefill the chunk, quantize-on-write the chunk ----
+    pw = inputs.prefill()
+    pool = ops.KVPool.empty(pw.num_rows, HKV, device=device)
+    hist = torch.from_numpy(pw.hist_slots).to(device)
+    ops.store_quant(pool, to_dev(pw.hist_k), to_dev(pw.hist_v), hist)
+    slots_all = torch.from_numpy(np.concatenate([pw.hist_slots, pw.new_slots])).to(device)
+    qd, kd, vd = to_dev(pw.q), to_dev(pw.k), to_dev(pw.v)
+    H, C = pw.hist_slots.shape[0], pw.chunk
+    ws_k = torch.empty(H + 3 * C, HKV, D, dtype=torch.bfloat16, device=device)
+    ws_v = torch.empty_like(ws_k)
+    outp = torch.empty_like(qd)
+    pplan = ops.PrefillPlan(0, device)
+
+    def pipeline():
+        for c in range(pw.num_chunks):
+            c0, c1 = c * C, (c + 1) * C
+            P = H + c0
+            ops.reconstruct_bf16(pool, slots_all[:P], ws_k[:P], ws_v[:P])
+            ops.prefill_attn(qd[c0:c1], kd[c0:c1], vd[c0:c1], ws_k[:P], ws_v[:P], out=outp[c0:c1], plan=pplan)
+            ops.store_quant(pool, kd[c0:c1], vd[c0:c1], slots_all[P:P + C])
+    g = graph_of(torch, stream, pipeline)
+    ms, _ = time_graph(torch, stream, g, max(10, steps // 4), 3)
+    flops = sum((C * (H + c * C) + C * (C + 1) // 2) * HQ * D * 4 for c in range(pw.num_chunks))
+    tf = flops / (ms * 1e-3) / 1e12
+    # oracle: the same pipeline on every 16th query row of each chunk (attention), full reconstruct and store
+    op = oracle.Pool(pw.num_rows, HKV, D)
+    oracle.store_quant(op, pw.hist_k, pw.hist_v, pw.hist_slots)
+    sall = np.concatenate([pw.hist_slots, pw.new_slots])
+
+    def oracle_pipeline():
+        for c in range(pw.num_chunks):
+            c0, c1 = c * C, (c + 1) * C
+            P = H + c0
+            owk, owv = oracle.reconstruct(op, sall[:P])
+            oracle.prefill_attn(pw.q[c0:c1], pw.k[c0:c1], pw.v[c0:c1], owk, owv, pw.sm_scale,
+                                np.arange(0, C, 16, dtype=np.int64))
+            oracle.store_quant(op, pw.k[c0:c1], pw.v[c0:c1], sall[P:P + C])
+    cpu = cpu_baseline_scaled(oracle_pipeline, 1, 1, "us/pipeline",
+                              "every 16th query row of each chunk (all heads), full reconstruct and store; not scaled",
+                              budget)
+    detail_line("config3_chunked_prefill_4x2048_over_8192", ms * 1e3, "us/pipeline",
+                {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak,
+                 "traffic": None, "kernel": "prefill_tc2_kernel (+ reconstruct, store)", "flops": flops,
+                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)"}, cpu,
+                {"note": "4 x (reconstruct -> prefill -> store) in one graph; flops count causal pairs only"})
+    del pool, g, ws_k, ws_v
+    torch.cuda.empty_cache()
+
+    # ---- reconstruct, cold: 8 distinct pools of 14,336 prefix rows into 8 distinct workspaces ----
+    P = H + 3 * C
+    rk, rv = inputs.kv_tokens(np.random.default_rng(5), P, 1.0)
+    rslots = torch.from_numpy(np.random.default_rng(6).permutation(pw.num_rows)[:P].astype(np.int32)).to(device)
+    rpools = []
+    for _ in range(8):
+        p = ops.KVPool.empty(pw.num_rows, HKV, device=device)
+        ops.store_quant(p, to_dev(rk), to_dev(rv), rslots)
+        rpools.append(p)
+    wss = [(torch.empty(P, HKV, D, dtype=torch.bfloat16, device=device),
+            torch.empty(P, HKV, D, dtype=torch.bfloat16, device=device)) for _ in range(8)]
+
+    def recon_all():
+        for p, (a, b) in zip(rpools, wss):
+            ops.reconstruct_bf16(p, rslots, a, b)
+    g = graph_of(torch, stream, recon_all)
+    ms, _ = time_graph(torch, stream, g, steps, warm)
+    nbytes = 8 * (P * (HKV * D + HKV * 4) * 2 + P * 4 + P * HKV * D * 2 * 2)
+    op = oracle.Pool(pw.num_rows, HKV, D)
+    oracle.store_quant(op, rk, rv, rslots.cpu().numpy())
+    rs = rslots.cpu().numpy()
+    cpu = cpu_baseline_scaled(lambda: oracle.reconstruct(op, rs), 1, 8, "us/iter", "1 of 8 pools, scaled x8", budget)
+    detail_line("reconstruct_14336_rows_x8_cold", ms * 1e3, "us/iter",
+                hbm_roof(nbytes, ms, hbm_peak, peak_src, "reconstruct_kernel"), cpu,
+                {"note": "8 distinct pools and workspaces per iteration (0.5 GB): cold in L2"})
+    del rpools, wss, g
+    torch.cuda.empty_cache()
+
+    # ---- config 4: batched multi-row decode, 64 requests, 1-8 rows, 2,000,000-row pool, one launch ----
+    bw = inputs.decode_batched()
+    Lb = bw.layer(0)
+    pool = ops.KVPool.empty(bw.num_rows, HKV, device=device)
+    ops.store_quant(pool, to_dev(Lb.k), to_dev(Lb.v), torch.from_numpy(Lb.slots).to(device))
+    qd = to_dev(Lb.q)
+    r2s = torch.from_numpy(bw.req_to_slot).to(device)
+    lens = torch.from_numpy(bw.seq_lens).to(device)
+    offs = torch.from_numpy(bw.q_row_offsets).to(device)
+    mq = int(np.diff(bw.q_row_offsets).max())
+    stride = int(bw.req_to_slot.shape[1])
+    plan = ops.DecodePlan(HQ, HKV, len(bw.seq_lens), int(bw.q_row_offsets[-1]), mq, stride, 0, device)
+    out = torch.empty_like(qd)
+    g = graph_of(torch, stream, lambda: ops.decode_attn(pool, qd, r2s, lens, offs, max_seq_len=stride,
+                                                        max_q_rows=mq, plan=plan, out=out))
+    ms, _ = time_graph(torch, stream, g, max(10, steps // 4), 3)
+    keys = int(bw.seq_lens.sum())
+    rows = int(bw.q_row_offsets[-1])
+    nbytes = keys * (HKV * D * 2 + HKV * 4 * 2 + 4) + rows * HQ * D * 2 * 2
+    op = oracle.Pool(bw.num_rows, HKV, D)
+    sample_req = [0, 1, 2, 3]
+    sub = np.concatenate([bw.req_to_slot[b, :bw.seq_lens[b]] for b in sample_req])
+    starts = np.concatenate([[0], np.cumsum(bw.seq_lens)[:-1]])
+    tok = np.concatenate([np.arange(starts[b], starts[b] + bw.seq_lens[b]) for b in sample_req])
+    oracle.store_quant(op, Lb.k[tok], Lb.v[tok], sub)
+    qrows = np.concatenate([np.arange(bw.q_row_offsets[b], bw.q_row_offsets[b + 1]) for b in sample_req])
+    offs_s = np.concatenate([[0], np.cumsum(np.diff(bw.q_row_offsets)[sample_req])]).astype(np.int32)
+    s_keys = int(bw.seq_lens[sample_req].sum())
+    del Lb
+    cpu = cpu_baseline_scaled(lambda: oracle.decode_attn(op, qd.view(torch.int16).cpu().numpy().view(np.uint16)[qrows],
+                                                         bw.req_to_slot[sample_req], bw.seq_lens[sample_req], offs_s,
+                                                         bw.sm_scale, HQ),
+                              s_keys, keys, "us/launch",
+                              f"requests {sample_req} ({s_keys} keys, all their rows), scaled by keys to all 64", budget)
+    detail_line("config4_batched_multirow_64req", ms * 1e3, "us/launch",
+                hbm_roof(nbytes, ms, hbm_peak, peak_src, "decode_split_kernel<2>"), cpu,
+                {"keys": keys, "rows": rows, "num_splits": plan.num_splits})
+    del pool, g
+    torch.cuda.empty_cache()
 
 
 def main():
     args = parse_args()
-    world, rank, local = dist_setup(args)
+    world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
         return

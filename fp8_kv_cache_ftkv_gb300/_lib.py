@@ -18,8 +18,9 @@ FTKV_ERR_UNSUPPORTED = -2
 FTKV_ERR_ALIGN = -3
 FTKV_ERR_WORKSPACE = -4
 FTKV_ERR_CUDA = -6
-FTKV_MAX_SPLITS = 64
+FTKV_MAX_SPLITS = 256
 FTKV_MAX_Q_ROWS = 8
+FTKV_DECODE_STABLE_HISTORY = 0x1
 FTKV_DEVERR_BAD_SLOT = 0x1
 FTKV_DEVERR_SEQ_LEN = 0x2
 FTKV_DEVERR_Q_ROWS = 0x4
@@ -30,10 +31,8 @@ FTKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 EXPORTS = (
     "ftkv_store_quant", "ftkv_reconstruct_bf16", "ftkv_decode_workspace_bytes", "ftkv_decode_auto_splits",
     "ftkv_decode_attn", "ftkv_prefill_attn", "ftkv_prefill_attn_ws", "ftkv_prefill_workspace_bytes",
-    "ftkv_prefill_attn_mma", "ftkv_e4m3_encode_f32",
-    "ftkv_e4m3_decode_f32", "ftkv_pool_bytes", "ftkv_device_errors", "ftkv_status_str",
-    "ftkv_last_cuda_error", "ftkv_abi_version", "ftkv_decode_attn_noalloc", "ftkv_decode_attn_tc",
-    "ftkv_decode_attn_store",
+    "ftkv_e4m3_encode_f32", "ftkv_e4m3_decode_f32", "ftkv_pool_bytes", "ftkv_device_errors", "ftkv_status_str",
+    "ftkv_last_cuda_error", "ftkv_abi_version", "ftkv_decode_attn_noalloc", "ftkv_decode_attn_store",
 )
 
 
@@ -67,22 +66,21 @@ def load() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libftkv.so is not built ({LIB_PATH}); run fp8_kv_cache_ftkv_gb300.build.build()")
         lib = ctypes.CDLL(LIB_PATH)
-        P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        P, I32, I64, F32, SZ, U32 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t,
+                                     ctypes.c_uint32)
         PP = ctypes.POINTER(FtkvPool)
         sig = {
             "ftkv_store_quant": (ctypes.c_int, [PP, P, P, P, I64, P]),
             "ftkv_reconstruct_bf16": (ctypes.c_int, [PP, P, I64, P, P, P]),
             "ftkv_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I64, I32]),
             "ftkv_decode_auto_splits": (I32, [I32, I32, I64, I32]),
-            "ftkv_decode_attn": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P, SZ, P, P]),
-            "ftkv_decode_attn_tc": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P, SZ, P,
-                                                   P]),
+            "ftkv_decode_attn": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, U32, P, SZ,
+                                                P, P]),
             "ftkv_decode_attn_store": (ctypes.c_int, [PP, I32, P, P, P, P, I64, P, P, I32, I64, I32, I64, F32, I32,
-                                                      P, SZ, P, P]),
+                                                      U32, P, SZ, P, P]),
             "ftkv_decode_attn_noalloc": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P,
                                                         P]),
             "ftkv_prefill_attn": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),
-            "ftkv_prefill_attn_mma": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),
             "ftkv_prefill_attn_ws": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, I32, P, I64, P, P]),
             "ftkv_prefill_workspace_bytes": (I64, [I32]),
             "ftkv_e4m3_encode_f32": (ctypes.c_int, [P, P, I64, P]),

@@ -149,7 +149,8 @@ size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, in
   if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim != FTKV_HEAD_DIM || batch < 0 || total_q_rows < 0)
     return 0;
   if (num_splits <= 0 || num_splits > FTKV_MAX_SPLITS) num_splits = FTKV_MAX_SPLITS;
-  const int64_t parts = total_q_rows * num_q_heads * num_splits;
+  // room for the kernel with the most partials per key slice (the single-row kernel: one per key group)
+  const int64_t parts = total_q_rows * num_q_heads * num_splits * ftkv::decode_parts_per_slice(1, num_kv_heads);
   const int64_t ctr = ceil_div((int64_t(batch) * num_kv_heads + 2) * 4, 256) * 256;  // + the grid barrier
   return static_cast<size_t>(ws_acc_bytes(parts) + ws_ml_bytes(parts) + ctr);
 }
@@ -159,14 +160,19 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
   DeviceInfo* di = nullptr;
   int sms = 152;
   if (device_info(&di) == FTKV_OK) sms = di->num_sms;
-  const int64_t resident = int64_t(sms) * ftkv::decode_ctas_per_sm(max_q_rows);
-  const int64_t groups = int64_t(batch) * num_kv_heads;
-  // Few (request, KV head) groups: one wave of CTAs (the grid is resident at once and merges cooperatively).
+  const int64_t per_sm = ftkv::decode_ctas_per_sm(max_q_rows);
+  // A CTA of the single-row kernel covers every KV head of its keys (up to 4 per CTA); the multi-row kernel
+  // takes one KV head per CTA.
+  const int64_t heads_per_cta = max_q_rows <= 1 ? ftkv::decode_tok_heads_per_cta(num_kv_heads) : 1;
+  const int64_t groups = int64_t(batch) * (num_kv_heads / heads_per_cta);
+  // Few (request, head group) pairs (at most one per 8 SMs): one CTA per SM (the grid is resident at once and
+  // merges cooperatively; with the single-row kernel the other CTA slot of every SM is left to the next launch
+  // in the stream).
   // Many: about 8 waves of slices, so that long requests are cut into pieces and the waves stay balanced;
   // 16 for multi-row batches, whose CTAs are issue-bound and balance better in finer pieces (64 requests
   // of 1-8 rows: 5 splits 1,326 us, 10 splits 1,247 us).
   const int64_t waves = max_q_rows > 1 ? 16 : 8;
-  int64_t s = (2 * groups <= resident) ? resident / groups : ceil_div(waves * resident, groups);
+  int64_t s = (8 * groups <= sms) ? sms / groups : ceil_div(waves * sms * per_sm, groups);
   const int64_t by_len = ceil_div(max_seq_len, 128);  // at least ~128 keys per slice
   if (s > by_len) s = by_len;
   if (s > FTKV_MAX_SPLITS) s = FTKV_MAX_SPLITS;
@@ -174,39 +180,72 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
   return static_cast<int32_t>(s);
 }
 
-static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
-                         int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
-                         int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                         int32_t num_splits, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream,
-                         bool use_tc, const uint16_t* k_new = nullptr, const uint16_t* v_new = nullptr) {
+}  // extern "C"
+
+namespace ftkv {
+
+int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
+                    int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
+                    int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
+                    int32_t num_splits, uint32_t flags, const void* workspace, size_t workspace_bytes,
+                    const uint16_t* out, bool check_workspace, DecodeGeom* geom) {
+  *geom = DecodeGeom{};
   int st = check_pool(pool);
   if (st != FTKV_OK) return st;
   if ((st = check_heads(num_q_heads, pool->num_kv_heads)) != FTKV_OK) return st;
   if (batch < 0 || total_q_rows < 0 || max_seq_len < 0 || req_stride < 0) return FTKV_ERR_INVALID;
   if (max_q_rows < 1 || max_q_rows > FTKV_MAX_Q_ROWS) return FTKV_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > FTKV_MAX_SPLITS) return FTKV_ERR_INVALID;
+  if (flags & ~static_cast<uint32_t>(FTKV_DECODE_STABLE_HISTORY)) return FTKV_ERR_INVALID;
   if (max_seq_len > req_stride) return FTKV_ERR_INVALID;
   if (max_seq_len > (int64_t(1) << 31) - 1 - 4096) return FTKV_ERR_UNSUPPORTED;
   if (!q_row_offsets && total_q_rows != batch) return FTKV_ERR_INVALID;
   if (total_q_rows > int64_t(batch) * max_q_rows) return FTKV_ERR_INVALID;
   if (!(sm_scale == sm_scale)) return FTKV_ERR_INVALID;
-  if (batch == 0 || total_q_rows == 0) return FTKV_OK;
-  if (!q || !req_to_slot || !seq_lens || !workspace || !out) return FTKV_ERR_INVALID;
+  if (batch == 0 || total_q_rows == 0) {
+    geom->empty = true;
+    return FTKV_OK;
+  }
+  if (!q || !req_to_slot || !seq_lens || !out || (check_workspace && !workspace)) return FTKV_ERR_INVALID;
   if (!aligned16(q) || !aligned16(out)) return FTKV_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u)) return FTKV_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(req_to_slot) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(q_row_offsets) & 3u))
+    return FTKV_ERR_ALIGN;
+  if (check_workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FTKV_ERR_ALIGN;
   if (total_q_rows > (int64_t(1) << 31) - 1) return FTKV_ERR_UNSUPPORTED;
 
   if (num_splits == 0) num_splits = ftkv_decode_auto_splits(batch, pool->num_kv_heads, max_seq_len, max_q_rows);
+  // keys per slice: a multiple of 8 for the single-row kernel (its blocks of 16 keys may end inside a slice),
+  // of 16 for the multi-row kernel
+  const int64_t align = max_q_rows <= 1 ? 8 : 16;
   int64_t chunk = ceil_div(max_seq_len > 0 ? max_seq_len : 1, num_splits);
-  chunk = ceil_div(chunk, 16) * 16;
-  const int64_t eff_splits = max_seq_len > 0 ? ceil_div(max_seq_len, chunk) : 1;
-  const size_t need = ftkv_decode_workspace_bytes(num_q_heads, pool->num_kv_heads, FTKV_HEAD_DIM, batch,
-                                                  total_q_rows, static_cast<int32_t>(eff_splits));
-  if (workspace_bytes < need) return FTKV_ERR_WORKSPACE;
+  chunk = ceil_div(chunk, align) * align;
+  geom->chunk = chunk;
+  geom->splits = max_seq_len > 0 ? ceil_div(max_seq_len, chunk) : 1;
+  geom->need = ftkv_decode_workspace_bytes(num_q_heads, pool->num_kv_heads, FTKV_HEAD_DIM, batch, total_q_rows,
+                                           static_cast<int32_t>(geom->splits));
+  geom->parts = total_q_rows * num_q_heads * geom->splits * ftkv::decode_parts_per_slice(1, pool->num_kv_heads);
+  if (check_workspace && workspace_bytes < geom->need) return FTKV_ERR_WORKSPACE;
+  return FTKV_OK;
+}
 
+}  // namespace ftkv
+
+extern "C" {
+
+static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
+                         int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
+                         int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
+                         int32_t num_splits, uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out,
+                         void* stream, const uint16_t* k_new = nullptr, const uint16_t* v_new = nullptr) {
+  ftkv::DecodeGeom geom;
+  int st = ftkv::decode_validate(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch,
+                                 total_q_rows, max_q_rows, max_seq_len, sm_scale, num_splits, flags, workspace,
+                                 workspace_bytes, out, true, &geom);
+  if (st != FTKV_OK || geom.empty) return st;
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FTKV_OK) return st;
-  const int64_t parts = total_q_rows * num_q_heads * eff_splits;
+  const int64_t parts = geom.parts;  // the layout ftkv_decode_workspace_bytes sizes
   float* part_acc = static_cast<float*>(workspace);
   char* ws = static_cast<char*>(workspace);
   float* part_ml = reinterpret_cast<float*>(ws + ws_acc_bytes(parts));
@@ -230,8 +269,8 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   a.total_q_rows = total_q_rows;
   a.max_q_rows = max_q_rows;
   a.max_seq_len = max_seq_len;
-  a.num_splits = static_cast<int>(eff_splits);
-  a.chunk = chunk;
+  a.num_splits = static_cast<int>(geom.splits);
+  a.chunk = geom.chunk;
   a.qk_scale_log2 = sm_scale * 1.4426950408889634f;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
@@ -239,7 +278,10 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   a.gbar = counters + int64_t(batch) * pool->num_kv_heads;
   a.out = out;
   a.err = di->err_word;
-  a.use_tc = use_tc ? 1 : 0;
+  a.early = (flags & FTKV_DECODE_STABLE_HISTORY) ? 1 : 0;
+  // When the requests' keys may cover at least half of the pool rows, the kernel reads the scale arrays
+  // into L2 sequentially at its start instead of leaving them to scattered 4-byte reads.
+  a.scan_scales = (int64_t(batch) * max_seq_len * 2 >= pool->num_rows) ? 1 : 0;
   a.k_new = k_new;
   a.v_new = v_new;
   cudaError_t e = ftkv::launch_decode(a, static_cast<cudaStream_t>(stream));
@@ -249,38 +291,30 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
 int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
                      int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                      int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                     int32_t num_splits, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
+                     int32_t num_splits, uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out,
+                     void* stream) {
   return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
-                       max_q_rows, max_seq_len, sm_scale, num_splits, workspace, workspace_bytes, out, stream, false);
-}
-
-int ftkv_decode_attn_tc(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
-                        int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
-                        int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                        int32_t num_splits, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
-  if (max_q_rows != 1) return FTKV_ERR_UNSUPPORTED;
-  return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
-                       max_q_rows, max_seq_len, sm_scale, num_splits, workspace, workspace_bytes, out, stream, true);
+                       max_q_rows, max_seq_len, sm_scale, num_splits, flags, workspace, workspace_bytes, out, stream);
 }
 
 int ftkv_decode_attn_store(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const uint16_t* k_new,
                            const uint16_t* v_new, const int32_t* req_to_slot, int64_t req_stride,
                            const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
                            int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
-                           void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
+                           uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
   if (batch > 0 && total_q_rows > 0) {
     if (!k_new || !v_new) return FTKV_ERR_INVALID;
     if (!aligned16(k_new) || !aligned16(v_new)) return FTKV_ERR_ALIGN;
   }
   return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
-                       max_q_rows, max_seq_len, sm_scale, num_splits, workspace, workspace_bytes, out, stream, false,
+                       max_q_rows, max_seq_len, sm_scale, num_splits, flags, workspace, workspace_bytes, out, stream,
                        k_new, v_new);
 }
 
 static int prefill_common(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,
                           const uint16_t* k_chunk, const uint16_t* v_chunk, int64_t chunk_len,
                           const uint16_t* ws_k, const uint16_t* ws_v, int64_t prefix_len, float sm_scale,
-                          uint16_t* out, void* stream, bool tc, int32_t max_ctas = 0, void* workspace = nullptr,
+                          uint16_t* out, void* stream, int32_t max_ctas = 0, void* workspace = nullptr,
                           int64_t workspace_bytes = 0) {
   int st = check_heads(num_q_heads, num_kv_heads);
   if (st != FTKV_OK) return st;
@@ -304,8 +338,7 @@ static int prefill_common(int32_t num_q_heads, int32_t num_kv_heads, int32_t hea
                       prefix_len > 0 ? ws_k : k_chunk, prefix_len > 0 ? ws_v : v_chunk, prefix_len,
                       sm_scale * 1.4426950408889634f, out, di->err_word, workspace, workspace_bytes,
                       max_ctas};
-  cudaError_t e = tc ? ftkv::launch_prefill_tc(a, static_cast<cudaStream_t>(stream))
-                     : ftkv::launch_prefill_mma(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = ftkv::launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FTKV_OK : cuda_fail(e);
 }
 
@@ -313,7 +346,7 @@ int ftkv_prefill_attn(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_di
                       const uint16_t* k_chunk, const uint16_t* v_chunk, int64_t chunk_len, const uint16_t* ws_k,
                       const uint16_t* ws_v, int64_t prefix_len, float sm_scale, uint16_t* out, void* stream) {
   return prefill_common(num_q_heads, num_kv_heads, head_dim, q, k_chunk, v_chunk, chunk_len, ws_k, ws_v,
-                        prefix_len, sm_scale, out, stream, true);
+                        prefix_len, sm_scale, out, stream);
 }
 
 int ftkv_prefill_attn_ws(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,
@@ -322,7 +355,7 @@ int ftkv_prefill_attn_ws(int32_t num_q_heads, int32_t num_kv_heads, int32_t head
                          void* workspace, int64_t workspace_bytes, uint16_t* out, void* stream) {
   if (!workspace || workspace_bytes < 0) return FTKV_ERR_INVALID;
   return prefill_common(num_q_heads, num_kv_heads, head_dim, q, k_chunk, v_chunk, chunk_len, ws_k, ws_v,
-                        prefix_len, sm_scale, out, stream, true, max_ctas, workspace, workspace_bytes);
+                        prefix_len, sm_scale, out, stream, max_ctas, workspace, workspace_bytes);
 }
 
 int64_t ftkv_prefill_workspace_bytes(int32_t max_ctas) {
@@ -332,13 +365,6 @@ int64_t ftkv_prefill_workspace_bytes(int32_t max_ctas) {
     max_ctas = di->num_sms;
   }
   return ftkv::prefill_workspace_bytes(max_ctas);
-}
-
-int ftkv_prefill_attn_mma(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,
-                          const uint16_t* k_chunk, const uint16_t* v_chunk, int64_t chunk_len, const uint16_t* ws_k,
-                          const uint16_t* ws_v, int64_t prefix_len, float sm_scale, uint16_t* out, void* stream) {
-  return prefill_common(num_q_heads, num_kv_heads, head_dim, q, k_chunk, v_chunk, chunk_len, ws_k, ws_v,
-                        prefix_len, sm_scale, out, stream, false);
 }
 
 int ftkv_e4m3_encode_f32(const float* x, uint8_t* codes, int64_t n, void* stream) {

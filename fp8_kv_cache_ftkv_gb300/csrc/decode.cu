@@ -28,7 +28,9 @@
 //    to the FP32 accumulator with the exact factor 2^E.  Only the range within one block fits FP16.
 //  * The 8 query heads of a GQA group are the MMA N dimension, so G = 8 wastes nothing.
 #include <cfloat>
+#include <mutex>
 
+#include "decode_common.cuh"
 #include "decode_merge.cuh"
 #include "ftkv_device.cuh"
 #include "ftkv_internal.h"
@@ -77,157 +79,11 @@ constexpr int merge_area_bytes() {
 static_assert(merge_area_bytes<1>() <= Cfg<1>::WARPS * Cfg<1>::NSTAGE * STAGE_BYTES, "merge");
 static_assert(merge_area_bytes<2>() <= Cfg<2>::WARPS * Cfg<2>::NSTAGE * STAGE_BYTES, "merge");
 
-__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// D += A(16x32, e4m3, row) * B(32x8, e4m3, col), FP32 accumulate.
-__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // Shared-memory position of 16-byte chunk p of key `key` in a stage.  K rows are read as
 // (key g, chunks 2t and 2t+1), V rows as (keys 2t.., chunk g); the XOR swizzles make both reads and
 // the cp.async writes bank-conflict free.
 __device__ __forceinline__ uint32_t k_chunk_off(int key, int p) { return (key * 8 + (p ^ (key & 1))) * 16; }
 __device__ __forceinline__ uint32_t v_chunk_off(int key, int p) { return STAGE_K + (key * 8 + (p ^ (((key >> 1) & 3) << 1))) * 16; }
-
-__device__ __forceinline__ int64_t clamp_seq_len(const DecodeArgs& a, int b, bool report) {
-  int64_t n = a.seq_lens[b];
-  const int64_t nmax = a.max_seq_len < a.req_stride ? a.max_seq_len : a.req_stride;
-  if (n < 0 || n > nmax) {
-    if (report) flag_error(a.err, kDevErrSeqLen);
-    n = n < 0 ? 0 : nmax;
-  }
-  return n;
-}
-
-// ---- cooperative finish: the split merge after a grid barrier, spread over every warp of the grid ----
-// Used when the whole grid is resident at once (cooperative launch).  Every CTA calls it exactly once,
-// after publishing its partials (or instead of doing anything, if its slice holds no keys).  The barrier
-// waits until every CTA has arrived; then output item (query row, query head, 16 of the 128 d) i goes to
-// warp i / ncta of CTA i % ncta and merges that (row, head)'s slices (same arithmetic as the ticket merge:
-// M = max m_s, L = sum 2^(m_s - M) l_s, o = sum 2^(m_s - M) A_s / L).  The CTA that finishes last resets
-// the barrier for the next call.  All waits are bounded (a timeout is flagged).
-template <int WARPS>
-__device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ncta = gridDim.x * gridDim.y * gridDim.z;
-  const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-  __threadfence();  // this CTA's partials before its arrival
-  __syncthreads();
-  __shared__ int s_ok;
-  if (threadIdx.x == 0) {
-    atomicAdd(a.gbar, 1);
-    unsigned long long t0, t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    int v = 0;
-    bool ok = false;
-    for (;;) {
-      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.gbar) : "memory");
-      if (v >= ncta) {
-        ok = true;
-        break;
-      }
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-      if (t - t0 > 2000000000ull) break;
-      __nanosleep(32);
-    }
-    if (!ok) flag_error(a.err, kDevErrTimeout);
-    __threadfence();
-    s_ok = ok;
-  }
-  __syncthreads();
-  if (s_ok) {
-    const int64_t items = a.total_q_rows * a.num_q_heads * 8;
-    const int d4 = lane & 3, sg = lane >> 2;  // 4 d values, slice group (slices sg, sg + 8, ...)
-    for (int64_t it = cta + static_cast<int64_t>(ncta) * warp; it < items; it += static_cast<int64_t>(ncta) * WARPS) {
-      const int64_t t = it / (a.num_q_heads * 8);  // query row
-      const int rem = static_cast<int>(it - t * a.num_q_heads * 8);
-      const int qh = rem >> 3, qd = rem & 7;
-      int b = static_cast<int>(t), R = 1;
-      if (a.q_row_offsets) {  // request of row t
-        int lo = 0, hi = a.batch;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (a.q_row_offsets[mid + 1] <= t) lo = mid + 1; else hi = mid;
-        }
-        b = lo;
-        if (b >= a.batch) continue;
-        const int64_t r0 = a.q_row_offsets[b];
-        R = a.q_row_offsets[b + 1] - a.q_row_offsets[b];
-        if (R < 0 || R > a.max_q_rows || r0 < 0 || r0 + R > a.total_q_rows) continue;  // skipped request
-      }
-      int64_t n = a.seq_lens[b];
-      const int64_t nmax = a.max_seq_len < a.req_stride ? a.max_seq_len : a.req_stride;
-      n = n < 0 ? 0 : (n > nmax ? nmax : n);
-      const int64_t nsl64 = (n + a.chunk - 1) / a.chunk;
-      const int nslices = static_cast<int>(nsl64 < a.num_splits ? nsl64 : a.num_splits);
-      uint16_t* dst = a.out + (t * a.num_q_heads + qh) * kHeadDim + qd * 16;
-      if (nslices == 0) {  // no keys: zeros
-        if (lane < 16) dst[lane] = 0;
-        continue;
-      }
-      const int64_t prow0 = (t * a.num_q_heads + qh) * a.num_splits;
-      const bool h0 = lane < nslices, h1 = lane + 32 < nslices;
-      const float2 ml0 = h0 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml) + prow0 + lane) : make_float2(-INFINITY, 0.f);
-      const float2 ml1 = h1 ? __ldcg(reinterpret_cast<const float2*>(a.part_ml) + prow0 + lane + 32) : make_float2(-INFINITY, 0.f);
-      float4 v[8];  // slices sg + 8k (all 64 slices at most), every load in flight at once
-#pragma unroll
-      for (int k = 0; k < 8; k++) {
-        const int sl = sg + 8 * k;
-        v[k] = (sl < nslices) ? __ldcg(reinterpret_cast<const float4*>(a.part_acc + (prow0 + sl) * kHeadDim + qd * 16) + d4)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float M = fmaxf(ml0.x, ml1.x);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      const float e0 = (h0 && M != -INFINITY) ? exp2f(ml0.x - M) : 0.0f;
-      const float e1 = (h1 && M != -INFINITY) ? exp2f(ml1.x - M) : 0.0f;
-      float L = (h0 ? e0 * ml0.y : 0.0f) + (h1 ? e1 * ml1.y : 0.0f);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-      const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
-      const float w0 = e0 * invL, w1 = e1 * invL;
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < 8; k++) {
-        const int sl = sg + 8 * k;
-        const float wa = __shfl_sync(0xffffffffu, w0, sl & 31), wb = __shfl_sync(0xffffffffu, w1, sl & 31);
-        const float wv = (sl < nslices) ? (sl < 32 ? wa : wb) : 0.0f;
-        o.x = fmaf(wv, v[k].x, o.x);
-        o.y = fmaf(wv, v[k].y, o.y);
-        o.z = fmaf(wv, v[k].z, o.z);
-        o.w = fmaf(wv, v[k].w, o.w);
-      }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
-        o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
-        o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
-        o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
-      }
-      if (sg == 0)
-        *reinterpret_cast<uint2*>(dst + 4 * d4) = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(a.gbar + 1, 1) == ncta - 1) {  // every CTA is past the barrier
-    a.gbar[0] = 0;
-    a.gbar[1] = 0;
-  }
-}
 
 template <int RPW>
 __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(const DecodeArgs a) {
@@ -680,7 +536,7 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     A.z += __shfl_xor_sync(0xffffffffu, A.z, 1);
     A.w += __shfl_xor_sync(0xffffffffu, A.w, 1);
     if (half == 0) {
-      const int64_t prow = ((row0 + rr) * a.num_q_heads + h * a.group + hh) * a.num_splits + split;
+      const int64_t prow = ((row0 + rr) * a.num_q_heads + h * a.group + hh) * a.num_splits * a.pps + split;
       reinterpret_cast<float4*>(a.part_acc + prow * kHeadDim)[c] = A;
       if (c == 0) {
         a.part_ml[prow * 2] = w[WARPS];
@@ -717,30 +573,34 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
 
 template <int RPW>
 cudaError_t launch_split(const DecodeArgs& a, cudaStream_t s) {
-  static bool configured[64] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<RPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes<RPW>());
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-  // a grid that fits on the GPU at once is launched cooperatively and merges after a grid barrier
-  static int resident[64] = {};  // co-resident CTAs per device (0: not known yet, -1: no cooperative launch)
-  if (dev >= 0 && dev < 64 && resident[dev] == 0) {
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDecodeDevices) return cudaErrorInvalidDevice;
+  // per-device set-up, once: dynamic shared memory above 48 KB and the co-resident CTA count (0: no
+  // cooperative launch); a grid that fits on the GPU at once is launched cooperatively and merges after a
+  // grid barrier
+  static std::once_flag once[kMaxDecodeDevices];
+  static cudaError_t setup_err[kMaxDecodeDevices];
+  static int resident[kMaxDecodeDevices];
+  std::call_once(once[dev], [&] {
+    setup_err[dev] = cudaFuncSetAttribute(decode_split_kernel<RPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          smem_bytes<RPW>());
     int coop_ok = 0, sms = 0, per_sm = 0;
-    cudaDeviceGetAttribute(&coop_ok, cudaDevAttrCooperativeLaunch, dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<RPW>, Cfg<RPW>::WARPS * 32,
+    if (setup_err[dev] == cudaSuccess) setup_err[dev] = cudaDeviceGetAttribute(&coop_ok, cudaDevAttrCooperativeLaunch, dev);
+    if (setup_err[dev] == cudaSuccess) setup_err[dev] = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (setup_err[dev] == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<RPW>, Cfg<RPW>::WARPS * 32,
                                                       smem_bytes<RPW>()) != cudaSuccess)
       per_sm = 0;
-    resident[dev] = (coop_ok && per_sm > 0 && sms > 0) ? per_sm * sms : -1;
-  }
+    resident[dev] = (coop_ok && per_sm > 0 && sms > 0) ? per_sm * sms : 0;
+  });
+  if (setup_err[dev] != cudaSuccess) return setup_err[dev];
+  dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
   DecodeArgs c = a;
+  c.pps = 1;  // one partial per key slice
   const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
-  c.coop = (dev >= 0 && dev < 64 && resident[dev] > 0 && ctas <= resident[dev]) ? 1 : 0;
+  c.coop = (resident[dev] > 0 && ctas <= resident[dev]) ? 1 : 0;
   if (c.coop) return launch_k_coop(decode_split_kernel<RPW>, grid, dim3(Cfg<RPW>::WARPS * 32), smem_bytes<RPW>(), s, c);
   return launch_k(decode_split_kernel<RPW>, grid, dim3(Cfg<RPW>::WARPS * 32), smem_bytes<RPW>(), s, c);
 }
@@ -748,14 +608,14 @@ cudaError_t launch_split(const DecodeArgs& a, cudaStream_t s) {
 }  // namespace
 
 int decode_ctas_per_sm(int max_q_rows) {
-  (void)max_q_rows;
-  return 1;  // both configurations are shared-memory bound at one CTA per SM
+  // the token-major single-row kernel fits two CTAs per SM; the multi-row kernel is shared-memory bound at one
+  return max_q_rows <= 1 ? 2 : 1;
 }
 
-// The tcgen05 kernel (decode_tc.cu) when asked for (single-row batches), else this warp-level kernel.
+// Single-row batches: the token-major kernel (decode_tok.cu); multi-row batches: this kernel.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  if (a.use_tc && a.max_q_rows <= 1) return launch_decode_tc(a, s);
-  return (a.max_q_rows <= 1) ? launch_split<1>(a, s) : launch_split<2>(a, s);
+  if (a.max_q_rows <= 1) return launch_decode_tok(a, s);
+  return launch_split<2>(a, s);
 }
 
 }  // namespace ftkv

@@ -1,0 +1,187 @@
+// decode_common.cuh -- pieces shared by the two split-K decode kernels (decode.cu: one KV head per CTA,
+// multi-row batches; decode_tok.cu: every KV head of a token per CTA, single-row batches).
+//
+// The split merge after a grid barrier (cooperative launches) lives here as well:
+// for each (query row, query head), with per-slice maximum m_s (log2 units), sum l_s and unnormalized
+// accumulator O_s (FreeToken PR #897, "Fresh R9700 stage-1 A/B": a stage over key slices, then a merge)
+//     M = max_s m_s,   L = sum_s 2^(m_s - M) l_s,   o = sum_s (2^(m_s - M) / L) O_s      (o = 0 if L = 0).
+#pragma once
+
+#include <cfloat>
+
+#include "ftkv_device.cuh"
+#include "ftkv_internal.h"
+
+namespace ftkv {
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D += A(16x32, e4m3, row) * B(32x8, e4m3, col), FP32 accumulate.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ int64_t clamp_seq_len(const DecodeArgs& a, int b, bool report) {
+  int64_t n = a.seq_lens[b];
+  const int64_t nmax = a.max_seq_len < a.req_stride ? a.max_seq_len : a.req_stride;
+  if (n < 0 || n > nmax) {
+    if (report) flag_error(a.err, kDevErrSeqLen);
+    n = n < 0 ? 0 : nmax;
+  }
+  return n;
+}
+
+// Wait for the preceding grid of the stream (programmatic dependent launch) -- its completion and memory.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- merge of one output item: (query row t, query head qh, 4 of the 128 d), by one warp ----
+// Lane k takes the partials k, k + 32, ... of the (row, head) in rounds of 32 * CH (one round in the usual
+// case): their (m, l) and their 4 accumulators, every load of a round in flight at once; the round maximum by
+// a warp reduction, the lane's running (M, L, o) rescaled when it grows; L and o reduced across the lanes at
+// the end.  Requests whose row offsets are inconsistent were skipped by the main kernel (flagged there) and
+// are skipped here; a (row, head) without keys gets zeros.
+template <int CH>
+__device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int lane) {
+  constexpr int QUADS = kHeadDim / 4;
+  const int64_t t = it / (a.num_q_heads * QUADS);  // query row
+  const int rem = static_cast<int>(it - t * a.num_q_heads * QUADS);
+  const int qh = rem / QUADS, d4 = rem % QUADS;
+  int b = static_cast<int>(t);
+  if (a.q_row_offsets) {  // request of row t
+    int lo = 0, hi = a.batch;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (a.q_row_offsets[mid + 1] <= t) lo = mid + 1; else hi = mid;
+    }
+    b = lo;
+    if (b >= a.batch) return;
+    const int64_t r0 = a.q_row_offsets[b];
+    const int R = a.q_row_offsets[b + 1] - a.q_row_offsets[b];
+    if (R < 0 || R > a.max_q_rows || r0 < 0 || r0 + R > a.total_q_rows) return;  // skipped request
+  }
+  int64_t n = a.seq_lens[b];
+  const int64_t nmax = a.max_seq_len < a.req_stride ? a.max_seq_len : a.req_stride;
+  n = n < 0 ? 0 : (n > nmax ? nmax : n);
+  const int64_t nsl64 = (n + a.chunk - 1) / a.chunk;
+  const int nslices = static_cast<int>(nsl64 < a.num_splits ? nsl64 : a.num_splits) * a.pps;
+  uint16_t* dst = a.out + (t * a.num_q_heads + qh) * kHeadDim + 4 * d4;
+  if (nslices == 0) {  // no keys: zeros
+    if (lane == 0) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+    return;
+  }
+  const int64_t prow0 = (t * a.num_q_heads + qh) * static_cast<int64_t>(a.num_splits) * a.pps;
+  const float2* pml = reinterpret_cast<const float2*>(a.part_ml) + prow0;
+  const float4* pacc = reinterpret_cast<const float4*>(a.part_acc + prow0 * kHeadDim) + d4;
+  float M = -INFINITY, L = 0.0f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < nslices; base += 32 * CH) {  // warp-uniform
+    float2 ml[CH];
+    float4 v[CH];
+#pragma unroll
+    for (int k = 0; k < CH; k++) {
+      const int sl = base + lane + 32 * k;
+      const bool in = sl < nslices;
+      ml[k] = in ? __ldcg(pml + sl) : make_float2(-INFINITY, 0.f);
+      v[k] = in ? __ldcg(pacc + static_cast<int64_t>(sl) * QUADS) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float Mc = M;
+#pragma unroll
+    for (int k = 0; k < CH; k++) Mc = fmaxf(Mc, ml[k].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, off));
+    if (Mc == -INFINITY) continue;  // warp-uniform: nothing seen yet
+    const float sc = (M == -INFINITY) ? 0.0f : exp2f(M - Mc);
+    L *= sc;
+    o.x *= sc;
+    o.y *= sc;
+    o.z *= sc;
+    o.w *= sc;
+#pragma unroll
+    for (int k = 0; k < CH; k++) {
+      const float w = (ml[k].x == -INFINITY) ? 0.0f : exp2f(ml[k].x - Mc);
+      L = fmaf(w, ml[k].y, L);
+      o.x = fmaf(w, v[k].x, o.x);
+      o.y = fmaf(w, v[k].y, o.y);
+      o.z = fmaf(w, v[k].z, o.z);
+      o.w = fmaf(w, v[k].w, o.w);
+    }
+    M = Mc;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    L += __shfl_xor_sync(0xffffffffu, L, off);
+    o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
+    o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
+    o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
+    o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
+  }
+  const float invL = (M != -INFINITY && L > 0.0f) ? 1.0f / L : 0.0f;
+  if (lane == 0)
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(float2_to_bf16x2(o.x * invL, o.y * invL), float2_to_bf16x2(o.z * invL, o.w * invL));
+}
+
+// ---- cooperative finish: the split merge after a grid barrier, spread over every warp of the grid ----
+// Used when the whole grid is resident at once (cooperative launch).  Every CTA calls it exactly once,
+// after publishing its partials (or instead of doing anything, if its slice holds no keys).  The barrier
+// waits until every CTA has arrived (polled by thread 0, bounded at 2 s: a timeout is flagged and the merge
+// skipped).  Then output item (query row, query head, 4 of the 128 d) i goes to warp i / ncta of CTA
+// i % ncta (merge_item).  The CTA that finishes last resets the barrier for the next call.
+template <int WARPS>
+__device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ncta = gridDim.x * gridDim.y * gridDim.z;
+  const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  __threadfence();  // this CTA's partials before its arrival
+  __syncthreads();
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    atomicAdd(a.gbar, 1);
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    int v = 0;
+    bool ok = false;
+    for (;;) {
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.gbar) : "memory");
+      if (v >= ncta) {
+        ok = true;
+        break;
+      }
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > 2000000000ull) break;
+      __nanosleep(32);
+    }
+    if (!ok) flag_error(a.err, kDevErrTimeout);
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (s_ok) {
+    const int64_t items = a.total_q_rows * a.num_q_heads * (kHeadDim / 4);
+    for (int64_t it = cta + static_cast<int64_t>(ncta) * warp; it < items; it += static_cast<int64_t>(ncta) * WARPS)
+      merge_item<10>(a, it, lane);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(a.gbar + 1, 1) == ncta - 1) {  // every CTA is past the barrier
+    a.gbar[0] = 0;
+    a.gbar[1] = 0;
+  }
+}
+
+}  // namespace ftkv

@@ -62,8 +62,9 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
   const int G = a.group;
   const int npairs = nrows * G;  // pair pr = (row pr / G, head pr % G)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int64_t pstride = static_cast<int64_t>(a.num_splits) * a.pps;  // partial slots per (row, head)
   auto prow0 = [&](int pr) -> int64_t {  // partial row of (pair pr, slice 0)
-    return ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * a.num_splits;
+    return ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * pstride;
   };
   // Bulk path (even slice counts keep every copy a multiple of 16 bytes and 16-byte aligned): per (row, head),
   // one copy of its nslices x 128 accumulators and one of its nslices (m, l) pairs, completing on that pair's
@@ -73,9 +74,9 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
   const uint32_t acc_bytes = static_cast<uint32_t>(npairs) * nslices * kHeadDim * 4;
   const uint32_t ml_bytes = static_cast<uint32_t>(npairs) * nslices * 8;
   const uint32_t wgt_bytes = static_cast<uint32_t>(nwarps) * 64 * 4;
-  // (m, l) copies start at part_ml + 8 prow0 bytes, prow0 a multiple of num_splits: 16-byte aligned when
-  // num_splits is even; the accumulator copies start at 512 prow0 bytes.
-  const bool bulk = (nslices % 2 == 0) && (a.num_splits % 2 == 0) && nslices <= 64 && (nwarps % 2 == 0) &&
+  // (m, l) copies start at part_ml + 8 prow0 bytes, prow0 a multiple of the slot count per (row, head): 16-byte
+  // aligned when that count is even; the accumulator copies start at 512 prow0 bytes.
+  const bool bulk = (nslices % 2 == 0) && (pstride % 2 == 0) && nslices <= 64 && (nwarps % 2 == 0) &&
                     static_cast<uint64_t>(acc_bytes) + ml_bytes + wgt_bytes + 8ull * npairs <= buf_bytes;
   if (bulk) {
     const float* pacc = reinterpret_cast<const float*>(buf);              // [npairs][nslices][128]
@@ -162,60 +163,65 @@ __device__ __forceinline__ void merge_split_partials(const DecodeArgs& a, int64_
     }
     return;
   }
-  float* wts = reinterpret_cast<float*>(buf);  // [2][npairs][nslices]: m then l, m replaced by the weights
-  for (int i = threadIdx.x; i < npairs * nslices; i += blockDim.x) {
-    const int pr = i / nslices, sl = i % nslices;
-    const int64_t p = prow0(pr) + sl;
-    wts[i] = __ldcg(a.part_ml + p * 2);
-    wts[npairs * nslices + i] = __ldcg(a.part_ml + p * 2 + 1);
-  }
-  __syncthreads();
-  for (int pr = warp; pr < npairs; pr += nwarps)
-    merge_weights_warp(wts + pr * nslices, wts + npairs * nslices + pr * nslices, nslices, lane);
-  __syncthreads();
-  // Output: item (pair, 4 d values) split over 2 adjacent lanes, each summing every other slice with up to 16
-  // loads in flight; the two halves meet through one shuffle.  npairs * 64 and blockDim.x are multiples
-  // of 32, so every warp is either fully inside the range or fully outside it.
-  constexpr int SPLIT = 2, BATCH = 16;
-  const int total = npairs * (kHeadDim / 4) * SPLIT;
-  auto acc_src = [&](int it) {
-    const int item = it / SPLIT, d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);
-    return reinterpret_cast<const float4*>(a.part_acc + prow0(pr) * kHeadDim) + d4;
-  };
-  for (int it = threadIdx.x; it < total; it += blockDim.x) {
-    const int part = it % SPLIT, item = it / SPLIT;
-    const int d4 = item % (kHeadDim / 4), pr = item / (kHeadDim / 4);
-    const float* wm = wts + pr * nslices;
-    const float4* src = acc_src(it);
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = part; s0 < nslices; s0 += SPLIT * BATCH) {
-      float4 v[BATCH];
+  // L2 path, in chunks of pairs whose (m, l) fit in the buffer: [2][np][nslices], m then l, m replaced by the
+  // weights.
+  const int chunk_pairs = static_cast<int>(buf_bytes / (8u * static_cast<uint32_t>(nslices))) > 0
+                              ? static_cast<int>(buf_bytes / (8u * static_cast<uint32_t>(nslices)))
+                              : 1;
+  for (int pc = 0; pc < npairs; pc += chunk_pairs) {
+    const int np = (npairs - pc < chunk_pairs) ? npairs - pc : chunk_pairs;
+    float* wts = reinterpret_cast<float*>(buf);
+    __syncthreads();  // the previous chunk is done with the buffer
+    for (int i = threadIdx.x; i < np * nslices; i += blockDim.x) {
+      const int pr = pc + i / nslices, sl = i % nslices;
+      const int64_t p = prow0(pr) + sl;
+      wts[i] = __ldcg(a.part_ml + p * 2);
+      wts[np * nslices + i] = __ldcg(a.part_ml + p * 2 + 1);
+    }
+    __syncthreads();
+    for (int q = warp; q < np; q += nwarps)
+      merge_weights_warp(wts + q * nslices, wts + np * nslices + q * nslices, nslices, lane);
+    __syncthreads();
+    // Output: item (pair, 4 d values) split over 2 adjacent lanes, each summing every other slice with up to 16
+    // loads in flight; the two halves meet through one shuffle.  np * 64 and blockDim.x are multiples of 32, so
+    // every warp is either fully inside the range or fully outside it.
+    constexpr int SPLIT = 2, BATCH = 16;
+    const int total = np * (kHeadDim / 4) * SPLIT;
+    for (int it = threadIdx.x; it < total; it += blockDim.x) {
+      const int part = it % SPLIT, item = it / SPLIT;
+      const int d4 = item % (kHeadDim / 4), q = item / (kHeadDim / 4), pr = pc + q;
+      const float* wm = wts + q * nslices;
+      const float4* src = reinterpret_cast<const float4*>(a.part_acc + prow0(pr) * kHeadDim) + d4;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = part; s0 < nslices; s0 += SPLIT * BATCH) {
+        float4 v[BATCH];
 #pragma unroll
-      for (int u = 0; u < BATCH; u++) {
-        const int sl = s0 + SPLIT * u;
-        v[u] = (sl < nslices) ? __ldcg(src + static_cast<int64_t>(sl) * (kHeadDim / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < BATCH; u++) {
+          const int sl = s0 + SPLIT * u;
+          v[u] = (sl < nslices) ? __ldcg(src + static_cast<int64_t>(sl) * (kHeadDim / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; u++) {
+          const int sl = s0 + SPLIT * u;
+          const float wv = (sl < nslices) ? wm[sl] : 0.0f;
+          o.x += wv * v[u].x;
+          o.y += wv * v[u].y;
+          o.z += wv * v[u].z;
+          o.w += wv * v[u].w;
+        }
       }
 #pragma unroll
-      for (int u = 0; u < BATCH; u++) {
-        const int sl = s0 + SPLIT * u;
-        const float wv = (sl < nslices) ? wm[sl] : 0.0f;
-        o.x += wv * v[u].x;
-        o.y += wv * v[u].y;
-        o.z += wv * v[u].z;
-        o.w += wv * v[u].w;
+      for (int off = 1; off < SPLIT; off <<= 1) {
+        o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
+        o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
+        o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
+        o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
       }
-    }
-#pragma unroll
-    for (int off = 1; off < SPLIT; off <<= 1) {
-      o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
-      o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
-      o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
-      o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
-    }
-    if (part == 0) {
-      const uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
-      *reinterpret_cast<uint2*>(a.out + ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * kHeadDim + 4 * d4) =
-          packed;
+      if (part == 0) {
+        const uint2 packed = make_uint2(float2_to_bf16x2(o.x, o.y), float2_to_bf16x2(o.z, o.w));
+        *reinterpret_cast<uint2*>(a.out + ((row0 + pr / G) * a.num_q_heads + h * G + pr % G) * kHeadDim + 4 * d4) =
+            packed;
+      }
     }
   }
 }

@@ -11,14 +11,16 @@
 // with cudaGetSymbolAddress and keeps it; in host code the array's name is only a host-side stand-in
 // and must never be handed to a kernel.  Make that first call before any stream capture.
 // Every call shares the one array and it keeps the previous call's contents, so each call clears the
-// arrival counters it is about to use (cudaMemsetAsync on the caller's stream).  Calls that overlap on
-// the GPU -- on different streams, or from different threads -- race on the array; serialize them.
+// arrival counters it is about to use (cudaMemsetAsync on the caller's stream), after every argument has
+// been checked: a call that is refused enqueues nothing.  Calls that overlap on the GPU -- on different
+// streams, or from different threads -- race on the array; serialize them.
 #include <cstdint>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "../../include/ftkv.h"
+#include "ftkv_internal.h"
 
 namespace {
 
@@ -28,8 +30,7 @@ constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
 
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-int64_t round256(int64_t x) { return ceil_div(x, 256) * 256; }
+int64_t round256(int64_t x) { return (x + 255) / 256 * 256; }
 
 // Device address of the scratch array for the current device (looked up once per device).
 int scratch_address(void** out) {
@@ -53,31 +54,24 @@ extern "C" int ftkv_decode_attn_noalloc(const ftkv_pool* pool, int32_t num_q_hea
                                         const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
                                         int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
                                         int32_t num_splits, uint16_t* out, void* stream) {
-  if (!pool || pool->num_kv_heads <= 0 || num_q_heads <= 0 || batch < 0 || total_q_rows < 0 || max_seq_len < 0)
-    return FTKV_ERR_INVALID;
-  if (num_splits < 0 || num_splits > FTKV_MAX_SPLITS) return FTKV_ERR_INVALID;
-  if (batch == 0 || total_q_rows == 0) return FTKV_OK;
-  // the split geometry ftkv_decode_attn will use, hence the scratch layout of this call:
-  // [partial accumulators | partial (max, sum) | arrival counters], 256-byte aligned parts
-  const int32_t splits =
-      num_splits ? num_splits : ftkv_decode_auto_splits(batch, pool->num_kv_heads, max_seq_len, max_q_rows);
-  int64_t chunk = ceil_div(max_seq_len > 0 ? max_seq_len : 1, splits);
-  chunk = ceil_div(chunk, 16) * 16;
-  const int64_t eff = max_seq_len > 0 ? ceil_div(max_seq_len, chunk) : 1;
-  const size_t need = ftkv_decode_workspace_bytes(num_q_heads, pool->num_kv_heads, FTKV_HEAD_DIM, batch,
-                                                  total_q_rows, static_cast<int32_t>(eff));
-  if (need == 0) return FTKV_ERR_INVALID;
-  if (need > FTKV_NOALLOC_SCRATCH_BYTES) return FTKV_ERR_WORKSPACE;  // beyond the static maximum
+  // every argument check of ftkv_decode_attn, and its split geometry, before anything is enqueued
+  ftkv::DecodeGeom geom;
+  int st = ftkv::decode_validate(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch,
+                                 total_q_rows, max_q_rows, max_seq_len, sm_scale, num_splits, 0u, nullptr, 0, out,
+                                 false, &geom);
+  if (st != FTKV_OK || geom.empty) return st;
+  if (geom.need > FTKV_NOALLOC_SCRATCH_BYTES) return FTKV_ERR_WORKSPACE;  // beyond the static maximum
   void* scratch = nullptr;
-  int st = scratch_address(&scratch);
-  if (st != FTKV_OK) return st;
-  const int64_t parts = total_q_rows * num_q_heads * eff;
+  if ((st = scratch_address(&scratch)) != FTKV_OK) return st;
+  // scratch layout of this call (that of ftkv_decode_attn's workspace):
+  // [partial accumulators | partial (max, sum) | arrival counters], 256-byte aligned parts
+  const int64_t parts = geom.parts;
   const int64_t ctr_off = round256(parts * FTKV_HEAD_DIM * 4) + round256(parts * 2 * 4);
   const int64_t ctr_bytes = round256((static_cast<int64_t>(batch) * pool->num_kv_heads + 2) * 4);
   if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + ctr_off, 0, static_cast<size_t>(ctr_bytes),
                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FTKV_ERR_CUDA;
   return ftkv_decode_attn(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch,
-                          total_q_rows, max_q_rows, max_seq_len, sm_scale, splits, scratch,
-                          FTKV_NOALLOC_SCRATCH_BYTES, out, stream);
+                          total_q_rows, max_q_rows, max_seq_len, sm_scale, static_cast<int32_t>(geom.splits), 0u,
+                          scratch, FTKV_NOALLOC_SCRATCH_BYTES, out, stream);
 }

@@ -5,7 +5,12 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/ftkv.h"
+
 namespace ftkv {
+
+// Per-device set-up tables of the kernels cover device indices 0 .. kMaxDecodeDevices - 1.
+constexpr int kMaxDecodeDevices = 64;
 
 struct StoreArgs {
   const uint16_t* k;
@@ -54,14 +59,17 @@ struct DecodeArgs {
   int max_q_rows;
   int64_t max_seq_len;       // host bound used for the split geometry
   int num_splits;            // key slices per request
+  int pps;                   // partials per key slice (set by the launcher); partial p of slice s of a
+                             // (row, query head) is at index s * pps + p of num_splits * pps
   int64_t chunk;             // keys per slice (multiple of 16)
   float qk_scale_log2;       // sm_scale * log2(e)
-  float* part_acc;           // [total_q_rows][Hq][num_splits][128]
-  float* part_ml;            // [total_q_rows][Hq][num_splits][2]  (max in log2 units, sum)
+  float* part_acc;           // [total_q_rows][Hq][num_splits * pps][128]
+  float* part_ml;            // [total_q_rows][Hq][num_splits * pps][2]  (max in log2 units, sum)
   int* counters;             // [batch][Hkv] arrival tickets; zero between calls
   uint16_t* out;             // [total_q_rows][Hq][128]
   int* err;
-  int use_tc;                // 1: the tcgen05 kernel (single-row batches only)
+  int early;                 // FTKV_DECODE_STABLE_HISTORY: history loads may start before the preceding grid ends
+  int scan_scales;           // the slot tables may cover most of the pool: bring the scale arrays into L2 whole
   int coop;                  // set by the launcher: cooperative launch, merge after a grid barrier
   int* gbar;                 // [2] grid-barrier arrivals and finished CTAs; zero between calls
   const uint16_t* k_new;     // fused store: [total_q_rows][Hkv][128] K of the new tokens, or null
@@ -131,10 +139,30 @@ cudaError_t launch_store_quant(const StoreArgs& a, cudaStream_t s);
 cudaError_t launch_reconstruct(const ReconstructArgs& a, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* c, int64_t n, int num_sms, cudaStream_t s);
 cudaError_t launch_e4m3_decode(const uint8_t* c, float* x, int64_t n, int num_sms, cudaStream_t s);
+// Decode: single-row batches run the token-major kernel (decode_tok.cu), multi-row batches the kernel with
+// one KV head per CTA (decode.cu).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_tok(const DecodeArgs& a, cudaStream_t s);
 int decode_ctas_per_sm(int max_q_rows);
-cudaError_t launch_prefill_mma(const PrefillArgs& a, cudaStream_t s);
+int decode_tok_heads_per_cta(int num_kv_heads);
+// Partials per key slice: the single-row kernel publishes one per key group of a CTA.
+int decode_parts_per_slice(int max_q_rows, int num_kv_heads);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+
+// Host-side checks and split geometry of a decode call, shared by every decode entry point.  Returns
+// FTKV_OK or the status the entry point reports; nothing is enqueued.  `workspace` is not checked when
+// check_workspace is false (the allocation-free entry point supplies its own).
+struct DecodeGeom {
+  int64_t splits = 0;   // key slices per request
+  int64_t parts = 0;    // partial slots in the workspace (rows x query heads x slices x partials per slice)
+  int64_t chunk = 0;    // keys per slice
+  size_t need = 0;      // workspace bytes
+  bool empty = false;   // nothing to compute (batch or total_q_rows is 0)
+};
+int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
+                    int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
+                    int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
+                    int32_t num_splits, uint32_t flags, const void* workspace, size_t workspace_bytes,
+                    const uint16_t* out, bool check_workspace, DecodeGeom* geom);
 
 }  // namespace ftkv

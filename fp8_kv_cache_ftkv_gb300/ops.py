@@ -130,19 +130,17 @@ class DecodePlan:
 def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,
                 q_row_offsets: torch.Tensor = None, *, max_seq_len: int, max_q_rows: int = 1,
                 sm_scale: float = HEAD_DIM ** -0.5, num_splits: int = 0, plan: DecodePlan = None,
-                out: torch.Tensor = None, impl: str = "mma", k_new: torch.Tensor = None,
-                v_new: torch.Tensor = None, stream=None) -> torch.Tensor:
+                out: torch.Tensor = None, k_new: torch.Tensor = None, v_new: torch.Tensor = None,
+                stable_history: bool = False, stream=None) -> torch.Tensor:
     """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, 128].
-    ``impl``: "mma" (the warp-level kernel, every batch) or "tc" (the tcgen05 kernel, single-row batches).
     ``k_new``/``v_new`` (BF16 [total_q_rows, Hkv, 128], the new tokens' rows, one per query row): quantize them
-    into the pool at their positions' slots first, in the same launch (``ftkv_decode_attn_store``)."""
-    if impl not in ("mma", "tc"):
-        raise ValueError(f"unknown decode impl {impl!r}")
+    into the pool at their positions' slots first, in the same launch (``ftkv_decode_attn_store``).
+    ``stable_history``: pass FTKV_DECODE_STABLE_HISTORY -- the caller guarantees that no work still pending on the
+    stream writes the slot table, the sequence lengths or the history rows, so the kernel may start loading them
+    before the preceding kernel has finished."""
     if (k_new is None) != (v_new is None):
         raise ValueError("k_new and v_new go together")
     if k_new is not None:
-        if impl != "mma":
-            raise ValueError("the fused store runs on the warp-level kernel (impl='mma')")
         _req(k_new, torch.bfloat16, "k_new", 3)
         _req(v_new, torch.bfloat16, "v_new", 3)
     _req(q, torch.bfloat16, "q", 3)
@@ -159,6 +157,7 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
     if out is None:
         out = torch.empty_like(q)
     _req(out, torch.bfloat16, "out", 3)
+    flags = _lib.FTKV_DECODE_STABLE_HISTORY if stable_history else 0
     ps = pool.c_struct()
     if k_new is not None:
         if k_new.shape != (total, pool.num_kv_heads, HEAD_DIM) or v_new.shape != k_new.shape:
@@ -166,14 +165,13 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
         check(_lib.load().ftkv_decode_attn_store(
             ctypes.byref(ps), hq, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(req_to_slot), req_to_slot.shape[1],
             _ptr(seq_lens), _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale),
-            plan.num_splits, _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)),
+            plan.num_splits, flags, _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)),
             "ftkv_decode_attn_store")
         return out
-    name = "ftkv_decode_attn" if impl == "mma" else "ftkv_decode_attn_tc"
-    check(getattr(_lib.load(), name)(
+    check(_lib.load().ftkv_decode_attn(
         ctypes.byref(ps), hq, _ptr(q), _ptr(req_to_slot), req_to_slot.shape[1], _ptr(seq_lens),
-        _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale), plan.num_splits,
-        _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)), name)
+        _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale), plan.num_splits, flags,
+        _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)), "ftkv_decode_attn")
     return out
 
 
@@ -195,10 +193,9 @@ class PrefillPlan:
 
 def prefill_attn(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, ws_k: torch.Tensor = None,
                  ws_v: torch.Tensor = None, *, sm_scale: float = HEAD_DIM ** -0.5, out: torch.Tensor = None,
-                 impl: str = "tc", plan: PrefillPlan = None, stream=None) -> torch.Tensor:
-    """Causal prefill of the chunk over prefix (+) chunk.  ``impl``: "tc" (tcgen05) or "mma" (mma.sync).
-    With ``plan`` (tcgen05 only) the launch is scheduled stream-K over the plan's workspace
-    (``ftkv_prefill_attn_ws``)."""
+                 plan: PrefillPlan = None, stream=None) -> torch.Tensor:
+    """Causal prefill of the chunk over prefix (+) chunk on the tcgen05 kernel.  With ``plan`` the launch is
+    scheduled stream-K over the plan's workspace (``ftkv_prefill_attn_ws``)."""
     _req(q, torch.bfloat16, "q", 3)
     _req(k_chunk, torch.bfloat16, "k_chunk", 3)
     _req(v_chunk, torch.bfloat16, "v_chunk", 3)
@@ -214,13 +211,10 @@ def prefill_attn(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, 
     args = (hq, hkv, HEAD_DIM, _ptr(q), _ptr(k_chunk), _ptr(v_chunk), C, _ptr(ws_k) if P else None,
             _ptr(ws_v) if P else None, P, float(sm_scale))
     if plan is not None:
-        if impl != "tc":
-            raise ValueError("the stream-K plan is for the tcgen05 kernel (impl='tc')")
         check(_lib.load().ftkv_prefill_attn_ws(*args, plan.max_ctas, _ptr(plan.workspace), plan.workspace.numel(),
-                                                _ptr(out), _stream_ptr(stream)), "prefill[tc, stream-K]")
+                                                _ptr(out), _stream_ptr(stream)), "ftkv_prefill_attn_ws")
         return out
-    fn = _lib.load().ftkv_prefill_attn if impl == "tc" else _lib.load().ftkv_prefill_attn_mma
-    check(fn(*args, _ptr(out), _stream_ptr(stream)), f"prefill[{impl}]")
+    check(_lib.load().ftkv_prefill_attn(*args, _ptr(out), _stream_ptr(stream)), "ftkv_prefill_attn")
     return out
 
 

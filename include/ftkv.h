@@ -38,12 +38,25 @@
 extern "C" {
 #endif
 
-#define FTKV_ABI_VERSION 1
+#define FTKV_ABI_VERSION 2
 #define FTKV_HEAD_DIM 128
-/* Split-K cap of the decode kernel ([#897 "Fresh R9700 stage-1 A/B"]: 64 scratch slots / splits). */
-#define FTKV_MAX_SPLITS 64
+/* Split-K cap of decode.  The pages cap their kernel at 64 slices ([#897 "Fresh R9700 stage-1 A/B"]: 64
+ * scratch slots / splits, a limit of that kernel's scratch budget).  Here one slice of a single-row batch
+ * covers every KV head of its keys, so a batch-1 decode needs one slice per SM (152 on a GB300): the cap is
+ * 256. */
+#define FTKV_MAX_SPLITS 256
 /* Largest number of query rows per request in multi-row decode ([#897] opening description, #900). */
 #define FTKV_MAX_Q_ROWS 8
+
+/* Decode flags.
+ * FTKV_DECODE_STABLE_HISTORY: the caller guarantees that no work still pending on `stream` when the call is
+ *   enqueued writes req_to_slot, seq_lens, or the pool rows of the history -- the keys at positions below
+ *   seq_lens[b] - max_q_rows of every request (true between the layers of a decode step: a layer's KV cache
+ *   and the slot table are not written by the work of the layers before it).  The single-row kernel may then
+ *   read them, and start loading history rows, before the preceding kernel in the stream has finished
+ *   (programmatic dependent launch); the query, the new tokens and every output are touched only after it.
+ *   Without the flag every read waits for the preceding kernel.  The results are the same either way. */
+#define FTKV_DECODE_STABLE_HISTORY 0x1u
 
 typedef enum {
   FTKV_OK = 0,
@@ -100,8 +113,11 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
 /* ---------------------------------------------------------------------------------------------
  * Split-K decode attention over the FP8 pool ([#897 "Fresh R9700 stage-1 A/B"]: a stage over slices
  * of the keys followed by a merge; [#897] opening description: BF16 query, D128, GQA 4/8, per-row
- * scales; multi-row decode of up to 8 query rows per request).  One kernel launch: the last slice
- * of each (request, KV head) to finish performs the merge.
+ * scales; multi-row decode of up to 8 query rows per request).  One kernel launch: when the grid fits on
+ * the GPU at once, every slice publishes its partial, the slices meet at a grid barrier and the merge is
+ * spread over the whole grid; otherwise the last slice of each (request, KV head group) to finish merges.
+ * Single-row batches (max_q_rows == 1) run a kernel whose CTAs cover every KV head of their keys (token-
+ * contiguous loads); multi-row batches a kernel with one KV head per CTA.
  *
  *   q              : device BF16 [total_q_rows][num_q_heads][head_dim]
  *   req_to_slot    : device int32 [batch][req_stride]; key j of request b lives in pool row
@@ -116,21 +132,23 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
  *   max_seq_len    : host upper bound on seq_lens (<= req_stride); it fixes the split geometry
  *   sm_scale       : softmax scale (1/sqrt(head_dim) for the standard case)
  *   num_splits     : 0 = automatic (fills the SMs), else 1 .. FTKV_MAX_SPLITS key slices per request
+ *   flags          : 0 or FTKV_DECODE_STABLE_HISTORY (see above); other bits -> FTKV_ERR_INVALID
  *   workspace      : device scratch of at least ftkv_decode_workspace_bytes(...) bytes, 256-byte
  *                    aligned, ZERO-FILLED before its first use (e.g. cudaMemsetAsync).  It holds the
- *                    per-slice partials and one arrival counter per (request, KV head); every call
- *                    leaves the counters at zero again, so the zero fill is needed once.  Calls that
- *                    share a workspace must not overlap on the GPU.
+ *                    per-slice partials, one arrival counter per (request, KV head) and the grid barrier;
+ *                    every call leaves the counters at zero again, so the zero fill is needed once.  Calls
+ *                    that share a workspace must not overlap on the GPU.
  *   out            : device BF16 [total_q_rows][num_q_heads][head_dim]
- * A query row that sees no key gets zeros.
+ * A query row that sees no key gets zeros.  req_to_slot, seq_lens and q_row_offsets must be 4-byte
+ * aligned (FTKV_ERR_ALIGN).
  * --------------------------------------------------------------------------------------------- */
 size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                    int32_t batch, int64_t total_q_rows, int32_t num_splits);
 
 /* Number of key slices the automatic choice uses for this shape (what num_splits = 0 resolves to):
- * with few (request, KV head) groups, as many as fill the GPU in one wave of CTAs; with many, enough for
- * about eight waves (sixteen when max_q_rows > 1), so that long requests are cut into balanced pieces;
- * at least ~128 keys per slice, at most FTKV_MAX_SPLITS. */
+ * with few (request, KV head group) pairs, one CTA per SM; with many, enough for about eight waves
+ * (sixteen when max_q_rows > 1), so that long requests are cut into balanced pieces; at least ~128 keys
+ * per slice, at most FTKV_MAX_SPLITS. */
 int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max_seq_len,
                                 int32_t max_q_rows);
 
@@ -138,19 +156,7 @@ int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t*
                      const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens,
                      const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
                      int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
-                     void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
-
-/* Same operation, arguments, layouts, workspace and errors as ftkv_decode_attn, for single-row
- * batches (max_q_rows must be 1, else FTKV_ERR_UNSUPPORTED), on the tcgen05 kernel: TMA gathers of
- * the K and V code rows, QK on the stored E4M3 codes and PV in FP16 on the tensor cores with TMEM
- * accumulators.  ftkv_decode_attn runs the warp-level mma.sync kernel, measured faster for this
- * HBM-bound step at the 32K batch-1 shape (the tcgen05 kernel's loads are bound by the rate at which
- * one SM's TMA unit issues 4-row gathers); this entry point keeps the tcgen05 kernel available. */
-int ftkv_decode_attn_tc(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
-                        const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens,
-                        const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
-                        int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
-                        void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
+                     uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Quantize-on-write of the new tokens fused into decode: what ftkv_store_quant followed by
@@ -164,24 +170,24 @@ int ftkv_decode_attn_tc(const ftkv_pool* pool, int32_t num_q_heads, const uint16
  *                  ftkv_store_quant does and written to pool row req_to_slot[b * req_stride + that
  *                  position] before any key is read.  A position below 0 is not stored; a slot outside
  *                  the pool is flagged (ftkv_device_errors) and not written.
- * Every other argument, layout, the workspace rules and the errors are those of ftkv_decode_attn
- * (warp-level kernel); k_new or v_new NULL with work to do -> FTKV_ERR_INVALID, misaligned ->
- * FTKV_ERR_ALIGN.
+ * Every other argument, layout, the workspace rules, the flags and the errors are those of
+ * ftkv_decode_attn; k_new or v_new NULL with work to do -> FTKV_ERR_INVALID, misaligned -> FTKV_ERR_ALIGN.
  * --------------------------------------------------------------------------------------------- */
 int ftkv_decode_attn_store(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
                            const uint16_t* k_new, const uint16_t* v_new, const int32_t* req_to_slot,
                            int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets,
                            int32_t batch, int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len,
-                           float sm_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
-                           uint16_t* out, void* stream);
+                           float sm_scale, int32_t num_splits, uint32_t flags, void* workspace,
+                           size_t workspace_bytes, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Decode without any device allocation.  The pages describe no such entry point; it exists for
  * callers that cannot allocate device memory when they need decode attention (a runtime that forbids
  * out-of-band device allocations, a plug-in that only receives buffers from its host, code that must
- * never touch an allocator).  Same arguments and results as ftkv_decode_attn, minus the workspace: the
- * split partials and arrival counters live in a file-scope device array of FTKV_NOALLOC_SCRATCH_BYTES
- * (16 MiB) that every GPU which loads this library keeps until the process exits.
+ * never touch an allocator).  Same arguments and results as ftkv_decode_attn, minus the workspace and the
+ * flags (always 0): the split partials and arrival counters live in a file-scope device array of
+ * FTKV_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads this library keeps until the process exits.
+ *   - Every argument is checked before anything is enqueued; a refused call leaves the array untouched.
  *   - A call whose partials would not fit (roughly total_q_rows * num_q_heads * splits > 30,000 slices)
  *     returns FTKV_ERR_WORKSPACE without launching anything.
  *   - The first call on a device (with that device current) looks up the array's device address; make
@@ -239,12 +245,6 @@ int ftkv_prefill_attn_ws(int32_t num_q_heads, int32_t num_kv_heads, int32_t head
 /* Workspace bytes for ftkv_prefill_attn_ws with up to max_ctas CTAs (<= 0: the current device's SM
  * count); -1 if the device cannot be queried. */
 int64_t ftkv_prefill_workspace_bytes(int32_t max_ctas);
-
-/* Same operation on the legacy warp-level tensor-core path (mma.sync); kept as a comparison point. */
-int ftkv_prefill_attn_mma(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                          const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
-                          int64_t chunk_len, const uint16_t* ws_k, const uint16_t* ws_v,
-                          int64_t prefix_len, float sm_scale, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * E4M3FN codec on the GPU, the same device code the store and attention kernels use.

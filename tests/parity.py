@@ -1,14 +1,24 @@
 """Helpers shared by the GPU parity tests: moving seeded inputs to the device and the tolerance check.
 
-Attention tolerance (BF16 output against the FP64 oracle over the same dequantized values), per
-output vector o = out[row, head, :]:
-    max_d |o - ref| <= 1e-2 * max(1, max_d mag)      ("1e-2 max-abs", in units of the vector's scale)
-where mag = sum_j p_j |v_j| / sum_j p_j is the attention-weighted magnitude of the summed terms (the
-oracle computes it; mag >= |ref|), and over the whole output ||o - ref||_2 <= 1e-2 ||ref||_2.
-A bare absolute 1e-2 cannot hold once |ref| >= ~2: rounding the output to BF16 already costs up to
-2^-9 |ref|, the workloads with x1e3 rows reach |ref| ~ 1e5, and an element that cancels to a small value
-still carries the rounding of its large terms (FP32 logits of size ~1e4, 8-11 bit probabilities) --
-hence the scale of the terms, not of the result.
+Attention tolerance (BF16 output against the FP64 oracle over the same dequantized values).  The
+stated bar is "1e-2 max-abs and 1e-2 relative-L2"; read elementwise with a relative part, every
+parity check asserts
+
+    |o - ref| <= 1e-2 + 1e-2 |ref|        for every output element, and
+    ||o - ref||_2 <= 1e-2 ||ref||_2       over the whole output.
+
+A bare absolute 1e-2 cannot hold once |ref| >= ~5: rounding the output to BF16 alone costs up to
+2^-9 |ref|.  Hence the relative part.
+
+A few named cases hold rows scaled x1e3 (logits near 1e5, terms up to 1e5 that cancel to small
+outputs).  Their elements carry the rounding of terms far larger than the result, so for those cases
+only (``bound="terms"``) the elementwise part is measured against the attention-weighted magnitude of
+the summed terms, mag = sum_j p_j |v_j| / sum_j p_j (computed by the oracle), per output vector:
+
+    max_d |o - ref| <= 1e-2 max(1, max_d mag),
+
+and the relative-L2 part is unchanged.  Every check prints its max-abs error, max-abs / max|ref| and
+relative L2.
 """
 from __future__ import annotations
 
@@ -16,6 +26,7 @@ import numpy as np
 import torch
 
 ATOL = 1e-2
+RTOL = 1e-2
 REL_L2 = 1e-2
 
 
@@ -31,21 +42,31 @@ def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def check_attention(out: torch.Tensor, ref: np.ndarray, what: str = "", mag: np.ndarray = None) -> dict:
-    o = bf16_to_f64(out) if isinstance(out, torch.Tensor) else out
+def check_attention(out, ref: np.ndarray, what: str = "", mag: np.ndarray = None, bound: str = "strict") -> dict:
+    """Assert the attention tolerance.  ``bound="strict"`` (the default, every ordinary case) is the
+    elementwise |o - ref| <= 1e-2 + 1e-2 |ref|; ``bound="terms"`` (named x1e3 cases only, ``mag`` required)
+    scales the absolute part by the magnitude of the summed terms.  Both add relative L2 <= 1e-2."""
+    o = bf16_to_f64(out) if isinstance(out, torch.Tensor) else np.asarray(out, np.float64)
     assert o.shape == ref.shape, (o.shape, ref.shape)
     assert np.isfinite(o).all(), f"{what}: non-finite output"
     err = np.abs(o - ref)
-    m = np.abs(ref) if mag is None else np.maximum(np.abs(ref), mag)
-    scale = np.maximum(1.0, m.max(axis=-1, keepdims=True)) if ref.size else ref
-    bound = ATOL * scale
-    bad = err > bound
+    if bound == "strict":
+        lim = ATOL + RTOL * np.abs(ref)
+    elif bound == "terms":
+        assert mag is not None, "the terms bound needs the oracle's term magnitudes"
+        m = np.maximum(np.abs(ref), mag)
+        lim = ATOL * np.maximum(1.0, m.max(axis=-1, keepdims=True)) if ref.size else ref
+    else:
+        raise ValueError(bound)
+    bad = err > lim
     rel_l2 = float(np.linalg.norm(o - ref) / max(np.linalg.norm(ref), 1e-300))
     stats = {"max_abs": float(err.max()) if err.size else 0.0,
              "max_abs_over_max_ref": float(err.max() / max(np.abs(ref).max(), 1e-300)) if err.size else 0.0,
-             "rel_l2": rel_l2}
-    assert not bad.any(), f"{what}: {int(bad.sum())} elements out of tolerance; worst at " \
-                          f"{np.unravel_index(np.argmax(err - bound), err.shape)} stats={stats}"
+             "rel_l2": rel_l2, "bound": bound}
+    print(f"[parity] {what}: max_abs={stats['max_abs']:.3e} max_abs/max|ref|={stats['max_abs_over_max_ref']:.3e} "
+          f"rel_l2={rel_l2:.3e} bound={bound}")
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements out of tolerance ({bound}); worst at " \
+                          f"{np.unravel_index(np.argmax(err - lim), err.shape)} stats={stats}"
     assert rel_l2 <= REL_L2, f"{what}: relative L2 {rel_l2} > {REL_L2}"
     return stats
 

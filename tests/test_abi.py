@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.ftkv_abi_version() == 1
+    assert lib.ftkv_abi_version() == 2
     for code, name in [(0, "FTKV_OK"), (-1, "FTKV_ERR_INVALID"), (-2, "FTKV_ERR_UNSUPPORTED"), (-3, "FTKV_ERR_ALIGN"),
                        (-4, "FTKV_ERR_WORKSPACE"), (-6, "FTKV_ERR_CUDA"), (-99, "FTKV_ERR_UNKNOWN")]:
         assert _lib.status_str(code) == name
@@ -84,19 +84,22 @@ def test_decode_validation(lib):
     assert ws > 0 and ws % 256 == 0
     assert lib.ftkv_decode_workspace_bytes(32, 4, 64, 1, 1, 8) == 0
     base = dict(q=0x1000, r2s=0x2000, stride=64, lens=0x3000, offs=None, B=1, total=1, mq=1, maxlen=64,
-                sm=0.0884, splits=4, ws=0x100000, wsb=ws, out=0x4000)
+                sm=0.0884, splits=4, flags=0, ws=0x100000, wsb=ws, out=0x4000)
 
     def call(pool=None, hq=32, **kw):
         a = dict(base, **kw)
         return lib.ftkv_decode_attn(P(pool or _pool()), hq, a["q"], a["r2s"], a["stride"], a["lens"], a["offs"],
-                                    a["B"], a["total"], a["mq"], a["maxlen"], a["sm"], a["splits"], a["ws"],
-                                    a["wsb"], a["out"], None)
+                                    a["B"], a["total"], a["mq"], a["maxlen"], a["sm"], a["splits"], a["flags"],
+                                    a["ws"], a["wsb"], a["out"], None)
 
     assert call(hq=24) == _lib.FTKV_ERR_UNSUPPORTED          # group 6
     assert call(hq=30) == _lib.FTKV_ERR_UNSUPPORTED          # not a multiple of Hkv
     assert call(hq=64, pool=_pool(hkv=4)) == _lib.FTKV_ERR_UNSUPPORTED  # group 16
     assert call(mq=9) == _lib.FTKV_ERR_UNSUPPORTED
-    assert call(splits=65) == _lib.FTKV_ERR_INVALID
+    assert call(splits=_lib.FTKV_MAX_SPLITS + 1) == _lib.FTKV_ERR_INVALID
+    assert call(flags=2) == _lib.FTKV_ERR_INVALID             # unknown flag bits
+    assert call(flags=_lib.FTKV_DECODE_STABLE_HISTORY, q=0x1002) == _lib.FTKV_ERR_ALIGN
+    assert call(r2s=0x2002) == _lib.FTKV_ERR_ALIGN             # int32 tables are 4-byte aligned
     assert call(maxlen=65) == _lib.FTKV_ERR_INVALID          # above req_stride
     assert call(total=2) == _lib.FTKV_ERR_INVALID            # no offsets: one row per request
     assert call(q=0x1002) == _lib.FTKV_ERR_ALIGN
@@ -105,21 +108,11 @@ def test_decode_validation(lib):
     assert call(sm=float("nan")) == _lib.FTKV_ERR_INVALID
     assert call(B=0, total=0) == _lib.FTKV_OK                # nothing to do
 
-    def call_tc(**kw):
-        a = dict(base, **kw)
-        return lib.ftkv_decode_attn_tc(P(_pool()), 32, a["q"], a["r2s"], a["stride"], a["lens"], a["offs"], a["B"],
-                                       a["total"], a["mq"], a["maxlen"], a["sm"], a["splits"], a["ws"], a["wsb"],
-                                       a["out"], None)
-
-    assert call_tc(mq=2) == _lib.FTKV_ERR_UNSUPPORTED        # the tcgen05 kernel serves single-row batches
-    assert call_tc(q=0x1002) == _lib.FTKV_ERR_ALIGN
-    assert call_tc(B=0, total=0) == _lib.FTKV_OK
-
     def call_store(kn=0x7000, vn=0x8000, **kw):
         a = dict(base, **kw)
         return lib.ftkv_decode_attn_store(P(_pool()), 32, a["q"], kn, vn, a["r2s"], a["stride"], a["lens"],
                                           a["offs"], a["B"], a["total"], a["mq"], a["maxlen"], a["sm"],
-                                          a["splits"], a["ws"], a["wsb"], a["out"], None)
+                                          a["splits"], a["flags"], a["ws"], a["wsb"], a["out"], None)
 
     assert call_store(kn=None) == _lib.FTKV_ERR_INVALID       # the fused store needs the new rows
     assert call_store(vn=None) == _lib.FTKV_ERR_INVALID
@@ -128,22 +121,39 @@ def test_decode_validation(lib):
     assert call_store(mq=9) == _lib.FTKV_ERR_UNSUPPORTED       # the decode checks still apply
     assert call_store(kn=None, vn=None, B=0, total=0) == _lib.FTKV_OK
 
+    def call_noalloc(**kw):
+        a = dict(base, **kw)
+        return lib.ftkv_decode_attn_noalloc(P(_pool()), 32, a["q"], a["r2s"], a["stride"], a["lens"], a["offs"],
+                                            a["B"], a["total"], a["mq"], a["maxlen"], a["sm"], a["splits"], a["out"],
+                                            None)
+
+    # every decode check runs before the allocation-free entry point touches its scratch array
+    assert call_noalloc(q=0x1002) == _lib.FTKV_ERR_ALIGN
+    assert call_noalloc(out=None) == _lib.FTKV_ERR_INVALID
+    assert call_noalloc(mq=9) == _lib.FTKV_ERR_UNSUPPORTED
+    assert call_noalloc(maxlen=65) == _lib.FTKV_ERR_INVALID
+    assert call_noalloc(B=4096, total=4096, offs=0x5000, mq=1, splits=64) == _lib.FTKV_ERR_WORKSPACE
+    assert call_noalloc(B=0, total=0) == _lib.FTKV_OK
+
 
 def test_decode_auto_splits_host_logic(lib):
-    """The automatic split count (host only; without a GPU the SM count defaults to 152, one CTA each)."""
+    """The automatic split count (host only; without a GPU the SM count defaults to 152).  Single-row CTAs
+    cover 4 KV heads (two CTAs fit per SM); multi-row CTAs one KV head (one CTA per SM)."""
     if torch.cuda.is_available():
         pytest.skip("the expected values assume the 152-SM default")
     f = lib.ftkv_decode_auto_splits
-    assert f(1, 4, 32768, 1) == 38            # few groups: one wave, 152 // 4
+    assert f(1, 4, 32768, 1) == 152           # one group: one CTA per SM
+    assert f(1, 8, 32768, 1) == 76            # 8 KV heads: two groups of 4
     assert f(1, 4, 1000, 1) == 8              # at least ~128 keys per slice
-    assert f(64, 4, 40000, 1) == 5            # many groups: ~8 waves, ceil(8 * 152 / 256)
+    assert f(8, 4, 32768, 1) == 19            # 8 groups: still one wave, 152 // 8
+    assert f(64, 4, 40000, 1) == 38           # many groups: ~8 waves of two CTAs per SM, ceil(8 * 304 / 64)
     assert f(64, 4, 40000, 8) == 10           # multi-row: ~16 waves, ceil(16 * 152 / 256)
-    assert f(1, 1, 10 ** 9, 1) == 64          # capped at FTKV_MAX_SPLITS
+    assert f(1, 1, 10 ** 9, 1) == 152
     assert f(0, 4, 100, 1) == 1
 
 
 def test_prefill_validation(lib):
-    for fn in (lib.ftkv_prefill_attn, lib.ftkv_prefill_attn_mma):
+    for fn in (lib.ftkv_prefill_attn,):
         assert fn(32, 4, 64, 0x1000, 0x2000, 0x3000, 16, 0x4000, 0x5000, 16, 0.08, 0x6000, None) == \
             _lib.FTKV_ERR_UNSUPPORTED
         assert fn(32, 5, 128, 0x1000, 0x2000, 0x3000, 16, 0x4000, 0x5000, 16, 0.08, 0x6000, None) == \

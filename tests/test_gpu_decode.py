@@ -1,10 +1,11 @@
 """GPU parity: split-K FP8 decode attention against the FP64 oracle.
 
-Covers the 512-token single step, ragged key counts (1, 17, 513), split caps 1/8/64 and automatic,
-GQA group sizes 8/4/2/1, multi-row decode (1..8 rows, rows that see no key), the 32,768- and
-40,000-key batch-1 workloads at full size (sampled layers, every output element), and the batched
-64-request multi-row workload at full size.  Single-row cases run on both kernels: "mma" (the warp-level
-kernel behind ftkv_decode_attn) and "tc" (the tcgen05 kernel behind ftkv_decode_attn_tc).
+Covers the 512-token single step, ragged key counts (1, 17, 513, 4099), split counts 1/8/64/152/256 and
+automatic, GQA group sizes 8/4/2/1 and 8 KV heads, multi-row decode (1..8 rows, rows that see no key), the
+32,768- and 40,000-key batch-1 workloads at full size (sampled layers, every output element), the batched
+64-request multi-row workload at full size, and chains of decode launches in one stream with and without
+FTKV_DECODE_STABLE_HISTORY (history loads issued before the preceding kernel has finished).  Single-row
+cases run with the flag off and on ("stable").
 """
 import numpy as np
 import pytest
@@ -15,7 +16,7 @@ from fp8_kv_cache_ftkv_gb300 import inputs, ops
 from parity import bits_to_cuda_bf16, check_attention
 
 pytestmark = pytest.mark.gpu
-IMPLS = ["mma", "tc"]
+STABLE = [False, True]
 
 
 def _setup(wl: inputs.DecodeWorkload, layer: int = 0):
@@ -32,11 +33,11 @@ def _setup(wl: inputs.DecodeWorkload, layer: int = 0):
     return gp, op, L, dev
 
 
-def _run(wl, gp, dev, num_splits=0, max_q_rows=None, impl="mma"):
+def _run(wl, gp, dev, num_splits=0, max_q_rows=None, stable=False):
     R = np.diff(wl.q_row_offsets)
     mq = int(max(R.max(), 1)) if max_q_rows is None else max_q_rows
     return ops.decode_attn(gp, dev["q"], dev["r2s"], dev["lens"], dev["offs"], max_seq_len=int(wl.req_to_slot.shape[1]),
-                           max_q_rows=mq, sm_scale=wl.sm_scale, num_splits=num_splits, impl=impl)
+                           max_q_rows=mq, sm_scale=wl.sm_scale, num_splits=num_splits, stable_history=stable)
 
 
 def _ref(wl, op, L):
@@ -48,45 +49,47 @@ def _check(out, refs, what):
     return check_attention(out, refs[0], what, refs[1])
 
 
-@pytest.mark.parametrize("impl", IMPLS)
-def test_decode_small_step(impl):
+@pytest.mark.parametrize("stable", STABLE)
+def test_decode_small_step(stable):
     wl = inputs.decode_small()
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev, impl=impl)
+    out = _run(wl, gp, dev, stable=stable)
     stats = _check(out, _ref(wl, op, L), "decode_small")
     assert stats["max_abs"] < 0.05
     assert ops.device_errors() == 0
 
 
-@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("stable", STABLE)
 @pytest.mark.parametrize("n", [1, 17, 513, 4099])
-@pytest.mark.parametrize("splits", [0, 1, 8, 64])
-def test_decode_ragged_lengths_and_split_caps(n, splits, impl):
+@pytest.mark.parametrize("splits", [0, 1, 8, 64, 152, 256])
+def test_decode_ragged_lengths_and_split_caps(n, splits, stable):
     wl = inputs.decode_custom([n], [1], max(2 * n, 64), seed=n)
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev, num_splits=splits, impl=impl)
-    _check(out, _ref(wl, op, L), f"n={n} splits={splits} impl={impl}")
+    out = _run(wl, gp, dev, num_splits=splits, stable=stable)
+    _check(out, _ref(wl, op, L), f"n={n} splits={splits} stable={stable}")
 
 
-@pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("n,splits", [(9000, 1), (20000, 3), (131, 1), (131, 2)])
-def test_decode_long_slices_cross_slot_windows(n, splits, impl):
-    """Slices of thousands of keys (several 2,048-slot windows of the tcgen05 kernel's producer; several
-    4,096-slot windows of the warp-level kernel), a slice whose last 128-key tile holds 3 keys, and
-    slices shorter than one tile."""
+@pytest.mark.parametrize("stable", STABLE)
+@pytest.mark.parametrize("n,splits", [(9000, 1), (20000, 3), (2049, 2), (131, 1), (131, 2)])
+def test_decode_long_slices_cross_slot_windows(n, splits, stable):
+    """Slices of thousands of keys (several 1,024-slot windows of the single-row kernel, several 4,096-slot
+    windows of the multi-row kernel), a slice ending one key past a window, and slices shorter than one
+    16-key block per key group."""
     wl = inputs.decode_custom([n], [1], n + 7, seed=n + splits)
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev, num_splits=splits, impl=impl)
+    out = _run(wl, gp, dev, num_splits=splits, stable=stable)
     _check(out, _ref(wl, op, L), f"n={n} splits={splits}")
     assert ops.device_errors() == 0
 
 
-@pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("Hq,Hkv", [(32, 4), (16, 4), (8, 4), (4, 4), (64, 8)])
-def test_decode_gqa_groups(Hq, Hkv, impl):
+@pytest.mark.parametrize("stable", STABLE)
+@pytest.mark.parametrize("Hq,Hkv", [(32, 4), (16, 4), (8, 4), (4, 4), (64, 8), (16, 2), (8, 1), (12, 6)])
+def test_decode_gqa_groups(Hq, Hkv, stable):
+    """GQA groups 8/4/2/1 with 4 KV heads per CTA, 8 KV heads (two CTAs per key slice), and 2, 1 and 6 KV heads
+    (CTAs of 2 or 1 heads)."""
     wl = inputs.decode_custom([300, 1000], [1, 1], 4000, seed=Hq, Hq=Hq, Hkv=Hkv)
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev, impl=impl)
+    out = _run(wl, gp, dev, stable=stable)
     _check(out, _ref(wl, op, L), f"Hq={Hq} Hkv={Hkv}")
 
 
@@ -110,23 +113,23 @@ def test_decode_rows_that_see_no_key_are_zero():
     assert (out[:3].float() == 0).all()
 
 
-@pytest.mark.parametrize("impl", IMPLS)
-def test_decode_zero_length_request_and_single_row_path_with_offsets(impl):
+@pytest.mark.parametrize("stable", STABLE)
+def test_decode_zero_length_request_and_single_row_path_with_offsets(stable):
     wl = inputs.decode_custom([0, 33, 1], [1, 1, 1], 64, seed=4)
     gp, op, L, dev = _setup(wl)
-    out = _run(wl, gp, dev, impl=impl)
+    out = _run(wl, gp, dev, stable=stable)
     _check(out, _ref(wl, op, L), "zero-length request")
     assert (out[0].float() == 0).all()
 
 
-@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("stable", STABLE)
 @pytest.mark.parametrize("n,R", [(32768, 33059), (40000, 40290)])
-def test_decode_long_context_full_size(n, R, impl):
+def test_decode_long_context_full_size(n, R, stable):
     wl = inputs.decode_long(n, R, layers=48)
     for layer in (0, 47):
         gp, op, L, dev = _setup(wl, layer)
-        out = _run(wl, gp, dev, impl=impl)
-        stats = _check(out, _ref(wl, op, L), f"n={n} layer={layer} impl={impl}")
+        out = _run(wl, gp, dev, stable=stable)
+        stats = _check(out, _ref(wl, op, L), f"n={n} layer={layer} stable={stable}")
         assert stats["rel_l2"] < 2e-3
     assert ops.device_errors() == 0
 
@@ -145,23 +148,26 @@ def test_decode_batched_multirow_full_size():
     assert ops.device_errors() == 0
 
 
-@pytest.mark.parametrize("impl", IMPLS)
-def test_decode_bad_slot_and_seq_len_are_flagged_not_faulted(impl):
+@pytest.mark.parametrize("max_q_rows", [1, 2])
+@pytest.mark.parametrize("stable", STABLE)
+def test_decode_bad_slot_and_seq_len_are_flagged_not_faulted(stable, max_q_rows):
     wl = inputs.decode_custom([50], [1], 128, seed=5)
     gp, op, L, dev = _setup(wl)
     bad = dev["r2s"].clone()
     bad[0, 3] = 10 ** 6
     bad[0, 4] = -7
-    ops.decode_attn(gp, dev["q"], bad, dev["lens"], dev["offs"], max_seq_len=50, max_q_rows=1, impl=impl)
+    ops.decode_attn(gp, dev["q"], bad, dev["lens"], dev["offs"], max_seq_len=50, max_q_rows=max_q_rows,
+                    stable_history=stable)
     assert ops.device_errors() & 0x1
     lens = torch.tensor([60], dtype=torch.int32, device="cuda")
-    ops.decode_attn(gp, dev["q"], dev["r2s"], lens, dev["offs"], max_seq_len=50, max_q_rows=1, impl=impl)
+    ops.decode_attn(gp, dev["q"], dev["r2s"], lens, dev["offs"], max_seq_len=50, max_q_rows=max_q_rows,
+                    stable_history=stable)
     assert ops.device_errors() & 0x2
     assert ops.device_errors() == 0
 
 
-@pytest.mark.parametrize("max_q_rows,impl", [(1, "mma"), (1, "tc"), (2, "mma")])
-def test_decode_dominant_key_with_small_v_scale(max_q_rows, impl):
+@pytest.mark.parametrize("max_q_rows,stable", [(1, False), (1, True), (2, False)])
+def test_decode_dominant_key_with_small_v_scale(max_q_rows, stable):
     """A key holding almost all the probability has a V scale 1e6 x smaller than a key with tiny
     probability; both terms matter (ratio ~0.1) and the dominant one must keep full precision."""
     rng = np.random.default_rng(31)
@@ -184,15 +190,15 @@ def test_decode_dominant_key_with_small_v_scale(max_q_rows, impl):
     lens = np.array([n], np.int32)
     out = ops.decode_attn(gp, bits_to_cuda_bf16(qb), torch.from_numpy(slots[None]).cuda(),
                           torch.from_numpy(lens).cuda(), torch.from_numpy(offs).cuda(), max_seq_len=n,
-                          max_q_rows=max_q_rows, impl=impl)
+                          max_q_rows=max_q_rows, stable_history=stable)
     args = (op, qb, slots[None], lens, offs, inputs.SM_SCALE, 32)
     ref, mag = oracle.decode_attn(*args), oracle.decode_attn(*args, abs_v=True)
     stats = check_attention(out, ref, "dominant small-scale key", mag)
     assert stats["rel_l2"] < 2e-3
 
 
-@pytest.mark.parametrize("impl", IMPLS)
-def test_decode_one_hot_attention_with_huge_logits(impl):
+@pytest.mark.parametrize("stable", STABLE)
+def test_decode_one_hot_attention_with_huge_logits(stable):
     """Logits near 1e5 (a x1e3 key aligned with the query) make the attention one-hot: the output must
     be that key's dequantized value to BF16 rounding, which fails if the V scale is applied through an
     addition to the logit (its log would be rounded to the ulp of the logit)."""
@@ -211,7 +217,7 @@ def test_decode_one_hot_attention_with_huge_logits(impl):
     lens, offs = np.array([n], np.int32), np.array([0, 1], np.int32)
     out = ops.decode_attn(gp, bits_to_cuda_bf16(qb), torch.from_numpy(slots[None]).cuda(),
                           torch.from_numpy(lens).cuda(), torch.from_numpy(offs).cuda(), max_seq_len=n,
-                          impl=impl)
+                          stable_history=stable)
     args = (op, qb, slots[None], lens, offs, inputs.SM_SCALE, 32)
     ref, mag = oracle.decode_attn(*args), oracle.decode_attn(*args, abs_v=True)
     vhat = oracle.e4m3_decode(op.v_codes[slots[11]]) * op.v_scales[slots[11]][:, None]
@@ -247,11 +253,12 @@ def _new_tokens(wl, L):
     return k_new, v_new, new
 
 
+@pytest.mark.parametrize("stable", STABLE)
 @pytest.mark.parametrize("lens,rows,splits", [
-    ([512], [1], 0), ([33], [1], 1), ([4099], [1], 8), ([9000], [1], 1), ([1], [1], 0),
+    ([512], [1], 0), ([33], [1], 1), ([4099], [1], 8), ([9000], [1], 1), ([1], [1], 0), ([32768], [1], 0),
     ([200, 297, 394], [3, 1, 8], 0), ([200, 297, 394], [3, 1, 8], 5), ([2, 40], [5, 3], 0), ([0, 33, 1], [1, 1, 1], 0),
 ])
-def test_decode_fused_store_equals_store_then_decode(lens, rows, splits):
+def test_decode_fused_store_equals_store_then_decode(lens, rows, splits, stable):
     """The new tokens' rows land in the pool bit-exactly as the store kernel writes them (oracle store),
     and the attention over them matches the oracle; new tokens split across slices and windows, rows
     past the start of the sequence, and an empty request included."""
@@ -272,13 +279,13 @@ def test_decode_fused_store_equals_store_then_decode(lens, rows, splits):
                           torch.from_numpy(wl.seq_lens).cuda(), torch.from_numpy(wl.q_row_offsets).cuda(),
                           max_seq_len=int(wl.req_to_slot.shape[1]), max_q_rows=int(max(R.max(), 1)),
                           sm_scale=wl.sm_scale, num_splits=splits, k_new=bits_to_cuda_bf16(k_new),
-                          v_new=bits_to_cuda_bf16(v_new))
+                          v_new=bits_to_cuda_bf16(v_new), stable_history=stable)
     s = L.slots
     assert np.array_equal(gp.k_codes.cpu().numpy()[s], op.k_codes[s])
     assert np.array_equal(gp.v_codes.cpu().numpy()[s], op.v_codes[s])
     assert np.array_equal(gp.k_scales.cpu().numpy()[s].view(np.uint32), op.k_scales[s].view(np.uint32))
     assert np.array_equal(gp.v_scales.cpu().numpy()[s].view(np.uint32), op.v_scales[s].view(np.uint32))
-    _check(out, _ref(wl, op, L), f"fused lens={lens} rows={rows} splits={splits}")
+    _check(out, _ref(wl, op, L), f"fused lens={lens} rows={rows} splits={splits} stable={stable}")
     assert ops.device_errors() == 0
 
 
@@ -320,4 +327,85 @@ def test_decode_shared_merge_state_resets_between_calls(lens, rows):
             first = out.clone()
         else:
             assert torch.equal(out, first)
+    assert ops.device_errors() == 0
+
+
+# ---- chains of launches in one stream: history loads before the preceding kernel ends ----
+
+def _chain_layers(n, R, layers, seed):
+    """`layers` pools of one request with n keys; the last key of each is the new token (stored by the decode)."""
+    wl = inputs.decode_custom([n], [1], R, seed=seed)
+    wl.layers = layers
+    out = []
+    for l in range(layers):
+        L = wl.layer(l)
+        gp = ops.KVPool.empty(R, wl.Hkv)
+        ops.store_quant(gp, bits_to_cuda_bf16(L.k[:n - 1]), bits_to_cuda_bf16(L.v[:n - 1]),
+                        torch.from_numpy(L.slots[:n - 1]).cuda())
+        op = oracle.Pool(R, wl.Hkv, 128)
+        oracle.store_quant(op, L.k, L.v, L.slots)
+        out.append((L, gp, op))
+    return wl, out
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_decode_stable_history_chain_of_layers(graph):
+    """A decode step of 12 layers as back-to-back fused store + decode launches with FTKV_DECODE_STABLE_HISTORY
+    (eager, and as one CUDA graph replayed twice): every layer's new token lands bit-exact and every output
+    matches the oracle."""
+    n, R, layers = 6000, 6100, 12
+    wl, ls = _chain_layers(n, R, layers, seed=77)
+    r2s = torch.from_numpy(wl.req_to_slot).cuda()
+    lens = torch.from_numpy(wl.seq_lens).cuda()
+    plan = ops.DecodePlan(wl.Hq, wl.Hkv, 1, 1, 1, n, 0, "cuda")
+    q = [bits_to_cuda_bf16(L.q) for L, _, _ in ls]
+    kn = [bits_to_cuda_bf16(L.k[n - 1:n]) for L, _, _ in ls]
+    vn = [bits_to_cuda_bf16(L.v[n - 1:n]) for L, _, _ in ls]
+    outs = [torch.empty_like(x) for x in q]
+    stream = torch.cuda.Stream()
+
+    def step():
+        for l, (L, gp, op) in enumerate(ls):
+            ops.decode_attn(gp, q[l], r2s, lens, None, max_seq_len=n, plan=plan, out=outs[l], k_new=kn[l],
+                            v_new=vn[l], stable_history=True, stream=stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        step()
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            for o in outs:
+                o.zero_()
+            g.replay()
+            g.replay()
+    torch.cuda.synchronize()
+    s = ls[0][0].slots
+    for l, (L, gp, op) in enumerate(ls):
+        assert np.array_equal(gp.k_codes.cpu().numpy()[s], op.k_codes[s]), l
+        assert np.array_equal(gp.v_scales.cpu().numpy()[s].view(np.uint32), op.v_scales[s].view(np.uint32)), l
+        _check(outs[l], _ref(wl, op, L), f"chain layer {l} graph={graph}")
+    assert ops.device_errors() == 0
+
+
+@pytest.mark.parametrize("stable", STABLE)
+def test_decode_after_store_kernel_on_the_same_pool(stable):
+    """ftkv_store_quant writes the new token's rows, then ftkv_decode_attn reads the same pool, back to back in
+    one stream: the decode must see the stored rows.  The new token is not history, so this order is allowed
+    with FTKV_DECODE_STABLE_HISTORY as well (its block is loaded only after the store kernel has finished)."""
+    n, R = 4000, 4100
+    wl, ls = _chain_layers(n, R, 3, seed=78)
+    r2s = torch.from_numpy(wl.req_to_slot).cuda()
+    lens = torch.from_numpy(wl.seq_lens).cuda()
+    new_slot = torch.from_numpy(wl.req_to_slot[0, n - 1:n].copy()).cuda()
+    plan = ops.DecodePlan(wl.Hq, wl.Hkv, 1, 1, 1, n, 0, "cuda")
+    outs = []
+    for L, gp, op in ls:
+        ops.store_quant(gp, bits_to_cuda_bf16(L.k[n - 1:n]), bits_to_cuda_bf16(L.v[n - 1:n]), new_slot)
+        outs.append(ops.decode_attn(gp, bits_to_cuda_bf16(L.q), r2s, lens, None, max_seq_len=n, plan=plan,
+                                    stable_history=stable))
+    torch.cuda.synchronize()
+    for l, (L, gp, op) in enumerate(ls):
+        _check(outs[l], _ref(wl, op, L), f"store then decode layer {l} stable={stable}")
     assert ops.device_errors() == 0

@@ -3,7 +3,18 @@
 The chunked workload runs exactly as the benchmark does (8,192 historical rows, 8,192 new tokens in
 4 chunks of 2,048: reconstruct -> prefill -> quantize-on-write of the chunk) on both sides; every 16th
 query row of each chunk is compared (all heads, all d).  Small cases cover an empty prefix, ragged
-chunk and prefix lengths and GQA group sizes, for both tensor-core paths.
+chunk and prefix lengths and GQA group sizes, one CTA per work item ("tc") and stream-K ("tc_sk").
+
+Tolerance.  Prefill is BF16 attention over the BF16 workspace (FreeToken PR #853, "What changes": the
+historical rows are rebuilt into BF16 for the existing BF16 attention): the probabilities P enter the
+tensor-core PV product as BF16 (8 significant bits; A and B of one kind::f16 MMA share one type, and V is
+BF16).  Each term p_j v_j then carries a relative error up to 2^-9, so an output element that is small
+next to the terms it sums is off by ~2^-9 of those terms, not of itself: measured max-abs 0.06-0.19 for
+|ref| up to ~80 (max-abs / max|ref| 2e-3 - 5e-3), relative L2 1.1e-3 - 1.8e-3, and the elementwise
+|o - ref| <= 1e-2 + 1e-2 |ref| fails for a handful of elements per case.  These checks therefore use the
+"terms" bound of parity.py (absolute part scaled by the attention-weighted term magnitude, per output
+vector) plus relative L2 <= 1e-2.  Decode uses FP32 probabilities into its FP16 PV product and meets the
+elementwise bound.
 """
 import numpy as np
 import pytest
@@ -15,7 +26,8 @@ from parity import bits_to_cuda_bf16, check_attention
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["mma", "tc", "tc_sk"]
+IMPLS = ["tc", "tc_sk"]
+BOUND = "terms"  # see the module docstring
 _PLANS = {}
 
 
@@ -27,8 +39,8 @@ def _prefill(impl, q, kc, vc, wk, wv, ctas=5):
     if impl == "tc_sk":
         if ctas not in _PLANS:
             _PLANS[ctas] = ops.PrefillPlan(ctas)
-        return ops.prefill_attn(q, kc, vc, wk, wv, impl="tc", plan=_PLANS[ctas])
-    return ops.prefill_attn(q, kc, vc, wk, wv, impl=impl)
+        return ops.prefill_attn(q, kc, vc, wk, wv, plan=_PLANS[ctas])
+    return ops.prefill_attn(q, kc, vc, wk, wv)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -42,7 +54,7 @@ def test_prefill_small(impl, P, C):
     mag = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE, abs_v=True)
     out = _prefill(impl, bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
                    bits_to_cuda_bf16(wk) if P else None, bits_to_cuda_bf16(wv) if P else None)
-    check_attention(out, ref, f"{impl} P={P} C={C}", mag)
+    check_attention(out, ref, f"{impl} P={P} C={C}", mag, bound=BOUND)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -57,7 +69,7 @@ def test_prefill_gqa(impl, Hq, Hkv):
     mag = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE, abs_v=True)
     out = _prefill(impl, bits_to_cuda_bf16(q), bits_to_cuda_bf16(kc), bits_to_cuda_bf16(vc),
                    bits_to_cuda_bf16(wk), bits_to_cuda_bf16(wv))
-    check_attention(out, ref, f"{impl} Hq={Hq} Hkv={Hkv}", mag)
+    check_attention(out, ref, f"{impl} Hq={Hq} Hkv={Hkv}", mag, bound=BOUND)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -85,7 +97,7 @@ def test_chunked_prefill_full_workload(impl):
         ref = oracle.prefill_attn(wl.q[c0:c1], wl.k[c0:c1], wl.v[c0:c1], owk, owv, wl.sm_scale, rows)
         mag = oracle.prefill_attn(wl.q[c0:c1], wl.k[c0:c1], wl.v[c0:c1], owk, owv, wl.sm_scale, rows, abs_v=True)
         oracle.store_quant(op, wl.k[c0:c1], wl.v[c0:c1], slots_all[P:P + c1 - c0])
-        check_attention(out[torch.from_numpy(rows).cuda()], ref, f"{impl} chunk {c}", mag)
+        check_attention(out[torch.from_numpy(rows).cuda()], ref, f"{impl} chunk {c}", mag, bound=BOUND)
     assert ops.device_errors() == 0
 
 
@@ -103,10 +115,10 @@ def test_prefill_stream_k_cuts(ctas):
     mag = oracle.prefill_attn(q, kc, vc, wk, wv, inputs.SM_SCALE, abs_v=True)
     args = [bits_to_cuda_bf16(x) for x in (q, kc, vc, wk, wv)]
     plan = ops.PrefillPlan(ctas)
-    out1 = ops.prefill_attn(*args, impl="tc", plan=plan)
-    out2 = ops.prefill_attn(*args, impl="tc", plan=plan)
-    whole = ops.prefill_attn(*args, impl="tc")
-    check_attention(out1, ref, f"stream-K ctas={ctas}", mag)
+    out1 = ops.prefill_attn(*args, plan=plan)
+    out2 = ops.prefill_attn(*args, plan=plan)
+    whole = ops.prefill_attn(*args)
+    check_attention(out1, ref, f"stream-K ctas={ctas}", mag, bound=BOUND)
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
     tickets = ((ctas + 1) * 16 + 255) // 256 * 256
     assert torch.count_nonzero(plan.workspace[:tickets]).item() == 0  # every ticket back at zero

@@ -28,7 +28,7 @@ def _rank_body(rank: int, world: int, port: int, result_dir: str):
                       LOCAL_RANK=str(rank))
     sys.path.insert(0, ROOT)
     import bench
-    w, r, local = bench.dist_setup(None)
+    w, r, local = bench.dist_setup()
     dist.init_process_group("gloo", rank=r, world_size=w)
     try:
         bench.barrier(w)
@@ -54,7 +54,7 @@ def test_reference_arm_under_torchrun_two_ranks():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
            "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1", "--context", "512",
-           "--pool-rows", "1024", "--layers", "1", "--cpu-sample-layers", "1"]
+           "--pool-rows", "1024", "--layers", "1"]
     p = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert p.returncode == 0, p.stderr[-2000:]
     lines = [l for l in p.stdout.splitlines() if l.startswith("{")]

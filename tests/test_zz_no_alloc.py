@@ -4,8 +4,9 @@ Callers that cannot allocate device memory -- a runtime that forbids out-of-band
 plug-in that only receives buffers from its host -- use ftkv_decode_attn_noalloc, whose split partials
 and counters live in a static device array inside the library.  Through the C ABI (ctypes, no torch
 wrapper), two calls in a row with different shapes (so the second meets the first one's leftovers in
-the shared array), then the first shape again, must match the regular ftkv_decode_attn within the
-attention tolerance used by the other tests; a call too large for the array must be refused.
+the shared array), then the first shape again, must match the regular ftkv_decode_attn and the FP64
+oracle within the attention tolerance used by the other tests; a call too large for the array, or with a
+bad argument, must be refused without touching the array.
 This file is collected last and needs nothing from the other tests.
 """
 import ctypes
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from fp8_kv_cache_ftkv_gb300 import _lib, inputs, ops
 from parity import bits_to_cuda_bf16, check_attention
 
@@ -56,7 +58,12 @@ def test_noalloc_decode_matches_regular_entry_point():
         pool, dev = _setup(wl)
         got = _noalloc(wl, pool, dev, mq)
         ref = _regular(wl, pool, dev, mq)
-        check_attention(got, ref.float().cpu().numpy().astype(np.float64), f"noalloc {wl.name}")
+        check_attention(got, ref.float().cpu().numpy().astype(np.float64), f"noalloc vs ftkv_decode_attn {wl.name}")
+        L = wl.layer(0)
+        op = oracle.Pool(wl.num_rows, wl.Hkv, 128)
+        oracle.store_quant(op, L.k, L.v, L.slots)
+        exact = oracle.decode_attn(op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets, wl.sm_scale, wl.Hq)
+        check_attention(got, exact, f"noalloc vs oracle {wl.name}")
     assert ops.device_errors() == 0
 
 
@@ -71,3 +78,14 @@ def test_noalloc_refuses_requests_beyond_its_scratch():
                                       p(dev["lens"]), None, big_rows, big_rows, 1, 512, wl.sm_scale, 64,
                                       p(dev["q"]), None)
     assert st == _lib.FTKV_ERR_WORKSPACE
+    # a refused call enqueues nothing: a bad argument after a good call leaves the good call's output intact
+    good = _noalloc(wl, pool, dev, 1)
+    bad_out = torch.full_like(dev["q"], 7.0)
+    st = lib.ftkv_decode_attn_noalloc(ctypes.byref(ps), 32, ctypes.c_void_p(dev["q"].data_ptr() + 2), p(dev["r2s"]),
+                                      wl.req_to_slot.shape[1], p(dev["lens"]), None, 1, 1, 1, 512, wl.sm_scale, 0,
+                                      p(bad_out), None)
+    assert st == _lib.FTKV_ERR_ALIGN
+    torch.cuda.synchronize()
+    assert (bad_out.float() == 7.0).all()
+    again = _noalloc(wl, pool, dev, 1)
+    assert torch.equal(good, again)
