@@ -66,8 +66,10 @@ def _load():
         lib.ftkv_oracle_reconstruct.argtypes = [P, P, P, P, i64, i32, i32, P, i64, P, P]
         lib.ftkv_oracle_reconstruct.restype = i32
         lib.ftkv_oracle_decode_attn.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, i64, P, P, i32,
-                                                f64, i32, P]
+                                                f64, i64, i32, P]
         lib.ftkv_oracle_decode_attn.restype = i32
+        lib.ftkv_oracle_decode_attn_bf16.argtypes = [P, P, i64, i32, i32, i32, P, P, i64, P, P, i32, f64, i64, i32, P]
+        lib.ftkv_oracle_decode_attn_bf16.restype = i32
         lib.ftkv_oracle_prefill_attn.argtypes = [i32, i32, i32, P, P, P, i64, P, P, i64, f64, P, i64, i32, P]
         lib.ftkv_oracle_prefill_attn.restype = i32
         lib.ftkv_oracle_pool_bytes.argtypes = [i64, i64, i64, i64, P, P, P]
@@ -159,11 +161,7 @@ def reconstruct(pool: Pool, slots):
     return ws_k, ws_v
 
 
-def decode_attn(pool: Pool, q_bits, req_to_slot, seq_lens, q_row_offsets, sm_scale: float,
-                num_q_heads: int, abs_v: bool = False) -> np.ndarray:
-    """FP64 decode attention over the FP8 pool; returns float64 [total_rows, Hq, D].
-
-    ``abs_v=True`` returns sum_j p_j |v_j| / sum_j p_j instead (a test helper that sizes rounding bounds)."""
+def _decode_args(q_bits, req_to_slot, seq_lens, q_row_offsets, num_q_heads, D):
     q = _c(q_bits, np.uint16)
     r2s = _c(req_to_slot, np.int32)
     if r2s.ndim == 1:
@@ -172,12 +170,36 @@ def decode_attn(pool: Pool, q_bits, req_to_slot, seq_lens, q_row_offsets, sm_sca
     qo = _c(q_row_offsets, np.int32)
     B = sl.shape[0]
     total = int(qo[B])
-    assert q.shape == (total, num_q_heads, pool.D)
-    out = np.empty((total, num_q_heads, pool.D), np.float64)
+    assert q.shape == (total, num_q_heads, D)
+    return q, r2s, sl, qo, B, np.empty((total, num_q_heads, D), np.float64)
+
+
+def decode_attn(pool: Pool, q_bits, req_to_slot, seq_lens, q_row_offsets, sm_scale: float,
+                num_q_heads: int, abs_v: bool = False, window: int = 0) -> np.ndarray:
+    """FP64 decode attention over the FP8 pool; returns float64 [total_rows, Hq, D].
+
+    ``window`` > 0: sliding window of the last ``window`` visible keys.  ``abs_v=True`` returns
+    sum_j p_j |v_j| / sum_j p_j instead (a test helper that sizes rounding bounds)."""
+    q, r2s, sl, qo, B, out = _decode_args(q_bits, req_to_slot, seq_lens, q_row_offsets, num_q_heads, pool.D)
     rc = _load().ftkv_oracle_decode_attn(_ptr(pool.k_codes), _ptr(pool.v_codes), _ptr(pool.k_scales),
                                          _ptr(pool.v_scales), pool.num_rows, num_q_heads, pool.Hkv,
                                          pool.D, _ptr(q), _ptr(r2s), r2s.shape[1], _ptr(sl), _ptr(qo), B,
-                                         float(sm_scale), int(abs_v), _ptr(out))
+                                         float(sm_scale), int(window), int(abs_v), _ptr(out))
+    if rc != 0:
+        raise ValueError("invalid decode arguments")
+    return out
+
+
+def decode_attn_bf16(k_bits, v_bits, q_bits, req_to_slot, seq_lens, q_row_offsets, sm_scale: float,
+                     num_q_heads: int, abs_v: bool = False, window: int = 0) -> np.ndarray:
+    """FP64 decode attention over a BF16 pool (k, v: BF16 bit patterns [rows, Hkv, D])."""
+    k = _c(k_bits, np.uint16)
+    v = _c(v_bits, np.uint16)
+    assert k.shape == v.shape and k.ndim == 3
+    q, r2s, sl, qo, B, out = _decode_args(q_bits, req_to_slot, seq_lens, q_row_offsets, num_q_heads, k.shape[2])
+    rc = _load().ftkv_oracle_decode_attn_bf16(_ptr(k), _ptr(v), k.shape[0], num_q_heads, k.shape[1], k.shape[2],
+                                              _ptr(q), _ptr(r2s), r2s.shape[1], _ptr(sl), _ptr(qo), B,
+                                              float(sm_scale), int(window), int(abs_v), _ptr(out))
     if rc != 0:
         raise ValueError("invalid decode arguments")
     return out

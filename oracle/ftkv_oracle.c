@@ -207,41 +207,52 @@ int ftkv_oracle_reconstruct(const uint8_t* k_codes, const uint8_t* v_codes, cons
 /* Attention (FP64)                                                                            */
 /* ------------------------------------------------------------------------------------------ */
 
-/* ---- decode over the FP8 pool ---- */
+/* ---- decode over the FP8 pool, or over a BF16 pool ---- */
 typedef struct {
-  const uint8_t* codes;
+  const uint8_t* codes;    /* FP8 pool: E4M3 codes [rows][Hkv][D] and FP32 scales [rows][Hkv] */
   const float* scales;
-  const int32_t* slot_of; /* logical key j -> pool row */
+  const uint16_t* bf16;    /* BF16 pool: values [rows][Hkv][D] (codes == NULL) */
+  const int32_t* slot_of;  /* logical key j -> pool row */
   int Hkv, D, h;
 } pool_ctx;
 
-/* Dequantized row j of one KV head: decode(code) * scale, exact in double. */
+/* Row j of one KV head as doubles: decode(code) * scale for the FP8 pool (exact in double), the BF16 value
+ * itself for the BF16 pool (exact). */
 static void pool_row(const pool_ctx* c, int64_t j, double* out) {
   int64_t row = c->slot_of[j];
-  const uint8_t* code = c->codes + (row * c->Hkv + c->h) * c->D;
-  double s = (double)c->scales[row * c->Hkv + c->h];
-  for (int d = 0; d < c->D; d++) out[d] = g_dec[code[d]] * s; /* exact in double */
+  if (c->codes) {
+    const uint8_t* code = c->codes + (row * c->Hkv + c->h) * c->D;
+    double s = (double)c->scales[row * c->Hkv + c->h];
+    for (int d = 0; d < c->D; d++) out[d] = g_dec[code[d]] * s;
+  } else {
+    const uint16_t* v = c->bf16 + (row * c->Hkv + c->h) * c->D;
+    for (int d = 0; d < c->D; d++) out[d] = (double)bf16_to_f32(v[d]);
+  }
 }
 
-/* Decode attention over the FP8 pool.
+/* Decode attention over a pool (shared by the FP8 and the BF16 entry points below).
  *   q:            BF16 [total_rows][Hq][D]
  *   req_to_slot:  int32 [B][req_stride]; key j of request b lives in pool row req_to_slot[b*stride+j]
  *   seq_lens:     int32 [B]; request b has seq_lens[b] keys (the new rows included)
  *   q_row_offsets int32 [B+1]; request b owns query rows [q_row_offsets[b], q_row_offsets[b+1])
+ *   window:       0 = full attention; W >= 1 = sliding window: a row whose visible keys are 0 .. v-1
+ *                 attends to keys max(0, v-W) .. v-1 (its own position included)
  *   out:          double [total_rows][Hq][D]
  *   abs_v:        if nonzero, accumulate |v^| instead of v^ (the attention-weighted magnitude of the
  *                 summed terms, used by the tests to size the rounding bound; not part of the method)
  * [#897 "Fresh R9700 stage-1 A/B"]: the reference is CPU FP8 dequantization followed by attention;
  * split-K is an evaluation order and does not appear here.  Multi-row decode (up to 8 rows per
  * request, [#897 opening description]) is causal within the rows; reading: row r of R rows sees
- * keys 0 .. n-R+r.  Query head i reads KV head i / (Hq/Hkv). */
-int ftkv_oracle_decode_attn(const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scales,
-                            const float* v_scales, int64_t num_rows, int Hq, int Hkv, int D,
-                            const uint16_t* q, const int32_t* req_to_slot, int64_t req_stride,
-                            const int32_t* seq_lens, const int32_t* q_row_offsets, int B,
-                            double sm_scale, int abs_v, double* out) {
+ * keys 0 .. n-R+r.  Query head i reads KV head i / (Hq/Hkv).  The sliding window is one of the
+ * integration cases of [#897 "Regression and CUDA isolation"] ("odd sliding window"); its reading is the
+ * usual one (the last W positions up to the query's own). */
+static int decode_core(const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scales,
+                       const float* v_scales, const uint16_t* k_bf16, const uint16_t* v_bf16,
+                       int64_t num_rows, int Hq, int Hkv, int D, const uint16_t* q, const int32_t* req_to_slot,
+                       int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int B,
+                       double sm_scale, int64_t window, int abs_v, double* out) {
   init_mag_table();
-  if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+  if (Hkv <= 0 || Hq % Hkv != 0 || window < 0) return -1;
   int G = Hq / Hkv;
   int64_t max_n = 0;
   for (int b = 0; b < B; b++) {
@@ -269,14 +280,15 @@ int ftkv_oracle_decode_attn(const uint8_t* k_codes, const uint8_t* v_codes, cons
       int r = row - q_row_offsets[b];
       int64_t visible = (int64_t)seq_lens[b] - R + r + 1;
       if (visible < 0) visible = 0;
+      int64_t first = (window > 0 && visible > window) ? visible - window : 0;
       for (int d = 0; d < D; d++) qd[d] = (double)bf16_to_f32(q[((int64_t)row * Hq + i) * D + d]);
-      pool_ctx kc = {k_codes, k_scales, req_to_slot + b * req_stride, Hkv, D, i / G};
-      pool_ctx vc = {v_codes, v_scales, req_to_slot + b * req_stride, Hkv, D, i / G};
+      pool_ctx kc = {k_codes, k_scales, k_bf16, req_to_slot + b * req_stride, Hkv, D, i / G};
+      pool_ctx vc = {v_codes, v_scales, v_bf16, req_to_slot + b * req_stride, Hkv, D, i / G};
       double* o = out + ((int64_t)row * Hq + i) * D;
       for (int d = 0; d < D; d++) o[d] = 0.0;
-      if (visible > 0) {
+      if (visible > first) {
         double m = -INFINITY;
-        for (int64_t j = 0; j < visible; j++) {
+        for (int64_t j = first; j < visible; j++) {
           pool_row(&kc, j, kv);
           double dot = 0.0;
           for (int d = 0; d < D; d++) dot += qd[d] * kv[d];
@@ -284,7 +296,7 @@ int ftkv_oracle_decode_attn(const uint8_t* k_codes, const uint8_t* v_codes, cons
           if (s[j] > m) m = s[j];
         }
         double l = 0.0;
-        for (int64_t j = 0; j < visible; j++) {
+        for (int64_t j = first; j < visible; j++) {
           double p = exp(s[j] - m);
           l += p;
           pool_row(&vc, j, kv);
@@ -298,6 +310,28 @@ int ftkv_oracle_decode_attn(const uint8_t* k_codes, const uint8_t* v_codes, cons
     free(qd);
   }
   return 0;
+}
+
+/* Decode attention over the FP8 pool (codes [rows][Hkv][D], FP32 scales [rows][Hkv]). */
+int ftkv_oracle_decode_attn(const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scales,
+                            const float* v_scales, int64_t num_rows, int Hq, int Hkv, int D,
+                            const uint16_t* q, const int32_t* req_to_slot, int64_t req_stride,
+                            const int32_t* seq_lens, const int32_t* q_row_offsets, int B,
+                            double sm_scale, int64_t window, int abs_v, double* out) {
+  if (!k_codes || !v_codes || !k_scales || !v_scales) return -1;
+  return decode_core(k_codes, v_codes, k_scales, v_scales, NULL, NULL, num_rows, Hq, Hkv, D, q, req_to_slot,
+                     req_stride, seq_lens, q_row_offsets, B, sm_scale, window, abs_v, out);
+}
+
+/* Decode attention over a BF16 pool (values [rows][Hkv][D]): the BF16 KV cache the FP8 format replaces
+ * ([#853 "Follow-up model/workload search"]: 98,304 vs 50,688 bytes per token), same definition. */
+int ftkv_oracle_decode_attn_bf16(const uint16_t* k, const uint16_t* v, int64_t num_rows, int Hq, int Hkv, int D,
+                                 const uint16_t* q, const int32_t* req_to_slot, int64_t req_stride,
+                                 const int32_t* seq_lens, const int32_t* q_row_offsets, int B, double sm_scale,
+                                 int64_t window, int abs_v, double* out) {
+  if (!k || !v) return -1;
+  return decode_core(NULL, NULL, NULL, NULL, k, v, num_rows, Hq, Hkv, D, q, req_to_slot, req_stride, seq_lens,
+                     q_row_offsets, B, sm_scale, window, abs_v, out);
 }
 
 /* ---- prefill over the BF16 workspace prefix plus the BF16 chunk ---- */

@@ -193,3 +193,101 @@ def test_abs_mode_is_attention_over_absolute_values():
     absd = lambda b: inputs.to_bf16_bits(np.abs(inputs.bf16_bits_to_f32(b)))
     np.testing.assert_array_equal(oracle.prefill_attn(q, kc, vc, wk, wv, SM, abs_v=True),
                                   oracle.prefill_attn(q, kc, absd(vc), wk, absd(wv), SM))
+
+
+# ---- decode over a BF16 pool, and the sliding window ----
+
+def _bf16_pool(rng, R, n, Hkv=4, D=128, sigma=1.0):
+    k, v = inputs.kv_tokens(rng, n, sigma, Hkv=Hkv, head_dim=D)
+    slots = rng.permutation(R)[:n].astype(np.int32)
+    kp = np.zeros((R, Hkv, D), np.uint16)
+    vp = np.zeros_like(kp)
+    kp[slots], vp[slots] = k, v
+    return kp, vp, slots
+
+
+def _bf16_t(bits):
+    return torch.from_numpy(inputs.bf16_bits_to_f32(bits)).to(torch.float64)
+
+
+@pytest.mark.parametrize("Hq,Hkv,rows", [(32, 4, 1), (16, 4, 3), (8, 8, 1)])
+def test_decode_bf16_pool_matches_torch_sdpa(Hq, Hkv, rows):
+    rng = np.random.default_rng(61)
+    R, n = 90, 57
+    kp, vp, slots = _bf16_pool(rng, R, n, Hkv=Hkv)
+    q = inputs.queries(rng, rows, Hq)
+    got = oracle.decode_attn_bf16(kp, vp, q, slots[None], [n], [0, rows], SM, Hq)
+    kd = _bf16_t(kp[slots]).permute(1, 0, 2)
+    vd = _bf16_t(vp[slots]).permute(1, 0, 2)
+    qd = _bf16_t(q).permute(1, 0, 2)
+    mask = torch.arange(n)[None, :] <= (n - rows + torch.arange(rows)[:, None])
+    want = _sdpa(qd, kd, vd, mask).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_decode_bf16_pool_equals_fp8_pool_on_identical_values():
+    """With power-of-two scales every dequantized FP8 value is a BF16 value: both pool kinds then hold the
+    same numbers, and the two decodes must agree exactly (a dropped scale or a wrong row would show)."""
+    rng = np.random.default_rng(62)
+    R, n, Hkv = 64, 40, 4
+    pool = oracle.Pool(R, Hkv, 128)
+    codes = rng.integers(0, 256, size=(R, Hkv, 128), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38           # no NaN codes
+    pool.k_codes[:], pool.v_codes[:] = codes, codes[::-1]
+    pool.k_scales[:] = 2.0 ** rng.integers(-6, 6, size=(R, Hkv))
+    pool.v_scales[:] = 2.0 ** rng.integers(-6, 6, size=(R, Hkv))
+    kval = oracle.e4m3_decode(pool.k_codes) * pool.k_scales[..., None]
+    vval = oracle.e4m3_decode(pool.v_codes) * pool.v_scales[..., None]
+    kb, vb = inputs.to_bf16_bits(kval.astype(np.float32)), inputs.to_bf16_bits(vval.astype(np.float32))
+    assert np.array_equal(inputs.bf16_bits_to_f32(kb).astype(np.float64), kval)   # exact in BF16
+    slots = rng.permutation(R)[:n].astype(np.int32)
+    q = inputs.queries(rng, 2)
+    a = oracle.decode_attn(pool, q, slots[None], [n], [0, 2], SM, 32)
+    b = oracle.decode_attn_bf16(kb, vb, q, slots[None], [n], [0, 2], SM, 32)
+    np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("window,rows", [(1, 1), (7, 1), (13, 3), (56, 1), (1000, 2)])
+def test_decode_sliding_window_matches_torch_sdpa_with_banded_mask(window, rows):
+    rng = np.random.default_rng(63 + window)
+    R, n = 80, 57
+    pool, slots = _pool_from(rng, R, n)
+    q = inputs.queries(rng, rows)
+    got = oracle.decode_attn(pool, q, slots[None], [n], [0, rows], SM, 32, window=window)
+    kd = _torch_deq(pool.k_codes[slots], pool.k_scales[slots]).permute(1, 0, 2)
+    vd = _torch_deq(pool.v_codes[slots], pool.v_scales[slots]).permute(1, 0, 2)
+    qd = torch.from_numpy(inputs.bf16_bits_to_f32(q)).to(torch.float64).permute(1, 0, 2)
+    last = n - rows + torch.arange(rows)[:, None]             # last visible key of each row
+    j = torch.arange(n)[None, :]
+    mask = (j <= last) & (j > last - window)
+    want = _sdpa(qd, kd, vd, mask).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    # the same window over the BF16 pool holding the same values
+    kb = inputs.to_bf16_bits(kd.permute(1, 0, 2).numpy().astype(np.float32))
+    if np.array_equal(inputs.bf16_bits_to_f32(kb).astype(np.float64), kd.permute(1, 0, 2).numpy()):
+        vb = inputs.to_bf16_bits(vd.permute(1, 0, 2).numpy().astype(np.float32))
+        kp = np.zeros((R, 4, 128), np.uint16)
+        vp = np.zeros_like(kp)
+        kp[slots], vp[slots] = kb, vb
+        got_b = oracle.decode_attn_bf16(kp, vp, q, slots[None], [n], [0, rows], SM, 32, window=window)
+        np.testing.assert_allclose(got_b, want, rtol=1e-12, atol=1e-12)
+
+
+def test_decode_sliding_window_closed_forms():
+    rng = np.random.default_rng(64)
+    R, n = 50, 30
+    pool, slots = _pool_from(rng, R, n)
+    q = inputs.queries(rng, 1)
+    # window 1: the value of the last key alone
+    got = oracle.decode_attn(pool, q, slots[None], [n], [0, 1], SM, 32, window=1)[0]
+    vlast = oracle.e4m3_decode(pool.v_codes[slots[n - 1]]) * pool.v_scales[slots[n - 1]][:, None]
+    for i in range(32):
+        np.testing.assert_allclose(got[i], vlast[i // 8], rtol=1e-12, atol=1e-12)
+    # a window of n or more keys is full attention
+    full = oracle.decode_attn(pool, q, slots[None], [n], [0, 1], SM, 32)
+    np.testing.assert_array_equal(oracle.decode_attn(pool, q, slots[None], [n], [0, 1], SM, 32, window=n), full)
+    # window w equals full attention over the last w keys only
+    w = 9
+    sub = oracle.decode_attn(pool, q, slots[None, n - w:], [w], [0, 1], SM, 32)
+    np.testing.assert_allclose(oracle.decode_attn(pool, q, slots[None], [n], [0, 1], SM, 32, window=w), sub,
+                               rtol=1e-13, atol=1e-13)
