@@ -139,36 +139,40 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
 
 // ---- cooperative finish: the split merge after a grid barrier, spread over every warp of the grid ----
 // Used when the whole grid is resident at once (cooperative launch).  Every CTA calls it exactly once,
-// after publishing its partials (or instead of doing anything, if its slice holds no keys).  The barrier
-// waits until every CTA has arrived (polled by thread 0, bounded at 2 s: a timeout is flagged and the merge
-// skipped).  Then output item (query row, query head, 4 of the 128 d) i goes to warp i / ncta of CTA
-// i % ncta (merge_item).  The CTA that finishes last resets the barrier for the next call.
+// after publishing its partials (or instead of doing anything, if its slice holds no keys).
+// The barrier needs no reset: gbar[0] counts the arrivals of every call on this workspace (it only grows, and
+// wraps), and gbar[1] holds its value at the end of the previous call's barrier.  Each CTA reads gbar[1] = B
+// before it arrives, so every CTA of a call reads the same B; the CTA whose arrival completes the call (ticket
+// B + ncta - 1) stores B + ncta into gbar[1] for the next call, which reads it only after this kernel has
+// completed.  Waiting is polled by thread 0, bounded at 2 s (a timeout is flagged and the merge skipped).
+// Then output item (query row, query head, 4 of the 128 d) i goes to warp i / ncta of CTA i % ncta
+// (merge_item).
 template <int WARPS>
 __device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ncta = gridDim.x * gridDim.y * gridDim.z;
   const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-  __threadfence();  // this CTA's partials before its arrival
-  __syncthreads();
+  __syncthreads();  // every thread's partials are written before thread 0 releases them
   __shared__ int s_ok;
   if (threadIdx.x == 0) {
-    atomicAdd(a.gbar, 1);
+    // unsigned arithmetic: the counters wrap
+    const unsigned base = *reinterpret_cast<volatile unsigned*>(a.gbar + 1);
+    const unsigned target = base + static_cast<unsigned>(ncta);
+    unsigned ticket;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(a.gbar) : "memory");
+    if (ticket == target - 1u) a.gbar[1] = static_cast<int>(target);  // read by the next call only
     unsigned long long t0, t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    int v = 0;
-    bool ok = false;
-    for (;;) {
-      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.gbar) : "memory");
-      if (v >= ncta) {
-        ok = true;
-        break;
-      }
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-      if (t - t0 > 2000000000ull) break;
+    unsigned v = ticket + 1u;
+    bool ok = static_cast<int>(v - target) >= 0;
+    while (!ok) {
       __nanosleep(32);
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.gbar) : "memory");
+      ok = static_cast<int>(v - target) >= 0;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (!ok && t - t0 > 2000000000ull) break;
     }
     if (!ok) flag_error(a.err, kDevErrTimeout);
-    __threadfence();
     s_ok = ok;
   }
   __syncthreads();
@@ -176,11 +180,6 @@ __device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
     const int64_t items = a.total_q_rows * a.num_q_heads * (kHeadDim / 4);
     for (int64_t it = cta + static_cast<int64_t>(ncta) * warp; it < items; it += static_cast<int64_t>(ncta) * WARPS)
       merge_item<10>(a, it, lane);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(a.gbar + 1, 1) == ncta - 1) {  // every CTA is past the barrier
-    a.gbar[0] = 0;
-    a.gbar[1] = 0;
   }
 }
 

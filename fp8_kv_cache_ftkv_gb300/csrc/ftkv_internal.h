@@ -71,7 +71,8 @@ struct DecodeArgs {
   int early;                 // FTKV_DECODE_STABLE_HISTORY: history loads may start before the preceding grid ends
   int scan_scales;           // the slot tables may cover most of the pool: bring the scale arrays into L2 whole
   int coop;                  // set by the launcher: cooperative launch, merge after a grid barrier
-  int* gbar;                 // [2] grid-barrier arrivals and finished CTAs; zero between calls
+  int* gbar;                 // [2] grid barrier: arrivals of every call so far, and their count when the
+                             // previous call's barrier completed (zero-filled once; no reset between calls)
   const uint16_t* k_new;     // fused store: [total_q_rows][Hkv][128] K of the new tokens, or null
   const uint16_t* v_new;     //              V of the new tokens
 };

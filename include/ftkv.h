@@ -136,7 +136,7 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
  *   workspace      : device scratch of at least ftkv_decode_workspace_bytes(...) bytes, 256-byte
  *                    aligned, ZERO-FILLED before its first use (e.g. cudaMemsetAsync).  It holds the
  *                    per-slice partials, one arrival counter per (request, KV head) and the grid barrier;
- *                    every call leaves the counters at zero again, so the zero fill is needed once.  Calls
+ *                    every call leaves them ready for the next call, so the zero fill is needed once.  Calls
  *                    that share a workspace must not overlap on the GPU.
  *   out            : device BF16 [total_q_rows][num_q_heads][head_dim]
  * A query row that sees no key gets zeros.  req_to_slot, seq_lens and q_row_offsets must be 4-byte
