@@ -74,10 +74,10 @@ def load() -> ctypes.CDLL:
             "ftkv_reconstruct_bf16": (ctypes.c_int, [PP, P, I64, P, P, P]),
             "ftkv_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I64, I32]),
             "ftkv_decode_auto_splits": (I32, [I32, I32, I64, I32]),
-            "ftkv_decode_attn": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, U32, P, SZ,
-                                                P, P]),
-            "ftkv_decode_attn_store": (ctypes.c_int, [PP, I32, P, P, P, P, I64, P, P, I32, I64, I32, I64, F32, I32,
-                                                      U32, P, SZ, P, P]),
+            "ftkv_decode_attn": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I64, I32, U32, P,
+                                                SZ, P, P]),
+            "ftkv_decode_attn_store": (ctypes.c_int, [PP, I32, P, P, P, P, I64, P, P, I32, I64, I32, I64, F32, I64,
+                                                      I32, U32, P, SZ, P, P]),
             "ftkv_decode_attn_noalloc": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P,
                                                         P]),
             "ftkv_prefill_attn": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),

@@ -187,8 +187,8 @@ namespace ftkv {
 int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
                     int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                     int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                    int32_t num_splits, uint32_t flags, const void* workspace, size_t workspace_bytes,
-                    const uint16_t* out, bool check_workspace, DecodeGeom* geom) {
+                    int64_t window, int32_t num_splits, uint32_t flags, const void* workspace,
+                    size_t workspace_bytes, const uint16_t* out, bool check_workspace, DecodeGeom* geom) {
   *geom = DecodeGeom{};
   int st = check_pool(pool);
   if (st != FTKV_OK) return st;
@@ -202,6 +202,7 @@ int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* 
   if (!q_row_offsets && total_q_rows != batch) return FTKV_ERR_INVALID;
   if (total_q_rows > int64_t(batch) * max_q_rows) return FTKV_ERR_INVALID;
   if (!(sm_scale == sm_scale)) return FTKV_ERR_INVALID;
+  if (window < 0) return FTKV_ERR_INVALID;
   if (batch == 0 || total_q_rows == 0) {
     geom->empty = true;
     return FTKV_OK;
@@ -214,14 +215,18 @@ int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* 
   if (check_workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FTKV_ERR_ALIGN;
   if (total_q_rows > (int64_t(1) << 31) - 1) return FTKV_ERR_UNSUPPORTED;
 
-  if (num_splits == 0) num_splits = ftkv_decode_auto_splits(batch, pool->num_kv_heads, max_seq_len, max_q_rows);
+  // Keys a request attends to at most: all of them, or with a sliding window of W keys the last W + R - 1
+  // (the union of its R rows' windows); the slices cover only those.
+  const int64_t span = (window > 0 && window + max_q_rows - 1 < max_seq_len) ? window + max_q_rows - 1 : max_seq_len;
+  geom->span = span;
+  if (num_splits == 0) num_splits = ftkv_decode_auto_splits(batch, pool->num_kv_heads, span, max_q_rows);
   // keys per slice: a multiple of 8 for the single-row kernel (its blocks of 16 keys may end inside a slice),
   // of 16 for the multi-row kernel
   const int64_t align = max_q_rows <= 1 ? 8 : 16;
-  int64_t chunk = ceil_div(max_seq_len > 0 ? max_seq_len : 1, num_splits);
+  int64_t chunk = ceil_div(span > 0 ? span : 1, num_splits);
   chunk = ceil_div(chunk, align) * align;
   geom->chunk = chunk;
-  geom->splits = max_seq_len > 0 ? ceil_div(max_seq_len, chunk) : 1;
+  geom->splits = span > 0 ? ceil_div(span, chunk) : 1;
   geom->need = ftkv_decode_workspace_bytes(num_q_heads, pool->num_kv_heads, FTKV_HEAD_DIM, batch, total_q_rows,
                                            static_cast<int32_t>(geom->splits));
   geom->parts = total_q_rows * num_q_heads * geom->splits * ftkv::decode_parts_per_slice(1, pool->num_kv_heads);
@@ -236,12 +241,13 @@ extern "C" {
 static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
                          int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                          int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                         int32_t num_splits, uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out,
-                         void* stream, const uint16_t* k_new = nullptr, const uint16_t* v_new = nullptr) {
+                         int64_t window, int32_t num_splits, uint32_t flags, void* workspace,
+                         size_t workspace_bytes, uint16_t* out, void* stream, const uint16_t* k_new = nullptr,
+                         const uint16_t* v_new = nullptr) {
   ftkv::DecodeGeom geom;
   int st = ftkv::decode_validate(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch,
-                                 total_q_rows, max_q_rows, max_seq_len, sm_scale, num_splits, flags, workspace,
-                                 workspace_bytes, out, true, &geom);
+                                 total_q_rows, max_q_rows, max_seq_len, sm_scale, window, num_splits, flags,
+                                 workspace, workspace_bytes, out, true, &geom);
   if (st != FTKV_OK || geom.empty) return st;
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FTKV_OK) return st;
@@ -272,6 +278,7 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   a.num_splits = static_cast<int>(geom.splits);
   a.chunk = geom.chunk;
   a.qk_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.window = window;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
   a.counters = counters;
@@ -281,7 +288,7 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   a.early = (flags & FTKV_DECODE_STABLE_HISTORY) ? 1 : 0;
   // When the requests' keys may cover at least half of the pool rows, the kernel reads the scale arrays
   // into L2 sequentially at its start instead of leaving them to scattered 4-byte reads.
-  a.scan_scales = (int64_t(batch) * max_seq_len * 2 >= pool->num_rows) ? 1 : 0;
+  a.scan_scales = (int64_t(batch) * geom.span * 2 >= pool->num_rows) ? 1 : 0;
   a.k_new = k_new;
   a.v_new = v_new;
   cudaError_t e = ftkv::launch_decode(a, static_cast<cudaStream_t>(stream));
@@ -291,24 +298,26 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
 int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
                      int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                      int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                     int32_t num_splits, uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out,
-                     void* stream) {
+                     int64_t window, int32_t num_splits, uint32_t flags, void* workspace, size_t workspace_bytes,
+                     uint16_t* out, void* stream) {
   return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
-                       max_q_rows, max_seq_len, sm_scale, num_splits, flags, workspace, workspace_bytes, out, stream);
+                       max_q_rows, max_seq_len, sm_scale, window, num_splits, flags, workspace, workspace_bytes, out,
+                       stream);
 }
 
 int ftkv_decode_attn_store(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const uint16_t* k_new,
                            const uint16_t* v_new, const int32_t* req_to_slot, int64_t req_stride,
                            const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
-                           int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
-                           uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
+                           int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int64_t window,
+                           int32_t num_splits, uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out,
+                           void* stream) {
   if (batch > 0 && total_q_rows > 0) {
     if (!k_new || !v_new) return FTKV_ERR_INVALID;
     if (!aligned16(k_new) || !aligned16(v_new)) return FTKV_ERR_ALIGN;
   }
   return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
-                       max_q_rows, max_seq_len, sm_scale, num_splits, flags, workspace, workspace_bytes, out, stream,
-                       k_new, v_new);
+                       max_q_rows, max_seq_len, sm_scale, window, num_splits, flags, workspace, workspace_bytes, out,
+                       stream, k_new, v_new);
 }
 
 static int prefill_common(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,

@@ -122,8 +122,9 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     if (a.coop) coop_finish<WARPS>(a);
     return;
   }
-  // key indices fit in 32 bits (the host rejects max_seq_len >= 2^31)
-  const int j0 = split * static_cast<int>(a.chunk);
+  // key indices fit in 32 bits (the host rejects max_seq_len >= 2^31); slices cover keys [first, n)
+  const int kfirst = static_cast<int>(first_key(a, n, R));
+  const int j0 = kfirst + split * static_cast<int>(a.chunk);
   const int j1 = (static_cast<int64_t>(j0) + a.chunk < n) ? j0 + static_cast<int>(a.chunk) : static_cast<int>(n);
   if (j0 >= n || R == 0) {  // slices past the end hold no keys and take no ticket
     if (a.coop) coop_finish<WARPS>(a);
@@ -135,13 +136,14 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   const int wk = WARPS / nrg;
   const int rg = warp / wk, kw = warp % wk;
   const bool active = rg < nrg;
-  int lim[RPW];
+  int lim[RPW], low[RPW];  // keys low .. lim-1 of this slice are attended by the row
 #pragma unroll
   for (int i = 0; i < RPW; i++) {
     const int rabs = rg * RPW + i;
     const bool valid = active && rabs < R;
     const int vis = static_cast<int>(n) - R + rabs + 1;  // keys 0 .. vis-1 are visible to this row
     lim[i] = valid ? (vis < j1 ? vis : j1) : j0;
+    low[i] = (a.window > 0 && vis - a.window > 0) ? vis - static_cast<int>(a.window) : 0;  // sliding window
   }
 
   // The first slot window's indices are requested now and staged after the query pieces, so the two
@@ -360,10 +362,11 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
         float dot[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) dot[e] = fmaf(c[r][1][e], 1.0f / 16.0f, c[r][0][e]);
-        const float s0 = (jg < lr) ? dot[0] * (skg * fq[r][0]) : -INFINITY;
-        const float s1 = (jg < lr) ? dot[1] * (skg * fq[r][1]) : -INFINITY;
-        const float s2 = (jg8 < lr) ? dot[2] * (skg8 * fq[r][0]) : -INFINITY;
-        const float s3 = (jg8 < lr) ? dot[3] * (skg8 * fq[r][1]) : -INFINITY;
+        const bool in0 = jg < lr && jg >= low[r], in8 = jg8 < lr && jg8 >= low[r];
+        const float s0 = in0 ? dot[0] * (skg * fq[r][0]) : -INFINITY;
+        const float s1 = in0 ? dot[1] * (skg * fq[r][1]) : -INFINITY;
+        const float s2 = in8 ? dot[2] * (skg8 * fq[r][0]) : -INFINITY;
+        const float s3 = in8 ? dot[3] * (skg8 * fq[r][1]) : -INFINITY;
         float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -554,7 +557,7 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
   // all slices (o = sum_s 2^(M_s - M) A_s / sum_s 2^(M_s - M) L_s) and resets the counter for the
   // next call.  Nothing ever waits on another CTA.
   __shared__ int s_last;
-  const int64_t nsl64 = (n + a.chunk - 1) / a.chunk;
+  const int64_t nsl64 = (n - kfirst + a.chunk - 1) / a.chunk;
   const int nslices = static_cast<int>(nsl64 < a.num_splits ? nsl64 : a.num_splits);
   __threadfence();
   __syncthreads();

@@ -44,6 +44,15 @@ __device__ __forceinline__ int64_t clamp_seq_len(const DecodeArgs& a, int b, boo
   return n;
 }
 
+// First key of a request's attended range: 0, or with a sliding window of W keys the window start of its first
+// query row (row 0 of R sees keys 0 .. n-R, so its window starts at n-R+1-W).  The key slices of a request
+// cover keys [first, n).
+__device__ __forceinline__ int64_t first_key(const DecodeArgs& a, int64_t n, int R) {
+  if (a.window <= 0) return 0;
+  const int64_t lo = n - R + 1 - a.window;
+  return lo > 0 ? lo : 0;
+}
+
 // Wait for the preceding grid of the stream (programmatic dependent launch) -- its completion and memory.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
@@ -62,7 +71,7 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
   const int64_t t = it / (a.num_q_heads * QUADS);  // query row
   const int rem = static_cast<int>(it - t * a.num_q_heads * QUADS);
   const int qh = rem / QUADS, d4 = rem % QUADS;
-  int b = static_cast<int>(t);
+  int b = static_cast<int>(t), R = 1;
   if (a.q_row_offsets) {  // request of row t
     int lo = 0, hi = a.batch;
     while (lo < hi) {
@@ -72,13 +81,13 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
     b = lo;
     if (b >= a.batch) return;
     const int64_t r0 = a.q_row_offsets[b];
-    const int R = a.q_row_offsets[b + 1] - a.q_row_offsets[b];
+    R = a.q_row_offsets[b + 1] - a.q_row_offsets[b];
     if (R < 0 || R > a.max_q_rows || r0 < 0 || r0 + R > a.total_q_rows) return;  // skipped request
   }
   int64_t n = a.seq_lens[b];
   const int64_t nmax = a.max_seq_len < a.req_stride ? a.max_seq_len : a.req_stride;
   n = n < 0 ? 0 : (n > nmax ? nmax : n);
-  const int64_t nsl64 = (n + a.chunk - 1) / a.chunk;
+  const int64_t nsl64 = (n - first_key(a, n, R) + a.chunk - 1) / a.chunk;
   const int nslices = static_cast<int>(nsl64 < a.num_splits ? nsl64 : a.num_splits) * a.pps;
   uint16_t* dst = a.out + (t * a.num_q_heads + qh) * kHeadDim + 4 * d4;
   if (nslices == 0) {  // no keys: zeros

@@ -57,8 +57,8 @@ extern "C" int ftkv_decode_attn_noalloc(const ftkv_pool* pool, int32_t num_q_hea
   // every argument check of ftkv_decode_attn, and its split geometry, before anything is enqueued
   ftkv::DecodeGeom geom;
   int st = ftkv::decode_validate(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch,
-                                 total_q_rows, max_q_rows, max_seq_len, sm_scale, num_splits, 0u, nullptr, 0, out,
-                                 false, &geom);
+                                 total_q_rows, max_q_rows, max_seq_len, sm_scale, 0, num_splits, 0u, nullptr, 0,
+                                 out, false, &geom);
   if (st != FTKV_OK || geom.empty) return st;
   if (geom.need > FTKV_NOALLOC_SCRATCH_BYTES) return FTKV_ERR_WORKSPACE;  // beyond the static maximum
   void* scratch = nullptr;
@@ -72,6 +72,6 @@ extern "C" int ftkv_decode_attn_noalloc(const ftkv_pool* pool, int32_t num_q_hea
                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FTKV_ERR_CUDA;
   return ftkv_decode_attn(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch,
-                          total_q_rows, max_q_rows, max_seq_len, sm_scale, static_cast<int32_t>(geom.splits), 0u,
-                          scratch, FTKV_NOALLOC_SCRATCH_BYTES, out, stream);
+                          total_q_rows, max_q_rows, max_seq_len, sm_scale, 0, static_cast<int32_t>(geom.splits),
+                          0u, scratch, FTKV_NOALLOC_SCRATCH_BYTES, out, stream);
 }

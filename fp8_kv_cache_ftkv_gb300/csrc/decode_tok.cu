@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
 
   // ---- slice geometry (seq_lens and the slot table are stable before the wait under the contract) ----
   const int64_t n = clamp_seq_len(a, b, threadIdx.x == 0 && split == 0 && blockIdx.y == 0);
-  const int j0 = split * static_cast<int>(a.chunk);  // key indices fit in 32 bits (host check)
+  // slices cover keys [first, n): first = 0, or n - W with a sliding window (one query row per request)
+  const int j0 = static_cast<int>(first_key(a, n, 1)) + split * static_cast<int>(a.chunk);  // 32-bit (host check)
   const int j1 = (static_cast<int64_t>(j0) + a.chunk < n) ? j0 + static_cast<int>(a.chunk) : static_cast<int>(n);
   const bool has_keys = j0 < j1;
   const int hist_end = static_cast<int>(n) - a.max_q_rows;  // keys below are history (never written here)

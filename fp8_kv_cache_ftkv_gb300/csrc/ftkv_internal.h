@@ -63,6 +63,7 @@ struct DecodeArgs {
                              // (row, query head) is at index s * pps + p of num_splits * pps
   int64_t chunk;             // keys per slice (multiple of 16)
   float qk_scale_log2;       // sm_scale * log2(e)
+  int64_t window;            // 0: full attention; W > 0: each query row attends to its last W visible keys
   float* part_acc;           // [total_q_rows][Hq][num_splits * pps][128]
   float* part_ml;            // [total_q_rows][Hq][num_splits * pps][2]  (max in log2 units, sum)
   int* counters;             // [batch][Hkv] arrival tickets; zero between calls
@@ -157,13 +158,14 @@ struct DecodeGeom {
   int64_t splits = 0;   // key slices per request
   int64_t parts = 0;    // partial slots in the workspace (rows x query heads x slices x partials per slice)
   int64_t chunk = 0;    // keys per slice
+  int64_t span = 0;     // most keys one request attends to (max_seq_len, or less with a sliding window)
   size_t need = 0;      // workspace bytes
   bool empty = false;   // nothing to compute (batch or total_q_rows is 0)
 };
 int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
                     int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                     int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                    int32_t num_splits, uint32_t flags, const void* workspace, size_t workspace_bytes,
-                    const uint16_t* out, bool check_workspace, DecodeGeom* geom);
+                    int64_t window, int32_t num_splits, uint32_t flags, const void* workspace,
+                    size_t workspace_bytes, const uint16_t* out, bool check_workspace, DecodeGeom* geom);
 
 }  // namespace ftkv

@@ -118,21 +118,24 @@ class DecodePlan:
     on one stream; the kernels leave its arrival counters at zero)."""
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, batch: int, total_q_rows: int, max_q_rows: int,
-                 max_seq_len: int, num_splits: int = 0, device="cuda"):
+                 max_seq_len: int, num_splits: int = 0, device="cuda", window: int = 0):
         self.num_q_heads, self.num_kv_heads = num_q_heads, num_kv_heads
         self.batch, self.total_q_rows, self.max_q_rows = batch, total_q_rows, max_q_rows
-        self.max_seq_len = max_seq_len
-        self.num_splits = num_splits or decode_auto_splits(batch, num_kv_heads, max_seq_len, max_q_rows)
+        self.max_seq_len, self.window = max_seq_len, window
+        # keys one request attends to at most: with a sliding window, the union of its rows' windows
+        span = min(max_seq_len, window + max_q_rows - 1) if window > 0 else max_seq_len
+        self.num_splits = num_splits or decode_auto_splits(batch, num_kv_heads, span, max_q_rows)
         nbytes = decode_workspace_bytes(num_q_heads, num_kv_heads, batch, total_q_rows, self.num_splits)
         self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
 def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,
                 q_row_offsets: torch.Tensor = None, *, max_seq_len: int, max_q_rows: int = 1,
-                sm_scale: float = HEAD_DIM ** -0.5, num_splits: int = 0, plan: DecodePlan = None,
-                out: torch.Tensor = None, k_new: torch.Tensor = None, v_new: torch.Tensor = None,
-                stable_history: bool = False, stream=None) -> torch.Tensor:
+                sm_scale: float = HEAD_DIM ** -0.5, window: int = 0, num_splits: int = 0,
+                plan: DecodePlan = None, out: torch.Tensor = None, k_new: torch.Tensor = None,
+                v_new: torch.Tensor = None, stable_history: bool = False, stream=None) -> torch.Tensor:
     """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, 128].
+    ``window`` > 0: sliding window -- a row that sees keys 0 .. v-1 attends to keys max(0, v - window) .. v-1.
     ``k_new``/``v_new`` (BF16 [total_q_rows, Hkv, 128], the new tokens' rows, one per query row): quantize them
     into the pool at their positions' slots first, in the same launch (``ftkv_decode_attn_store``).
     ``stable_history``: pass FTKV_DECODE_STABLE_HISTORY -- the caller guarantees that no work still pending on the
@@ -153,7 +156,8 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
     batch = seq_lens.shape[0]
     total, hq, _ = q.shape
     if plan is None:
-        plan = DecodePlan(hq, pool.num_kv_heads, batch, total, max_q_rows, max_seq_len, num_splits, q.device)
+        plan = DecodePlan(hq, pool.num_kv_heads, batch, total, max_q_rows, max_seq_len, num_splits, q.device,
+                          window)
     if out is None:
         out = torch.empty_like(q)
     _req(out, torch.bfloat16, "out", 3)
@@ -165,12 +169,14 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
         check(_lib.load().ftkv_decode_attn_store(
             ctypes.byref(ps), hq, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(req_to_slot), req_to_slot.shape[1],
             _ptr(seq_lens), _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale),
-            plan.num_splits, flags, _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)),
+            int(window), plan.num_splits, flags, _ptr(plan.workspace), plan.workspace.numel(), _ptr(out),
+            _stream_ptr(stream)),
             "ftkv_decode_attn_store")
         return out
     check(_lib.load().ftkv_decode_attn(
         ctypes.byref(ps), hq, _ptr(q), _ptr(req_to_slot), req_to_slot.shape[1], _ptr(seq_lens),
-        _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale), plan.num_splits, flags,
+        _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale), int(window), plan.num_splits,
+        flags,
         _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)), "ftkv_decode_attn")
     return out
 

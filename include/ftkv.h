@@ -131,7 +131,12 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
  *   max_q_rows     : host upper bound on rows per request (1 .. FTKV_MAX_Q_ROWS)
  *   max_seq_len    : host upper bound on seq_lens (<= req_stride); it fixes the split geometry
  *   sm_scale       : softmax scale (1/sqrt(head_dim) for the standard case)
+ *   window         : 0 = full attention; W >= 1 = sliding window: a row that sees keys 0 .. v-1 attends
+ *                    only to keys max(0, v - W) .. v - 1 (the "odd sliding window" integration case of
+ *                    [#897 "Regression and CUDA isolation"]); the key slices then cover only the last
+ *                    W + R - 1 keys of each request.  window < 0 -> FTKV_ERR_INVALID.
  *   num_splits     : 0 = automatic (fills the SMs), else 1 .. FTKV_MAX_SPLITS key slices per request
+ *                    (over the window's keys when window > 0)
  *   flags          : 0 or FTKV_DECODE_STABLE_HISTORY (see above); other bits -> FTKV_ERR_INVALID
  *   workspace      : device scratch of at least ftkv_decode_workspace_bytes(...) bytes, 256-byte
  *                    aligned, ZERO-FILLED before its first use (e.g. cudaMemsetAsync).  It holds the
@@ -155,8 +160,9 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
 int ftkv_decode_attn(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q,
                      const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens,
                      const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
-                     int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int32_t num_splits,
-                     uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
+                     int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int64_t window,
+                     int32_t num_splits, uint32_t flags, void* workspace, size_t workspace_bytes,
+                     uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Quantize-on-write of the new tokens fused into decode: what ftkv_store_quant followed by
@@ -177,16 +183,17 @@ int ftkv_decode_attn_store(const ftkv_pool* pool, int32_t num_q_heads, const uin
                            const uint16_t* k_new, const uint16_t* v_new, const int32_t* req_to_slot,
                            int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets,
                            int32_t batch, int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len,
-                           float sm_scale, int32_t num_splits, uint32_t flags, void* workspace,
-                           size_t workspace_bytes, uint16_t* out, void* stream);
+                           float sm_scale, int64_t window, int32_t num_splits, uint32_t flags,
+                           void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Decode without any device allocation.  The pages describe no such entry point; it exists for
  * callers that cannot allocate device memory when they need decode attention (a runtime that forbids
  * out-of-band device allocations, a plug-in that only receives buffers from its host, code that must
- * never touch an allocator).  Same arguments and results as ftkv_decode_attn, minus the workspace and the
- * flags (always 0): the split partials and arrival counters live in a file-scope device array of
- * FTKV_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads this library keeps until the process exits.
+ * never touch an allocator).  Same arguments and results as ftkv_decode_attn, minus the workspace, the
+ * flags (always 0) and the window (always 0: full attention): the split partials and arrival counters
+ * live in a file-scope device array of FTKV_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU which loads
+ * this library keeps until the process exits.
  *   - Every argument is checked before anything is enqueued; a refused call leaves the array untouched.
  *   - A call whose partials would not fit (roughly total_q_rows * num_q_heads * splits > 30,000 slices)
  *     returns FTKV_ERR_WORKSPACE without launching anything.

@@ -84,13 +84,13 @@ def test_decode_validation(lib):
     assert ws > 0 and ws % 256 == 0
     assert lib.ftkv_decode_workspace_bytes(32, 4, 64, 1, 1, 8) == 0
     base = dict(q=0x1000, r2s=0x2000, stride=64, lens=0x3000, offs=None, B=1, total=1, mq=1, maxlen=64,
-                sm=0.0884, splits=4, flags=0, ws=0x100000, wsb=ws, out=0x4000)
+                sm=0.0884, win=0, splits=4, flags=0, ws=0x100000, wsb=ws, out=0x4000)
 
     def call(pool=None, hq=32, **kw):
         a = dict(base, **kw)
         return lib.ftkv_decode_attn(P(pool or _pool()), hq, a["q"], a["r2s"], a["stride"], a["lens"], a["offs"],
-                                    a["B"], a["total"], a["mq"], a["maxlen"], a["sm"], a["splits"], a["flags"],
-                                    a["ws"], a["wsb"], a["out"], None)
+                                    a["B"], a["total"], a["mq"], a["maxlen"], a["sm"], a["win"], a["splits"],
+                                    a["flags"], a["ws"], a["wsb"], a["out"], None)
 
     assert call(hq=24) == _lib.FTKV_ERR_UNSUPPORTED          # group 6
     assert call(hq=30) == _lib.FTKV_ERR_UNSUPPORTED          # not a multiple of Hkv
@@ -106,12 +106,14 @@ def test_decode_validation(lib):
     assert call(ws=0x100010) == _lib.FTKV_ERR_ALIGN          # workspace must be 256-B aligned
     assert call(wsb=ws - 1) == _lib.FTKV_ERR_WORKSPACE
     assert call(sm=float("nan")) == _lib.FTKV_ERR_INVALID
+    assert call(win=-1) == _lib.FTKV_ERR_INVALID             # sliding window: 0 (off) or >= 1 keys
+    assert call(win=8, wsb=255) == _lib.FTKV_ERR_WORKSPACE    # the workspace rule holds with a window too
     assert call(B=0, total=0) == _lib.FTKV_OK                # nothing to do
 
     def call_store(kn=0x7000, vn=0x8000, **kw):
         a = dict(base, **kw)
         return lib.ftkv_decode_attn_store(P(_pool()), 32, a["q"], kn, vn, a["r2s"], a["stride"], a["lens"],
-                                          a["offs"], a["B"], a["total"], a["mq"], a["maxlen"], a["sm"],
+                                          a["offs"], a["B"], a["total"], a["mq"], a["maxlen"], a["sm"], a["win"],
                                           a["splits"], a["flags"], a["ws"], a["wsb"], a["out"], None)
 
     assert call_store(kn=None) == _lib.FTKV_ERR_INVALID       # the fused store needs the new rows
@@ -119,6 +121,7 @@ def test_decode_validation(lib):
     assert call_store(kn=0x7008) == _lib.FTKV_ERR_ALIGN
     assert call_store(vn=0x8004) == _lib.FTKV_ERR_ALIGN
     assert call_store(mq=9) == _lib.FTKV_ERR_UNSUPPORTED       # the decode checks still apply
+    assert call_store(win=-2) == _lib.FTKV_ERR_INVALID
     assert call_store(kn=None, vn=None, B=0, total=0) == _lib.FTKV_OK
 
     def call_noalloc(**kw):

@@ -2,6 +2,7 @@
 
 Covers the 512-token single step, ragged key counts (1, 17, 513, 4099), split counts 1/8/64/152/256 and
 automatic, GQA group sizes 8/4/2/1 and 8 KV heads, multi-row decode (1..8 rows, rows that see no key), the
+sliding windows (1 key to more than the sequence, single- and multi-row, with the fused store), the
 32,768- and 40,000-key batch-1 workloads at full size (sampled layers, every output element), the batched
 64-request multi-row workload at full size, and chains of decode launches in one stream with and without
 FTKV_DECODE_STABLE_HISTORY (history loads issued before the preceding kernel has finished).  Single-row
@@ -33,16 +34,17 @@ def _setup(wl: inputs.DecodeWorkload, layer: int = 0):
     return gp, op, L, dev
 
 
-def _run(wl, gp, dev, num_splits=0, max_q_rows=None, stable=False):
+def _run(wl, gp, dev, num_splits=0, max_q_rows=None, stable=False, window=0):
     R = np.diff(wl.q_row_offsets)
     mq = int(max(R.max(), 1)) if max_q_rows is None else max_q_rows
     return ops.decode_attn(gp, dev["q"], dev["r2s"], dev["lens"], dev["offs"], max_seq_len=int(wl.req_to_slot.shape[1]),
-                           max_q_rows=mq, sm_scale=wl.sm_scale, num_splits=num_splits, stable_history=stable)
+                           max_q_rows=mq, sm_scale=wl.sm_scale, num_splits=num_splits, stable_history=stable,
+                           window=window)
 
 
-def _ref(wl, op, L):
+def _ref(wl, op, L, window=0):
     args = (op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets, wl.sm_scale, wl.Hq)
-    return oracle.decode_attn(*args), oracle.decode_attn(*args, abs_v=True)
+    return (oracle.decode_attn(*args, window=window), oracle.decode_attn(*args, abs_v=True, window=window))
 
 
 def _check(out, refs, what):
@@ -229,6 +231,44 @@ def test_decode_one_hot_attention_with_huge_logits(stable):
     check_attention(out, ref, "one-hot huge logits", mag)
 
 
+# ---- sliding window ----
+
+@pytest.mark.parametrize("stable", STABLE)
+@pytest.mark.parametrize("lens,rows,window,splits", [
+    ([4099], [1], 513, 0), ([4099], [1], 513, 8), ([4099], [1], 1, 0), ([4099], [1], 7, 1), ([300], [1], 299, 0),
+    ([300], [1], 300, 3), ([300], [1], 5000, 0), ([32768], [1], 4095, 0), ([1000, 17, 2500], [1, 1, 1], 127, 0),
+    ([200, 297, 394], [3, 1, 8], 9, 0), ([200, 297, 394], [3, 1, 8], 131, 5), ([900, 2000], [4, 2], 1, 1),
+    ([5, 40], [5, 3], 2, 0), ([0, 33, 1], [1, 1, 1], 16, 0),
+])
+def test_decode_sliding_window(lens, rows, window, splits, stable):
+    """Sliding windows of 1 key to more than the sequence, odd sizes, several slices over the window and
+    one; multi-row requests, whose rows each end their window at their own causal limit."""
+    wl = inputs.decode_custom(lens, rows, max(sum(lens) + 9, 64), seed=window + len(rows))
+    gp, op, L, dev = _setup(wl)
+    if stable and max(rows) > 1:
+        pytest.skip("the stable-history path is the single-row kernel's")
+    out = _run(wl, gp, dev, num_splits=splits, stable=stable, window=window)
+    _check(out, _ref(wl, op, L, window), f"window={window} lens={lens} rows={rows} splits={splits}")
+    assert ops.device_errors() == 0
+
+
+@pytest.mark.parametrize("lens,rows,window", [([4099], [1], 513), ([200, 297, 394], [3, 1, 8], 33)])
+def test_decode_sliding_window_reads_no_key_before_it(lens, rows, window):
+    """Slot entries before a request's first window key are set outside the pool: nothing is flagged, so no
+    CTA reads them, and the result is unchanged."""
+    wl = inputs.decode_custom(lens, rows, sum(lens) + 9, seed=window)
+    gp, op, L, dev = _setup(wl)
+    R = np.diff(wl.q_row_offsets)
+    r2s = dev["r2s"].clone()
+    for b, n in enumerate(wl.seq_lens):
+        first = max(0, int(n) - int(R[b]) + 1 - window)
+        r2s[b, :first] = 10 ** 7
+    out = ops.decode_attn(gp, dev["q"], r2s, dev["lens"], dev["offs"], max_seq_len=int(wl.req_to_slot.shape[1]),
+                          max_q_rows=int(R.max()), sm_scale=wl.sm_scale, window=window)
+    assert ops.device_errors() == 0
+    _check(out, _ref(wl, op, L, window), f"window={window} poisoned history")
+
+
 # ---- fused store + decode (ftkv_decode_attn_store) ----
 
 def _new_tokens(wl, L):
@@ -258,7 +298,8 @@ def _new_tokens(wl, L):
     ([512], [1], 0), ([33], [1], 1), ([4099], [1], 8), ([9000], [1], 1), ([1], [1], 0), ([32768], [1], 0),
     ([200, 297, 394], [3, 1, 8], 0), ([200, 297, 394], [3, 1, 8], 5), ([2, 40], [5, 3], 0), ([0, 33, 1], [1, 1, 1], 0),
 ])
-def test_decode_fused_store_equals_store_then_decode(lens, rows, splits, stable):
+@pytest.mark.parametrize("window", [0, 77])
+def test_decode_fused_store_equals_store_then_decode(lens, rows, splits, stable, window):
     """The new tokens' rows land in the pool bit-exactly as the store kernel writes them (oracle store),
     and the attention over them matches the oracle; new tokens split across slices and windows, rows
     past the start of the sequence, and an empty request included."""
@@ -279,13 +320,13 @@ def test_decode_fused_store_equals_store_then_decode(lens, rows, splits, stable)
                           torch.from_numpy(wl.seq_lens).cuda(), torch.from_numpy(wl.q_row_offsets).cuda(),
                           max_seq_len=int(wl.req_to_slot.shape[1]), max_q_rows=int(max(R.max(), 1)),
                           sm_scale=wl.sm_scale, num_splits=splits, k_new=bits_to_cuda_bf16(k_new),
-                          v_new=bits_to_cuda_bf16(v_new), stable_history=stable)
+                          v_new=bits_to_cuda_bf16(v_new), stable_history=stable, window=window)
     s = L.slots
     assert np.array_equal(gp.k_codes.cpu().numpy()[s], op.k_codes[s])
     assert np.array_equal(gp.v_codes.cpu().numpy()[s], op.v_codes[s])
     assert np.array_equal(gp.k_scales.cpu().numpy()[s].view(np.uint32), op.k_scales[s].view(np.uint32))
     assert np.array_equal(gp.v_scales.cpu().numpy()[s].view(np.uint32), op.v_scales[s].view(np.uint32))
-    _check(out, _ref(wl, op, L), f"fused lens={lens} rows={rows} splits={splits} stable={stable}")
+    _check(out, _ref(wl, op, L, window), f"fused lens={lens} rows={rows} splits={splits} stable={stable} W={window}")
     assert ops.device_errors() == 0
 
 
