@@ -291,6 +291,44 @@ def build_decode(args, torch, ops, inputs, device, context=None, pool_rows=None)
     return dict(step=step, q_all=q_all, kv_all=kv_all, out_all=out_all, plan=plan, pools=pools, n=n)
 
 
+def bf16_bytes_per_layer(n):
+    """Algorithmic bytes of one BF16-pool decode launch at n keys (batch 1): K and V rows of every key, the
+    slot table, the query and the output, plus the copy of the new token's K/V rows into the pool."""
+    return n * HKV * D * 2 * 2 + n * 4 + HQ * D * 2 * 2 + HKV * D * 2 * 2 * 2
+
+
+def build_decode_bf16(args, torch, ops, inputs, device, context=None, pool_rows=None):
+    """The headline step over BF16 pools (the unquantized comparison point): per layer one
+    ftkv_decode_attn_bf16 launch that copies the new token into the pool and attends over all n keys."""
+    n = context or args.context
+    wl = inputs.decode_long(n, pool_rows or args.pool_rows, layers=args.layers)
+    slots_d = torch.from_numpy(wl.req_to_slot).to(device)
+    lens_d = torch.from_numpy(wl.seq_lens).to(device)
+    to_dev = to_dev_fn(torch, device)
+    idx = torch.from_numpy(wl.token_slots.astype(np.int64)).to(device)
+    pools, q, newk, newv, outs = [], [], [], [], []
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
+        for L in ex.map(wl.layer, range(args.layers)):
+            pool = ops.BF16Pool.empty(wl.num_rows, HKV, device=device)
+            pool.k[idx[:n - 1]] = to_dev(L.k[:n - 1])
+            pool.v[idx[:n - 1]] = to_dev(L.v[:n - 1])
+            pools.append(pool)
+            q.append(to_dev(L.q))
+            newk.append(to_dev(L.k[n - 1:n]))
+            newv.append(to_dev(L.v[n - 1:n]))
+            outs.append(torch.empty(1, HQ, D, dtype=torch.bfloat16, device=device))
+    plan = ops.DecodePlan(HQ, HKV, 1, 1, 1, n, args.num_splits, device)
+    torch.cuda.synchronize()
+
+    def step():
+        for l in range(args.layers):
+            ops.decode_attn_bf16(pools[l], q[l], slots_d, lens_d, None, max_seq_len=n, max_q_rows=1, plan=plan,
+                                 out=outs[l], k_new=newk[l], v_new=newv[l],
+                                 stable_history=not args.no_stable_history)
+
+    return dict(step=step, plan=plan, pools=pools, n=n, wl=wl)
+
+
 def graph_of(torch, stream, work):
     """Run `work` once eagerly (per-device set-up outside capture), then capture it as a CUDA graph."""
     with torch.cuda.stream(stream):
@@ -335,10 +373,11 @@ def run_ours(args, world, rank, local):
     hbm_peak, bf16_peak, peak_src = peaks()
     stream = torch.cuda.Stream(device)
 
+    fp8_ms = None
     if not args.details_only:
-        run_headline(args, world, rank, local, torch, ops, inputs, device, stream, hbm_peak, peak_src)
+        fp8_ms = run_headline(args, world, rank, local, torch, ops, inputs, device, stream, hbm_peak, peak_src)
     if not args.no_details and rank == 0 and world == 1:
-        run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, peak_src)
+        run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, peak_src, fp8_ms)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -413,6 +452,7 @@ def run_headline(args, world, rank, local, torch, ops, inputs, device, stream, h
         }), flush=True)
     del st, graph
     torch.cuda.empty_cache()
+    return ms_step
 
 
 # ------------------------------------------------------------------------------------------------
@@ -430,7 +470,7 @@ def hbm_roof(nbytes, ms, peak, src, kernel):
             "kernel": kernel, "bytes": nbytes, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"}
 
 
-def run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, peak_src):
+def run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, peak_src, fp8_ms=None):
     import oracle
     to_dev = to_dev_fn(torch, device)
     budget = args.cpu_budget_s
@@ -495,6 +535,34 @@ def run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, p
                 hbm_roof(args.layers * decode_bytes_per_layer(40000), ms, hbm_peak, peak_src, "decode_tok_kernel<4>"),
                 cpu, {"num_splits": st["plan"].num_splits})
     del st, g
+    torch.cuda.empty_cache()
+
+    # ---- the BF16-KV comparison point: the headline step (32K keys, batch 1, 48 layers, fused new-token write,
+    # stable history) over BF16 pools ----
+    st = build_decode_bf16(args, torch, ops, inputs, device)
+    g = graph_of(torch, stream, st["step"])
+    ms, _ = time_graph(torch, stream, g, steps, warm)
+    n = args.context
+    wlb = st["wl"]
+    Lb = wlb.layer(0)
+    hk = np.zeros((wlb.num_rows, HKV, D), np.uint16)
+    hv = np.zeros_like(hk)
+    hk[Lb.slots] = Lb.k
+    hv[Lb.slots] = Lb.v
+    cpu = cpu_baseline_scaled(lambda: oracle.decode_attn_bf16(hk, hv, Lb.q, wlb.req_to_slot, wlb.seq_lens,
+                                                              wlb.q_row_offsets, wlb.sm_scale, HQ),
+                              1, args.layers, "us/step",
+                              f"1 of {args.layers} layers (FP64 decode over {n} BF16 keys), scaled x{args.layers}",
+                              budget)
+    extra = {"num_splits": st["plan"].num_splits, "kv_bytes_per_token_per_layer": HKV * D * 2 * 2,
+             "fp8_kv_bytes_per_token_per_layer": HKV * D * 2 + HKV * 4 * 2}
+    if fp8_ms:
+        extra["fp8_us_per_step"] = fp8_ms * 1e3
+        extra["bf16_over_fp8_time"] = ms / fp8_ms
+    detail_line(f"bf16kv_decode_{n}_b1_{args.layers}layers", ms * 1e3, "us/step",
+                hbm_roof(args.layers * bf16_bytes_per_layer(n), ms, hbm_peak, peak_src, "decode_bf16_kernel<4>"),
+                cpu, extra)
+    del st, g, hk, hv, Lb
     torch.cuda.empty_cache()
 
     # ---- config 3: chunked prefill pipeline, one layer: for each of 4 chunks of 2,048 new tokens,

@@ -33,6 +33,7 @@ EXPORTS = (
     "ftkv_decode_attn", "ftkv_prefill_attn", "ftkv_prefill_attn_ws", "ftkv_prefill_workspace_bytes",
     "ftkv_e4m3_encode_f32", "ftkv_e4m3_decode_f32", "ftkv_pool_bytes", "ftkv_device_errors", "ftkv_status_str",
     "ftkv_last_cuda_error", "ftkv_abi_version", "ftkv_decode_attn_noalloc", "ftkv_decode_attn_store",
+    "ftkv_decode_attn_bf16", "ftkv_gather_bf16",
 )
 
 
@@ -42,6 +43,16 @@ class FtkvPool(ctypes.Structure):
         ("v_codes", ctypes.c_void_p),
         ("k_scales", ctypes.c_void_p),
         ("v_scales", ctypes.c_void_p),
+        ("num_rows", ctypes.c_int64),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+    ]
+
+
+class FtkvBf16Pool(ctypes.Structure):
+    _fields_ = [
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
         ("num_rows", ctypes.c_int64),
         ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
@@ -69,6 +80,7 @@ def load() -> ctypes.CDLL:
         P, I32, I64, F32, SZ, U32 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t,
                                      ctypes.c_uint32)
         PP = ctypes.POINTER(FtkvPool)
+        PB = ctypes.POINTER(FtkvBf16Pool)
         sig = {
             "ftkv_store_quant": (ctypes.c_int, [PP, P, P, P, I64, P]),
             "ftkv_reconstruct_bf16": (ctypes.c_int, [PP, P, I64, P, P, P]),
@@ -78,6 +90,9 @@ def load() -> ctypes.CDLL:
                                                 SZ, P, P]),
             "ftkv_decode_attn_store": (ctypes.c_int, [PP, I32, P, P, P, P, I64, P, P, I32, I64, I32, I64, F32, I64,
                                                       I32, U32, P, SZ, P, P]),
+            "ftkv_decode_attn_bf16": (ctypes.c_int, [PB, I32, P, P, P, P, I64, P, P, I32, I64, I32, I64, F32, I64,
+                                                     I32, U32, P, SZ, P, P]),
+            "ftkv_gather_bf16": (ctypes.c_int, [PB, P, I64, P, P, P]),
             "ftkv_decode_attn_noalloc": (ctypes.c_int, [PP, I32, P, P, I64, P, P, I32, I64, I32, I64, F32, I32, P,
                                                         P]),
             "ftkv_prefill_attn": (ctypes.c_int, [I32, I32, I32, P, P, P, I64, P, P, I64, F32, P, P]),

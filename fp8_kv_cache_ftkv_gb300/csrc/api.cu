@@ -67,6 +67,15 @@ int check_pool(const ftkv_pool* pool) {
   return FTKV_OK;
 }
 
+int check_bf16_pool(const ftkv_bf16_pool* pool) {
+  if (!pool || !pool->k || !pool->v) return FTKV_ERR_INVALID;
+  if (pool->num_rows <= 0 || pool->num_kv_heads <= 0 || pool->num_rows > (int64_t(1) << 31) - 1)
+    return FTKV_ERR_INVALID;
+  if (pool->head_dim != FTKV_HEAD_DIM) return FTKV_ERR_UNSUPPORTED;
+  if (!aligned16(pool->k) || !aligned16(pool->v)) return FTKV_ERR_ALIGN;
+  return FTKV_OK;
+}
+
 int check_heads(int32_t hq, int32_t hkv) {
   if (hq <= 0 || hkv <= 0) return FTKV_ERR_INVALID;
   if (hq % hkv != 0) return FTKV_ERR_UNSUPPORTED;
@@ -184,15 +193,14 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
 
 namespace ftkv {
 
-int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
-                    int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
-                    int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
-                    int64_t window, int32_t num_splits, uint32_t flags, const void* workspace,
-                    size_t workspace_bytes, const uint16_t* out, bool check_workspace, DecodeGeom* geom) {
+int decode_validate_dims(int32_t num_kv_heads, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
+                         int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
+                         int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
+                         int64_t window, int32_t num_splits, uint32_t flags, const void* workspace,
+                         size_t workspace_bytes, const uint16_t* out, bool check_workspace, DecodeGeom* geom) {
   *geom = DecodeGeom{};
-  int st = check_pool(pool);
-  if (st != FTKV_OK) return st;
-  if ((st = check_heads(num_q_heads, pool->num_kv_heads)) != FTKV_OK) return st;
+  int st;
+  if ((st = check_heads(num_q_heads, num_kv_heads)) != FTKV_OK) return st;
   if (batch < 0 || total_q_rows < 0 || max_seq_len < 0 || req_stride < 0) return FTKV_ERR_INVALID;
   if (max_q_rows < 1 || max_q_rows > FTKV_MAX_Q_ROWS) return FTKV_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > FTKV_MAX_SPLITS) return FTKV_ERR_INVALID;
@@ -219,7 +227,7 @@ int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* 
   // (the union of its R rows' windows); the slices cover only those.
   const int64_t span = (window > 0 && window + max_q_rows - 1 < max_seq_len) ? window + max_q_rows - 1 : max_seq_len;
   geom->span = span;
-  if (num_splits == 0) num_splits = ftkv_decode_auto_splits(batch, pool->num_kv_heads, span, max_q_rows);
+  if (num_splits == 0) num_splits = ftkv_decode_auto_splits(batch, num_kv_heads, span, max_q_rows);
   // keys per slice: a multiple of 8 for the single-row kernel (its blocks of 16 keys may end inside a slice),
   // of 16 for the multi-row kernel
   const int64_t align = max_q_rows <= 1 ? 8 : 16;
@@ -227,11 +235,24 @@ int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* 
   chunk = ceil_div(chunk, align) * align;
   geom->chunk = chunk;
   geom->splits = span > 0 ? ceil_div(span, chunk) : 1;
-  geom->need = ftkv_decode_workspace_bytes(num_q_heads, pool->num_kv_heads, FTKV_HEAD_DIM, batch, total_q_rows,
+  geom->need = ftkv_decode_workspace_bytes(num_q_heads, num_kv_heads, FTKV_HEAD_DIM, batch, total_q_rows,
                                            static_cast<int32_t>(geom->splits));
-  geom->parts = total_q_rows * num_q_heads * geom->splits * ftkv::decode_parts_per_slice(1, pool->num_kv_heads);
+  geom->parts = total_q_rows * num_q_heads * geom->splits * ftkv::decode_parts_per_slice(1, num_kv_heads);
   if (check_workspace && workspace_bytes < geom->need) return FTKV_ERR_WORKSPACE;
   return FTKV_OK;
+}
+
+int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
+                    int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
+                    int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
+                    int64_t window, int32_t num_splits, uint32_t flags, const void* workspace,
+                    size_t workspace_bytes, const uint16_t* out, bool check_workspace, DecodeGeom* geom) {
+  *geom = DecodeGeom{};
+  const int st = check_pool(pool);
+  if (st != FTKV_OK) return st;
+  return decode_validate_dims(pool->num_kv_heads, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets,
+                              batch, total_q_rows, max_q_rows, max_seq_len, sm_scale, window, num_splits, flags,
+                              workspace, workspace_bytes, out, check_workspace, geom);
 }
 
 }  // namespace ftkv
@@ -318,6 +339,74 @@ int ftkv_decode_attn_store(const ftkv_pool* pool, int32_t num_q_heads, const uin
   return decode_common(pool, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets, batch, total_q_rows,
                        max_q_rows, max_seq_len, sm_scale, window, num_splits, flags, workspace, workspace_bytes, out,
                        stream, k_new, v_new);
+}
+
+int ftkv_decode_attn_bf16(const ftkv_bf16_pool* pool, int32_t num_q_heads, const uint16_t* q, const uint16_t* k_new,
+                          const uint16_t* v_new, const int32_t* req_to_slot, int64_t req_stride,
+                          const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch, int64_t total_q_rows,
+                          int32_t max_q_rows, int64_t max_seq_len, float sm_scale, int64_t window,
+                          int32_t num_splits, uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out,
+                          void* stream) {
+  int st = check_bf16_pool(pool);
+  if (st != FTKV_OK) return st;
+  ftkv::DecodeGeom geom;
+  st = ftkv::decode_validate_dims(pool->num_kv_heads, num_q_heads, q, req_to_slot, req_stride, seq_lens,
+                                  q_row_offsets, batch, total_q_rows, max_q_rows, max_seq_len, sm_scale, window,
+                                  num_splits, flags, workspace, workspace_bytes, out, true, &geom);
+  if (st != FTKV_OK || geom.empty) return st;
+  if ((k_new == nullptr) != (v_new == nullptr)) return FTKV_ERR_INVALID;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return FTKV_ERR_ALIGN;
+  if (total_q_rows > 65535) return FTKV_ERR_UNSUPPORTED;  // one grid row per query row
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FTKV_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  ftkv::DecodeArgs a{};
+  a.num_rows = pool->num_rows;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.group = num_q_heads / pool->num_kv_heads;
+  a.q = q;
+  a.req_to_slot = req_to_slot;
+  a.req_stride = req_stride;
+  a.seq_lens = seq_lens;
+  a.q_row_offsets = q_row_offsets;
+  a.batch = batch;
+  a.total_q_rows = total_q_rows;
+  a.max_q_rows = max_q_rows;
+  a.max_seq_len = max_seq_len;
+  a.num_splits = static_cast<int>(geom.splits);
+  a.chunk = geom.chunk;
+  a.qk_scale_log2 = sm_scale * 1.4426950408889634f;
+  a.window = window;
+  a.part_acc = static_cast<float*>(workspace);  // the layout ftkv_decode_workspace_bytes sizes
+  a.part_ml = reinterpret_cast<float*>(ws + ws_acc_bytes(geom.parts));
+  a.counters = reinterpret_cast<int*>(ws + ws_acc_bytes(geom.parts) + ws_ml_bytes(geom.parts));
+  a.gbar = a.counters + int64_t(batch) * pool->num_kv_heads;
+  a.out = out;
+  a.err = di->err_word;
+  a.early = (flags & FTKV_DECODE_STABLE_HISTORY) ? 1 : 0;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_bf16 = pool->k;
+  a.v_bf16 = pool->v;
+  cudaError_t e = ftkv::launch_decode_bf16(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FTKV_OK : cuda_fail(e);
+}
+
+int ftkv_gather_bf16(const ftkv_bf16_pool* pool, const int32_t* slots, int64_t num_prefix, uint16_t* ws_k,
+                     uint16_t* ws_v, void* stream) {
+  int st = check_bf16_pool(pool);
+  if (st != FTKV_OK) return st;
+  if (num_prefix < 0) return FTKV_ERR_INVALID;
+  if (num_prefix == 0) return FTKV_OK;
+  if (!slots || !ws_k || !ws_v) return FTKV_ERR_INVALID;
+  if (!aligned16(ws_k) || !aligned16(ws_v) || (reinterpret_cast<uintptr_t>(slots) & 3u)) return FTKV_ERR_ALIGN;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FTKV_OK) return st;
+  ftkv::GatherArgs a{pool->k, pool->v, pool->num_rows, pool->num_kv_heads, slots, num_prefix, ws_k, ws_v,
+                     di->err_word};
+  cudaError_t e = ftkv::launch_gather_bf16(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FTKV_OK : cuda_fail(e);
 }
 
 static int prefill_common(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, const uint16_t* q,

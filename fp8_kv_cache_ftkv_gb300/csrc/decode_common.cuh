@@ -1,5 +1,6 @@
-// decode_common.cuh -- pieces shared by the two split-K decode kernels (decode.cu: one KV head per CTA,
-// multi-row batches; decode_tok.cu: every KV head of a token per CTA, single-row batches).
+// decode_common.cuh -- pieces shared by the split-K decode kernels (decode.cu: one KV head per CTA,
+// multi-row batches; decode_tok.cu: every KV head of a token per CTA, single-row batches; decode_bf16.cu:
+// the same over a BF16 pool).
 //
 // The split merge after a grid barrier (cooperative launches) lives here as well:
 // for each (query row, query head), with per-slice maximum m_s (log2 units), sum l_s and unnormalized
@@ -57,6 +58,30 @@ __device__ __forceinline__ int64_t first_key(const DecodeArgs& a, int64_t n, int
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Barrier of key group gi (named barrier 1 + gi, immediate ids so that only NG + 1 barriers are used).
+template <int NG>
+__device__ __forceinline__ void group_barrier(int gi, int count) {
+  if (NG == 1 || gi == 0) { asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory"); return; }
+  if (NG == 2 || gi == 1) { asm volatile("bar.sync 2, %0;" ::"r"(count) : "memory"); return; }
+  if (NG == 4) {
+    if (gi == 2) asm volatile("bar.sync 3, %0;" ::"r"(count) : "memory");
+    else asm volatile("bar.sync 4, %0;" ::"r"(count) : "memory");
+    return;
+  }
+  switch (gi) {
+    case 2: asm volatile("bar.sync 3, %0;" ::"r"(count) : "memory"); break;
+    case 3: asm volatile("bar.sync 4, %0;" ::"r"(count) : "memory"); break;
+    case 4: asm volatile("bar.sync 5, %0;" ::"r"(count) : "memory"); break;
+    case 5: asm volatile("bar.sync 6, %0;" ::"r"(count) : "memory"); break;
+    case 6: asm volatile("bar.sync 7, %0;" ::"r"(count) : "memory"); break;
+    default: asm volatile("bar.sync 8, %0;" ::"r"(count) : "memory"); break;
+  }
+}
+
+__device__ __forceinline__ float exp2i(int e) {  // 2^e for -126 <= e <= 127, exact
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
 // ---- merge of one output item: (query row t, query head qh, 4 of the 128 d), by one warp ----
@@ -190,6 +215,18 @@ __device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
     for (int64_t it = cta + static_cast<int64_t>(ncta) * warp; it < items; it += static_cast<int64_t>(ncta) * WARPS)
       merge_item<10>(a, it, lane);
   }
+}
+
+// ---- the split merge as a kernel of its own, launched right behind a split-K decode kernel whose grid does not
+// fit on the GPU at once (no cooperative launch, hence no grid barrier).  One warp per output item (query row,
+// query head, 4 of the 128 d); the grid waits for the decode kernel (programmatic dependent launch). ----
+constexpr int kMergeWarps = 4;  // warps per merge CTA
+template <int MW>
+__global__ void __launch_bounds__(MW * 32) decode_merge_kernel(const DecodeArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int64_t it = static_cast<int64_t>(blockIdx.x) * MW + (threadIdx.x >> 5);
+  if (it < a.total_q_rows * a.num_q_heads * (kHeadDim / 4)) merge_item<10>(a, it, threadIdx.x & 31);
 }
 
 }  // namespace ftkv

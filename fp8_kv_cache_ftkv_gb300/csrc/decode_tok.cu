@@ -92,30 +92,6 @@ __device__ __forceinline__ uint32_t tv_off(int key, int hd, int p) {
   return Tok<HC>::V_OFF + key * Tok<HC>::RUN + hd * kHeadDim + ((p ^ (((key >> 1) & 3) << 1)) << 4);
 }
 
-// Barrier of key group gi (named barrier 1 + gi, immediate ids so that only NG + 1 barriers are used).
-template <int NG>
-__device__ __forceinline__ void group_barrier(int gi, int count) {
-  if (NG == 1 || gi == 0) { asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory"); return; }
-  if (NG == 2 || gi == 1) { asm volatile("bar.sync 2, %0;" ::"r"(count) : "memory"); return; }
-  if (NG == 4) {
-    if (gi == 2) asm volatile("bar.sync 3, %0;" ::"r"(count) : "memory");
-    else asm volatile("bar.sync 4, %0;" ::"r"(count) : "memory");
-    return;
-  }
-  switch (gi) {
-    case 2: asm volatile("bar.sync 3, %0;" ::"r"(count) : "memory"); break;
-    case 3: asm volatile("bar.sync 4, %0;" ::"r"(count) : "memory"); break;
-    case 4: asm volatile("bar.sync 5, %0;" ::"r"(count) : "memory"); break;
-    case 5: asm volatile("bar.sync 6, %0;" ::"r"(count) : "memory"); break;
-    case 6: asm volatile("bar.sync 7, %0;" ::"r"(count) : "memory"); break;
-    default: asm volatile("bar.sync 8, %0;" ::"r"(count) : "memory"); break;
-  }
-}
-
-__device__ __forceinline__ float exp2i(int e) {  // 2^e for -126 <= e <= 127, exact
-  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-}
-
 template <int HC>
 __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs a) {
   using T = Tok<HC>;
@@ -534,17 +510,6 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
   if (a.coop) coop_finish<TW>(a);  // grid barrier, then the merge spread over the grid
 }
 
-// ---- the split merge as a kernel of its own, launched right behind decode_tok_kernel when its grid does not
-// fit on the GPU at once (no cooperative launch, hence no grid barrier).  One warp per output item (query row,
-// query head, 4 of the 128 d); the grid waits for the decode kernel (programmatic dependent launch). ----
-constexpr int MW = 4;  // warps per merge CTA
-__global__ void __launch_bounds__(MW * 32) decode_merge_kernel(const DecodeArgs a) {
-  griddep_launch_dependents();
-  griddep_wait();
-  const int64_t it = static_cast<int64_t>(blockIdx.x) * MW + (threadIdx.x >> 5);
-  if (it < a.total_q_rows * a.num_q_heads * (kHeadDim / 4)) merge_item<10>(a, it, threadIdx.x & 31);
-}
-
 template <int HC>
 cudaError_t launch_tok(const DecodeArgs& a, cudaStream_t s, int dev) {
   static std::once_flag once[kMaxDecodeDevices];
@@ -572,7 +537,8 @@ cudaError_t launch_tok(const DecodeArgs& a, cudaStream_t s, int dev) {
   cudaError_t e = launch_k(decode_tok_kernel<HC>, grid, dim3(TW * 32), Tok<HC>::SMEM, s, c);
   if (e != cudaSuccess) return e;
   const int64_t items = a.total_q_rows * a.num_q_heads * (kHeadDim / 4);
-  return launch_k(decode_merge_kernel, dim3(static_cast<unsigned>((items + MW - 1) / MW)), dim3(MW * 32), 0, s, c);
+  return launch_k(decode_merge_kernel<kMergeWarps>, dim3(static_cast<unsigned>((items + kMergeWarps - 1) / kMergeWarps)),
+                  dim3(kMergeWarps * 32), 0, s, c);
 }
 
 }  // namespace

@@ -76,6 +76,21 @@ struct DecodeArgs {
                              // previous call's barrier completed (zero-filled once; no reset between calls)
   const uint16_t* k_new;     // fused store: [total_q_rows][Hkv][128] K of the new tokens, or null
   const uint16_t* v_new;     //              V of the new tokens
+  const uint16_t* k_bf16;    // BF16 pool (decode_bf16 only): [num_rows][Hkv][128] K rows
+  const uint16_t* v_bf16;    //                               V rows
+};
+
+// Prefix gather from a BF16 pool into the shared workspace (the BF16 counterpart of reconstruction).
+struct GatherArgs {
+  const uint16_t* k;         // [num_rows][Hkv][128]
+  const uint16_t* v;
+  int64_t num_rows;
+  int num_kv_heads;
+  const int32_t* slots;      // [num_prefix]
+  int64_t num_prefix;
+  uint16_t* ws_k;            // [num_prefix][Hkv][128]
+  uint16_t* ws_v;
+  int* err;
 };
 
 struct PrefillArgs {
@@ -145,6 +160,9 @@ cudaError_t launch_e4m3_decode(const uint8_t* c, float* x, int64_t n, int num_sm
 // one KV head per CTA (decode.cu).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tok(const DecodeArgs& a, cudaStream_t s);
+// Decode over a BF16 pool (bf16_pool.cu): one grid row per query row, any number of rows per request.
+cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_gather_bf16(const GatherArgs& a, cudaStream_t s);
 int decode_ctas_per_sm(int max_q_rows);
 int decode_tok_heads_per_cta(int num_kv_heads);
 // Partials per key slice: the single-row kernel publishes one per key group of a CTA.
@@ -162,6 +180,14 @@ struct DecodeGeom {
   size_t need = 0;      // workspace bytes
   bool empty = false;   // nothing to compute (batch or total_q_rows is 0)
 };
+// Every argument check of a decode call except the pool's (the caller checks its pool first), and the split
+// geometry.
+int decode_validate_dims(int32_t num_kv_heads, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
+                         int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
+                         int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
+                         int64_t window, int32_t num_splits, uint32_t flags, const void* workspace,
+                         size_t workspace_bytes, const uint16_t* out, bool check_workspace, DecodeGeom* geom);
+// The FP8 pool's checks, then decode_validate_dims.
 int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
                     int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                     int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,

@@ -12,7 +12,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import FtkvPool, check
+from ._lib import FtkvBf16Pool, FtkvPool, check
 
 HEAD_DIM = 128
 
@@ -69,6 +69,33 @@ class KVPool:
         return FtkvPool(self.k_codes.data_ptr(), self.v_codes.data_ptr(), self.k_scales.data_ptr(),
                         self.v_scales.data_ptr(), self.k_codes.shape[0], self.k_codes.shape[1],
                         self.k_codes.shape[2])
+
+
+@dataclass
+class BF16Pool:
+    """One layer's unquantized pool on the GPU (the comparison point): K and V bfloat16 [rows, Hkv, 128]."""
+    k: torch.Tensor
+    v: torch.Tensor
+
+    @staticmethod
+    def empty(num_rows: int, num_kv_heads: int, device="cuda", head_dim: int = HEAD_DIM) -> "BF16Pool":
+        return BF16Pool(torch.zeros(num_rows, num_kv_heads, head_dim, dtype=torch.bfloat16, device=device),
+                        torch.zeros(num_rows, num_kv_heads, head_dim, dtype=torch.bfloat16, device=device))
+
+    @property
+    def num_rows(self) -> int:
+        return self.k.shape[0]
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.k.shape[1]
+
+    def c_struct(self) -> FtkvBf16Pool:
+        _req(self.k, torch.bfloat16, "k", 3)
+        _req(self.v, torch.bfloat16, "v", 3)
+        if self.v.shape != self.k.shape:
+            raise ValueError("k and v pools disagree")
+        return FtkvBf16Pool(self.k.data_ptr(), self.v.data_ptr(), self.k.shape[0], self.k.shape[1], self.k.shape[2])
 
 
 def store_quant(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slots: torch.Tensor, stream=None) -> None:
@@ -179,6 +206,65 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
         flags,
         _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)), "ftkv_decode_attn")
     return out
+
+
+def decode_attn_bf16(pool: BF16Pool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,
+                     q_row_offsets: torch.Tensor = None, *, max_seq_len: int, max_q_rows: int = 1,
+                     sm_scale: float = HEAD_DIM ** -0.5, window: int = 0, num_splits: int = 0,
+                     plan: DecodePlan = None, out: torch.Tensor = None, k_new: torch.Tensor = None,
+                     v_new: torch.Tensor = None, stable_history: bool = False, stream=None) -> torch.Tensor:
+    """Split-K decode attention over a BF16 pool (``ftkv_decode_attn_bf16``); the arguments of ``decode_attn``.
+    ``k_new``/``v_new``: the new tokens' rows are copied into the pool and attended from these tensors."""
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    _req(q, torch.bfloat16, "q", 3)
+    if req_to_slot.dim() == 1:
+        req_to_slot = req_to_slot.view(1, -1)
+    _req(req_to_slot, torch.int32, "req_to_slot", 2)
+    _req(seq_lens, torch.int32, "seq_lens", 1)
+    if q_row_offsets is not None:
+        _req(q_row_offsets, torch.int32, "q_row_offsets", 1)
+    batch = seq_lens.shape[0]
+    total, hq, _ = q.shape
+    if k_new is not None:
+        _req(k_new, torch.bfloat16, "k_new", 3)
+        _req(v_new, torch.bfloat16, "v_new", 3)
+        if k_new.shape != (total, pool.num_kv_heads, HEAD_DIM) or v_new.shape != k_new.shape:
+            raise ValueError(f"k_new/v_new must be [{total}, {pool.num_kv_heads}, {HEAD_DIM}]")
+    if plan is None:
+        plan = DecodePlan(hq, pool.num_kv_heads, batch, total, max_q_rows, max_seq_len, num_splits, q.device,
+                          window)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, torch.bfloat16, "out", 3)
+    flags = _lib.FTKV_DECODE_STABLE_HISTORY if stable_history else 0
+    ps = pool.c_struct()
+    check(_lib.load().ftkv_decode_attn_bf16(
+        ctypes.byref(ps), hq, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(req_to_slot), req_to_slot.shape[1],
+        _ptr(seq_lens), _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale), int(window),
+        plan.num_splits, flags, _ptr(plan.workspace), plan.workspace.numel(), _ptr(out), _stream_ptr(stream)),
+        "ftkv_decode_attn_bf16")
+    return out
+
+
+def gather_bf16(pool: BF16Pool, slots: torch.Tensor, ws_k: torch.Tensor = None, ws_v: torch.Tensor = None,
+                stream=None):
+    """Gather BF16 pool rows ``slots`` (logical order) into workspaces [P, Hkv, 128]; returns (ws_k, ws_v)."""
+    _req(slots, torch.int32, "slots", 1)
+    P = slots.shape[0]
+    shape = (P, pool.num_kv_heads, HEAD_DIM)
+    if ws_k is None:
+        ws_k = torch.empty(shape, dtype=torch.bfloat16, device=slots.device)
+    if ws_v is None:
+        ws_v = torch.empty(shape, dtype=torch.bfloat16, device=slots.device)
+    _req(ws_k, torch.bfloat16, "ws_k", 3)
+    _req(ws_v, torch.bfloat16, "ws_v", 3)
+    if ws_k.shape[0] < P or ws_v.shape[0] < P:
+        raise ValueError("workspace too small")
+    ps = pool.c_struct()
+    check(_lib.load().ftkv_gather_bf16(ctypes.byref(ps), _ptr(slots), P, _ptr(ws_k), _ptr(ws_v),
+                                       _stream_ptr(stream)), "ftkv_gather_bf16")
+    return ws_k, ws_v
 
 
 def prefill_workspace_bytes(max_ctas: int = 0) -> int:

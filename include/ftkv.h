@@ -213,6 +213,53 @@ int ftkv_decode_attn_noalloc(const ftkv_pool* pool, int32_t num_q_heads, const u
                              uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * The BF16 comparison point: the same decode and the prefill's prefix read over an unquantized BF16
+ * pool, FreeToken's default KV format ("KV_FMT none" among the kernel variants of [#897] opening
+ * description; FP8 is opt-in, [#853 "What changes"]).  The pages weigh FP8 against it by bytes per
+ * token ([#853 "Validation"]: 98,304 BF16 vs 50,688 FP8) and by speed; these entry points let the two
+ * formats run side by side on one GPU.
+ *   k, v : device BF16 [num_rows][num_kv_heads][head_dim] K and V rows, caller-owned, 16-byte aligned
+ * --------------------------------------------------------------------------------------------- */
+typedef struct ftkv_bf16_pool {
+  uint16_t* k;
+  uint16_t* v;
+  int64_t num_rows;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+} ftkv_bf16_pool;
+
+/* Decode attention over a BF16 pool: for every query row, per query head i (KV head i / G),
+ * o = sum_j softmax(q . k_j * sm_scale)_j v_j over the row's visible keys -- the values ftkv_decode_attn
+ * computes from dequantized rows, here from the BF16 rows themselves.  Every argument, layout, flag, the
+ * window, the split geometry, the workspace (ftkv_decode_workspace_bytes) and the errors are those of
+ * ftkv_decode_attn, with these differences:
+ *   k_new, v_new : both NULL (the new tokens' rows are already in the pool), or device BF16
+ *                  [total_q_rows][num_kv_heads][head_dim]: query row r of request b (R rows) is the token at
+ *                  position seq_lens[b] - R + r; its K/V rows are copied (bit for bit) to pool row
+ *                  req_to_slot[b * req_stride + position], and the attention reads the new tokens from k_new /
+ *                  v_new.  One NULL and the other not -> FTKV_ERR_INVALID.
+ *   Every query row runs as its own set of CTAs (multi-row requests re-read their keys per row);
+ *   total_q_rows above 65,535 -> FTKV_ERR_UNSUPPORTED.  FTKV_DECODE_STABLE_HISTORY takes effect only with
+ *   q_row_offsets NULL.
+ * --------------------------------------------------------------------------------------------- */
+int ftkv_decode_attn_bf16(const ftkv_bf16_pool* pool, int32_t num_q_heads, const uint16_t* q,
+                          const uint16_t* k_new, const uint16_t* v_new, const int32_t* req_to_slot,
+                          int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets,
+                          int32_t batch, int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len,
+                          float sm_scale, int64_t window, int32_t num_splits, uint32_t flags,
+                          void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
+
+/* Prefix gather from a BF16 pool into the shared BF16 workspace, in logical order: the BF16 pool's
+ * counterpart of ftkv_reconstruct_bf16, ahead of ftkv_prefill_attn / ftkv_prefill_attn_ws.
+ *   slots      : device int32 [num_prefix] (4-byte aligned); logical token i lives in pool row slots[i]
+ *   ws_k, ws_v : device BF16 [num_prefix][num_kv_heads][head_dim]; ws[i][h][:] = pool[slots[i]][h][:]
+ * A slot outside the pool is flagged (FTKV_DEVERR_BAD_SLOT) and its workspace rows are written as zeros.
+ * num_prefix == 0 is a no-op.
+ * --------------------------------------------------------------------------------------------- */
+int ftkv_gather_bf16(const ftkv_bf16_pool* pool, const int32_t* slots, int64_t num_prefix,
+                     uint16_t* ws_k, uint16_t* ws_v, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Prefill (extend) attention of the current chunk over the reconstructed BF16 prefix plus the BF16
  * chunk itself ([#853 "What changes"]: current-chunk K/V remains BF16; [#853 "Paired end-to-end
  * A/B"]: the historical-prefix + new-token operator).

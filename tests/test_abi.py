@@ -189,3 +189,43 @@ def test_codec_validation(lib):
     assert lib.ftkv_e4m3_encode_f32(None, None, 0, None) == _lib.FTKV_OK
     assert lib.ftkv_e4m3_encode_f32(None, 0x1000, 4, None) == _lib.FTKV_ERR_INVALID
     assert lib.ftkv_e4m3_decode_f32(0x1000, 0x2002, 4, None) == _lib.FTKV_ERR_ALIGN
+
+
+def _bpool(k=0x10000, v=0x20000, rows=100, hkv=4, d=128):
+    return _lib.FtkvBf16Pool(k, v, rows, hkv, d)
+
+
+def test_bf16_pool_validation(lib):
+    """The BF16-pool entry points check their pool, then every decode check of ftkv_decode_attn."""
+    P = ctypes.byref
+    ws = lib.ftkv_decode_workspace_bytes(32, 4, 128, 1, 1, 4)
+    base = dict(q=0x1000, kn=None, vn=None, r2s=0x2000, stride=64, lens=0x3000, offs=None, B=1, total=1, mq=1,
+                maxlen=64, sm=0.0884, win=0, splits=4, flags=0, ws=0x100000, wsb=ws, out=0x4000)
+
+    def call(pool=None, hq=32, **kw):
+        a = dict(base, **kw)
+        return lib.ftkv_decode_attn_bf16(P(pool or _bpool()), hq, a["q"], a["kn"], a["vn"], a["r2s"], a["stride"],
+                                         a["lens"], a["offs"], a["B"], a["total"], a["mq"], a["maxlen"], a["sm"],
+                                         a["win"], a["splits"], a["flags"], a["ws"], a["wsb"], a["out"], None)
+
+    assert call(pool=_bpool(k=0)) == _lib.FTKV_ERR_INVALID          # null pool array
+    assert call(pool=_bpool(rows=0)) == _lib.FTKV_ERR_INVALID
+    assert call(pool=_bpool(d=256)) == _lib.FTKV_ERR_UNSUPPORTED
+    assert call(pool=_bpool(v=0x20008)) == _lib.FTKV_ERR_ALIGN
+    assert call(hq=24) == _lib.FTKV_ERR_UNSUPPORTED                  # group 6
+    assert call(mq=9) == _lib.FTKV_ERR_UNSUPPORTED
+    assert call(win=-1) == _lib.FTKV_ERR_INVALID
+    assert call(q=0x1002) == _lib.FTKV_ERR_ALIGN
+    assert call(wsb=255) == _lib.FTKV_ERR_WORKSPACE
+    assert call(kn=0x7000) == _lib.FTKV_ERR_INVALID                 # k_new without v_new
+    assert call(kn=0x7000, vn=0x8008) == _lib.FTKV_ERR_ALIGN
+    assert call(B=70000, total=70000, wsb=1 << 40) == _lib.FTKV_ERR_UNSUPPORTED  # one grid row per query row
+    assert call(B=0, total=0) == _lib.FTKV_OK
+
+    g = lib.ftkv_gather_bf16
+    assert g(P(_bpool()), 0x3000, -1, 0x5000, 0x6000, None) == _lib.FTKV_ERR_INVALID
+    assert g(P(_bpool()), None, 5, 0x5000, 0x6000, None) == _lib.FTKV_ERR_INVALID
+    assert g(P(_bpool()), 0x3002, 5, 0x5000, 0x6000, None) == _lib.FTKV_ERR_ALIGN
+    assert g(P(_bpool()), 0x3000, 5, 0x5008, 0x6000, None) == _lib.FTKV_ERR_ALIGN
+    assert g(P(_bpool(d=64)), 0x3000, 5, 0x5000, 0x6000, None) == _lib.FTKV_ERR_UNSUPPORTED
+    assert g(P(_bpool()), None, 0, None, None, None) == _lib.FTKV_OK
