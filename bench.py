@@ -57,6 +57,9 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-details", action="store_true", help="headline line only")
     p.add_argument("--details-only", action="store_true", help="detail lines only (no headline)")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timings (profiling runs)")
+    p.add_argument("--detail", default="", help="comma-separated detail lines to run (default all): config0, "
+                   "config1, config2_40k, bf16kv, config3, reconstruct, config4")
     p.add_argument("--cpu-budget-s", type=float, default=20.0, help="bound on the oracle time of a sample")
     return p.parse_args()
 
@@ -196,9 +199,14 @@ def cpu_decode_layer_fn(context, pool_rows, layer=0):
     return run
 
 
+SKIP_CPU = False  # --no-cpu-baseline (profiling runs): cpu_baseline is null
+
+
 def cpu_baseline_scaled(fn, units_in_sample, units_in_metric, unit, sample, budget_s, to_unit=1e6):
     """Time fn (one sample) on all host cores and on one thread (if that takes at most budget_s); scale the
     seconds to the metric's unit (to_unit: 1e6 for microseconds) and from the sample to the metric."""
+    if SKIP_CPU:
+        return None
     ncores = os.cpu_count() or 1
     cores = oracle_threads(ncores)
     t_all = timed_min(fn)
@@ -421,7 +429,7 @@ def run_headline(args, world, rank, local, torch, ops, inputs, device, stream, h
         e2e = {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not SKIP_CPU:
         fn = cpu_decode_layer_fn(n, args.pool_rows)
         cpu = cpu_baseline_scaled(fn, 1, args.layers, "us/step",
                                   f"1 of {args.layers} layers (store of the new token + FP64 decode over {n} keys), "
@@ -474,217 +482,230 @@ def run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, p
     import oracle
     to_dev = to_dev_fn(torch, device)
     budget = args.cpu_budget_s
+    chosen = set(args.detail.split(",")) if args.detail else None
+
+    def want(key):
+        return chosen is None or key in chosen
     steps, warm = max(20, args.steps // 4), 5
 
     # ---- config 0: one decode step, one layer, 512 keys in a 1,024-row pool (latency-dominated) ----
-    wl = inputs.decode_small()
-    L = wl.layer(0)
-    n = int(wl.seq_lens[0])
-    pool = ops.KVPool.empty(wl.num_rows, wl.Hkv, device=device)
-    ops.store_quant(pool, to_dev(L.k[:n - 1]), to_dev(L.v[:n - 1]), torch.from_numpy(L.slots[:n - 1]).to(device))
-    qd, kn, vn = to_dev(L.q), to_dev(L.k[n - 1:n]), to_dev(L.v[n - 1:n])
-    r2s, lens = torch.from_numpy(wl.req_to_slot).to(device), torch.from_numpy(wl.seq_lens).to(device)
-    plan = ops.DecodePlan(HQ, HKV, 1, 1, 1, n, 0, device)
-    out = torch.empty_like(qd)
-    g = graph_of(torch, stream, lambda: ops.decode_attn(pool, qd, r2s, lens, None, max_seq_len=n, plan=plan, out=out,
-                                                         k_new=kn, v_new=vn))
-    ms, clk = time_graph(torch, stream, g, steps, warm)
-    op = oracle.Pool(wl.num_rows, wl.Hkv, D)
-    oracle.store_quant(op, L.k, L.v, L.slots)
-    cpu = cpu_baseline_scaled(lambda: oracle.decode_attn(op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets,
-                                                         wl.sm_scale, HQ), 1, 1, "us/call", "the whole call", budget)
-    detail_line("config0_decode_512_b1", ms * 1e3, "us/call",
-                hbm_roof(decode_bytes_per_layer(n), ms, hbm_peak, peak_src, "decode_tok_kernel<4>"), cpu,
-                {"note": "one launch of 0.56 MB: latency-bound and L2-warm across replays"})
-    del pool, g
+    if want("config0"):
+        wl = inputs.decode_small()
+        L = wl.layer(0)
+        n = int(wl.seq_lens[0])
+        pool = ops.KVPool.empty(wl.num_rows, wl.Hkv, device=device)
+        ops.store_quant(pool, to_dev(L.k[:n - 1]), to_dev(L.v[:n - 1]), torch.from_numpy(L.slots[:n - 1]).to(device))
+        qd, kn, vn = to_dev(L.q), to_dev(L.k[n - 1:n]), to_dev(L.v[n - 1:n])
+        r2s, lens = torch.from_numpy(wl.req_to_slot).to(device), torch.from_numpy(wl.seq_lens).to(device)
+        plan = ops.DecodePlan(HQ, HKV, 1, 1, 1, n, 0, device)
+        out = torch.empty_like(qd)
+        g = graph_of(torch, stream, lambda: ops.decode_attn(pool, qd, r2s, lens, None, max_seq_len=n, plan=plan, out=out,
+                                                             k_new=kn, v_new=vn))
+        ms, clk = time_graph(torch, stream, g, steps, warm)
+        op = oracle.Pool(wl.num_rows, wl.Hkv, D)
+        oracle.store_quant(op, L.k, L.v, L.slots)
+        cpu = cpu_baseline_scaled(lambda: oracle.decode_attn(op, L.q, wl.req_to_slot, wl.seq_lens, wl.q_row_offsets,
+                                                             wl.sm_scale, HQ), 1, 1, "us/call", "the whole call", budget)
+        detail_line("config0_decode_512_b1", ms * 1e3, "us/call",
+                    hbm_roof(decode_bytes_per_layer(n), ms, hbm_peak, peak_src, "decode_tok_kernel<4>"), cpu,
+                    {"note": "one launch of 0.56 MB: latency-bound and L2-warm across replays"})
+        del pool, g
 
     # ---- config 1: quantize-on-write, 8,192 tokens x 48 layers into 48 distinct 33,059-row pools ----
-    sw = inputs.store(layers=48)
-    slots = torch.from_numpy(sw.slots).to(device)
-    kv = []
-    for l in range(sw.layers):
-        k, v = sw.layer(l)
-        kv.append((to_dev(k), to_dev(v)))
-    pools = [ops.KVPool.empty(sw.num_rows, HKV, device=device) for _ in range(sw.layers)]
+    if want("config1"):
+        sw = inputs.store(layers=48)
+        slots = torch.from_numpy(sw.slots).to(device)
+        kv = []
+        for l in range(sw.layers):
+            k, v = sw.layer(l)
+            kv.append((to_dev(k), to_dev(v)))
+        pools = [ops.KVPool.empty(sw.num_rows, HKV, device=device) for _ in range(sw.layers)]
 
-    def store_all():
-        for (k, v), p in zip(kv, pools):
-            ops.store_quant(p, k, v, slots)
-    g = graph_of(torch, stream, store_all)
-    ms, _ = time_graph(torch, stream, g, steps, warm)
-    T = sw.slots.shape[0]
-    nbytes = sw.layers * (T * HKV * D * 2 * 2 + T * (HKV * D + HKV * 4) * 2 + T * 4)
-    k0, v0 = sw.layer(0)
-    op = oracle.Pool(sw.num_rows, HKV, D)
-    cpu = cpu_baseline_scaled(lambda: oracle.store_quant(op, k0, v0, sw.slots), 1, sw.layers, "us/step",
-                              f"1 of {sw.layers} layers (8,192 tokens), scaled x{sw.layers}", budget)
-    detail_line("config1_store_8192x48", ms * 1e3, "us/step", hbm_roof(nbytes, ms, hbm_peak, peak_src, "store_quant_kernel"),
-                cpu, {"note": "48 distinct destination pools (1.67 GB): the written rows leave L2"})
-    del kv, pools, g
-    torch.cuda.empty_cache()
+        def store_all():
+            for (k, v), p in zip(kv, pools):
+                ops.store_quant(p, k, v, slots)
+        g = graph_of(torch, stream, store_all)
+        ms, _ = time_graph(torch, stream, g, steps, warm)
+        T = sw.slots.shape[0]
+        nbytes = sw.layers * (T * HKV * D * 2 * 2 + T * (HKV * D + HKV * 4) * 2 + T * 4)
+        k0, v0 = sw.layer(0)
+        op = oracle.Pool(sw.num_rows, HKV, D)
+        cpu = cpu_baseline_scaled(lambda: oracle.store_quant(op, k0, v0, sw.slots), 1, sw.layers, "us/step",
+                                  f"1 of {sw.layers} layers (8,192 tokens), scaled x{sw.layers}", budget)
+        detail_line("config1_store_8192x48", ms * 1e3, "us/step", hbm_roof(nbytes, ms, hbm_peak, peak_src, "store_quant_kernel"),
+                    cpu, {"note": "48 distinct destination pools (1.67 GB): the written rows leave L2"})
+        del kv, pools, g
+        torch.cuda.empty_cache()
 
     # ---- config 2 at 40,000 keys in 40,290-row pools, 48 layers ----
-    st = build_decode(args, torch, ops, inputs, device, context=40000, pool_rows=40290)
-    g = graph_of(torch, stream, st["step"])
-    ms, _ = time_graph(torch, stream, g, steps, warm)
-    fn = cpu_decode_layer_fn(40000, 40290)
-    cpu = cpu_baseline_scaled(fn, 1, args.layers, "us/step",
-                              f"1 of {args.layers} layers (store + FP64 decode over 40000 keys), scaled x{args.layers}",
-                              budget)
-    detail_line("config2_decode_40000_b1_48layers", ms * 1e3, "us/step",
-                hbm_roof(args.layers * decode_bytes_per_layer(40000), ms, hbm_peak, peak_src, "decode_tok_kernel<4>"),
-                cpu, {"num_splits": st["plan"].num_splits})
-    del st, g
-    torch.cuda.empty_cache()
+    if want("config2_40k"):
+        st = build_decode(args, torch, ops, inputs, device, context=40000, pool_rows=40290)
+        g = graph_of(torch, stream, st["step"])
+        ms, _ = time_graph(torch, stream, g, steps, warm)
+        fn = cpu_decode_layer_fn(40000, 40290)
+        cpu = cpu_baseline_scaled(fn, 1, args.layers, "us/step",
+                                  f"1 of {args.layers} layers (store + FP64 decode over 40000 keys), scaled x{args.layers}",
+                                  budget)
+        detail_line("config2_decode_40000_b1_48layers", ms * 1e3, "us/step",
+                    hbm_roof(args.layers * decode_bytes_per_layer(40000), ms, hbm_peak, peak_src, "decode_tok_kernel<4>"),
+                    cpu, {"num_splits": st["plan"].num_splits})
+        del st, g
+        torch.cuda.empty_cache()
 
     # ---- the BF16-KV comparison point: the headline step (32K keys, batch 1, 48 layers, fused new-token write,
-    # stable history) over BF16 pools ----
-    st = build_decode_bf16(args, torch, ops, inputs, device)
-    g = graph_of(torch, stream, st["step"])
-    ms, _ = time_graph(torch, stream, g, steps, warm)
-    n = args.context
-    wlb = st["wl"]
-    Lb = wlb.layer(0)
-    hk = np.zeros((wlb.num_rows, HKV, D), np.uint16)
-    hv = np.zeros_like(hk)
-    hk[Lb.slots] = Lb.k
-    hv[Lb.slots] = Lb.v
-    cpu = cpu_baseline_scaled(lambda: oracle.decode_attn_bf16(hk, hv, Lb.q, wlb.req_to_slot, wlb.seq_lens,
-                                                              wlb.q_row_offsets, wlb.sm_scale, HQ),
-                              1, args.layers, "us/step",
-                              f"1 of {args.layers} layers (FP64 decode over {n} BF16 keys), scaled x{args.layers}",
-                              budget)
-    extra = {"num_splits": st["plan"].num_splits, "kv_bytes_per_token_per_layer": HKV * D * 2 * 2,
-             "fp8_kv_bytes_per_token_per_layer": HKV * D * 2 + HKV * 4 * 2}
-    if fp8_ms:
-        extra["fp8_us_per_step"] = fp8_ms * 1e3
-        extra["bf16_over_fp8_time"] = ms / fp8_ms
-    detail_line(f"bf16kv_decode_{n}_b1_{args.layers}layers", ms * 1e3, "us/step",
-                hbm_roof(args.layers * bf16_bytes_per_layer(n), ms, hbm_peak, peak_src, "decode_bf16_kernel<4>"),
-                cpu, extra)
-    del st, g, hk, hv, Lb
-    torch.cuda.empty_cache()
+    if want("bf16kv"):
+        # stable history) over BF16 pools ----
+        st = build_decode_bf16(args, torch, ops, inputs, device)
+        g = graph_of(torch, stream, st["step"])
+        ms, _ = time_graph(torch, stream, g, steps, warm)
+        n = args.context
+        wlb = st["wl"]
+        Lb = wlb.layer(0)
+        hk = np.zeros((wlb.num_rows, HKV, D), np.uint16)
+        hv = np.zeros_like(hk)
+        hk[Lb.slots] = Lb.k
+        hv[Lb.slots] = Lb.v
+        cpu = cpu_baseline_scaled(lambda: oracle.decode_attn_bf16(hk, hv, Lb.q, wlb.req_to_slot, wlb.seq_lens,
+                                                                  wlb.q_row_offsets, wlb.sm_scale, HQ),
+                                  1, args.layers, "us/step",
+                                  f"1 of {args.layers} layers (FP64 decode over {n} BF16 keys), scaled x{args.layers}",
+                                  budget)
+        extra = {"num_splits": st["plan"].num_splits, "kv_bytes_per_token_per_layer": HKV * D * 2 * 2,
+                 "fp8_kv_bytes_per_token_per_layer": HKV * D * 2 + HKV * 4 * 2}
+        if fp8_ms:
+            extra["fp8_us_per_step"] = fp8_ms * 1e3
+            extra["bf16_over_fp8_time"] = ms / fp8_ms
+        detail_line(f"bf16kv_decode_{n}_b1_{args.layers}layers", ms * 1e3, "us/step",
+                    hbm_roof(args.layers * bf16_bytes_per_layer(n), ms, hbm_peak, peak_src, "decode_bf16_kernel<4>"),
+                    cpu, extra)
+        del st, g, hk, hv, Lb
+        torch.cuda.empty_cache()
 
     # ---- config 3: chunked prefill pipeline, one layer: for each of 4 chunks of 2,048 new tokens,
-    # reconstruct the FP8 prefix into the BF16 workspace, prefill the chunk, quantize-on-write the chunk ----
-    pw = inputs.prefill()
-    pool = ops.KVPool.empty(pw.num_rows, HKV, device=device)
-    hist = torch.from_numpy(pw.hist_slots).to(device)
-    ops.store_quant(pool, to_dev(pw.hist_k), to_dev(pw.hist_v), hist)
-    slots_all = torch.from_numpy(np.concatenate([pw.hist_slots, pw.new_slots])).to(device)
-    qd, kd, vd = to_dev(pw.q), to_dev(pw.k), to_dev(pw.v)
-    H, C = pw.hist_slots.shape[0], pw.chunk
-    ws_k = torch.empty(H + 3 * C, HKV, D, dtype=torch.bfloat16, device=device)
-    ws_v = torch.empty_like(ws_k)
-    outp = torch.empty_like(qd)
-    pplan = ops.PrefillPlan(0, device)
+    if want("config3"):
+        # reconstruct the FP8 prefix into the BF16 workspace, prefill the chunk, quantize-on-write the chunk ----
+        pw = inputs.prefill()
+        pool = ops.KVPool.empty(pw.num_rows, HKV, device=device)
+        hist = torch.from_numpy(pw.hist_slots).to(device)
+        ops.store_quant(pool, to_dev(pw.hist_k), to_dev(pw.hist_v), hist)
+        slots_all = torch.from_numpy(np.concatenate([pw.hist_slots, pw.new_slots])).to(device)
+        qd, kd, vd = to_dev(pw.q), to_dev(pw.k), to_dev(pw.v)
+        H, C = pw.hist_slots.shape[0], pw.chunk
+        ws_k = torch.empty(H + 3 * C, HKV, D, dtype=torch.bfloat16, device=device)
+        ws_v = torch.empty_like(ws_k)
+        outp = torch.empty_like(qd)
+        pplan = ops.PrefillPlan(0, device)
 
-    def pipeline():
-        for c in range(pw.num_chunks):
-            c0, c1 = c * C, (c + 1) * C
-            P = H + c0
-            ops.reconstruct_bf16(pool, slots_all[:P], ws_k[:P], ws_v[:P])
-            ops.prefill_attn(qd[c0:c1], kd[c0:c1], vd[c0:c1], ws_k[:P], ws_v[:P], out=outp[c0:c1], plan=pplan)
-            ops.store_quant(pool, kd[c0:c1], vd[c0:c1], slots_all[P:P + C])
-    g = graph_of(torch, stream, pipeline)
-    ms, _ = time_graph(torch, stream, g, max(10, steps // 4), 3)
-    flops = sum((C * (H + c * C) + C * (C + 1) // 2) * HQ * D * 4 for c in range(pw.num_chunks))
-    tf = flops / (ms * 1e-3) / 1e12
-    # oracle: the same pipeline on every 16th query row of each chunk (attention), full reconstruct and store
-    op = oracle.Pool(pw.num_rows, HKV, D)
-    oracle.store_quant(op, pw.hist_k, pw.hist_v, pw.hist_slots)
-    sall = np.concatenate([pw.hist_slots, pw.new_slots])
+        def pipeline():
+            for c in range(pw.num_chunks):
+                c0, c1 = c * C, (c + 1) * C
+                P = H + c0
+                ops.reconstruct_bf16(pool, slots_all[:P], ws_k[:P], ws_v[:P])
+                ops.prefill_attn(qd[c0:c1], kd[c0:c1], vd[c0:c1], ws_k[:P], ws_v[:P], out=outp[c0:c1], plan=pplan)
+                ops.store_quant(pool, kd[c0:c1], vd[c0:c1], slots_all[P:P + C])
+        g = graph_of(torch, stream, pipeline)
+        ms, _ = time_graph(torch, stream, g, max(10, steps // 4), 3)
+        flops = sum((C * (H + c * C) + C * (C + 1) // 2) * HQ * D * 4 for c in range(pw.num_chunks))
+        tf = flops / (ms * 1e-3) / 1e12
+        # oracle: the same pipeline on every 16th query row of each chunk (attention), full reconstruct and store
+        op = oracle.Pool(pw.num_rows, HKV, D)
+        oracle.store_quant(op, pw.hist_k, pw.hist_v, pw.hist_slots)
+        sall = np.concatenate([pw.hist_slots, pw.new_slots])
 
-    def oracle_pipeline():
-        for c in range(pw.num_chunks):
-            c0, c1 = c * C, (c + 1) * C
-            P = H + c0
-            owk, owv = oracle.reconstruct(op, sall[:P])
-            oracle.prefill_attn(pw.q[c0:c1], pw.k[c0:c1], pw.v[c0:c1], owk, owv, pw.sm_scale,
-                                np.arange(0, C, 16, dtype=np.int64))
-            oracle.store_quant(op, pw.k[c0:c1], pw.v[c0:c1], sall[P:P + C])
-    cpu = cpu_baseline_scaled(oracle_pipeline, 1, 1, "us/pipeline",
-                              "every 16th query row of each chunk (all heads), full reconstruct and store; not scaled",
-                              budget)
-    detail_line("config3_chunked_prefill_4x2048_over_8192", ms * 1e3, "us/pipeline",
-                {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak,
-                 "traffic": None, "kernel": "prefill_tc2_kernel (+ reconstruct, store)", "flops": flops,
-                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)"}, cpu,
-                {"note": "4 x (reconstruct -> prefill -> store) in one graph; flops count causal pairs only"})
-    del pool, g, ws_k, ws_v
-    torch.cuda.empty_cache()
+        def oracle_pipeline():
+            for c in range(pw.num_chunks):
+                c0, c1 = c * C, (c + 1) * C
+                P = H + c0
+                owk, owv = oracle.reconstruct(op, sall[:P])
+                oracle.prefill_attn(pw.q[c0:c1], pw.k[c0:c1], pw.v[c0:c1], owk, owv, pw.sm_scale,
+                                    np.arange(0, C, 16, dtype=np.int64))
+                oracle.store_quant(op, pw.k[c0:c1], pw.v[c0:c1], sall[P:P + C])
+        cpu = cpu_baseline_scaled(oracle_pipeline, 1, 1, "us/pipeline",
+                                  "every 16th query row of each chunk (all heads), full reconstruct and store; not scaled",
+                                  budget)
+        detail_line("config3_chunked_prefill_4x2048_over_8192", ms * 1e3, "us/pipeline",
+                    {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak,
+                     "traffic": None, "kernel": "prefill_tc2_kernel (+ reconstruct, store)", "flops": flops,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)"}, cpu,
+                    {"note": "4 x (reconstruct -> prefill -> store) in one graph; flops count causal pairs only"})
+        del pool, g, ws_k, ws_v
+        torch.cuda.empty_cache()
 
     # ---- reconstruct, cold: 8 distinct pools of 14,336 prefix rows into 8 distinct workspaces ----
-    P = H + 3 * C
-    rk, rv = inputs.kv_tokens(np.random.default_rng(5), P, 1.0)
-    rslots = torch.from_numpy(np.random.default_rng(6).permutation(pw.num_rows)[:P].astype(np.int32)).to(device)
-    rpools = []
-    for _ in range(8):
-        p = ops.KVPool.empty(pw.num_rows, HKV, device=device)
-        ops.store_quant(p, to_dev(rk), to_dev(rv), rslots)
-        rpools.append(p)
-    wss = [(torch.empty(P, HKV, D, dtype=torch.bfloat16, device=device),
-            torch.empty(P, HKV, D, dtype=torch.bfloat16, device=device)) for _ in range(8)]
+    if want("reconstruct"):
+        P = H + 3 * C
+        rk, rv = inputs.kv_tokens(np.random.default_rng(5), P, 1.0)
+        rslots = torch.from_numpy(np.random.default_rng(6).permutation(pw.num_rows)[:P].astype(np.int32)).to(device)
+        rpools = []
+        for _ in range(8):
+            p = ops.KVPool.empty(pw.num_rows, HKV, device=device)
+            ops.store_quant(p, to_dev(rk), to_dev(rv), rslots)
+            rpools.append(p)
+        wss = [(torch.empty(P, HKV, D, dtype=torch.bfloat16, device=device),
+                torch.empty(P, HKV, D, dtype=torch.bfloat16, device=device)) for _ in range(8)]
 
-    def recon_all():
-        for p, (a, b) in zip(rpools, wss):
-            ops.reconstruct_bf16(p, rslots, a, b)
-    g = graph_of(torch, stream, recon_all)
-    ms, _ = time_graph(torch, stream, g, steps, warm)
-    nbytes = 8 * (P * (HKV * D + HKV * 4) * 2 + P * 4 + P * HKV * D * 2 * 2)
-    op = oracle.Pool(pw.num_rows, HKV, D)
-    oracle.store_quant(op, rk, rv, rslots.cpu().numpy())
-    rs = rslots.cpu().numpy()
-    cpu = cpu_baseline_scaled(lambda: oracle.reconstruct(op, rs), 1, 8, "us/iter", "1 of 8 pools, scaled x8", budget)
-    detail_line("reconstruct_14336_rows_x8_cold", ms * 1e3, "us/iter",
-                hbm_roof(nbytes, ms, hbm_peak, peak_src, "reconstruct_kernel"), cpu,
-                {"note": "8 distinct pools and workspaces per iteration (0.5 GB): cold in L2"})
-    del rpools, wss, g
-    torch.cuda.empty_cache()
+        def recon_all():
+            for p, (a, b) in zip(rpools, wss):
+                ops.reconstruct_bf16(p, rslots, a, b)
+        g = graph_of(torch, stream, recon_all)
+        ms, _ = time_graph(torch, stream, g, steps, warm)
+        nbytes = 8 * (P * (HKV * D + HKV * 4) * 2 + P * 4 + P * HKV * D * 2 * 2)
+        op = oracle.Pool(pw.num_rows, HKV, D)
+        oracle.store_quant(op, rk, rv, rslots.cpu().numpy())
+        rs = rslots.cpu().numpy()
+        cpu = cpu_baseline_scaled(lambda: oracle.reconstruct(op, rs), 1, 8, "us/iter", "1 of 8 pools, scaled x8", budget)
+        detail_line("reconstruct_14336_rows_x8_cold", ms * 1e3, "us/iter",
+                    hbm_roof(nbytes, ms, hbm_peak, peak_src, "reconstruct_kernel"), cpu,
+                    {"note": "8 distinct pools and workspaces per iteration (0.5 GB): cold in L2"})
+        del rpools, wss, g
+        torch.cuda.empty_cache()
 
     # ---- config 4: batched multi-row decode, 64 requests, 1-8 rows, 2,000,000-row pool, one launch ----
-    bw = inputs.decode_batched()
-    Lb = bw.layer(0)
-    pool = ops.KVPool.empty(bw.num_rows, HKV, device=device)
-    ops.store_quant(pool, to_dev(Lb.k), to_dev(Lb.v), torch.from_numpy(Lb.slots).to(device))
-    qd = to_dev(Lb.q)
-    r2s = torch.from_numpy(bw.req_to_slot).to(device)
-    lens = torch.from_numpy(bw.seq_lens).to(device)
-    offs = torch.from_numpy(bw.q_row_offsets).to(device)
-    mq = int(np.diff(bw.q_row_offsets).max())
-    stride = int(bw.req_to_slot.shape[1])
-    plan = ops.DecodePlan(HQ, HKV, len(bw.seq_lens), int(bw.q_row_offsets[-1]), mq, stride, 0, device)
-    out = torch.empty_like(qd)
-    g = graph_of(torch, stream, lambda: ops.decode_attn(pool, qd, r2s, lens, offs, max_seq_len=stride,
-                                                        max_q_rows=mq, plan=plan, out=out))
-    ms, _ = time_graph(torch, stream, g, max(10, steps // 4), 3)
-    keys = int(bw.seq_lens.sum())
-    rows = int(bw.q_row_offsets[-1])
-    nbytes = keys * (HKV * D * 2 + HKV * 4 * 2 + 4) + rows * HQ * D * 2 * 2
-    op = oracle.Pool(bw.num_rows, HKV, D)
-    sample_req = [0, 1, 2, 3]
-    sub = np.concatenate([bw.req_to_slot[b, :bw.seq_lens[b]] for b in sample_req])
-    starts = np.concatenate([[0], np.cumsum(bw.seq_lens)[:-1]])
-    tok = np.concatenate([np.arange(starts[b], starts[b] + bw.seq_lens[b]) for b in sample_req])
-    oracle.store_quant(op, Lb.k[tok], Lb.v[tok], sub)
-    qrows = np.concatenate([np.arange(bw.q_row_offsets[b], bw.q_row_offsets[b + 1]) for b in sample_req])
-    offs_s = np.concatenate([[0], np.cumsum(np.diff(bw.q_row_offsets)[sample_req])]).astype(np.int32)
-    s_keys = int(bw.seq_lens[sample_req].sum())
-    del Lb
-    cpu = cpu_baseline_scaled(lambda: oracle.decode_attn(op, qd.view(torch.int16).cpu().numpy().view(np.uint16)[qrows],
-                                                         bw.req_to_slot[sample_req], bw.seq_lens[sample_req], offs_s,
-                                                         bw.sm_scale, HQ),
-                              s_keys, keys, "us/launch",
-                              f"requests {sample_req} ({s_keys} keys, all their rows), scaled by keys to all 64", budget)
-    detail_line("config4_batched_multirow_64req", ms * 1e3, "us/launch",
-                hbm_roof(nbytes, ms, hbm_peak, peak_src, "decode_split_kernel<2>"), cpu,
-                {"keys": keys, "rows": rows, "num_splits": plan.num_splits})
-    del pool, g
-    torch.cuda.empty_cache()
+    if want("config4"):
+        bw = inputs.decode_batched()
+        Lb = bw.layer(0)
+        pool = ops.KVPool.empty(bw.num_rows, HKV, device=device)
+        ops.store_quant(pool, to_dev(Lb.k), to_dev(Lb.v), torch.from_numpy(Lb.slots).to(device))
+        qd = to_dev(Lb.q)
+        r2s = torch.from_numpy(bw.req_to_slot).to(device)
+        lens = torch.from_numpy(bw.seq_lens).to(device)
+        offs = torch.from_numpy(bw.q_row_offsets).to(device)
+        mq = int(np.diff(bw.q_row_offsets).max())
+        stride = int(bw.req_to_slot.shape[1])
+        plan = ops.DecodePlan(HQ, HKV, len(bw.seq_lens), int(bw.q_row_offsets[-1]), mq, stride, 0, device)
+        out = torch.empty_like(qd)
+        g = graph_of(torch, stream, lambda: ops.decode_attn(pool, qd, r2s, lens, offs, max_seq_len=stride,
+                                                            max_q_rows=mq, plan=plan, out=out))
+        ms, _ = time_graph(torch, stream, g, max(10, steps // 4), 3)
+        keys = int(bw.seq_lens.sum())
+        rows = int(bw.q_row_offsets[-1])
+        nbytes = keys * (HKV * D * 2 + HKV * 4 * 2 + 4) + rows * HQ * D * 2 * 2
+        op = oracle.Pool(bw.num_rows, HKV, D)
+        sample_req = [0, 1, 2, 3]
+        sub = np.concatenate([bw.req_to_slot[b, :bw.seq_lens[b]] for b in sample_req])
+        starts = np.concatenate([[0], np.cumsum(bw.seq_lens)[:-1]])
+        tok = np.concatenate([np.arange(starts[b], starts[b] + bw.seq_lens[b]) for b in sample_req])
+        oracle.store_quant(op, Lb.k[tok], Lb.v[tok], sub)
+        qrows = np.concatenate([np.arange(bw.q_row_offsets[b], bw.q_row_offsets[b + 1]) for b in sample_req])
+        offs_s = np.concatenate([[0], np.cumsum(np.diff(bw.q_row_offsets)[sample_req])]).astype(np.int32)
+        s_keys = int(bw.seq_lens[sample_req].sum())
+        del Lb
+        cpu = cpu_baseline_scaled(lambda: oracle.decode_attn(op, qd.view(torch.int16).cpu().numpy().view(np.uint16)[qrows],
+                                                             bw.req_to_slot[sample_req], bw.seq_lens[sample_req], offs_s,
+                                                             bw.sm_scale, HQ),
+                                  s_keys, keys, "us/launch",
+                                  f"requests {sample_req} ({s_keys} keys, all their rows), scaled by keys to all 64", budget)
+        detail_line("config4_batched_multirow_64req", ms * 1e3, "us/launch",
+                    hbm_roof(nbytes, ms, hbm_peak, peak_src, "decode_split_kernel<2>"), cpu,
+                    {"keys": keys, "rows": rows, "num_splits": plan.num_splits})
+        del pool, g
+        torch.cuda.empty_cache()
 
 
 def main():
+    global SKIP_CPU
     args = parse_args()
+    SKIP_CPU = args.no_cpu_baseline
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -158,8 +158,7 @@ size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, in
   if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim != FTKV_HEAD_DIM || batch < 0 || total_q_rows < 0)
     return 0;
   if (num_splits <= 0 || num_splits > FTKV_MAX_SPLITS) num_splits = FTKV_MAX_SPLITS;
-  // room for the kernel with the most partials per key slice (the single-row kernel: one per key group)
-  const int64_t parts = total_q_rows * num_q_heads * num_splits * ftkv::decode_parts_per_slice(1, num_kv_heads);
+  const int64_t parts = total_q_rows * num_q_heads * num_splits;  // one partial per (row, query head, slice)
   const int64_t ctr = ceil_div((int64_t(batch) * num_kv_heads + 2) * 4, 256) * 256;  // + the grid barrier
   return static_cast<size_t>(ws_acc_bytes(parts) + ws_ml_bytes(parts) + ctr);
 }
@@ -237,7 +236,7 @@ int decode_validate_dims(int32_t num_kv_heads, int32_t num_q_heads, const uint16
   geom->splits = span > 0 ? ceil_div(span, chunk) : 1;
   geom->need = ftkv_decode_workspace_bytes(num_q_heads, num_kv_heads, FTKV_HEAD_DIM, batch, total_q_rows,
                                            static_cast<int32_t>(geom->splits));
-  geom->parts = total_q_rows * num_q_heads * geom->splits * ftkv::decode_parts_per_slice(1, num_kv_heads);
+  geom->parts = total_q_rows * num_q_heads * geom->splits;
   if (check_workspace && workspace_bytes < geom->need) return FTKV_ERR_WORKSPACE;
   return FTKV_OK;
 }

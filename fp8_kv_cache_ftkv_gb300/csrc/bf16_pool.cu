@@ -16,8 +16,8 @@
 //  * A CTA covers one key slice of one query row for HC (up to 4) KV heads: a token's K (and V) rows for those
 //    heads are one contiguous run of HC x 256 bytes, copied with 16-byte cp.async by whole warps.
 //  * 4 warps in NG = 4 / HC key groups of HC warps (one per KV head); a group shares a 3-stage ring of
-//    16-key blocks and publishes its own partial, so a key slice yields NG partials.  96 KB of ring plus the
-//    slot window: two CTAs per SM.
+//    16-key blocks; the groups' partials are combined in shared memory at the end, so a key slice yields one
+//    partial.  96 KB of ring plus the slot window: two CTAs per SM.
 //  * Per 16-key block and warp: S^T = K Q^T on BF16 tensor cores (keys as M, the KV head's 8 query heads as
 //    N; K fragments by ldmatrix from an XOR-swizzled stage), a softmax with a lazy running maximum, then
 //    O^T += V^T P^T (V^T fragments by ldmatrix.trans, P transposed with movmatrix).  The MMA's A and B share
@@ -57,9 +57,6 @@ struct Bf {
 };
 static_assert(Bf<4>::SMEM <= 113 * 1024 && Bf<2>::SMEM <= 113 * 1024 && Bf<1>::SMEM <= 113 * 1024,
               "two CTAs per SM");
-// NG = BW / HC partials per key slice, no more than the FP8 single-row kernel's (8 / HC), for which
-// ftkv_decode_workspace_bytes sizes the workspace
-static_assert(BW <= 8, "partials per slice");
 
 // Shared-memory offset of 16-byte chunk p (d = 8p .. 8p+7) of KV head hd of key `key` (0..15) within a stage
 // half.  The XOR with key & 7 makes the 8 rows of every ldmatrix phase, and the cp.async run writes, free of
@@ -338,24 +335,64 @@ __global__ void __launch_bounds__(BW * 32, 2) decode_bf16_kernel(const DecodeArg
     cp_async_wait<0>();
   }
 
-  // ---- publish this group's partial per query head (index split * NG + gi of the row's partials) ----
+  // ---- one partial per (row, query head) and key slice: groups 1 .. NG-1 leave m, l and the accumulator in the
+  // ring area, group 0 folds them into its own and writes the result in the transposed layout ----
 #pragma unroll
   for (int hx = 0; hx < 2; hx++)
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l[hx] += __shfl_xor_sync(0xffffffffu, l[hx], off);
-  const int64_t pstride = static_cast<int64_t>(a.num_splits) * a.pps;
+  const int64_t nsl = a.num_splits;  // one partial per slice (pps = 1)
+  if constexpr (NG > 1) {
+    float* gacc = reinterpret_cast<float*>(smem);                   // [NG-1][HC][8][128]
+    float* gml = gacc + (NG - 1) * HC * 8 * kHeadDim;               // [NG-1][HC][8][2]
+    __syncthreads();  // every group is done with the ring
+    if (gi > 0) {
+#pragma unroll
+      for (int hx = 0; hx < 2; hx++) {
+        float* dst = gacc + (((gi - 1) * HC + hh) * 8 + 2 * t + hx) * kHeadDim;
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++) {
+          dst[16 * mt + g] = acc[mt][hx];
+          dst[16 * mt + g + 8] = acc[mt][2 + hx];
+        }
+        if (g == 0) *reinterpret_cast<float2*>(gml + (((gi - 1) * HC + hh) * 8 + 2 * t + hx) * 2) = make_float2(m[hx], l[hx]);
+      }
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int go = 1; go < NG && gi == 0; go++) {
+#pragma unroll
+      for (int hx = 0; hx < 2; hx++) {
+        const int slot = ((go - 1) * HC + hh) * 8 + 2 * t + hx;
+        const float2 mlo = *reinterpret_cast<const float2*>(gml + slot * 2);
+        const float mn = fmaxf(m[hx], mlo.x);
+        if (mn == -INFINITY) continue;  // neither holds a key
+        const float f = (m[hx] == -INFINITY) ? 0.0f : fast_exp2(m[hx] - mn);
+        const float fo = (mlo.x == -INFINITY) ? 0.0f : fast_exp2(mlo.x - mn);
+        const float* src = gacc + slot * kHeadDim;
+#pragma unroll
+        for (int mt = 0; mt < 8; mt++) {
+          acc[mt][hx] = fmaf(acc[mt][hx], f, src[16 * mt + g] * fo);
+          acc[mt][2 + hx] = fmaf(acc[mt][2 + hx], f, src[16 * mt + g + 8] * fo);
+        }
+        l[hx] = fmaf(l[hx], f, mlo.y * fo);
+        m[hx] = mn;
+      }
+    }
+  }
 #pragma unroll
   for (int hx = 0; hx < 2; hx++) {
     const int hq = 2 * t + hx;
-    if (hq < G) {
-      const int64_t prow = (row * a.num_q_heads + (h0 + hh) * G + hq) * pstride + split * NG + gi;
-      float* dst = a.part_acc + prow * kHeadDim;
+    if (gi == 0 && hq < G) {
+      const int64_t prow = row * a.num_q_heads + (h0 + hh) * G + hq;
+      float* dst = a.part_acc + prow * kHeadDim * nsl;  // element d of slice s at ((d / 4) nsl + s) 4 + d % 4
 #pragma unroll
       for (int mt = 0; mt < 8; mt++) {
-        dst[16 * mt + g] = acc[mt][hx];
-        dst[16 * mt + g + 8] = acc[mt][2 + hx];
+        const int d0 = 16 * mt + g, d1 = d0 + 8;
+        dst[((d0 >> 2) * nsl + split) * 4 + (d0 & 3)] = acc[mt][hx];
+        dst[((d1 >> 2) * nsl + split) * 4 + (d1 & 3)] = acc[mt][2 + hx];
       }
-      if (g == 0) *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(m[hx], l[hx]);
+      if (g == 0) *reinterpret_cast<float2*>(a.part_ml + (prow * nsl + split) * 2) = make_float2(m[hx], l[hx]);
     }
   }
   if (a.coop) coop_finish<BW>(a);
@@ -381,7 +418,8 @@ cudaError_t launch_bf16(const DecodeArgs& a, cudaStream_t s, int dev) {
   if (setup_err[dev] != cudaSuccess) return setup_err[dev];
   const dim3 grid(a.num_splits, a.num_kv_heads / HC, static_cast<unsigned>(a.total_q_rows));
   DecodeArgs c = a;
-  c.pps = Bf<HC>::NG;
+  c.pps = 1;
+  c.ptrans = 1;
   const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
   c.coop = (resident[dev] > 0 && ctas <= resident[dev]) ? 1 : 0;
   if (c.coop) return launch_k_coop(decode_bf16_kernel<HC>, grid, dim3(BW * 32), Bf<HC>::SMEM, s, c);

@@ -119,9 +119,14 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
     if (lane == 0) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
     return;
   }
-  const int64_t prow0 = (t * a.num_q_heads + qh) * static_cast<int64_t>(a.num_splits) * a.pps;
+  const int64_t np = static_cast<int64_t>(a.num_splits) * a.pps;  // partial slots per (row, head)
+  const int64_t prow0 = (t * a.num_q_heads + qh) * np;
   const float2* pml = reinterpret_cast<const float2*>(a.part_ml) + prow0;
-  const float4* pacc = reinterpret_cast<const float4*>(a.part_acc + prow0 * kHeadDim) + d4;
+  // slice sl's 4 accumulators: pacc[sl * pst]
+  const float4* pacc = a.ptrans
+                           ? reinterpret_cast<const float4*>(a.part_acc) + ((t * a.num_q_heads + qh) * QUADS + d4) * np
+                           : reinterpret_cast<const float4*>(a.part_acc + prow0 * kHeadDim) + d4;
+  const int pst = a.ptrans ? 1 : QUADS;
   float M = -INFINITY, L = 0.0f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int base = 0; base < nslices; base += 32 * CH) {  // warp-uniform
@@ -132,7 +137,7 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
       const int sl = base + lane + 32 * k;
       const bool in = sl < nslices;
       ml[k] = in ? __ldcg(pml + sl) : make_float2(-INFINITY, 0.f);
-      v[k] = in ? __ldcg(pacc + static_cast<int64_t>(sl) * QUADS) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[k] = in ? __ldcg(pacc + static_cast<int64_t>(sl) * pst) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float Mc = M;
 #pragma unroll

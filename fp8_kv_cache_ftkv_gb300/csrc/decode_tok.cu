@@ -15,9 +15,9 @@
 //    1.5x the rate of random 128-byte rows (the rows of one token read by four different CTAs).
 //  * Warps form NG = 8 / HC key groups of HC warps, one warp per KV head.  A group shares a 3-stage ring
 //    of 16-key blocks (K and V runs of all HC heads plus their scales); the HC warps of a group load a
-//    block together and meet at a named barrier before computing it.  Each group publishes its own
-//    partial (m, l, accumulator) per query head, so no CTA-wide merge precedes the split merge: a key slice
-//    yields NG partials.
+//    block together and meet at a named barrier before computing it.  At the end the groups' partials
+//    (m, l, accumulator) are combined in shared memory, so a key slice yields one partial per query head,
+//    written transposed (one quad of d over the slices is contiguous) for the merge's loads.
 //  * The split merge: when the grid fits on the GPU at once (batch 1), a cooperative launch, a grid barrier
 //    and the merge spread over the whole grid (coop_finish); otherwise a second small kernel behind this
 //    one (decode_merge_kernel).
@@ -483,28 +483,76 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
     cp_async_wait<0>();
   }
 
-  // ---- publish this group's partial per query head: m, l (reduced over the lanes that share a head) and the
-  // accumulator in units of 2^m, straight from registers.  Partial index within (row, query head):
-  // split * NG + gi, so a key slice yields NG partials ----
+  // ---- one partial per (row, query head) and key slice: the NG key groups' partials are combined in shared
+  // memory first (groups 1 .. NG-1 leave m, l and the accumulator, scaled to units of 2^m, in the ring area;
+  // group 0 folds them into its own), then written in the transposed layout (see DecodeArgs::ptrans) ----
 #pragma unroll
   for (int hx = 0; hx < 2; hx++)
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l[hx] += __shfl_xor_sync(0xffffffffu, l[hx], off);
   const int G = a.group;
-  const int64_t pstride = static_cast<int64_t>(a.num_splits) * a.pps;
+  // lane (g, t) holds d = 16g + 4q4 + {0..3} of query head 2t + hx: acc[2q4][hx], acc[2q4][2+hx],
+  // acc[2q4+1][hx], acc[2q4+1][2+hx]; bring it to units of 2^m
+#pragma unroll
+  for (int hx = 0; hx < 2; hx++) {
+    const float up = exp2i(E[hx]);
+#pragma unroll
+    for (int mt = 0; mt < 8; mt++) {
+      acc[mt][hx] *= up;
+      acc[mt][2 + hx] *= up;
+    }
+  }
+  if constexpr (NG > 1) {
+    float* gacc = reinterpret_cast<float*>(smem);                   // [NG-1][HC][8][128]
+    float* gml = gacc + (NG - 1) * HC * 8 * kHeadDim;               // [NG-1][HC][8][2]
+    __syncthreads();  // every group is done with the ring
+    if (gi > 0) {
+#pragma unroll
+      for (int hx = 0; hx < 2; hx++) {
+        const int slot = ((gi - 1) * HC + hh) * 8 + 2 * t + hx;
+        float4* dst = reinterpret_cast<float4*>(gacc + slot * kHeadDim + 16 * g);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; q4++)
+          dst[q4] = make_float4(acc[2 * q4][hx], acc[2 * q4][2 + hx], acc[2 * q4 + 1][hx], acc[2 * q4 + 1][2 + hx]);
+        if (g == 0) *reinterpret_cast<float2*>(gml + slot * 2) = make_float2(m[hx], l[hx]);
+      }
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int go = 1; go < NG && gi == 0; go++) {
+#pragma unroll
+      for (int hx = 0; hx < 2; hx++) {
+        const int slot = ((go - 1) * HC + hh) * 8 + 2 * t + hx;
+        const float2 mlo = *reinterpret_cast<const float2*>(gml + slot * 2);
+        const float mn = fmaxf(m[hx], mlo.x);
+        if (mn == -INFINITY) continue;  // neither holds a key
+        const float f = (m[hx] == -INFINITY) ? 0.0f : fast_exp2(m[hx] - mn);
+        const float fo = (mlo.x == -INFINITY) ? 0.0f : fast_exp2(mlo.x - mn);
+        const float4* src = reinterpret_cast<const float4*>(gacc + slot * kHeadDim + 16 * g);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; q4++) {
+          const float4 v = src[q4];
+          acc[2 * q4][hx] = fmaf(acc[2 * q4][hx], f, v.x * fo);
+          acc[2 * q4][2 + hx] = fmaf(acc[2 * q4][2 + hx], f, v.y * fo);
+          acc[2 * q4 + 1][hx] = fmaf(acc[2 * q4 + 1][hx], f, v.z * fo);
+          acc[2 * q4 + 1][2 + hx] = fmaf(acc[2 * q4 + 1][2 + hx], f, v.w * fo);
+        }
+        l[hx] = fmaf(l[hx], f, mlo.y * fo);
+        m[hx] = mn;
+      }
+    }
+  }
+  const int64_t nsl = a.num_splits;  // one partial per slice (pps = 1)
 #pragma unroll
   for (int hx = 0; hx < 2; hx++) {
     const int hq = 2 * t + hx;  // query head within the KV head's group (N column)
-    if (hq < G) {
-      const int64_t prow = (row0 * a.num_q_heads + (h0 + hh) * G + hq) * pstride + split * NG + gi;
-      const float up = exp2i(E[hx]);
-      float* dst = a.part_acc + prow * kHeadDim + 16 * g;
-      // lane (g, t) holds d = 16g + 2mt + {0, 1} of head hx at acc[mt][hx], acc[mt][2 + hx]: 16 contiguous d
+    if (gi == 0 && hq < G) {
+      const int64_t prow = row0 * a.num_q_heads + (h0 + hh) * G + hq;
+      float4* dst = reinterpret_cast<float4*>(a.part_acc) + (prow * (kHeadDim / 4) + 4 * g) * nsl + split;
 #pragma unroll
       for (int q4 = 0; q4 < 4; q4++)
-        reinterpret_cast<float4*>(dst)[q4] = make_float4(acc[2 * q4][hx] * up, acc[2 * q4][2 + hx] * up,
-                                                         acc[2 * q4 + 1][hx] * up, acc[2 * q4 + 1][2 + hx] * up);
-      if (g == 0) *reinterpret_cast<float2*>(a.part_ml + prow * 2) = make_float2(m[hx], l[hx]);
+        dst[q4 * nsl] = make_float4(acc[2 * q4][hx], acc[2 * q4][2 + hx], acc[2 * q4 + 1][hx], acc[2 * q4 + 1][2 + hx]);
+      if (g == 0) *reinterpret_cast<float2*>(a.part_ml + (prow * nsl + split) * 2) = make_float2(m[hx], l[hx]);
     }
   }
   if (a.coop) coop_finish<TW>(a);  // grid barrier, then the merge spread over the grid
@@ -530,7 +578,8 @@ cudaError_t launch_tok(const DecodeArgs& a, cudaStream_t s, int dev) {
   if (setup_err[dev] != cudaSuccess) return setup_err[dev];
   const dim3 grid(a.num_splits, a.num_kv_heads / HC, a.batch);
   DecodeArgs c = a;
-  c.pps = Tok<HC>::NG;
+  c.pps = 1;
+  c.ptrans = 1;
   const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
   c.coop = (resident[dev] > 0 && ctas <= resident[dev]) ? 1 : 0;
   if (c.coop) return launch_k_coop(decode_tok_kernel<HC>, grid, dim3(TW * 32), Tok<HC>::SMEM, s, c);
@@ -545,10 +594,6 @@ cudaError_t launch_tok(const DecodeArgs& a, cudaStream_t s, int dev) {
 
 int decode_tok_heads_per_cta(int num_kv_heads) {
   return (num_kv_heads % 4 == 0) ? 4 : (num_kv_heads % 2 == 0) ? 2 : 1;
-}
-
-int decode_parts_per_slice(int max_q_rows, int num_kv_heads) {
-  return max_q_rows <= 1 ? TW / decode_tok_heads_per_cta(num_kv_heads) : 1;
 }
 
 cudaError_t launch_decode_tok(const DecodeArgs& a, cudaStream_t s) {

@@ -64,7 +64,10 @@ struct DecodeArgs {
   int64_t chunk;             // keys per slice (multiple of 16)
   float qk_scale_log2;       // sm_scale * log2(e)
   int64_t window;            // 0: full attention; W > 0: each query row attends to its last W visible keys
-  float* part_acc;           // [total_q_rows][Hq][num_splits * pps][128]
+  int ptrans;                // partial accumulators transposed: [total_q_rows][Hq][32 quads][num_splits * pps]
+                             // float4 (the merge's loads of one quad over the slices are contiguous); else
+                             // [total_q_rows][Hq][num_splits * pps][128] floats
+  float* part_acc;
   float* part_ml;            // [total_q_rows][Hq][num_splits * pps][2]  (max in log2 units, sum)
   int* counters;             // [batch][Hkv] arrival tickets; zero between calls
   uint16_t* out;             // [total_q_rows][Hq][128]
@@ -165,8 +168,6 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_gather_bf16(const GatherArgs& a, cudaStream_t s);
 int decode_ctas_per_sm(int max_q_rows);
 int decode_tok_heads_per_cta(int num_kv_heads);
-// Partials per key slice: the single-row kernel publishes one per key group of a CTA.
-int decode_parts_per_slice(int max_q_rows, int num_kv_heads);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
 // Host-side checks and split geometry of a decode call, shared by every decode entry point.  Returns
