@@ -60,7 +60,7 @@ int check_pool(const ftkv_pool* pool) {
   if (!pool || !pool->k_codes || !pool->v_codes || !pool->k_scales || !pool->v_scales) return FTKV_ERR_INVALID;
   if (pool->num_rows <= 0 || pool->num_kv_heads <= 0 || pool->num_rows > (int64_t(1) << 31) - 1)
     return FTKV_ERR_INVALID;
-  if (pool->head_dim != FTKV_HEAD_DIM) return FTKV_ERR_UNSUPPORTED;
+  if (pool->head_dim != FTKV_HEAD_DIM && pool->head_dim != FTKV_HEAD_DIM_256) return FTKV_ERR_UNSUPPORTED;
   if (!aligned16(pool->k_codes) || !aligned16(pool->v_codes)) return FTKV_ERR_ALIGN;
   if ((reinterpret_cast<uintptr_t>(pool->k_scales) & 3u) || (reinterpret_cast<uintptr_t>(pool->v_scales) & 3u))
     return FTKV_ERR_ALIGN;
@@ -127,7 +127,7 @@ int ftkv_store_quant(const ftkv_pool* pool, const uint16_t* k, const uint16_t* v
   if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slots) & 3u)) return FTKV_ERR_ALIGN;
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FTKV_OK) return st;
-  ftkv::StoreArgs a{k, v, slots, num_tokens, pool->num_kv_heads, pool->k_codes, pool->v_codes,
+  ftkv::StoreArgs a{k, v, slots, num_tokens, pool->num_kv_heads, pool->head_dim, pool->k_codes, pool->v_codes,
                     pool->k_scales, pool->v_scales, pool->num_rows, di->err_word};
   cudaError_t e = ftkv::launch_store_quant(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FTKV_OK : cuda_fail(e);
@@ -137,6 +137,7 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
                           uint16_t* ws_v, void* stream) {
   int st = check_pool(pool);
   if (st != FTKV_OK) return st;
+  if (pool->head_dim != FTKV_HEAD_DIM) return FTKV_ERR_UNSUPPORTED;  // the prefill path is 128-d
   if (num_prefix < 0) return FTKV_ERR_INVALID;
   if (num_prefix == 0) return FTKV_OK;
   if (!slots || !ws_k || !ws_v) return FTKV_ERR_INVALID;
@@ -150,17 +151,18 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
 }
 
 // Workspace layout: [partial accumulators | partial (max, sum) | arrival counters], 256-B aligned parts.
-static int64_t ws_acc_bytes(int64_t parts) { return ceil_div(parts * FTKV_HEAD_DIM * 4, 256) * 256; }
+static int64_t ws_acc_bytes(int64_t parts, int head_dim) { return ceil_div(parts * head_dim * 4, 256) * 256; }
 static int64_t ws_ml_bytes(int64_t parts) { return ceil_div(parts * 2 * 4, 256) * 256; }
 
 size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t batch,
                                    int64_t total_q_rows, int32_t num_splits) {
-  if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim != FTKV_HEAD_DIM || batch < 0 || total_q_rows < 0)
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || batch < 0 || total_q_rows < 0 ||
+      (head_dim != FTKV_HEAD_DIM && head_dim != FTKV_HEAD_DIM_256))
     return 0;
   if (num_splits <= 0 || num_splits > FTKV_MAX_SPLITS) num_splits = FTKV_MAX_SPLITS;
   const int64_t parts = total_q_rows * num_q_heads * num_splits;  // one partial per (row, query head, slice)
   const int64_t ctr = ceil_div((int64_t(batch) * num_kv_heads + 2) * 4, 256) * 256;  // + the grid barrier
-  return static_cast<size_t>(ws_acc_bytes(parts) + ws_ml_bytes(parts) + ctr);
+  return static_cast<size_t>(ws_acc_bytes(parts, head_dim) + ws_ml_bytes(parts) + ctr);
 }
 
 int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max_seq_len, int32_t max_q_rows) {
@@ -192,7 +194,7 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
 
 namespace ftkv {
 
-int decode_validate_dims(int32_t num_kv_heads, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
+int decode_validate_dims(int32_t num_kv_heads, int32_t head_dim, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
                          int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                          int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
                          int64_t window, int32_t num_splits, uint32_t flags, const void* workspace,
@@ -200,8 +202,10 @@ int decode_validate_dims(int32_t num_kv_heads, int32_t num_q_heads, const uint16
   *geom = DecodeGeom{};
   int st;
   if ((st = check_heads(num_q_heads, num_kv_heads)) != FTKV_OK) return st;
+  if (head_dim != FTKV_HEAD_DIM && head_dim != FTKV_HEAD_DIM_256) return FTKV_ERR_UNSUPPORTED;
   if (batch < 0 || total_q_rows < 0 || max_seq_len < 0 || req_stride < 0) return FTKV_ERR_INVALID;
   if (max_q_rows < 1 || max_q_rows > FTKV_MAX_Q_ROWS) return FTKV_ERR_UNSUPPORTED;
+  if (head_dim == FTKV_HEAD_DIM_256 && max_q_rows > 1) return FTKV_ERR_UNSUPPORTED;  // single-row kernel only
   if (num_splits < 0 || num_splits > FTKV_MAX_SPLITS) return FTKV_ERR_INVALID;
   if (flags & ~static_cast<uint32_t>(FTKV_DECODE_STABLE_HISTORY)) return FTKV_ERR_INVALID;
   if (max_seq_len > req_stride) return FTKV_ERR_INVALID;
@@ -234,7 +238,7 @@ int decode_validate_dims(int32_t num_kv_heads, int32_t num_q_heads, const uint16
   chunk = ceil_div(chunk, align) * align;
   geom->chunk = chunk;
   geom->splits = span > 0 ? ceil_div(span, chunk) : 1;
-  geom->need = ftkv_decode_workspace_bytes(num_q_heads, num_kv_heads, FTKV_HEAD_DIM, batch, total_q_rows,
+  geom->need = ftkv_decode_workspace_bytes(num_q_heads, num_kv_heads, head_dim, batch, total_q_rows,
                                            static_cast<int32_t>(geom->splits));
   geom->parts = total_q_rows * num_q_heads * geom->splits;
   if (check_workspace && workspace_bytes < geom->need) return FTKV_ERR_WORKSPACE;
@@ -249,7 +253,7 @@ int decode_validate(const ftkv_pool* pool, int32_t num_q_heads, const uint16_t* 
   *geom = DecodeGeom{};
   const int st = check_pool(pool);
   if (st != FTKV_OK) return st;
-  return decode_validate_dims(pool->num_kv_heads, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets,
+  return decode_validate_dims(pool->num_kv_heads, pool->head_dim, num_q_heads, q, req_to_slot, req_stride, seq_lens, q_row_offsets,
                               batch, total_q_rows, max_q_rows, max_seq_len, sm_scale, window, num_splits, flags,
                               workspace, workspace_bytes, out, check_workspace, geom);
 }
@@ -274,8 +278,8 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   const int64_t parts = geom.parts;  // the layout ftkv_decode_workspace_bytes sizes
   float* part_acc = static_cast<float*>(workspace);
   char* ws = static_cast<char*>(workspace);
-  float* part_ml = reinterpret_cast<float*>(ws + ws_acc_bytes(parts));
-  int* counters = reinterpret_cast<int*>(ws + ws_acc_bytes(parts) + ws_ml_bytes(parts));
+  float* part_ml = reinterpret_cast<float*>(ws + ws_acc_bytes(parts, pool->head_dim));
+  int* counters = reinterpret_cast<int*>(ws + ws_acc_bytes(parts, pool->head_dim) + ws_ml_bytes(parts));
 
   ftkv::DecodeArgs a{};
   a.k_codes = pool->k_codes;
@@ -286,6 +290,7 @@ static int decode_common(const ftkv_pool* pool, int32_t num_q_heads, const uint1
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = pool->num_kv_heads;
   a.group = num_q_heads / pool->num_kv_heads;
+  a.head_dim = pool->head_dim;
   a.q = q;
   a.req_to_slot = req_to_slot;
   a.req_stride = req_stride;
@@ -349,7 +354,7 @@ int ftkv_decode_attn_bf16(const ftkv_bf16_pool* pool, int32_t num_q_heads, const
   int st = check_bf16_pool(pool);
   if (st != FTKV_OK) return st;
   ftkv::DecodeGeom geom;
-  st = ftkv::decode_validate_dims(pool->num_kv_heads, num_q_heads, q, req_to_slot, req_stride, seq_lens,
+  st = ftkv::decode_validate_dims(pool->num_kv_heads, FTKV_HEAD_DIM, num_q_heads, q, req_to_slot, req_stride, seq_lens,
                                   q_row_offsets, batch, total_q_rows, max_q_rows, max_seq_len, sm_scale, window,
                                   num_splits, flags, workspace, workspace_bytes, out, true, &geom);
   if (st != FTKV_OK || geom.empty) return st;
@@ -364,6 +369,7 @@ int ftkv_decode_attn_bf16(const ftkv_bf16_pool* pool, int32_t num_q_heads, const
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = pool->num_kv_heads;
   a.group = num_q_heads / pool->num_kv_heads;
+  a.head_dim = FTKV_HEAD_DIM;
   a.q = q;
   a.req_to_slot = req_to_slot;
   a.req_stride = req_stride;
@@ -378,8 +384,8 @@ int ftkv_decode_attn_bf16(const ftkv_bf16_pool* pool, int32_t num_q_heads, const
   a.qk_scale_log2 = sm_scale * 1.4426950408889634f;
   a.window = window;
   a.part_acc = static_cast<float*>(workspace);  // the layout ftkv_decode_workspace_bytes sizes
-  a.part_ml = reinterpret_cast<float*>(ws + ws_acc_bytes(geom.parts));
-  a.counters = reinterpret_cast<int*>(ws + ws_acc_bytes(geom.parts) + ws_ml_bytes(geom.parts));
+  a.part_ml = reinterpret_cast<float*>(ws + ws_acc_bytes(geom.parts, FTKV_HEAD_DIM));
+  a.counters = reinterpret_cast<int*>(ws + ws_acc_bytes(geom.parts, FTKV_HEAD_DIM) + ws_ml_bytes(geom.parts));
   a.gbar = a.counters + int64_t(batch) * pool->num_kv_heads;
   a.out = out;
   a.err = di->err_word;

@@ -92,7 +92,7 @@ __device__ __forceinline__ float exp2i(int e) {  // 2^e for -126 <= e <= 127, ex
 // are skipped here; a (row, head) without keys gets zeros.
 template <int CH>
 __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int lane) {
-  constexpr int QUADS = kHeadDim / 4;
+  const int QUADS = a.head_dim / 4;
   const int64_t t = it / (a.num_q_heads * QUADS);  // query row
   const int rem = static_cast<int>(it - t * a.num_q_heads * QUADS);
   const int qh = rem / QUADS, d4 = rem % QUADS;
@@ -114,7 +114,7 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
   n = n < 0 ? 0 : (n > nmax ? nmax : n);
   const int64_t nsl64 = (n - first_key(a, n, R) + a.chunk - 1) / a.chunk;
   const int nslices = static_cast<int>(nsl64 < a.num_splits ? nsl64 : a.num_splits) * a.pps;
-  uint16_t* dst = a.out + (t * a.num_q_heads + qh) * kHeadDim + 4 * d4;
+  uint16_t* dst = a.out + (t * a.num_q_heads + qh) * a.head_dim + 4 * d4;
   if (nslices == 0) {  // no keys: zeros
     if (lane == 0) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
     return;
@@ -125,7 +125,7 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
   // slice sl's 4 accumulators: pacc[sl * pst]
   const float4* pacc = a.ptrans
                            ? reinterpret_cast<const float4*>(a.part_acc) + ((t * a.num_q_heads + qh) * QUADS + d4) * np
-                           : reinterpret_cast<const float4*>(a.part_acc + prow0 * kHeadDim) + d4;
+                           : reinterpret_cast<const float4*>(a.part_acc + prow0 * a.head_dim) + d4;
   const int pst = a.ptrans ? 1 : QUADS;
   float M = -INFINITY, L = 0.0f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -216,7 +216,7 @@ __device__ __forceinline__ void coop_finish(const DecodeArgs& a) {
   }
   __syncthreads();
   if (s_ok) {
-    const int64_t items = a.total_q_rows * a.num_q_heads * (kHeadDim / 4);
+    const int64_t items = a.total_q_rows * a.num_q_heads * (a.head_dim / 4);
     for (int64_t it = cta + static_cast<int64_t>(ncta) * warp; it < items; it += static_cast<int64_t>(ncta) * WARPS)
       merge_item<10>(a, it, lane);
   }
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(MW * 32) decode_merge_kernel(const DecodeArgs 
   griddep_launch_dependents();
   griddep_wait();
   const int64_t it = static_cast<int64_t>(blockIdx.x) * MW + (threadIdx.x >> 5);
-  if (it < a.total_q_rows * a.num_q_heads * (kHeadDim / 4)) merge_item<10>(a, it, threadIdx.x & 31);
+  if (it < a.total_q_rows * a.num_q_heads * (a.head_dim / 4)) merge_item<10>(a, it, threadIdx.x & 31);
 }
 
 }  // namespace ftkv

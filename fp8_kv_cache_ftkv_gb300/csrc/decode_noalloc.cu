@@ -66,7 +66,7 @@ extern "C" int ftkv_decode_attn_noalloc(const ftkv_pool* pool, int32_t num_q_hea
   // scratch layout of this call (that of ftkv_decode_attn's workspace):
   // [partial accumulators | partial (max, sum) | arrival counters], 256-byte aligned parts
   const int64_t parts = geom.parts;
-  const int64_t ctr_off = round256(parts * FTKV_HEAD_DIM * 4) + round256(parts * 2 * 4);
+  const int64_t ctr_off = round256(parts * pool->head_dim * 4) + round256(parts * 2 * 4);
   const int64_t ctr_bytes = round256((static_cast<int64_t>(batch) * pool->num_kv_heads + 2) * 4);
   if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + ctr_off, 0, static_cast<size_t>(ctr_bytes),
                       static_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -8,9 +8,14 @@
 // FP8 tensor cores on the stored codes (the query in two exact E4M3 pieces) and PV on FP16 tensor cores on
 // the exactly converted V codes, as in decode.cu.
 //
+// Head dimension D = 128, or 256 (the full-attention layers of FreeToken's Qwen3.6 case, PR #897 "Known
+// regression and uncertainty"): a 256-d head is two 128-d halves, each loaded, multiplied and accumulated
+// like a 128-d head; the 256-d kernel runs one CTA per SM (its ring alone takes ~198 KB, and each lane holds
+// 64 accumulators).
+//
 // The unit of work and of memory traffic:
 //  * A CTA covers one key slice of a request for HC (up to 4) KV heads at once.  The codes of one token
-//    for those heads are one contiguous run of HC x 128 bytes in the pool ([rows][Hkv][128]), and a warp
+//    for those heads are one contiguous run of HC x D bytes in the pool ([rows][Hkv][D]), and a warp
 //    loads whole runs with one 16-byte cp.async per lane.  Random 512-byte runs stream from HBM at about
 //    1.5x the rate of random 128-byte rows (the rows of one token read by four different CTAs).
 //  * Warps form NG = 8 / HC key groups of HC warps, one warp per KV head.  A group shares a 3-stage ring
@@ -21,7 +26,7 @@
 //  * The split merge: when the grid fits on the GPU at once (batch 1), a cooperative launch, a grid barrier
 //    and the merge spread over the whole grid (coop_finish); otherwise a second small kernel behind this
 //    one (decode_merge_kernel).
-//  * 112 KB of shared memory and 8 warps of at most 128 registers: two CTAs fit on one SM, so the CTAs
+//  * (D = 128) 112 KB of shared memory and 8 warps of at most 128 registers: two CTAs fit on one SM, so the CTAs
 //    of the next decode launch in the stream (programmatic dependent launch) become resident while this
 //    launch's CTAs still run.  With FTKV_DECODE_STABLE_HISTORY (the caller guarantees that no pending
 //    work writes the slot table, the sequence lengths or the history rows), a CTA fills its whole ring
@@ -63,38 +68,45 @@ constexpr int TWIN = 1024; // slot indices staged in shared memory at a time
 constexpr float kLazyMax = 8.0f;   // log2 slack of the running maximum
 constexpr int kLazyExp = 12;       // w may reach 2^(E + kLazyExp) before E is raised
 
-template <int HC>
+// HC KV heads per CTA, head dimension D (128 or 256).
+template <int HC, int D>
 struct Tok {
   static constexpr int NG = TW / HC;                      // key groups
-  static constexpr int RUN = HC * kHeadDim;               // bytes of one token's codes for the HC heads
+  static constexpr int RUN = HC * D;                      // bytes of one token's codes for the HC heads
   static constexpr int V_OFF = TKB * RUN;                 // stage: K runs [16][RUN], V runs [16][RUN],
   static constexpr int S_OFF = 2 * TKB * RUN;             //        K scales [16][HC], V scales [16][HC]
   static constexpr int STAGE = 2 * TKB * RUN + 2 * TKB * HC * 4;
   static constexpr int RING = NG * TNS * STAGE;
   static constexpr int SLOT_OFF = RING;                   // [TWIN] int32 slot indices
-  static constexpr int Q_OFF = SLOT_OFF + TWIN * 4;       // [HC][8 heads][2 pieces][128] E4M3 codes
-  static constexpr int QM_OFF = Q_OFF + HC * 8 * 2 * kHeadDim;  // [HC][8] FP32 multipliers
-  static constexpr int NEW_OFF = QM_OFF + HC * 8 * 4;     // new token: [HC][K 128 | V 128] codes, [HC][2] scales
-  static constexpr int SMEM = NEW_OFF + HC * (2 * kHeadDim + 8);
+  static constexpr int Q_OFF = SLOT_OFF + TWIN * 4;       // [HC][8 heads][2 pieces][D] E4M3 codes
+  static constexpr int QM_OFF = Q_OFF + HC * 8 * 2 * D;   // [HC][8] FP32 multipliers
+  static constexpr int NEW_OFF = QM_OFF + HC * 8 * 4;     // new token: [HC][K D | V D] codes, [HC][2] scales
+  static constexpr int SMEM = NEW_OFF + HC * (2 * D + 8);
+  static constexpr int CTAS_PER_SM = D == 128 ? 2 : 1;    // D = 256: the ring alone takes ~198 KB
+  static constexpr int KSTEP = 512 / D;                   // keys whose runs one load round covers
+  static constexpr int NSW = 8 / KSTEP;                   // load rounds before the swizzle pattern repeats
 };
-static_assert(Tok<4>::SMEM <= 113 * 1024 && Tok<2>::SMEM <= 113 * 1024 && Tok<1>::SMEM <= 113 * 1024,
+static_assert(Tok<4, 128>::SMEM <= 113 * 1024 && Tok<2, 128>::SMEM <= 113 * 1024 && Tok<1, 128>::SMEM <= 113 * 1024,
               "two CTAs per SM");
+static_assert(Tok<4, 256>::SMEM <= 227 * 1024 && Tok<2, 256>::SMEM <= 227 * 1024 && Tok<1, 256>::SMEM <= 227 * 1024,
+              "one CTA per SM");
 
 // Shared-memory offsets of 16-byte chunk p of KV head hd of key `key` within a stage.  K is read as
-// (key g, chunks 2t and 2t+1) and V as (keys 2t.., chunk g); the XOR swizzles keep both reads and the
-// run-wide cp.async writes free of bank conflicts.
-template <int HC>
+// (key g, chunks 2t and 2t+1 of each 128-d half) and V as (keys 2t.., chunk g of each half); the XOR swizzles
+// (on the chunk's low three bits) keep both reads and the run-wide cp.async writes free of bank conflicts.
+template <int HC, int D>
 __device__ __forceinline__ uint32_t tk_off(int key, int hd, int p) {
-  return key * Tok<HC>::RUN + hd * kHeadDim + ((p ^ (key & 7)) << 4);
+  return key * Tok<HC, D>::RUN + hd * D + ((p ^ (key & 7)) << 4);
 }
-template <int HC>
+template <int HC, int D>
 __device__ __forceinline__ uint32_t tv_off(int key, int hd, int p) {
-  return Tok<HC>::V_OFF + key * Tok<HC>::RUN + hd * kHeadDim + ((p ^ (((key >> 1) & 3) << 1)) << 4);
+  return Tok<HC, D>::V_OFF + key * Tok<HC, D>::RUN + hd * D + ((p ^ (((key >> 1) & 3) << 1)) << 4);
 }
 
-template <int HC>
-__global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs a) {
-  using T = Tok<HC>;
+template <int HC, int D>
+__global__ void __launch_bounds__(TW * 32, Tok<HC, D>::CTAS_PER_SM) decode_tok_kernel(const DecodeArgs a) {
+  using T = Tok<HC, D>;
+  constexpr int NH = D / 128;  // 128-d halves
   constexpr int NG = T::NG;
   extern __shared__ __align__(128) uint8_t smem[];
   int32_t* sslot = reinterpret_cast<int32_t*>(smem + T::SLOT_OFF);
@@ -109,7 +121,7 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
   const int gi = warp / HC, hh = warp % HC;          // key group, KV head within the CTA
   const int lt = threadIdx.x - gi * 32 * HC;         // thread within the key group
   const int64_t hkv = a.num_kv_heads;
-  const int64_t tok_stride = hkv * kHeadDim;         // bytes between consecutive pool rows' codes
+  const int64_t tok_stride = hkv * D;                // bytes between consecutive pool rows' codes
 
   griddep_launch_dependents();
   if (a.scan_scales && threadIdx.x < 2) {  // this CTA's share of the K (thread 0) and V (thread 1) scale array
@@ -138,13 +150,17 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
   const uint32_t ring = smem_addr(smem) + gi * TNS * T::STAGE;
 
   // ---- per-thread load plan: every block, this thread copies 16 bytes of the K run and of the V run of
-  // keys kb, kb + KSTEP, kb + 2 KSTEP, kb + 3 KSTEP (chunk `rem` of the HC-head run), and one scale ----
-  constexpr int KSTEP = 4;                      // 32 HC threads cover 4 keys' runs per round
-  const int kb = lt / (8 * HC), rem = lt % (8 * HC);
-  const int ld_hd = rem >> 3, ld_p = rem & 7;
-  const uint32_t dk0 = tk_off<HC>(kb, ld_hd, ld_p), dk1 = tk_off<HC>(kb + KSTEP, ld_hd, ld_p);
-  const uint32_t dv0 = tv_off<HC>(kb, ld_hd, ld_p), dv1 = tv_off<HC>(kb + KSTEP, ld_hd, ld_p);
-  const int64_t goff = h0 * kHeadDim + rem * 16;
+  // keys kb, kb + KSTEP, .. (16 / KSTEP keys; chunk `rem` of the HC-head run), and one scale ----
+  constexpr int KSTEP = T::KSTEP, NSW = T::NSW, CPH = D / 16;  // CPH: 16-byte chunks per head row
+  const int kb = lt / (CPH * HC), rem = lt % (CPH * HC);
+  const int ld_hd = rem / CPH, ld_p = rem % CPH;
+  uint32_t dko[NSW], dvo[NSW];  // the swizzled destinations of keys kb + r KSTEP repeat every 8 keys
+#pragma unroll
+  for (int r = 0; r < NSW; r++) {
+    dko[r] = tk_off<HC, D>(kb + r * KSTEP, ld_hd, ld_p);
+    dvo[r] = tv_off<HC, D>(kb + r * KSTEP, ld_hd, ld_p);
+  }
+  const int64_t goff = h0 * D + rem * 16;
   const int s_sel = lt / (TKB * HC), s_idx = lt % (TKB * HC);   // scale: tensor, (key, head) index
   const int s_key = s_idx / HC, s_hd = s_idx % HC;
   const float* s_base = (s_sel ? a.v_scales : a.k_scales) + h0 + s_hd;
@@ -169,10 +185,10 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
       const int key0 = (gi + i * NG) * TKB;
       const uint32_t st = ring + (i % TNS) * T::STAGE;
 #pragma unroll
-      for (int r = 0; r < 4; r++) {
+      for (int r = 0; r < TKB / KSTEP; r++) {
         const int key = key0 + kb + r * KSTEP;
-        const uint32_t dk = st + ((r & 1) ? dk1 : dk0) + (r >> 1) * 2 * KSTEP * T::RUN;
-        const uint32_t dv = st + ((r & 1) ? dv1 : dv0) + (r >> 1) * 2 * KSTEP * T::RUN;
+        const uint32_t dk = st + dko[r % NSW] + (r / NSW) * 8 * T::RUN;
+        const uint32_t dv = st + dvo[r % NSW] + (r / NSW) * 8 * T::RUN;
         if (key < nk) {
           if (js + key != new_pos) {
             const int64_t off = static_cast<int64_t>(sslot[key]) * tok_stride + goff;
@@ -198,8 +214,10 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
     return nblk > gi ? (nblk - gi + NG - 1) / NG : 0;
   };
 
-  // ---- before the wait (contract): first slot window, as many history blocks as the ring holds, and
-  // the rest of the window's history requested into L2 ----
+  // ---- before the wait (contract): first slot window and as many history blocks as the ring holds.  (An L2
+  // prefetch of the rest of the window's history here measured slower on the 48-layer 32K step: 711 us issued
+  // at once, 706 us gated on the preceding launch's barrier, against 689 us without; so did triggering the next
+  // launch only after the key loop, 719 us.) ----
   const int nk0 = has_keys ? ((j1 - j0 < TWIN) ? j1 - j0 : TWIN) : 0;
   int pre = 0;  // blocks of window 0 already issued (a prefix of this group's blocks)
   if (early) {
@@ -215,8 +233,8 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
     {
       // the query rows of the CTA's heads (written by the preceding work in a model, so usually in L2
       // already; a prefetch is a hint and reads nothing)
-      if (!a.q_row_offsets && threadIdx.x < HC * a.group * 2)
-        prefetch_l2_keep(a.q + (static_cast<int64_t>(b) * a.num_q_heads + h0 * a.group) * kHeadDim + threadIdx.x * 64);
+      if (!a.q_row_offsets && threadIdx.x < HC * a.group * 2 * NH)
+        prefetch_l2_keep(a.q + (static_cast<int64_t>(b) * a.num_q_heads + h0 * a.group) * D + threadIdx.x * 64);
     }
     griddep_wait();
   }
@@ -243,34 +261,39 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
 
   // ---- query loads (one warp per (KV head, query head of its group), every load in flight at once) ----
   constexpr int NPR = (HC * 8 + TW - 1) / TW;
-  uint2 qv[NPR];
+  constexpr int EPL = D / 32;  // query elements per lane (4 or 8)
+  uint2 qv[NPR][NH];
 #pragma unroll
   for (int u = 0; u < NPR; u++) {
     const int pr = warp + u * TW, hd = pr >> 3, hq = pr & 7;
-    qv[u] = (pr < HC * 8 && hq < a.group)
-                ? __ldg(reinterpret_cast<const uint2*>(a.q + (row0 * a.num_q_heads + (h0 + hd) * a.group + hq) * kHeadDim +
-                                                      4 * lane))
-                : make_uint2(0u, 0u);
+    const bool ok = pr < HC * 8 && hq < a.group;
+    const uint2* src = reinterpret_cast<const uint2*>(a.q + (row0 * a.num_q_heads + (h0 + hd) * a.group + hq) * D +
+                                                      EPL * lane);
+#pragma unroll
+    for (int hf = 0; hf < NH; hf++) qv[u][hf] = ok ? __ldg(src + hf) : make_uint2(0u, 0u);
   }
 
   // ---- fused store of the request's new token (position n - 1), if it falls in this slice: one warp per
   // KV head, K row on lanes 0-15 and V row on lanes 16-31, with the store kernel's arithmetic; the codes and
   // scales also go to shared memory, from where they are patched into the token's block ----
   const bool has_new = new_pos >= j0 && new_pos < j1;  // CTA-uniform (R == 1 here)
-  if (has_new && warp < HC) {
-    const int hd = warp, half = lane >> 4, l = lane & 15;
-    const uint16_t* src = (half ? a.v_new : a.k_new) + (row0 * hkv + h0 + hd) * kHeadDim + l * 8;
+  // (D = 256: one warp per (KV head, tensor), 32 lanes x 8 elements)
+  constexpr int LPR = D / 8;  // lanes per row
+  if (has_new && warp < HC * NH) {
+    const int hd = (NH == 1) ? warp : warp >> 1;
+    const int half = (NH == 1) ? lane >> 4 : warp & 1, l = lane % LPR;
+    const uint16_t* src = (half ? a.v_new : a.k_new) + (row0 * hkv + h0 + hd) * D + l * 8;
     const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
     const int32_t sv = a.req_to_slot[static_cast<int64_t>(b) * a.req_stride + new_pos];
     float sc;
-    const uint2 packed = quantize_row_lane8(raw, sc);
-    *reinterpret_cast<uint2*>(newtok + hd * 2 * kHeadDim + half * kHeadDim + l * 8) = packed;
-    if (l == 0) reinterpret_cast<float*>(newtok + HC * 2 * kHeadDim)[hd * 2 + half] = sc;
+    const uint2 packed = quantize_row_lane8<LPR>(raw, sc);
+    *reinterpret_cast<uint2*>(newtok + hd * 2 * D + half * D + l * 8) = packed;
+    if (l == 0) reinterpret_cast<float*>(newtok + HC * 2 * D)[hd * 2 + half] = sc;
     if (sv >= 0 && sv < a.num_rows) {  // a bad slot is flagged when staged; nothing is written
       const int64_t row = static_cast<int64_t>(sv) * hkv + h0 + hd;
       // the pool is the caller's writable memory (ftkv_pool holds non-const pointers); later kernels see
       // these rows once this one has completed, and this kernel reads the token from shared memory
-      *reinterpret_cast<uint2*>(const_cast<uint8_t*>(half ? a.v_codes : a.k_codes) + row * kHeadDim + l * 8) = packed;
+      *reinterpret_cast<uint2*>(const_cast<uint8_t*>(half ? a.v_codes : a.k_codes) + row * D + l * 8) = packed;
       if (l == 0) const_cast<float*>(half ? a.v_scales : a.k_scales)[row] = sc;
     }
   }
@@ -282,59 +305,76 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
   for (int u = 0; u < NPR; u++) {
     const int pr = warp + u * TW;
     if (pr >= HC * 8) break;  // warp-uniform
-    float x[4] = {bf16_lo(qv[u].x), bf16_hi(qv[u].x), bf16_lo(qv[u].y), bf16_hi(qv[u].y)};
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    float x[NH][4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int hf = 0; hf < NH; hf++) {
+      x[hf][0] = bf16_lo(qv[u][hf].x);
+      x[hf][1] = bf16_hi(qv[u][hf].x);
+      x[hf][2] = bf16_lo(qv[u][hf].y);
+      x[hf][3] = bf16_hi(qv[u][hf].y);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[hf][0]), fabsf(x[hf][1])), fmaxf(fabsf(x[hf][2]), fabsf(x[hf][3]))));
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     int ex = (amax > 0.0f) ? ilogbf(amax) : 0;
     ex = ex < -120 ? -120 : ex;
     const float up = __uint_as_float(static_cast<uint32_t>(127 + 7 - ex) << 23);
+    uint8_t* dst = qsm + pr * 2 * D + EPL * lane;  // lane holds d = EPL lane .. EPL lane + EPL - 1
 #pragma unroll
-    for (int e = 0; e < 4; e++) x[e] *= up;
-    uint8_t* dst = qsm + pr * 2 * kHeadDim + 4 * lane;
+    for (int hf = 0; hf < NH; hf++) {
+      float* xh = x[hf];
 #pragma unroll
-    for (int p = 0; p < 2; p++) {
-      const uint32_t c01 = e4m3x2_encode(x[0], x[1]), c23 = e4m3x2_encode(x[2], x[3]);
-      *reinterpret_cast<uint32_t*>(dst + p * kHeadDim) = c01 | (c23 << 16);
-      if (p == 0) {
-        const float2 v01 = f16x2_to_float2(e4m3x2_to_f16x2(c01));
-        const float2 v23 = f16x2_to_float2(e4m3x2_to_f16x2(c23));
-        x[0] = (x[0] - v01.x) * 16.0f;
-        x[1] = (x[1] - v01.y) * 16.0f;
-        x[2] = (x[2] - v23.x) * 16.0f;
-        x[3] = (x[3] - v23.y) * 16.0f;
+      for (int e = 0; e < 4; e++) xh[e] *= up;
+#pragma unroll
+      for (int p = 0; p < 2; p++) {
+        const uint32_t c01 = e4m3x2_encode(xh[0], xh[1]), c23 = e4m3x2_encode(xh[2], xh[3]);
+        *reinterpret_cast<uint32_t*>(dst + p * D + 4 * hf) = c01 | (c23 << 16);
+        if (p == 0) {
+          const float2 v01 = f16x2_to_float2(e4m3x2_to_f16x2(c01));
+          const float2 v23 = f16x2_to_float2(e4m3x2_to_f16x2(c23));
+          xh[0] = (xh[0] - v01.x) * 16.0f;
+          xh[1] = (xh[1] - v01.y) * 16.0f;
+          xh[2] = (xh[2] - v23.x) * 16.0f;
+          xh[3] = (xh[3] - v23.y) * 16.0f;
+        }
       }
     }
     if (lane == 0) qmul[pr] = __uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * a.qk_scale_log2;
   }
   __syncthreads();  // slots, pieces and the new token's codes before any block is computed or (re)loaded
 
-  // B operand of QK^T for this warp's KV head: query head g, d = 32t + 8kk + {0..3} (b0) / {4..7} (b1)
-  uint32_t qp[2][4][2];
+  // B operand of QK^T for this warp's KV head: query head g, d = 128hf + 32t + 8kk' + {0..3} (b0) / {4..7}
+  // (b1) for k-step kk = 4hf + kk'
+  uint32_t qp[2][4 * NH][2];
   float fq[2];
   {
-    const uint32_t src = smem_addr(qsm) + (hh * 8 + g) * 2 * kHeadDim + 32 * t;
+    const uint32_t src = smem_addr(qsm) + (hh * 8 + g) * 2 * D + 32 * t;
 #pragma unroll
-    for (int p = 0; p < 2; p++) {
-      const uint4 w0 = ld_shared_v4(src + p * kHeadDim);
-      const uint4 w1 = ld_shared_v4(src + p * kHeadDim + 16);
-      qp[p][0][0] = w0.x; qp[p][0][1] = w0.y; qp[p][1][0] = w0.z; qp[p][1][1] = w0.w;
-      qp[p][2][0] = w1.x; qp[p][2][1] = w1.y; qp[p][3][0] = w1.z; qp[p][3][1] = w1.w;
-    }
+    for (int p = 0; p < 2; p++)
+#pragma unroll
+      for (int hf = 0; hf < NH; hf++) {
+        const uint4 w0 = ld_shared_v4(src + p * D + 128 * hf);
+        const uint4 w1 = ld_shared_v4(src + p * D + 128 * hf + 16);
+        qp[p][4 * hf + 0][0] = w0.x; qp[p][4 * hf + 0][1] = w0.y; qp[p][4 * hf + 1][0] = w0.z; qp[p][4 * hf + 1][1] = w0.w;
+        qp[p][4 * hf + 2][0] = w1.x; qp[p][4 * hf + 2][1] = w1.y; qp[p][4 * hf + 3][0] = w1.z; qp[p][4 * hf + 3][1] = w1.w;
+      }
     fq[0] = qmul[hh * 8 + 2 * t];
     fq[1] = qmul[hh * 8 + 2 * t + 1];
   }
   // fragment offsets within a stage (loop-invariant)
-  const uint32_t oK0 = tk_off<HC>(g, hh, 2 * t), oK1 = tk_off<HC>(g, hh, 2 * t + 1);
-  const uint32_t oK2 = tk_off<HC>(g + 8, hh, 2 * t), oK3 = tk_off<HC>(g + 8, hh, 2 * t + 1);
-  const uint32_t oV0 = tv_off<HC>(2 * t, hh, g), oV1 = tv_off<HC>(2 * t + 1, hh, g);
-  const uint32_t oV2 = tv_off<HC>(2 * t + 8, hh, g), oV3 = tv_off<HC>(2 * t + 9, hh, g);
+  // (the second 128-d half: chunks 8 + the first half's, same swizzle; tk_off(key, hd, p + 8) = that + 128)
+  const uint32_t oK0 = tk_off<HC, D>(g, hh, 2 * t), oK1 = tk_off<HC, D>(g, hh, 2 * t + 1);
+  const uint32_t oK2 = tk_off<HC, D>(g + 8, hh, 2 * t), oK3 = tk_off<HC, D>(g + 8, hh, 2 * t + 1);
+  const uint32_t oV0 = tv_off<HC, D>(2 * t, hh, g), oV1 = tv_off<HC, D>(2 * t + 1, hh, g);
+  const uint32_t oV2 = tv_off<HC, D>(2 * t + 8, hh, g), oV3 = tv_off<HC, D>(2 * t + 9, hh, g);
   const uint32_t oS0 = T::S_OFF + (g * HC + hh) * 4, oS1 = T::S_OFF + ((g + 8) * HC + hh) * 4;
   constexpr uint32_t VS = TKB * HC * 4;  // V scales follow the K scales
 
-  float acc[8][4];
+  constexpr int MT = D / 16;  // accumulator tiles: d = 128hf + 16g + ..
+  float acc[MT][4];
 #pragma unroll
-  for (int mt = 0; mt < 8; mt++) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+  for (int mt = 0; mt < MT; mt++) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
   float m[2] = {-INFINITY, -INFINITY};  // running maximum of s (log2 units), per query head 2t, 2t+1
   float l[2] = {0.0f, 0.0f};            // this lane's share of sum 2^(s - m)
   int E[2] = {-126, -126};              // FP16 operand exponent: PV takes w * 2^-E
@@ -365,34 +405,38 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
       const int key0 = (gi + i * NG) * TKB;
       if (new_key >= key0 && new_key < key0 + TKB) {  // warp-uniform: patch this head's new token in
         const int kk = new_key - key0;
-        const uint8_t* nt = newtok + hh * 2 * kHeadDim;
-        if (lane < 8)
-          st_shared_v4(st + tk_off<HC>(kk, hh, lane), *reinterpret_cast<const uint4*>(nt + lane * 16));
-        else if (lane < 16)
-          st_shared_v4(st + tv_off<HC>(kk, hh, lane - 8), *reinterpret_cast<const uint4*>(nt + kHeadDim + (lane - 8) * 16));
-        else if (lane < 18)
-          st_shared_u32(st + T::S_OFF + (lane - 16) * VS + (kk * HC + hh) * 4,
-                        __float_as_uint(reinterpret_cast<const float*>(newtok + HC * 2 * kHeadDim)[hh * 2 + lane - 16]));
+        const uint8_t* nt = newtok + hh * 2 * D;
+        if (lane < CPH)
+          st_shared_v4(st + tk_off<HC, D>(kk, hh, lane), *reinterpret_cast<const uint4*>(nt + lane * 16));
+        else if (lane < 2 * CPH)
+          st_shared_v4(st + tv_off<HC, D>(kk, hh, lane - CPH), *reinterpret_cast<const uint4*>(nt + D + (lane - CPH) * 16));
+        if (lane < 2)
+          st_shared_u32(st + T::S_OFF + lane * VS + (kk * HC + hh) * 4,
+                        __float_as_uint(reinterpret_cast<const float*>(newtok + HC * 2 * D)[hh * 2 + lane]));
         __syncwarp();
       }
       const int jb = js + key0;
 
       // ---- S^T = K Q^T on E4M3 codes: keys as M (rows g, g+8), query heads as N, 2 query pieces ----
-      const uint4 kA0 = ld_shared_v4(st + oK0);
-      const uint4 kA1 = ld_shared_v4(st + oK1);
-      const uint4 kB0 = ld_shared_v4(st + oK2);
-      const uint4 kB1 = ld_shared_v4(st + oK3);
       float c[2][4];
 #pragma unroll
       for (int p = 0; p < 2; p++) c[p][0] = c[p][1] = c[p][2] = c[p][3] = 0.0f;
 #pragma unroll
-      for (int kk = 0; kk < 4; kk++) {
-        const uint4& A = kk < 2 ? kA0 : kA1;
-        const uint4& B = kk < 2 ? kB0 : kB1;
-        const uint32_t a0 = word(A, 2 * (kk & 1)), a2 = word(A, 2 * (kk & 1) + 1);
-        const uint32_t a1 = word(B, 2 * (kk & 1)), a3 = word(B, 2 * (kk & 1) + 1);
+      for (int hf = 0; hf < NH; hf++) {
+        const uint4 kA0 = ld_shared_v4(st + oK0 + 128 * hf);
+        const uint4 kA1 = ld_shared_v4(st + oK1 + 128 * hf);
+        const uint4 kB0 = ld_shared_v4(st + oK2 + 128 * hf);
+        const uint4 kB1 = ld_shared_v4(st + oK3 + 128 * hf);
 #pragma unroll
-        for (int p = 0; p < 2; p++) mma_e4m3_16832(c[p], a0, a1, a2, a3, qp[p][kk][0], qp[p][kk][1]);
+        for (int kk = 0; kk < 4; kk++) {
+          const uint4& A = kk < 2 ? kA0 : kA1;
+          const uint4& B = kk < 2 ? kB0 : kB1;
+          const uint32_t a0 = word(A, 2 * (kk & 1)), a2 = word(A, 2 * (kk & 1) + 1);
+          const uint32_t a1 = word(B, 2 * (kk & 1)), a3 = word(B, 2 * (kk & 1) + 1);
+#pragma unroll
+          for (int p = 0; p < 2; p++)
+            mma_e4m3_16832(c[p], a0, a1, a2, a3, qp[p][4 * hf + kk][0], qp[p][4 * hf + kk][1]);
+        }
       }
       const float skg = ld_shared_f32(st + oS0), skg8 = ld_shared_f32(st + oS1);
       const float svg = ld_shared_f32(st + oS0 + VS), svg8 = ld_shared_f32(st + oS1 + VS);
@@ -419,7 +463,7 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
         l[0] *= al0;
         l[1] *= al1;
 #pragma unroll
-        for (int mt = 0; mt < 8; mt++) {
+        for (int mt = 0; mt < MT; mt++) {
           acc[mt][0] *= al0;
           acc[mt][1] *= al1;
           acc[mt][2] *= al0;
@@ -456,7 +500,7 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
         iw[0] = exp2i(-ne0);
         iw[1] = exp2i(-ne1);
 #pragma unroll
-        for (int mt = 0; mt < 8; mt++) {
+        for (int mt = 0; mt < MT; mt++) {
           acc[mt][0] *= f0;
           acc[mt][1] *= f1;
           acc[mt][2] *= f0;
@@ -466,18 +510,23 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
       const uint32_t pb0 = movmatrix_trans(float2_to_f16x2(w0 * iw[0], w1 * iw[1]));   // keys 0..7
       const uint32_t pb1 = movmatrix_trans(float2_to_f16x2(w2 * iw[0], w3 * iw[1]));   // keys 8..15
 
-      // ---- O^T += V^T P'^T in place: d as M (d = 16g + 2mt [+1]), query heads as N, keys as K ----
-      const uint4 v0 = ld_shared_v4(st + oV0);
-      const uint4 v1 = ld_shared_v4(st + oV1);
-      const uint4 v8 = ld_shared_v4(st + oV2);
-      const uint4 v9 = ld_shared_v4(st + oV3);
+      // ---- O^T += V^T P'^T in place: d as M (tile 8hf + 2w + {0, 1}: d = 128hf + 16g + 4w + {0, 1} / {2, 3}),
+      // query heads as N, keys as K ----
 #pragma unroll
-      for (int w = 0; w < 4; w++) {
-        const uint32_t x0 = word(v0, w), x1 = word(v1, w), x8 = word(v8, w), x9 = word(v9, w);
-        const uint32_t lo01 = prmt(x0, x1, 0x5140), hi01 = prmt(x0, x1, 0x7362);
-        const uint32_t lo89 = prmt(x8, x9, 0x5140), hi89 = prmt(x8, x9, 0x7362);
-        mma_f16_16816(acc[2 * w], e4m3_lo2(lo01), e4m3_hi2(lo01), e4m3_lo2(lo89), e4m3_hi2(lo89), pb0, pb1);
-        mma_f16_16816(acc[2 * w + 1], e4m3_lo2(hi01), e4m3_hi2(hi01), e4m3_lo2(hi89), e4m3_hi2(hi89), pb0, pb1);
+      for (int hf = 0; hf < NH; hf++) {
+        const uint4 v0 = ld_shared_v4(st + oV0 + 128 * hf);
+        const uint4 v1 = ld_shared_v4(st + oV1 + 128 * hf);
+        const uint4 v8 = ld_shared_v4(st + oV2 + 128 * hf);
+        const uint4 v9 = ld_shared_v4(st + oV3 + 128 * hf);
+#pragma unroll
+        for (int w = 0; w < 4; w++) {
+          const uint32_t x0 = word(v0, w), x1 = word(v1, w), x8 = word(v8, w), x9 = word(v9, w);
+          const uint32_t lo01 = prmt(x0, x1, 0x5140), hi01 = prmt(x0, x1, 0x7362);
+          const uint32_t lo89 = prmt(x8, x9, 0x5140), hi89 = prmt(x8, x9, 0x7362);
+          mma_f16_16816(acc[8 * hf + 2 * w], e4m3_lo2(lo01), e4m3_hi2(lo01), e4m3_lo2(lo89), e4m3_hi2(lo89), pb0, pb1);
+          mma_f16_16816(acc[8 * hf + 2 * w + 1], e4m3_lo2(hi01), e4m3_hi2(hi01), e4m3_lo2(hi89), e4m3_hi2(hi89), pb0,
+                        pb1);
+        }
       }
     }
     cp_async_wait<0>();
@@ -491,29 +540,34 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l[hx] += __shfl_xor_sync(0xffffffffu, l[hx], off);
   const int G = a.group;
-  // lane (g, t) holds d = 16g + 4q4 + {0..3} of query head 2t + hx: acc[2q4][hx], acc[2q4][2+hx],
-  // acc[2q4+1][hx], acc[2q4+1][2+hx]; bring it to units of 2^m
+  // lane (g, t) holds d = 128hf + 16g + 4q4 + {0..3} of query head 2t + hx: acc[8hf+2q4][hx], acc[8hf+2q4][2+hx],
+  // acc[8hf+2q4+1][hx], acc[8hf+2q4+1][2+hx]; bring it to units of 2^m
 #pragma unroll
   for (int hx = 0; hx < 2; hx++) {
     const float up = exp2i(E[hx]);
 #pragma unroll
-    for (int mt = 0; mt < 8; mt++) {
+    for (int mt = 0; mt < MT; mt++) {
       acc[mt][hx] *= up;
       acc[mt][2 + hx] *= up;
     }
   }
   if constexpr (NG > 1) {
-    float* gacc = reinterpret_cast<float*>(smem);                   // [NG-1][HC][8][128]
-    float* gml = gacc + (NG - 1) * HC * 8 * kHeadDim;               // [NG-1][HC][8][2]
+    float* gacc = reinterpret_cast<float*>(smem);                   // [NG-1][HC][8][D]
+    float* gml = gacc + (NG - 1) * HC * 8 * D;                      // [NG-1][HC][8][2]
     __syncthreads();  // every group is done with the ring
     if (gi > 0) {
 #pragma unroll
       for (int hx = 0; hx < 2; hx++) {
         const int slot = ((gi - 1) * HC + hh) * 8 + 2 * t + hx;
-        float4* dst = reinterpret_cast<float4*>(gacc + slot * kHeadDim + 16 * g);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; q4++)
-          dst[q4] = make_float4(acc[2 * q4][hx], acc[2 * q4][2 + hx], acc[2 * q4 + 1][hx], acc[2 * q4 + 1][2 + hx]);
+        for (int hf = 0; hf < NH; hf++) {
+          float4* dst = reinterpret_cast<float4*>(gacc + slot * D + 128 * hf + 16 * g);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; q4++) {
+            const int mt = 8 * hf + 2 * q4;
+            dst[q4] = make_float4(acc[mt][hx], acc[mt][2 + hx], acc[mt + 1][hx], acc[mt + 1][2 + hx]);
+          }
+        }
         if (g == 0) *reinterpret_cast<float2*>(gml + slot * 2) = make_float2(m[hx], l[hx]);
       }
     }
@@ -528,14 +582,18 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
         if (mn == -INFINITY) continue;  // neither holds a key
         const float f = (m[hx] == -INFINITY) ? 0.0f : fast_exp2(m[hx] - mn);
         const float fo = (mlo.x == -INFINITY) ? 0.0f : fast_exp2(mlo.x - mn);
-        const float4* src = reinterpret_cast<const float4*>(gacc + slot * kHeadDim + 16 * g);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; q4++) {
-          const float4 v = src[q4];
-          acc[2 * q4][hx] = fmaf(acc[2 * q4][hx], f, v.x * fo);
-          acc[2 * q4][2 + hx] = fmaf(acc[2 * q4][2 + hx], f, v.y * fo);
-          acc[2 * q4 + 1][hx] = fmaf(acc[2 * q4 + 1][hx], f, v.z * fo);
-          acc[2 * q4 + 1][2 + hx] = fmaf(acc[2 * q4 + 1][2 + hx], f, v.w * fo);
+        for (int hf = 0; hf < NH; hf++) {
+          const float4* src = reinterpret_cast<const float4*>(gacc + slot * D + 128 * hf + 16 * g);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; q4++) {
+            const float4 v = src[q4];
+            const int mt = 8 * hf + 2 * q4;
+            acc[mt][hx] = fmaf(acc[mt][hx], f, v.x * fo);
+            acc[mt][2 + hx] = fmaf(acc[mt][2 + hx], f, v.y * fo);
+            acc[mt + 1][hx] = fmaf(acc[mt + 1][hx], f, v.z * fo);
+            acc[mt + 1][2 + hx] = fmaf(acc[mt + 1][2 + hx], f, v.w * fo);
+          }
         }
         l[hx] = fmaf(l[hx], f, mlo.y * fo);
         m[hx] = mn;
@@ -548,29 +606,35 @@ __global__ void __launch_bounds__(TW * 32, 2) decode_tok_kernel(const DecodeArgs
     const int hq = 2 * t + hx;  // query head within the KV head's group (N column)
     if (gi == 0 && hq < G) {
       const int64_t prow = row0 * a.num_q_heads + (h0 + hh) * G + hq;
-      float4* dst = reinterpret_cast<float4*>(a.part_acc) + (prow * (kHeadDim / 4) + 4 * g) * nsl + split;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; q4++)
-        dst[q4 * nsl] = make_float4(acc[2 * q4][hx], acc[2 * q4][2 + hx], acc[2 * q4 + 1][hx], acc[2 * q4 + 1][2 + hx]);
+      for (int hf = 0; hf < NH; hf++) {
+        float4* dst = reinterpret_cast<float4*>(a.part_acc) + (prow * (D / 4) + 32 * hf + 4 * g) * nsl + split;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; q4++) {
+          const int mt = 8 * hf + 2 * q4;
+          dst[q4 * nsl] = make_float4(acc[mt][hx], acc[mt][2 + hx], acc[mt + 1][hx], acc[mt + 1][2 + hx]);
+        }
+      }
       if (g == 0) *reinterpret_cast<float2*>(a.part_ml + (prow * nsl + split) * 2) = make_float2(m[hx], l[hx]);
     }
   }
   if (a.coop) coop_finish<TW>(a);  // grid barrier, then the merge spread over the grid
 }
 
-template <int HC>
+template <int HC, int D>
 cudaError_t launch_tok(const DecodeArgs& a, cudaStream_t s, int dev) {
+  using T = Tok<HC, D>;
   static std::once_flag once[kMaxDecodeDevices];
   static cudaError_t setup_err[kMaxDecodeDevices];
   static int resident[kMaxDecodeDevices];
   std::call_once(once[dev], [&] {
-    setup_err[dev] = cudaFuncSetAttribute(decode_tok_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          Tok<HC>::SMEM);
+    setup_err[dev] = cudaFuncSetAttribute(decode_tok_kernel<HC, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          T::SMEM);
     int coop_ok = 0, sms = 0, per_sm = 0;
     if (setup_err[dev] == cudaSuccess) setup_err[dev] = cudaDeviceGetAttribute(&coop_ok, cudaDevAttrCooperativeLaunch, dev);
     if (setup_err[dev] == cudaSuccess) setup_err[dev] = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (setup_err[dev] == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tok_kernel<HC>, TW * 32, Tok<HC>::SMEM) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tok_kernel<HC, D>, TW * 32, T::SMEM) !=
             cudaSuccess)
       per_sm = 0;
     resident[dev] = (coop_ok && per_sm > 0 && sms > 0) ? per_sm * sms : -1;
@@ -582,10 +646,10 @@ cudaError_t launch_tok(const DecodeArgs& a, cudaStream_t s, int dev) {
   c.ptrans = 1;
   const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
   c.coop = (resident[dev] > 0 && ctas <= resident[dev]) ? 1 : 0;
-  if (c.coop) return launch_k_coop(decode_tok_kernel<HC>, grid, dim3(TW * 32), Tok<HC>::SMEM, s, c);
-  cudaError_t e = launch_k(decode_tok_kernel<HC>, grid, dim3(TW * 32), Tok<HC>::SMEM, s, c);
+  if (c.coop) return launch_k_coop(decode_tok_kernel<HC, D>, grid, dim3(TW * 32), T::SMEM, s, c);
+  cudaError_t e = launch_k(decode_tok_kernel<HC, D>, grid, dim3(TW * 32), T::SMEM, s, c);
   if (e != cudaSuccess) return e;
-  const int64_t items = a.total_q_rows * a.num_q_heads * (kHeadDim / 4);
+  const int64_t items = a.total_q_rows * a.num_q_heads * (D / 4);
   return launch_k(decode_merge_kernel<kMergeWarps>, dim3(static_cast<unsigned>((items + kMergeWarps - 1) / kMergeWarps)),
                   dim3(kMergeWarps * 32), 0, s, c);
 }
@@ -601,10 +665,18 @@ cudaError_t launch_decode_tok(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDecodeDevices) return cudaErrorInvalidDevice;
-  switch (decode_tok_heads_per_cta(a.num_kv_heads)) {
-    case 4: return launch_tok<4>(a, s, dev);
-    case 2: return launch_tok<2>(a, s, dev);
-    default: return launch_tok<1>(a, s, dev);
+  const int hc = decode_tok_heads_per_cta(a.num_kv_heads);
+  if (a.head_dim == 256) {
+    switch (hc) {
+      case 4: return launch_tok<4, 256>(a, s, dev);
+      case 2: return launch_tok<2, 256>(a, s, dev);
+      default: return launch_tok<1, 256>(a, s, dev);
+    }
+  }
+  switch (hc) {
+    case 4: return launch_tok<4, 128>(a, s, dev);
+    case 2: return launch_tok<2, 128>(a, s, dev);
+    default: return launch_tok<1, 128>(a, s, dev);
   }
 }
 

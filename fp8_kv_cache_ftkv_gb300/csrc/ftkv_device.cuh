@@ -66,6 +66,7 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Every lane of the warp calls it: the max reduction shuffles within each 16-lane half.  Returns the
 // lane's 8 codes (element 8l in the lowest byte) and sets `scale`.  The store kernel and the decode
 // kernel's fused store both use this one definition.
+template <int LANES = 16>  // lanes that carry one row (8 elements each): 16 for 128-d rows, 32 for 256-d
 __device__ __forceinline__ uint2 quantize_row_lane8(const uint4 raw, float& scale) {
   float x[8];
   x[0] = bf16_lo(raw.x); x[1] = bf16_hi(raw.x);
@@ -76,7 +77,7 @@ __device__ __forceinline__ uint2 quantize_row_lane8(const uint4 raw, float& scal
 #pragma unroll
   for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
-  for (int off = 1; off < 16; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  for (int off = 1; off < LANES; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   scale = __fdiv_rn(amax, 448.0f);
   const float div = (scale == 0.0f) ? 1.0f : scale;
   float q[8];

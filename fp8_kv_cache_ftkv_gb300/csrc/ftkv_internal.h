@@ -18,6 +18,7 @@ struct StoreArgs {
   const int32_t* slots;
   int64_t num_tokens;
   int num_kv_heads;
+  int head_dim;              // 128 or 256
   uint8_t* k_codes;
   uint8_t* v_codes;
   float* k_scales;
@@ -49,7 +50,8 @@ struct DecodeArgs {
   int num_q_heads;
   int num_kv_heads;
   int group;                 // num_q_heads / num_kv_heads (1, 2, 4 or 8)
-  const uint16_t* q;         // [total_q_rows][Hq][128]
+  int head_dim;              // D: 128, or 256 (single-row kernel only)
+  const uint16_t* q;         // [total_q_rows][Hq][D]
   const int32_t* req_to_slot;
   int64_t req_stride;
   const int32_t* seq_lens;
@@ -64,13 +66,13 @@ struct DecodeArgs {
   int64_t chunk;             // keys per slice (multiple of 16)
   float qk_scale_log2;       // sm_scale * log2(e)
   int64_t window;            // 0: full attention; W > 0: each query row attends to its last W visible keys
-  int ptrans;                // partial accumulators transposed: [total_q_rows][Hq][32 quads][num_splits * pps]
+  int ptrans;                // partial accumulators transposed: [total_q_rows][Hq][D / 4 quads][num_splits * pps]
                              // float4 (the merge's loads of one quad over the slices are contiguous); else
-                             // [total_q_rows][Hq][num_splits * pps][128] floats
+                             // [total_q_rows][Hq][num_splits * pps][D] floats
   float* part_acc;
   float* part_ml;            // [total_q_rows][Hq][num_splits * pps][2]  (max in log2 units, sum)
   int* counters;             // [batch][Hkv] arrival tickets; zero between calls
-  uint16_t* out;             // [total_q_rows][Hq][128]
+  uint16_t* out;             // [total_q_rows][Hq][D]
   int* err;
   int early;                 // FTKV_DECODE_STABLE_HISTORY: history loads may start before the preceding grid ends
   int scan_scales;           // the slot tables may cover most of the pool: bring the scale arrays into L2 whole
@@ -183,8 +185,8 @@ struct DecodeGeom {
 };
 // Every argument check of a decode call except the pool's (the caller checks its pool first), and the split
 // geometry.
-int decode_validate_dims(int32_t num_kv_heads, int32_t num_q_heads, const uint16_t* q, const int32_t* req_to_slot,
-                         int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
+int decode_validate_dims(int32_t num_kv_heads, int32_t head_dim, int32_t num_q_heads, const uint16_t* q,
+                         const int32_t* req_to_slot, int64_t req_stride, const int32_t* seq_lens, const int32_t* q_row_offsets, int32_t batch,
                          int64_t total_q_rows, int32_t max_q_rows, int64_t max_seq_len, float sm_scale,
                          int64_t window, int32_t num_splits, uint32_t flags, const void* workspace,
                          size_t workspace_bytes, const uint16_t* out, bool check_workspace, DecodeGeom* geom);

@@ -2,7 +2,8 @@
 // the BF16 workspace, and the bare E4M3FN codec.
 //
 // Row format (FreeToken PR #853, "What changes"; issue #280, "Proof of concept"): one row = one
-// token x one KV head = 128 E4M3FN codes + one FP32 scale.  scale = absmax / 448 (IEEE FP32
+// token x one KV head = head_dim (128, or 256 for the store and the single-row decode) E4M3FN codes + one
+// FP32 scale.  scale = absmax / 448 (IEEE FP32
 // division), code = E4M3FN_rne_satfinite(x / scale) (IEEE FP32 division); a row of zeros keeps scale
 // 0 and divides by 1.  Both kernels are pure HBM streams; a warp moves whole rows with 16-byte
 // accesses so every request is a full 32-byte sector run.
@@ -12,7 +13,8 @@
 namespace ftkv {
 
 // ---------------------------------------------------------------------------------------------
-// Quantize-on-write.  Half a warp carries one row (token, KV head, tensor): 16 lanes x 8 BF16 elements.
+// Quantize-on-write.  Half a warp carries one 128-d row (token, KV head, tensor): 16 lanes x 8 BF16
+// elements; a 256-d row takes a whole warp (32 lanes x 8), and a (token, head) pair two warps (K, V).
 // A warp handles STORE_UNITS (token, head) pairs -- K and V rows of each -- and issues all its loads
 // before any arithmetic.  One pair per warp: more warps in flight hide the division's latency better
 // than longer load batches per warp (48-layer store: 1 pair 431 us, 2 pairs 468 us, 4 pairs 618 us).
@@ -40,12 +42,16 @@ __device__ __forceinline__ void split_unit(int64_t unit, int hkv, int64_t& t, in
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
   pdl_enter();
-  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  constexpr int LPR = D / 8;    // lanes per row, 8 elements each
+  const int64_t gwarp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;   // 0: K, 1: V
-  const int l = lane & 15;      // 8 elements per lane
+  // D = 128: one warp per pair, K on lanes 0-15 and V on 16-31; D = 256: warp 2u carries K, 2u + 1 V
+  const int64_t warp_id = (D == 128) ? gwarp : gwarp >> 1;
+  const int half = (D == 128) ? lane >> 4 : static_cast<int>(gwarp & 1);  // 0: K, 1: V
+  const int l = lane % LPR;
   const int64_t total = a.num_tokens * a.num_kv_heads;
   uint4 raw[STORE_UNITS];
   int32_t slot[STORE_UNITS];
@@ -59,7 +65,7 @@ __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
       int h;
       split_unit(unit, a.num_kv_heads, t, h);
       slot[u] = __ldg(a.slots + t);
-      raw[u] = ldg_stream16((half ? a.v : a.k) + (t * a.num_kv_heads + h) * kHeadDim + l * 8);
+      raw[u] = ldg_stream16((half ? a.v : a.k) + (t * a.num_kv_heads + h) * D + l * 8);
     }
   }
 #pragma unroll
@@ -70,13 +76,13 @@ __global__ void __launch_bounds__(256) store_quant_kernel(StoreArgs a) {
     int h;
     split_unit(unit, a.num_kv_heads, t, h);
     float scale;
-    const uint2 packed = quantize_row_lane8(raw[u], scale);  // every lane: the reduction shuffles
+    const uint2 packed = quantize_row_lane8<LPR>(raw[u], scale);  // every lane: the reduction shuffles
     if (slot[u] < 0 || slot[u] >= a.num_rows) {
       if (lane == 0) flag_error(a.err, kDevErrBadSlot);
       continue;
     }
     const int64_t row = static_cast<int64_t>(slot[u]) * a.num_kv_heads + h;
-    __stcs(reinterpret_cast<uint2*>((half ? a.v_codes : a.k_codes) + row * kHeadDim + l * 8), packed);
+    __stcs(reinterpret_cast<uint2*>((half ? a.v_codes : a.k_codes) + row * D + l * 8), packed);
     if (l == 0) __stcs((half ? a.v_scales : a.k_scales) + row, scale);
   }
 }
@@ -170,9 +176,11 @@ __global__ void e4m3_decode_kernel(const uint8_t* __restrict__ c, float* __restr
 
 // ---------------------------------------------------------------------------------------------
 cudaError_t launch_store_quant(const StoreArgs& a, cudaStream_t s) {
-  const int64_t warps = (a.num_tokens * a.num_kv_heads + STORE_UNITS - 1) / STORE_UNITS;
+  const int64_t warps = (a.num_tokens * a.num_kv_heads + STORE_UNITS - 1) / STORE_UNITS * (a.head_dim / 128);
   const int64_t blocks = (warps * 32 + 255) / 256;
-  return launch_k(store_quant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
+  if (a.head_dim == 256)
+    return launch_k(store_quant_kernel<256>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
+  return launch_k(store_quant_kernel<128>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_reconstruct(const ReconstructArgs& a, cudaStream_t s) {

@@ -61,6 +61,10 @@ class KVPool:
     def num_kv_heads(self) -> int:
         return self.k_codes.shape[1]
 
+    @property
+    def head_dim(self) -> int:
+        return self.k_codes.shape[2]
+
     def c_struct(self) -> FtkvPool:
         for n in ("k_codes", "v_codes"):
             _req(getattr(self, n), torch.uint8, n, 3)
@@ -99,12 +103,14 @@ class BF16Pool:
 
 
 def store_quant(pool: KVPool, k: torch.Tensor, v: torch.Tensor, slots: torch.Tensor, stream=None) -> None:
-    """Quantize-on-write of BF16 K/V [T, Hkv, 128] into pool rows ``slots`` (int32 [T])."""
+    """Quantize-on-write of BF16 K/V [T, Hkv, D] into pool rows ``slots`` (int32 [T]); D = the pool's head_dim."""
     _req(k, torch.bfloat16, "k", 3)
     _req(v, torch.bfloat16, "v", 3)
     _req(slots, torch.int32, "slots", 1)
     if k.shape != v.shape or k.shape[0] != slots.shape[0]:
         raise ValueError("k, v, slots disagree")
+    if k.shape[1:] != (pool.num_kv_heads, pool.head_dim):
+        raise ValueError(f"k/v rows must be [{pool.num_kv_heads}, {pool.head_dim}]")
     ps = pool.c_struct()
     check(_lib.load().ftkv_store_quant(ctypes.byref(ps), _ptr(k), _ptr(v), _ptr(slots), k.shape[0],
                                        _stream_ptr(stream)), "ftkv_store_quant")
@@ -131,8 +137,8 @@ def reconstruct_bf16(pool: KVPool, slots: torch.Tensor, ws_k: torch.Tensor = Non
 
 
 def decode_workspace_bytes(num_q_heads: int, num_kv_heads: int, batch: int, total_q_rows: int,
-                           num_splits: int) -> int:
-    return int(_lib.load().ftkv_decode_workspace_bytes(num_q_heads, num_kv_heads, HEAD_DIM, batch, total_q_rows,
+                           num_splits: int, head_dim: int = HEAD_DIM) -> int:
+    return int(_lib.load().ftkv_decode_workspace_bytes(num_q_heads, num_kv_heads, head_dim, batch, total_q_rows,
                                                        num_splits))
 
 
@@ -145,23 +151,24 @@ class DecodePlan:
     on one stream; the kernels leave its arrival counters at zero)."""
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, batch: int, total_q_rows: int, max_q_rows: int,
-                 max_seq_len: int, num_splits: int = 0, device="cuda", window: int = 0):
+                 max_seq_len: int, num_splits: int = 0, device="cuda", window: int = 0, head_dim: int = HEAD_DIM):
         self.num_q_heads, self.num_kv_heads = num_q_heads, num_kv_heads
         self.batch, self.total_q_rows, self.max_q_rows = batch, total_q_rows, max_q_rows
         self.max_seq_len, self.window = max_seq_len, window
         # keys one request attends to at most: with a sliding window, the union of its rows' windows
         span = min(max_seq_len, window + max_q_rows - 1) if window > 0 else max_seq_len
         self.num_splits = num_splits or decode_auto_splits(batch, num_kv_heads, span, max_q_rows)
-        nbytes = decode_workspace_bytes(num_q_heads, num_kv_heads, batch, total_q_rows, self.num_splits)
+        nbytes = decode_workspace_bytes(num_q_heads, num_kv_heads, batch, total_q_rows, self.num_splits, head_dim)
         self.workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
 def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_lens: torch.Tensor,
                 q_row_offsets: torch.Tensor = None, *, max_seq_len: int, max_q_rows: int = 1,
-                sm_scale: float = HEAD_DIM ** -0.5, window: int = 0, num_splits: int = 0,
+                sm_scale: float = None, window: int = 0, num_splits: int = 0,
                 plan: DecodePlan = None, out: torch.Tensor = None, k_new: torch.Tensor = None,
                 v_new: torch.Tensor = None, stable_history: bool = False, stream=None) -> torch.Tensor:
-    """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, 128].
+    """Split-K decode attention over the FP8 pool.  q/out: BF16 [total_q_rows, Hq, D] (D = the pool's head_dim,
+    128 or 256; 256 with one row per request).  ``sm_scale`` defaults to D^-1/2.
     ``window`` > 0: sliding window -- a row that sees keys 0 .. v-1 attends to keys max(0, v - window) .. v-1.
     ``k_new``/``v_new`` (BF16 [total_q_rows, Hkv, 128], the new tokens' rows, one per query row): quantize them
     into the pool at their positions' slots first, in the same launch (``ftkv_decode_attn_store``).
@@ -181,18 +188,22 @@ def decode_attn(pool: KVPool, q: torch.Tensor, req_to_slot: torch.Tensor, seq_le
     if q_row_offsets is not None:
         _req(q_row_offsets, torch.int32, "q_row_offsets", 1)
     batch = seq_lens.shape[0]
-    total, hq, _ = q.shape
+    total, hq, D = q.shape
+    if D != pool.head_dim:
+        raise ValueError(f"q has head_dim {D}, the pool {pool.head_dim}")
+    if sm_scale is None:
+        sm_scale = D ** -0.5
     if plan is None:
         plan = DecodePlan(hq, pool.num_kv_heads, batch, total, max_q_rows, max_seq_len, num_splits, q.device,
-                          window)
+                          window, D)
     if out is None:
         out = torch.empty_like(q)
     _req(out, torch.bfloat16, "out", 3)
     flags = _lib.FTKV_DECODE_STABLE_HISTORY if stable_history else 0
     ps = pool.c_struct()
     if k_new is not None:
-        if k_new.shape != (total, pool.num_kv_heads, HEAD_DIM) or v_new.shape != k_new.shape:
-            raise ValueError(f"k_new/v_new must be [{total}, {pool.num_kv_heads}, {HEAD_DIM}]")
+        if k_new.shape != (total, pool.num_kv_heads, D) or v_new.shape != k_new.shape:
+            raise ValueError(f"k_new/v_new must be [{total}, {pool.num_kv_heads}, {D}]")
         check(_lib.load().ftkv_decode_attn_store(
             ctypes.byref(ps), hq, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(req_to_slot), req_to_slot.shape[1],
             _ptr(seq_lens), _ptr(q_row_offsets), batch, total, max_q_rows, max_seq_len, float(sm_scale),

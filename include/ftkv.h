@@ -24,8 +24,9 @@
  *     that only the GPU can see (a slot outside the pool, a sequence length above the declared
  *     maximum) make the kernel skip the offending row and raise a flag in a per-device error word,
  *     read and cleared with ftkv_device_errors().
- *   - Supported: head_dim == 128, num_q_heads % num_kv_heads == 0 with group size 1, 2, 4 or 8
- *     (MHA/GQA), page size 1, one GPU (TP = 1).  Anything else returns FTKV_ERR_UNSUPPORTED, the
+ *   - Supported: head_dim == 128 (and 256 for ftkv_store_quant and single-row decode, see
+ *     FTKV_HEAD_DIM_256), num_q_heads % num_kv_heads == 0 with group size 1, 2, 4 or 8 (MHA/GQA),
+ *     page size 1, one GPU (TP = 1).  Anything else returns FTKV_ERR_UNSUPPORTED, the
  *     configuration-time rejection of [#853 "What changes"] and [#280 limitations].
  */
 #ifndef FTKV_H_
@@ -40,6 +41,9 @@ extern "C" {
 
 #define FTKV_ABI_VERSION 2
 #define FTKV_HEAD_DIM 128
+/* The 256-d head of FreeToken's Qwen3.6 full-attention layers ([#897 "Known regression and uncertainty"]):
+ * supported by ftkv_store_quant and by single-row decode (max_q_rows == 1) over the FP8 pool. */
+#define FTKV_HEAD_DIM_256 256
 /* Split-K cap of decode.  The pages cap their kernel at 64 slices ([#897 "Fresh R9700 stage-1 A/B"]: 64
  * scratch slots / splits, a limit of that kernel's scratch budget).  Here one slice of a single-row batch
  * covers every KV head of its keys, so a batch-1 decode needs one slice per SM (152 on a GB300): the cap is
@@ -119,7 +123,8 @@ int ftkv_reconstruct_bf16(const ftkv_pool* pool, const int32_t* slots, int64_t n
  * Single-row batches (max_q_rows == 1) run a kernel whose CTAs cover every KV head of their keys (token-
  * contiguous loads); multi-row batches a kernel with one KV head per CTA.
  *
- *   q              : device BF16 [total_q_rows][num_q_heads][head_dim]
+ *   q              : device BF16 [total_q_rows][num_q_heads][head_dim]; head_dim is the pool's (128, or
+ *                    256 with max_q_rows == 1, else FTKV_ERR_UNSUPPORTED)
  *   req_to_slot    : device int32 [batch][req_stride]; key j of request b lives in pool row
  *                    req_to_slot[b * req_stride + j]
  *   seq_lens       : device int32 [batch]; request b attends to keys 0 .. seq_lens[b]-1 (the keys of

@@ -73,6 +73,7 @@ def test_store_validation(lib):
 
 def test_reconstruct_validation(lib):
     P = ctypes.byref
+    assert lib.ftkv_reconstruct_bf16(P(_pool(d=256)), 0x3000, 5, 0x5000, 0x6000, None) == _lib.FTKV_ERR_UNSUPPORTED
     assert lib.ftkv_reconstruct_bf16(P(_pool()), 0x3000, 5, 0x5008, 0x6000, None) == _lib.FTKV_ERR_ALIGN
     assert lib.ftkv_reconstruct_bf16(P(_pool()), None, 5, 0x5000, 0x6000, None) == _lib.FTKV_ERR_INVALID
     assert lib.ftkv_reconstruct_bf16(P(_pool()), None, 0, None, None, None) == _lib.FTKV_OK
@@ -83,6 +84,8 @@ def test_decode_validation(lib):
     ws = lib.ftkv_decode_workspace_bytes(32, 4, 128, 1, 1, 4)
     assert ws > 0 and ws % 256 == 0
     assert lib.ftkv_decode_workspace_bytes(32, 4, 64, 1, 1, 8) == 0
+    ws256 = lib.ftkv_decode_workspace_bytes(32, 4, 256, 1, 1, 4)
+    assert ws256 > ws and ws256 % 256 == 0                    # 256-d partials: twice the accumulators
     base = dict(q=0x1000, r2s=0x2000, stride=64, lens=0x3000, offs=None, B=1, total=1, mq=1, maxlen=64,
                 sm=0.0884, win=0, splits=4, flags=0, ws=0x100000, wsb=ws, out=0x4000)
 
@@ -107,6 +110,9 @@ def test_decode_validation(lib):
     assert call(wsb=ws - 1) == _lib.FTKV_ERR_WORKSPACE
     assert call(sm=float("nan")) == _lib.FTKV_ERR_INVALID
     assert call(win=-1) == _lib.FTKV_ERR_INVALID             # sliding window: 0 (off) or >= 1 keys
+    assert call(pool=_pool(d=256), mq=2) == _lib.FTKV_ERR_UNSUPPORTED  # 256-d heads: single-row decode only
+    assert call(pool=_pool(d=256)) == _lib.FTKV_ERR_WORKSPACE  # 256-d: the 128-d workspace is too small
+    assert call(pool=_pool(d=192)) == _lib.FTKV_ERR_UNSUPPORTED
     assert call(win=8, wsb=255) == _lib.FTKV_ERR_WORKSPACE    # the workspace rule holds with a window too
     assert call(B=0, total=0) == _lib.FTKV_OK                # nothing to do
 

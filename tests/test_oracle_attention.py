@@ -54,6 +54,23 @@ def test_decode_matches_torch_sdpa(Hq, Hkv):
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(32, 4), (16, 2)])
+def test_decode_256d_matches_torch_sdpa(Hq, Hkv):
+    """256-d heads (the Qwen3.6 full-attention case of PR #897): the same definition, scale 1/16."""
+    rng = np.random.default_rng(23)
+    R, n = 90, 57
+    pool, slots = _pool_from(rng, R, n, Hkv=Hkv, D=256)
+    q = inputs.queries(rng, 1, Hq, 256)
+    got = oracle.decode_attn(pool, q, slots[None], [n], [0, 1], 1.0 / 16.0, Hq)[0]
+    kd = _torch_deq(pool.k_codes[slots], pool.k_scales[slots]).permute(1, 0, 2)
+    vd = _torch_deq(pool.v_codes[slots], pool.v_scales[slots]).permute(1, 0, 2)
+    qd = torch.from_numpy(inputs.bf16_bits_to_f32(q[0])).to(torch.float64)[:, None, :]
+    G = Hq // Hkv
+    want = F.scaled_dot_product_attention(qd, kd.repeat_interleave(G, 0), vd.repeat_interleave(G, 0),
+                                          scale=1.0 / 16.0)[:, 0, :].numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
 def test_decode_multirow_matches_torch_sdpa_with_causal_mask():
     rng = np.random.default_rng(22)
     R, n, rows = 128, 50, 5

@@ -60,6 +60,20 @@ def test_store_matches_independent_restatement():
     assert not pool.k_codes[untouched].any() and not pool.k_scales[untouched].any()
 
 
+def test_store_256d_matches_independent_restatement():
+    """The 256-d row (FTKV_HEAD_DIM_256) is quantized by the same definition over all 256 elements."""
+    rng = np.random.default_rng(12)
+    T, R = 120, 300
+    k, v = inputs.kv_tokens(rng, T, 2.0, big_frac=0.05, zero_frac=0.05, head_dim=256)
+    slots = rng.permutation(R)[:T].astype(np.int32)
+    pool = oracle.Pool(R, 4, 256)
+    oracle.store_quant(pool, k, v, slots)
+    for src, codes, scales in ((k, pool.k_codes, pool.k_scales), (v, pool.v_codes, pool.v_scales)):
+        want_c, want_s = _independent_quantize(src)
+        assert np.array_equal(codes[slots], want_c)
+        assert np.array_equal(scales[slots].view(np.uint32), want_s.view(np.uint32))
+
+
 def test_store_error_bound_and_landmarks():
     rng = np.random.default_rng(12)
     T = 200
