@@ -18,8 +18,8 @@ Printed (rank 0): ONE JSON line on stdout, value = microseconds per step (lower 
                   and new K/V, the step, D2H of the outputs, synchronized every step;
   clocks       -- nvidia-smi samples taken during the timed region.
 Then one "detail" JSON line per other workload on stderr (configs 0, 1, 3, 4, the 40,000-key decode, cold
-reconstruct, and the BF16-KV comparison), each with its own roofline and cpu_baseline; --no-details skips
-them.  ``--impl reference`` times the oracle alone (the CPU reference arm).
+reconstruct, the BF16-KV comparison, 256-d heads and a sliding window), each with its own roofline and
+cpu_baseline; --no-details skips them.  ``--impl reference`` times the oracle alone (the CPU reference arm).
 """
 from __future__ import annotations
 
@@ -59,7 +59,7 @@ def parse_args():
     p.add_argument("--details-only", action="store_true", help="detail lines only (no headline)")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timings (profiling runs)")
     p.add_argument("--detail", default="", help="comma-separated detail lines to run (default all): config0, "
-                   "config1, config2_40k, bf16kv, config3, reconstruct, config4")
+                   "config1, config2_40k, bf16kv, d256, window, config3, reconstruct, config4")
     p.add_argument("--cpu-budget-s", type=float, default=20.0, help="bound on the oracle time of a sample")
     return p.parse_args()
 
@@ -153,15 +153,15 @@ def barrier(world):
         dist.barrier()
 
 
-def decode_bytes_per_layer(n):
-    """Algorithmic bytes of one decode launch at n keys (batch 1): K and V codes and scales of every key,
-    the slot table, the query and the output, plus the fused store of the new token (its BF16 K/V read,
+def decode_bytes_per_layer(n, head_dim=D):
+    """Algorithmic bytes of one decode launch attending to n keys (batch 1): K and V codes and scales of every
+    key, the slot table, the query and the output, plus the fused store of the new token (its BF16 K/V read,
     its codes and scales written)."""
-    codes = n * HKV * D * 2
+    codes = n * HKV * head_dim * 2
     scales = n * HKV * 4 * 2
     slots = n * 4
-    qo = HQ * D * 2 * 2
-    store = HKV * D * 2 * 2 + (HKV * D + HKV * 4) * 2
+    qo = HQ * head_dim * 2 * 2
+    store = HKV * head_dim * 2 * 2 + (HKV * head_dim + HKV * 4) * 2
     return codes + scales + slots + qo + store
 
 
@@ -264,21 +264,24 @@ def to_dev_fn(torch, device):
     return lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).to(device)
 
 
-def build_decode(args, torch, ops, inputs, device, context=None, pool_rows=None):
+def build_decode(args, torch, ops, inputs, device, context=None, pool_rows=None, head_dim=D, window=0):
+    """The headline step (or a variant: head_dim 256, a sliding window) on the FP8 pool."""
     n = context or args.context
     wl = inputs.decode_long(n, pool_rows or args.pool_rows, layers=args.layers)
+    wl.head_dim = head_dim
+    wl.sm_scale = head_dim ** -0.5
     slots_d = torch.from_numpy(wl.req_to_slot).to(device)
     lens_d = torch.from_numpy(wl.seq_lens).to(device)
     to_dev = to_dev_fn(torch, device)
     # contiguous per-step inputs/outputs (views per layer), so a step's host<->device traffic is 3 copies
-    q_all = torch.empty(args.layers, 1, HQ, D, dtype=torch.bfloat16, device=device)
-    kv_all = torch.empty(args.layers, 2, 1, HKV, D, dtype=torch.bfloat16, device=device)
-    out_all = torch.empty(args.layers, 1, HQ, D, dtype=torch.bfloat16, device=device)
+    q_all = torch.empty(args.layers, 1, HQ, head_dim, dtype=torch.bfloat16, device=device)
+    kv_all = torch.empty(args.layers, 2, 1, HKV, head_dim, dtype=torch.bfloat16, device=device)
+    out_all = torch.empty(args.layers, 1, HQ, head_dim, dtype=torch.bfloat16, device=device)
     pools = []
     all_slots = torch.from_numpy(wl.token_slots.astype(np.int32)).to(device)
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         for l, L in enumerate(ex.map(wl.layer, range(args.layers))):
-            pool = ops.KVPool.empty(wl.num_rows, HKV, device=device)
+            pool = ops.KVPool.empty(wl.num_rows, HKV, device=device, head_dim=head_dim)
             ops.store_quant(pool, to_dev(L.k[:n - 1]), to_dev(L.v[:n - 1]), all_slots[:n - 1])
             pools.append(pool)
             q_all[l].copy_(to_dev(L.q))
@@ -287,16 +290,17 @@ def build_decode(args, torch, ops, inputs, device, context=None, pool_rows=None)
     q = [q_all[l] for l in range(args.layers)]
     newk = [kv_all[l, 0] for l in range(args.layers)]
     newv = [kv_all[l, 1] for l in range(args.layers)]
-    plan = ops.DecodePlan(HQ, HKV, 1, 1, 1, n, args.num_splits, device)
+    plan = ops.DecodePlan(HQ, HKV, 1, 1, 1, n, args.num_splits, device, window, head_dim)
     outs = [out_all[l] for l in range(args.layers)]
     torch.cuda.synchronize()
 
     def step():
         for l in range(args.layers):
             ops.decode_attn(pools[l], q[l], slots_d, lens_d, None, max_seq_len=n, max_q_rows=1, plan=plan,
-                            out=outs[l], k_new=newk[l], v_new=newv[l], stable_history=not args.no_stable_history)
+                            out=outs[l], k_new=newk[l], v_new=newv[l], stable_history=not args.no_stable_history,
+                            window=window, sm_scale=wl.sm_scale)
 
-    return dict(step=step, q_all=q_all, kv_all=kv_all, out_all=out_all, plan=plan, pools=pools, n=n)
+    return dict(step=step, q_all=q_all, kv_all=kv_all, out_all=out_all, plan=plan, pools=pools, n=n, wl=wl)
 
 
 def bf16_bytes_per_layer(n):
@@ -581,6 +585,55 @@ def run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, p
         del st, g, hk, hv, Lb
         torch.cuda.empty_cache()
 
+    # ---- 256-d heads: the headline step with head_dim 256 (the Qwen3.6 full-attention case) ----
+    if want("d256"):
+        st = build_decode(args, torch, ops, inputs, device, head_dim=256)
+        g = graph_of(torch, stream, st["step"])
+        ms, _ = time_graph(torch, stream, g, steps, warm)
+        n = args.context
+        cpu = None
+        if not SKIP_CPU:
+            wl2 = st["wl"]
+            L2 = wl2.layer(0)
+            op = oracle.Pool(wl2.num_rows, HKV, 256)
+            oracle.store_quant(op, L2.k, L2.v, L2.slots)
+            cpu = cpu_baseline_scaled(lambda: oracle.decode_attn(op, L2.q, wl2.req_to_slot, wl2.seq_lens,
+                                                                 wl2.q_row_offsets, wl2.sm_scale, HQ),
+                                      1, args.layers, "us/step",
+                                      f"1 of {args.layers} layers (FP64 decode over {n} 256-d keys), scaled x{args.layers}",
+                                      budget)
+            del op, L2
+        detail_line(f"d256_decode_{n}_b1_{args.layers}layers", ms * 1e3, "us/step",
+                    hbm_roof(args.layers * decode_bytes_per_layer(n, 256), ms, hbm_peak, peak_src,
+                             "decode_tok_kernel<4,256>"), cpu, {"num_splits": st["plan"].num_splits, "head_dim": 256})
+        del st, g
+        torch.cuda.empty_cache()
+
+    # ---- sliding window: the headline step attending to the last 4,095 keys (an odd window) ----
+    if want("window"):
+        W = 4095
+        st = build_decode(args, torch, ops, inputs, device, window=W)
+        g = graph_of(torch, stream, st["step"])
+        ms, _ = time_graph(torch, stream, g, steps, warm)
+        cpu = None
+        if not SKIP_CPU:
+            wl2 = st["wl"]
+            L2 = wl2.layer(0)
+            op = oracle.Pool(wl2.num_rows, HKV, D)
+            oracle.store_quant(op, L2.k, L2.v, L2.slots)
+            cpu = cpu_baseline_scaled(lambda: oracle.decode_attn(op, L2.q, wl2.req_to_slot, wl2.seq_lens,
+                                                                 wl2.q_row_offsets, wl2.sm_scale, HQ, window=W),
+                                      1, args.layers, "us/step",
+                                      f"1 of {args.layers} layers (FP64 decode over the last {W} of {args.context} keys), "
+                                      f"scaled x{args.layers}", budget)
+            del op, L2
+        detail_line(f"window{W}_decode_{args.context}_b1_{args.layers}layers", ms * 1e3, "us/step",
+                    hbm_roof(args.layers * decode_bytes_per_layer(W), ms, hbm_peak, peak_src, "decode_tok_kernel<4>"),
+                    cpu, {"num_splits": st["plan"].num_splits, "window": W,
+                          "note": "bytes count the window's keys only: the slices cover nothing else"})
+        del st, g
+        torch.cuda.empty_cache()
+
     # ---- config 3: chunked prefill pipeline, one layer: for each of 4 chunks of 2,048 new tokens,
     if want("config3"):
         # reconstruct the FP8 prefix into the BF16 workspace, prefill the chunk, quantize-on-write the chunk ----
@@ -633,7 +686,8 @@ def run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, p
 
     # ---- reconstruct, cold: 8 distinct pools of 14,336 prefix rows into 8 distinct workspaces ----
     if want("reconstruct"):
-        P = H + 3 * C
+        pw = inputs.prefill()
+        P = pw.hist_slots.shape[0] + 3 * pw.chunk  # the last chunk's prefix: 14,336 rows
         rk, rv = inputs.kv_tokens(np.random.default_rng(5), P, 1.0)
         rslots = torch.from_numpy(np.random.default_rng(6).permutation(pw.num_rows)[:P].astype(np.int32)).to(device)
         rpools = []

@@ -183,7 +183,10 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
   // of 1-8 rows: 5 splits 1,326 us, 10 splits 1,247 us).
   const int64_t waves = max_q_rows > 1 ? 16 : 8;
   int64_t s = (8 * groups <= sms) ? sms / groups : ceil_div(waves * sms * per_sm, groups);
-  const int64_t by_len = ceil_div(max_seq_len, 128);  // at least ~128 keys per slice
+  // at least ~32 keys per slice for the single-row kernel (a block of 16 for each of its two key groups: short
+  // requests, e.g. a sliding window, still spread over the SMs, so the split merge is spread too), ~128 for the
+  // multi-row kernel
+  const int64_t by_len = ceil_div(max_seq_len, max_q_rows <= 1 ? 32 : 128);
   if (s > by_len) s = by_len;
   if (s > FTKV_MAX_SPLITS) s = FTKV_MAX_SPLITS;
   if (s < 1) s = 1;
