@@ -145,7 +145,7 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, off));
     if (Mc == -INFINITY) continue;  // warp-uniform: nothing seen yet
-    const float sc = (M == -INFINITY) ? 0.0f : exp2f(M - Mc);
+    const float sc = (M == -INFINITY) ? 0.0f : fast_exp2(M - Mc);
     L *= sc;
     o.x *= sc;
     o.y *= sc;
@@ -153,7 +153,7 @@ __device__ __forceinline__ void merge_item(const DecodeArgs& a, int64_t it, int 
     o.w *= sc;
 #pragma unroll
     for (int k = 0; k < CH; k++) {
-      const float w = (ml[k].x == -INFINITY) ? 0.0f : exp2f(ml[k].x - Mc);
+      const float w = (ml[k].x == -INFINITY) ? 0.0f : fast_exp2(ml[k].x - Mc);
       L = fmaf(w, ml[k].y, L);
       o.x = fmaf(w, v[k].x, o.x);
       o.y = fmaf(w, v[k].y, o.y);

@@ -82,9 +82,7 @@ struct Tok {
   static constexpr int STAGE = 2 * TKB * RUN + 2 * TKB * HC * 4;
   static constexpr int RING = NG * TNS * STAGE;
   static constexpr int SLOT_OFF = RING;                   // [TWIN] int32 slot indices
-  static constexpr int Q_OFF = SLOT_OFF + TWIN * 4;       // [HC][8 heads][2 pieces][D] E4M3 codes
-  static constexpr int QM_OFF = Q_OFF + HC * 8 * 2 * D;   // [HC][8] FP32 multipliers
-  static constexpr int NEW_OFF = QM_OFF + HC * 8 * 4;     // new token: [HC][K D | V D] codes, [HC][2] scales
+  static constexpr int NEW_OFF = SLOT_OFF + TWIN * 4;     // new token: [HC][K D | V D] codes, [HC][2] scales
   static constexpr int SMEM = NEW_OFF + HC * (2 * D + 8);
   static constexpr int CTAS_PER_SM = D == 128 ? 2 : 1;    // D = 256: the ring alone takes ~198 KB
   static constexpr int KSTEP = 512 / D;                   // keys whose runs one load round covers
@@ -114,8 +112,6 @@ __global__ void __launch_bounds__(TW * 32, Tok<HC, D>::CTAS_PER_SM) decode_tok_k
   constexpr int NG = T::NG;
   extern __shared__ __align__(128) uint8_t smem[];
   int32_t* sslot = reinterpret_cast<int32_t*>(smem + T::SLOT_OFF);
-  uint8_t* qsm = smem + T::Q_OFF;
-  float* qmul = reinterpret_cast<float*>(smem + T::QM_OFF);
   uint8_t* newtok = smem + T::NEW_OFF;
 
   const int split = blockIdx.x, b = blockIdx.z;
@@ -263,18 +259,17 @@ __global__ void __launch_bounds__(TW * 32, Tok<HC, D>::CTAS_PER_SM) decode_tok_k
 
   if (!early) stage_slots(j0, nk0);
 
-  // ---- query loads (one warp per (KV head, query head of its group), every load in flight at once) ----
-  constexpr int NPR = (HC * 8 + TW - 1) / TW;
-  constexpr int EPL = D / 32;  // query elements per lane (4 or 8)
-  uint2 qv[NPR][NH];
+  // ---- query loads: each warp its own KV head's query heads; lane (g, t) takes d = 128hf + 32t .. +31 of
+  // query head g (every load in flight at once) ----
+  const int G = a.group;
+  const bool qok = g < G;  // heads past the group pad the 8-wide MMA N dimension with zeros
+  uint4 qr[NH][4];
+  {
+    const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (row0 * a.num_q_heads + (h0 + hh) * G + (qok ? g : 0)) * D);
 #pragma unroll
-  for (int u = 0; u < NPR; u++) {
-    const int pr = warp + u * TW, hd = pr >> 3, hq = pr & 7;
-    const bool ok = pr < HC * 8 && hq < a.group;
-    const uint2* src = reinterpret_cast<const uint2*>(a.q + (row0 * a.num_q_heads + (h0 + hd) * a.group + hq) * D +
-                                                      EPL * lane);
+    for (int hf = 0; hf < NH; hf++)
 #pragma unroll
-    for (int hf = 0; hf < NH; hf++) qv[u][hf] = ok ? __ldg(src + hf) : make_uint2(0u, 0u);
+      for (int c = 0; c < 4; c++) qr[hf][c] = qok ? __ldg(qsrc + 16 * hf + 4 * t + c) : make_uint4(0u, 0u, 0u, 0u);
   }
 
   // ---- fused store of the request's new token (position n - 1), if it falls in this slice: one warp per
@@ -304,68 +299,51 @@ __global__ void __launch_bounds__(TW * 32, Tok<HC, D>::CTAS_PER_SM) decode_tok_k
 
   // ---- query pieces: x = q * 2^(7-ex), ex the exponent of max|q| over the head: |x| < 256; pieces
   // x = h1 + h2/16, both E4M3 (exact unless |q| < 2^-13 max|q|); multiplier 2^(ex-7) * sm_scale * log2(e).
-  // Query heads past the group (padding of the 8-wide MMA N dimension) get zero pieces. ----
-#pragma unroll
-  for (int u = 0; u < NPR; u++) {
-    const int pr = warp + u * TW;
-    if (pr >= HC * 8) break;  // warp-uniform
-    float x[NH][4];
-    float amax = 0.0f;
-#pragma unroll
-    for (int hf = 0; hf < NH; hf++) {
-      x[hf][0] = bf16_lo(qv[u][hf].x);
-      x[hf][1] = bf16_hi(qv[u][hf].x);
-      x[hf][2] = bf16_lo(qv[u][hf].y);
-      x[hf][3] = bf16_hi(qv[u][hf].y);
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[hf][0]), fabsf(x[hf][1])), fmaxf(fabsf(x[hf][2]), fabsf(x[hf][3]))));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    int ex = (amax > 0.0f) ? ilogbf(amax) : 0;
-    ex = ex < -120 ? -120 : ex;
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + 7 - ex) << 23);
-    uint8_t* dst = qsm + pr * 2 * D + EPL * lane;  // lane holds d = EPL lane .. EPL lane + EPL - 1
-#pragma unroll
-    for (int hf = 0; hf < NH; hf++) {
-      float* xh = x[hf];
-#pragma unroll
-      for (int e = 0; e < 4; e++) xh[e] *= up;
-#pragma unroll
-      for (int p = 0; p < 2; p++) {
-        const uint32_t c01 = e4m3x2_encode(xh[0], xh[1]), c23 = e4m3x2_encode(xh[2], xh[3]);
-        *reinterpret_cast<uint32_t*>(dst + p * D + 4 * hf) = c01 | (c23 << 16);
-        if (p == 0) {
-          const float2 v01 = f16x2_to_float2(e4m3x2_to_f16x2(c01));
-          const float2 v23 = f16x2_to_float2(e4m3x2_to_f16x2(c23));
-          xh[0] = (xh[0] - v01.x) * 16.0f;
-          xh[1] = (xh[1] - v01.y) * 16.0f;
-          xh[2] = (xh[2] - v23.x) * 16.0f;
-          xh[3] = (xh[3] - v23.y) * 16.0f;
-        }
-      }
-    }
-    if (lane == 0) qmul[pr] = __uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * a.qk_scale_log2;
-  }
-  __syncthreads();  // slots, pieces and the new token's codes before any block is computed or (re)loaded
-
-  // B operand of QK^T for this warp's KV head: query head g, d = 128hf + 32t + 8kk' + {0..3} (b0) / {4..7}
-  // (b1) for k-step kk = 4hf + kk'
+  // They are the B operand of QK^T: query head g, d = 128hf + 32t + 8kk' + {0..3} (b0) / {4..7} (b1) for
+  // k-step kk = 4hf + kk'.  The head's max comes from the 4 lanes that hold it; lane (g, t) then takes the
+  // multipliers of query heads 2t, 2t+1 (its accumulator columns) from the lanes of those heads. ----
   uint32_t qp[2][4 * NH][2];
   float fq[2];
   {
-    const uint32_t src = smem_addr(qsm) + (hh * 8 + g) * 2 * D + 32 * t;
+    float amax = 0.0f;
 #pragma unroll
-    for (int p = 0; p < 2; p++)
+    for (int hf = 0; hf < NH; hf++)
 #pragma unroll
-      for (int hf = 0; hf < NH; hf++) {
-        const uint4 w0 = ld_shared_v4(src + p * D + 128 * hf);
-        const uint4 w1 = ld_shared_v4(src + p * D + 128 * hf + 16);
-        qp[p][4 * hf + 0][0] = w0.x; qp[p][4 * hf + 0][1] = w0.y; qp[p][4 * hf + 1][0] = w0.z; qp[p][4 * hf + 1][1] = w0.w;
-        qp[p][4 * hf + 2][0] = w1.x; qp[p][4 * hf + 2][1] = w1.y; qp[p][4 * hf + 3][0] = w1.z; qp[p][4 * hf + 3][1] = w1.w;
+      for (int c = 0; c < 4; c++) {
+        const uint4 w = qr[hf][c];
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))), fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))), fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w)))));
       }
-    fq[0] = qmul[hh * 8 + 2 * t];
-    fq[1] = qmul[hh * 8 + 2 * t + 1];
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int ex = (amax > 0.0f) ? ilogbf(amax) : 0;
+    ex = ex < -120 ? -120 : ex;
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + 7 - ex) << 23);
+    auto pieces4 = [&](uint32_t w01, uint32_t w23, uint32_t& p0, uint32_t& p1) {  // 4 elements -> 2 words
+      float x0 = bf16_lo(w01) * up, x1 = bf16_hi(w01) * up, x2 = bf16_lo(w23) * up, x3 = bf16_hi(w23) * up;
+      const uint32_t c01 = e4m3x2_encode(x0, x1), c23 = e4m3x2_encode(x2, x3);
+      p0 = c01 | (c23 << 16);
+      const float2 v01 = f16x2_to_float2(e4m3x2_to_f16x2(c01));
+      const float2 v23 = f16x2_to_float2(e4m3x2_to_f16x2(c23));
+      x0 = (x0 - v01.x) * 16.0f;
+      x1 = (x1 - v01.y) * 16.0f;
+      x2 = (x2 - v23.x) * 16.0f;
+      x3 = (x3 - v23.y) * 16.0f;
+      p1 = e4m3x2_encode(x0, x1) | (e4m3x2_encode(x2, x3) << 16);
+    };
+#pragma unroll
+    for (int hf = 0; hf < NH; hf++)
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        const uint4 w = qr[hf][c];
+        pieces4(w.x, w.y, qp[0][4 * hf + c][0], qp[1][4 * hf + c][0]);
+        pieces4(w.z, w.w, qp[0][4 * hf + c][1], qp[1][4 * hf + c][1]);
+      }
+    const float mult = __uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * a.qk_scale_log2;
+    fq[0] = __shfl_sync(0xffffffffu, mult, (2 * t) * 4);
+    fq[1] = __shfl_sync(0xffffffffu, mult, (2 * t + 1) * 4);
   }
+  if (!early || has_new) __syncthreads();  // the staged slots (after the wait) and the new token's codes
   // fragment offsets within a stage (loop-invariant)
   // (the second 128-d half: chunks 8 + the first half's, same swizzle; tk_off(key, hd, p + 8) = that + 128)
   const uint32_t oK0 = tk_off<HC, D>(g, hh, 2 * t), oK1 = tk_off<HC, D>(g, hh, 2 * t + 1);
@@ -543,7 +521,6 @@ __global__ void __launch_bounds__(TW * 32, Tok<HC, D>::CTAS_PER_SM) decode_tok_k
   for (int hx = 0; hx < 2; hx++)
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l[hx] += __shfl_xor_sync(0xffffffffu, l[hx], off);
-  const int G = a.group;
   // lane (g, t) holds d = 128hf + 16g + 4q4 + {0..3} of query head 2t + hx: acc[8hf+2q4][hx], acc[8hf+2q4][2+hx],
   // acc[8hf+2q4+1][hx], acc[8hf+2q4+1][2+hx]; bring it to units of 2^m
 #pragma unroll
