@@ -24,6 +24,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "ftkv_device.cuh"
 #include "ftkv_internal.h"
 
@@ -905,14 +907,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // ---------------------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // looked up once (thread-safe static initialisation); null if the driver lacks it
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -940,16 +943,20 @@ int64_t prefill_workspace_bytes(int max_ctas) {
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
-  static bool configured[64] = {};
+  // per-device set-up, once per device even with several host threads
+  static std::once_flag once[kMaxDecodeDevices];
+  static cudaError_t setup_err[kMaxDecodeDevices];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc2::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return ge;
+  if (dev < 0 || dev >= kMaxDecodeDevices) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    setup_err[dev] = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    if (setup_err[dev] == cudaSuccess)
+      setup_err[dev] =
+          cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc2::SMEM_ALLOC);
+  });
+  if (setup_err[dev] != cudaSuccess) return setup_err[dev];
   CUtensorMap tq, tkc, tvc, twk, twv;
   if (!make_map(&tq, a.q, a.num_q_heads, a.chunk_len) || !make_map(&tkc, a.k_chunk, a.num_kv_heads, a.chunk_len) ||
       !make_map(&tvc, a.v_chunk, a.num_kv_heads, a.chunk_len))
