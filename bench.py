@@ -303,6 +303,12 @@ def build_decode(args, torch, ops, inputs, device, context=None, pool_rows=None,
     return dict(step=step, q_all=q_all, kv_all=kv_all, out_all=out_all, plan=plan, pools=pools, n=n, wl=wl)
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode_tok_kernel<4, 128> launch of the 32K
+# batch-1 step, from an ncu capture of this kernel on the same launch geometry (4 distinct pools, cold L2); to be
+# re-taken whenever the kernel changes.
+TOK_TRAFFIC_PER_LAUNCH = 34_820_864
+
+
 def bf16_bytes_per_layer(n):
     """Algorithmic bytes of one BF16-pool decode launch at n keys (batch 1): K and V rows of every key, the
     slot table, the query and the output, plus the copy of the new token's K/V rows into the pool."""
@@ -455,7 +461,8 @@ def run_headline(args, world, rank, local, torch, ops, inputs, device, stream, h
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "hbm_gbs": achieved, "hbm_frac": achieved / hbm_peak,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "kernel": "decode_tok_kernel<4>",
+                         "frac": achieved / hbm_peak, "traffic": TOK_TRAFFIC_PER_LAUNCH,
+                         "kernel": "decode_tok_kernel<4, 128>",
                          "bytes_per_launch": layer_bytes, "per_launch_us": ms_step * 1e3 / args.layers,
                          "basis": "step level: algorithmic bytes of 48 launches / graph-timed step",
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
