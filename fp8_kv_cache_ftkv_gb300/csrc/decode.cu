@@ -20,12 +20,15 @@
 //    within 13 binades of the head's largest one is represented without error.  The two partial dot
 //    products are recombined in FP32 with the per-key K scale.
 //  * PV runs on FP16 tensor cores (m16n8k16): V codes are converted exactly with the packed
-//    hardware converter and the V scale is folded into the probabilities.  FP16 has a narrow exponent
-//    range and the per-row V scales of a slice can span 2^30, so each 16-key block is scaled by its own
-//    maximum W of the value-weighted probabilities w_j = 2^(s_j - m) * scaleV_j (FP32 products, no
-//    logarithms: an added log2(scale) would be rounded to the ulp of a large logit).  With 2^E the power
-//    of two of W, P'_j = w_j * 2^-E < 2 goes through the MMA into a zeroed register tile, which is added
-//    to the FP32 accumulator with the exact factor 2^E.  Only the range within one block fits FP16.
+//    hardware converter and the V scale is folded into the probabilities, w_j = 2^(s_j - m) * scaleV_j
+//    (FP32 products, no logarithms: an added log2(scale) would be rounded to the ulp of a large logit).
+//    The softmax maximum is lazy, as in decode_tok.cu: m is raised, and the accumulator rescaled, only
+//    when a score exceeds it by more than 8 (a warp vote).  PV accumulates in place: FP16 has a narrow
+//    exponent range and the per-row V scales of a slice can span 2^30, so the MMA takes w_j * 2^-E with
+//    one power-of-two exponent E per (row, head) that only grows (raised, and the accumulator rescaled
+//    exactly, when some w would exceed 2^(E + 12)).  (A normalisation of every 16-key block by its own
+//    maximum, with the block's tile added into the accumulator by FMAs, measured 1,241 us against 1,143 us
+//    on the batched 64-request launch.)
 //  * The 8 query heads of a GQA group are the MMA N dimension, so G = 8 wastes nothing.
 #include <cfloat>
 #include <mutex>
@@ -44,6 +47,8 @@ constexpr int STAGE_V = KB * kHeadDim;       // 2048 B of V codes
 constexpr int STAGE_S = KB * 4 * 2;          // 16 K scales + 16 V scales
 constexpr int STAGE_BYTES = STAGE_K + STAGE_V + STAGE_S;
 constexpr int MAX_SUB = 4096;                // slot indices staged in shared memory at a time
+constexpr float kLazyMax = 8.0f;             // log2 slack of the running maximum
+constexpr int kLazyExp = 12;                 // w may reach 2^(E + kLazyExp) before E is raised
 
 template <int RPW>
 struct Cfg;
@@ -248,14 +253,22 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     fq[i][1] = valid ? qmul[rsafe * 8 + 2 * t + 1] : 0.0f;
   }
 
-  float acc[RPW][8][4];
-  float m[RPW][2], l[RPW][2];  // running max of s (log2 units) and running sum of 2^(s - m)
+  float acc[RPW][8][4];         // in units of 2^E
+  float m[RPW][2], l[RPW][2];   // running (lazy) max of s (log2 units) and running sum of 2^(s - m)
+  int E[RPW][2];                // FP16 operand exponent: PV takes w * 2^-E
+  float wlim[RPW][2], iw[RPW][2];
 #pragma unroll
   for (int i = 0; i < RPW; i++) {
 #pragma unroll
     for (int mt = 0; mt < 8; mt++) acc[i][mt][0] = acc[i][mt][1] = acc[i][mt][2] = acc[i][mt][3] = 0.0f;
-    m[i][0] = m[i][1] = -INFINITY;
-    l[i][0] = l[i][1] = 0.0f;
+#pragma unroll
+    for (int hx = 0; hx < 2; hx++) {
+      m[i][hx] = -INFINITY;
+      l[i][hx] = 0.0f;
+      E[i][hx] = -126;
+      wlim[i][hx] = exp2i(-126 + kLazyExp);
+      iw[i][hx] = exp2i(126);
+    }
   }
 
   const uint32_t ring = smem_addr(smem) + warp * NSTAGE * STAGE_BYTES;
@@ -352,10 +365,12 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
       const float skg = ld_shared_f32(ss + g * 4), skg8 = ld_shared_f32(ss + (g + 8) * 4);
       const float svg = ld_shared_f32(ss + 64 + g * 4), svg8 = ld_shared_f32(ss + 64 + (g + 8) * 4);
 
-      // ---- online softmax (log2 domain), P' = p * scaleV * 2^-E into B fragments of PV ----
+      // ---- softmax with a lazy maximum (log2 domain): m is raised, and the accumulator rescaled, only when a score
+      // exceeds it by more than kLazyMax (a warp vote); P' = p * scaleV * 2^-E into the B fragments of PV, with
+      // one power-of-two exponent E per (row, head) that only grows (raised, and the accumulator rescaled exactly,
+      // when some w would exceed 2^(E + kLazyExp)) ----
       const int jg = jb + g, jg8 = jb + g + 8;
       uint32_t pb0[RPW], pb1[RPW];
-      float fb[RPW][2];  // FP32 factor that brings the block's PV tile to the accumulator's scale 2^m
 #pragma unroll
       for (int r = 0; r < RPW; r++) {
         const int lr = lim[r] < je ? lim[r] : je;
@@ -367,49 +382,66 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
         const float s1 = in0 ? dot[1] * (skg * fq[r][1]) : -INFINITY;
         const float s2 = in8 ? dot[2] * (skg8 * fq[r][0]) : -INFINITY;
         const float s3 = in8 ? dot[3] * (skg8 * fq[r][1]) : -INFINITY;
-        float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+        const bool raise = fmaxf(s0, s2) > m[r][0] + kLazyMax || fmaxf(s1, s3) > m[r][1] + kLazyMax;
+        if (__any_sync(0xffffffffu, raise)) {  // new maximum: exact block max, rescale
+          float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-          bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-        }
-        const float mn0 = fmaxf(m[r][0], bm0), mn1 = fmaxf(m[r][1], bm1);
-        const float mu0 = (mn0 == -INFINITY) ? 0.0f : mn0;
-        const float mu1 = (mn1 == -INFINITY) ? 0.0f : mn1;
-        const float al0 = fast_exp2(m[r][0] - mu0), al1 = fast_exp2(m[r][1] - mu1);
-        const float p0 = fast_exp2(s0 - mu0), p1 = fast_exp2(s1 - mu1);
-        const float p2 = fast_exp2(s2 - mu0), p3 = fast_exp2(s3 - mu1);
-        l[r][0] = l[r][0] * al0 + (p0 + p2);
-        l[r][1] = l[r][1] * al1 + (p1 + p3);
-        m[r][0] = mn0;
-        m[r][1] = mn1;
-        // value-weighted probabilities and their block maximum per head
-        const float w0 = p0 * svg, w1 = p1 * svg, w2 = p2 * svg8, w3 = p3 * svg8;
-        float W0 = fmaxf(w0, w2), W1 = fmaxf(w1, w3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          W0 = fmaxf(W0, __shfl_xor_sync(0xffffffffu, W0, off));
-          W1 = fmaxf(W1, __shfl_xor_sync(0xffffffffu, W1, off));
-        }
-        // normalize by the power of two of W (exact, no overflow for tiny or subnormal W): P' in [0, 2)
-        const int e0 = min(max(static_cast<int>(__float_as_uint(W0) >> 23), 1), 253);
-        const int e1 = min(max(static_cast<int>(__float_as_uint(W1) >> 23), 1), 253);
-        fb[r][0] = __uint_as_float(static_cast<uint32_t>(e0) << 23);         // 2^(e0-127)
-        fb[r][1] = __uint_as_float(static_cast<uint32_t>(e1) << 23);
-        const float iw0 = __uint_as_float(static_cast<uint32_t>(254 - e0) << 23);  // 2^(127-e0)
-        const float iw1 = __uint_as_float(static_cast<uint32_t>(254 - e1) << 23);
-        const float ac0 = al0, ac1 = al1;
-        if (__any_sync(0xffffffffu, ac0 != 1.0f || ac1 != 1.0f)) {
+          for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+          }
+          const float mn0 = fmaxf(m[r][0], bm0), mn1 = fmaxf(m[r][1], bm1);
+          const float al0 = (m[r][0] == -INFINITY) ? 1.0f : fast_exp2(m[r][0] - mn0);
+          const float al1 = (m[r][1] == -INFINITY) ? 1.0f : fast_exp2(m[r][1] - mn1);
+          m[r][0] = mn0;
+          m[r][1] = mn1;
+          l[r][0] *= al0;
+          l[r][1] *= al1;
 #pragma unroll
           for (int mt = 0; mt < 8; mt++) {
-            acc[r][mt][0] *= ac0;
-            acc[r][mt][1] *= ac1;
-            acc[r][mt][2] *= ac0;
-            acc[r][mt][3] *= ac1;
+            acc[r][mt][0] *= al0;
+            acc[r][mt][1] *= al1;
+            acc[r][mt][2] *= al0;
+            acc[r][mt][3] *= al1;
           }
         }
-        pb0[r] = movmatrix_trans(float2_to_f16x2(w0 * iw0, w1 * iw1));   // keys 0..7
-        pb1[r] = movmatrix_trans(float2_to_f16x2(w2 * iw0, w3 * iw1));   // keys 8..15
+        const float mu0 = (m[r][0] == -INFINITY) ? 0.0f : m[r][0], mu1 = (m[r][1] == -INFINITY) ? 0.0f : m[r][1];
+        const float p0 = fast_exp2(s0 - mu0), p1 = fast_exp2(s1 - mu1);
+        const float p2 = fast_exp2(s2 - mu0), p3 = fast_exp2(s3 - mu1);
+        l[r][0] += p0 + p2;
+        l[r][1] += p1 + p3;
+        const float w0 = p0 * svg, w1 = p1 * svg, w2 = p2 * svg8, w3 = p3 * svg8;
+        const bool grow = fmaxf(w0, w2) > wlim[r][0] || fmaxf(w1, w3) > wlim[r][1];
+        if (__any_sync(0xffffffffu, grow)) {
+          float W0 = fmaxf(w0, w2), W1 = fmaxf(w1, w3);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            W0 = fmaxf(W0, __shfl_xor_sync(0xffffffffu, W0, off));
+            W1 = fmaxf(W1, __shfl_xor_sync(0xffffffffu, W1, off));
+          }
+          // exponent of W (a subnormal W counts as -126); E never decreases
+          const int e0 = max(E[r][0], max(static_cast<int>(__float_as_uint(W0) >> 23), 1) - 127);
+          const int e1 = max(E[r][1], max(static_cast<int>(__float_as_uint(W1) >> 23), 1) - 127);
+          const int ne0 = min(e0, 127 - kLazyExp), ne1 = min(e1, 127 - kLazyExp);
+          // <= 1, exact (0 below 2^-126: the earlier terms vanish next to the new ones)
+          const float f0 = (E[r][0] - ne0 < -126) ? 0.0f : exp2i(E[r][0] - ne0);
+          const float f1 = (E[r][1] - ne1 < -126) ? 0.0f : exp2i(E[r][1] - ne1);
+          E[r][0] = ne0;
+          E[r][1] = ne1;
+          wlim[r][0] = exp2i(ne0 + kLazyExp);
+          wlim[r][1] = exp2i(ne1 + kLazyExp);
+          iw[r][0] = exp2i(-ne0);
+          iw[r][1] = exp2i(-ne1);
+#pragma unroll
+          for (int mt = 0; mt < 8; mt++) {
+            acc[r][mt][0] *= f0;
+            acc[r][mt][1] *= f1;
+            acc[r][mt][2] *= f0;
+            acc[r][mt][3] *= f1;
+          }
+        }
+        pb0[r] = movmatrix_trans(float2_to_f16x2(w0 * iw[r][0], w1 * iw[r][1]));   // keys 0..7
+        pb1[r] = movmatrix_trans(float2_to_f16x2(w2 * iw[r][0], w3 * iw[r][1]));   // keys 8..15
       }
 
       // ---- O^T += V^T P'^T : d as M (d = 16g + 2mt [+1]), heads as N, keys as K ----
@@ -426,23 +458,13 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
           const uint32_t a0 = e4m3_lo2(lo01), a1 = e4m3_hi2(lo01);
           const uint32_t a2 = e4m3_lo2(lo89), a3 = e4m3_hi2(lo89);
 #pragma unroll
-          for (int r = 0; r < RPW; r++) {
-            float tile[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            mma_f16_16816(tile, a0, a1, a2, a3, pb0[r], pb1[r]);
-#pragma unroll
-            for (int e = 0; e < 4; e++) acc[r][2 * w][e] = fmaf(tile[e], fb[r][e & 1], acc[r][2 * w][e]);
-          }
+          for (int r = 0; r < RPW; r++) mma_f16_16816(acc[r][2 * w], a0, a1, a2, a3, pb0[r], pb1[r]);
         }
         {
           const uint32_t a0 = e4m3_lo2(hi01), a1 = e4m3_hi2(hi01);
           const uint32_t a2 = e4m3_lo2(hi89), a3 = e4m3_hi2(hi89);
 #pragma unroll
-          for (int r = 0; r < RPW; r++) {
-            float tile[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            mma_f16_16816(tile, a0, a1, a2, a3, pb0[r], pb1[r]);
-#pragma unroll
-            for (int e = 0; e < 4; e++) acc[r][2 * w + 1][e] = fmaf(tile[e], fb[r][e & 1], acc[r][2 * w + 1][e]);
-          }
+          for (int r = 0; r < RPW; r++) mma_f16_16816(acc[r][2 * w + 1], a0, a1, a2, a3, pb0[r], pb1[r]);
         }
       }
       __syncwarp();
@@ -450,13 +472,20 @@ __global__ void __launch_bounds__(Cfg<RPW>::WARPS * 32, 1) decode_split_kernel(c
     cp_async_wait<0>();
   }
 
-  // ---- finalize this warp: full row sums (the accumulator is already relative to 2^m) ----
+  // ---- finalize this warp: full row sums; the accumulator brought from units of 2^E to units of 2^m ----
 #pragma unroll
   for (int r = 0; r < RPW; r++)
 #pragma unroll
-    for (int hh = 0; hh < 2; hh++)
+    for (int hh = 0; hh < 2; hh++) {
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) l[r][hh] += __shfl_xor_sync(0xffffffffu, l[r][hh], off);
+      const float up = exp2i(E[r][hh]);
+#pragma unroll
+      for (int mt = 0; mt < 8; mt++) {
+        acc[r][mt][hh] *= up;
+        acc[r][mt][2 + hh] *= up;
+      }
+    }
 
   __syncthreads();  // the rings are free: reuse them as the merge area
   // ---- merge the wk warps of each row group into this slice's partial ----
