@@ -47,6 +47,10 @@ constexpr int STAGE_V = KB * kHeadDim;       // 2048 B of V codes
 constexpr int STAGE_S = KB * 4 * 2;          // 16 K scales + 16 V scales
 constexpr int STAGE_BYTES = STAGE_K + STAGE_V + STAGE_S;
 constexpr int MAX_SUB = 4096;                // slot indices staged in shared memory at a time
+#ifndef FTKV_MR_TC
+#define FTKV_MR_TC 1
+#endif
+constexpr bool kMultiRowTensorMemory = FTKV_MR_TC != 0;  // multi-row requests: decode_mr.cu
 constexpr float kLazyMax = 8.0f;             // log2 slack of the running maximum
 constexpr int kLazyExp = 12;                 // w may reach 2^(E + kLazyExp) before E is raised
 
@@ -647,6 +651,7 @@ int decode_ctas_per_sm(int max_q_rows) {
 // Single-row batches: the token-major kernel (decode_tok.cu); multi-row batches: this kernel.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (a.max_q_rows <= 1) return launch_decode_tok(a, s);
+  if (kMultiRowTensorMemory) return launch_decode_mr(a, s);
   return launch_split<2>(a, s);
 }
 
