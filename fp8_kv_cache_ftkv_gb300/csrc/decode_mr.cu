@@ -46,8 +46,8 @@ constexpr int MR_BN = 128;   // keys per tile
 constexpr uint32_t MR_BOX = 128 * 128;         // one 128-row x 128-byte swizzle box: 128 E4M3 or 64 FP16 a row
 constexpr uint32_t MR_TILE = 2 * MR_BOX;       // FP16 V tile: 128 keys x 128 FP16
 // ring stages: K (E4M3 codes, read by the MMA as they land), V codes as they land, V as FP16, scales
-constexpr int MR_NSK = 4, MR_NSR = 3, MR_NSV = 2, MR_NSC = 6;
-constexpr int MR_DK = 2, MR_DV = 2;  // tiles whose copies stay in flight while a copy warp completes the oldest
+constexpr int MR_NSK = 3, MR_NSR = 4, MR_NSV = 2, MR_NSC = 6;
+constexpr int MR_DK = 2, MR_DV = 3;  // tiles whose copies stay in flight while a copy warp completes the oldest
 constexpr uint32_t MR_OFF_Q = 0;                             // Q high and low E4M3 pieces (one box each)
 constexpr uint32_t MR_OFF_K = MR_OFF_Q + 2 * MR_BOX;
 constexpr uint32_t MR_OFF_R = MR_OFF_K + MR_NSK * MR_BOX;
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
 
   griddep_launch_dependents();
   griddep_wait();
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
 
@@ -339,8 +339,10 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
       }
       int ex = (amax > 0.0f) ? ilogbf(amax) : 0;
       ex = ex < -120 ? -120 : ex;
-      const float up = __uint_as_float(static_cast<uint32_t>(127 + 7 - ex) << 23);
-      qmul = __uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * a.qk_scale_log2;
+      // the sign of the softmax scale goes into the pieces (exact), so the multiplier qmul is positive
+      const float up = copysignf(__uint_as_float(static_cast<uint32_t>(127 + 7 - ex) << 23), a.qk_scale_log2);
+      // (> 0: a zero softmax scale still gives finite products s' qmul and -inf for the masked columns)
+      qmul = fmaxf(__uint_as_float(static_cast<uint32_t>(127 - 7 + ex) << 23) * fabsf(a.qk_scale_log2), FLT_MIN);
       const int m = lg * 32 + lane;
 #pragma unroll
       for (int c = 0; c < 8; c++) {  // 16 d per chunk: two uint4 of BF16
@@ -387,8 +389,8 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
       const int c0 = lo - kb, c1 = hi - kb;  // visible columns [c0, c1) of this warp's CW
       const bool full = __all_sync(0xffffffffu, c0 <= 0 && c1 >= CW);
       const uint32_t sb = lane_base + bb * 128 + cb;
-      // pass 1: s and its maximum (four partial maxima: the warp is alone on its sub-partition, so the chains'
-      // latency is not hidden by other warps)
+      // pass 1: s' = S scaleK and its maximum (four partial maxima: the warp is alone on its sub-partition, so the
+      // chains' latency is not hidden by other warps); s = s' qmul, qmul > 0
       float sv[CW];  // this warp's columns of S, all loads in flight at once
       mr_fence_after();
 #pragma unroll
@@ -400,10 +402,10 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
 #pragma unroll
       for (int e4 = 0; e4 < CW / 4; e4++) {
         const float4 k4 = *reinterpret_cast<const float4*>(ks + 4 * e4);
-        sv[4 * e4] *= k4.x * qmul;  // s
-        sv[4 * e4 + 1] *= k4.y * qmul;
-        sv[4 * e4 + 2] *= k4.z * qmul;
-        sv[4 * e4 + 3] *= k4.w * qmul;
+        sv[4 * e4] *= k4.x;
+        sv[4 * e4 + 1] *= k4.y;
+        sv[4 * e4 + 2] *= k4.z;
+        sv[4 * e4 + 3] *= k4.w;
       }
       if (!full) {  // the slice's boundary tiles: columns outside the row's visible keys drop out
 #pragma unroll
@@ -412,7 +414,7 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
       float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < CW; c++) tm[c & 3] = fmaxf(tm[c & 3], sv[c]);
-      const float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
+      const float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])) * qmul;
       // lazy maximum and FP16 exponent; f rescales O (and l: fm)
       float fm = 1.0f;
       if (tmax > mrow + kMrLazyMax) {
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
 #pragma unroll
         for (int e = 0; e < 4; e++) {
           const int c = 4 * e4 + e;
-          const float p = fast_exp2(sv[c] - sub);
+          const float p = fast_exp2(fmaf(sv[c], qmul, -sub));
           pa[e] += p;
           sv[c] = p * vv[e];
           wa[e] = fmaxf(wa[e], sv[c]);
@@ -637,7 +639,10 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
     };
     // wait for this lane's copies of tile t, with `newer` younger groups left in flight
     auto wait_tile = [&](int newer) {
-      if (newer >= 2)
+      static_assert(MR_DK <= 3 && MR_DV <= 3, "cp.async groups in flight");
+      if (newer >= 3)
+        asm volatile("cp.async.wait_group 3;" ::: "memory");
+      else if (newer == 2)
         asm volatile("cp.async.wait_group 2;" ::: "memory");
       else if (newer == 1)
         asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -730,7 +735,7 @@ cudaError_t launch_decode_mr(const DecodeArgs& a, cudaStream_t s) {
   c.pps = 1;  // one partial per key slice
   c.ptrans = 0;
   c.coop = 0;
-  return launch_k(decode_mr_kernel, dim3(a.num_splits, a.num_kv_heads, a.batch), dim3(MR_THREADS), MR_SMEM, s, c);
+  return launch_k(decode_mr_kernel, dim3(a.num_kv_heads, a.num_splits, a.batch), dim3(MR_THREADS), MR_SMEM, s, c);
 }
 
 }  // namespace ftkv

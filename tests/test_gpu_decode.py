@@ -4,7 +4,7 @@ Covers the 512-token single step, ragged key counts (1, 17, 513, 4099), split co
 automatic, GQA group sizes 8/4/2/1 and 8 KV heads, multi-row decode (1..8 rows, rows that see no key), the
 sliding windows (1 key to more than the sequence, single- and multi-row, with the fused store), the
 32,768- and 40,000-key batch-1 workloads at full size (sampled layers, every output element), the batched
-64-request multi-row workload at full size, and chains of decode launches in one stream with and without
+64-request multi-row workload at full size, negative and zero softmax scales, and chains of decode launches in one stream with and without
 FTKV_DECODE_STABLE_HISTORY (history loads issued before the preceding kernel has finished).  Single-row
 cases run with the flag off and on ("stable").
 """
@@ -103,6 +103,21 @@ def test_decode_multirow(rows):
     for splits in (0, 1, 5):
         out = _run(wl, gp, dev, num_splits=splits)
         _check(out, _ref(wl, op, L), f"rows={rows} splits={splits}")
+
+
+@pytest.mark.parametrize("rows", [[1], [3, 8]])
+@pytest.mark.parametrize("scale", [-0.0883883, 0.0, 2.0])
+def test_decode_softmax_scale_sign_and_zero(rows, scale):
+    """A negative softmax scale (the scores change sign), a zero one (uniform weights over the visible keys) and
+    a large one, on the single-row and the multi-row kernels (one and two groups of 32 query rows)."""
+    lens = [700 + 301 * i for i in range(len(rows))]
+    wl = inputs.decode_custom(lens, rows, 4000, seed=11 + len(rows))
+    wl.sm_scale = scale
+    gp, op, L, dev = _setup(wl)
+    for splits in (0, 3):
+        out = _run(wl, gp, dev, num_splits=splits)
+        _check(out, _ref(wl, op, L), f"rows={rows} scale={scale} splits={splits}")
+    assert ops.device_errors() == 0
 
 
 def test_decode_rows_that_see_no_key_are_zero():
