@@ -757,7 +757,7 @@ def run_details(args, torch, ops, inputs, device, stream, hbm_peak, bf16_peak, p
                                   s_keys, keys, "us/launch",
                                   f"requests {sample_req} ({s_keys} keys, all their rows), scaled by keys to all 64", budget)
         detail_line("config4_batched_multirow_64req", ms * 1e3, "us/launch",
-                    hbm_roof(nbytes, ms, hbm_peak, peak_src, "decode_split_kernel<2>"), cpu,
+                    hbm_roof(nbytes, ms, hbm_peak, peak_src, "decode_mr_kernel"), cpu,
                     {"keys": keys, "rows": rows, "num_splits": plan.num_splits})
         del pool, g
         torch.cuda.empty_cache()

@@ -1,5 +1,5 @@
-// decode_common.cuh -- pieces shared by the split-K decode kernels (decode.cu: one KV head per CTA,
-// multi-row batches; decode_tok.cu: every KV head of a token per CTA, single-row batches; decode_bf16.cu:
+// decode_common.cuh -- pieces shared by the split-K decode kernels (decode_mr.cu: one KV head per CTA,
+// multi-row batches; decode_tok.cu: every KV head of a token per CTA, single-row batches; bf16_pool.cu:
 // the same over a BF16 pool).
 //
 // The split merge after a grid barrier (cooperative launches) lives here as well:

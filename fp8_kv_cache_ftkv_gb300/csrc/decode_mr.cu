@@ -1,19 +1,23 @@
 // decode_mr.cu -- split-K decode attention for multi-row requests on the sm_100-family tensor cores (tcgen05 +
-// TMEM): the same result as decode.cu (FreeToken PR #897, opening description and "Fresh R9700 stage-1 A/B";
-// row r of a request's R rows sees keys 0 .. n-R+r, or the last W of them with a sliding window):
+// TMEM), computing what decode.cu defines (FreeToken PR #897, opening description and "Fresh R9700 stage-1
+// A/B"; row r of a request's R rows sees keys 0 .. n-R+r, or the last W of them with a sliding window):
 //     s_j = (q . k^_j) * sm_scale,   k^_j = decode(codeK_j) * scaleK_j,   v^_j likewise,   o = softmax(s) v^.
 //
-// One CTA = (key slice, KV head, request): its R x G query rows (R <= 8 rows, G <= 8 query heads of the KV head)
-// are the M = 128 rows of the products (rows past R G are zero), the keys of the slice come in tiles of 128.
-//  * Exact 16-bit operands.  E4M3 codes convert exactly to FP16, so the K and V tiles hold the stored codes as
-//    FP16 (the scales stay out of the products); the query row is brought to |x| < 256 by a power of two
-//    (2^(7-e), e the exponent of the row's largest element) and held as FP16, exact for every element within
-//    2^-31 of the largest.  S = Q K^T accumulates FP16 x FP16 products (exact in FP32) in TMEM; the softmax takes
+// One CTA = (KV head, key slice, request): its R x G query rows (R <= 8 rows, G <= 8 query heads of the KV head)
+// are the M = 128 rows of the products, the keys of the slice come in tiles of 128.
+//  * QK^T on the stored codes: the K codes are copied as they are (cp.async) into the 128-byte-swizzled
+//    K-major tile that kind::f8f6f4 MMAs read.  The query row is brought to |x| < 256 by a power of two
+//    (x = q 2^(7-e), e the exponent of the row's largest element) and split into two E4M3 pieces,
+//    x = hi + lo with lo = E4M3(x - hi): error at most 2^-8 |x| + 2^-10 against max |x| >= 128.  S = hi K^T +
+//    lo K^T accumulates exact E4M3 products in FP32 in TMEM; the softmax takes
 //    s = S * scaleK * 2^(e-7) * sm_scale * log2(e).
+//  * PV on FP16: E4M3 codes convert exactly to FP16, so the V tile holds the stored codes as FP16 (the V codes
+//    land in a staging ring and are converted in shared memory) and the V scale stays out of the product.
 //  * The V scale goes into the probabilities: w = 2^(s - m) * scaleV.  FP16 has a narrow exponent range and the
 //    per-row V scales of a slice can span 2^30, so P' = w 2^-E with one power-of-two exponent E per row that only
 //    grows (raised when some w would exceed 2^(E + 12)); the maximum m is lazy (raised when a score exceeds it by
-//    more than 8).  Either raise rescales the row of O in TMEM (rare); O is in units of 2^E.
+//    more than 8).  Either raise rescales the row of O in TMEM (rare); O is in units of 2^E.  The sign of
+//    sm_scale goes into the query pieces, so the multiplier of S is positive.
 //  * Rows and lane quarters.  A warp reaches only its own quarter of the TMEM lanes (32 (w % 4) .. +31), so a
 //    request of up to 32 live rows would leave three SM sub-partitions idle.  The Q tile therefore repeats the
 //    live rows in every quarter (one row group of 32 rows in all four, or two groups of 32 in two quarters
@@ -21,12 +25,15 @@
 //    maximum, sum, exponent and rows of O (its PV product sees P' = 0 outside its columns), and the quarters of
 //    a row are merged like split-K partials at the end of the slice.
 //  * Warps: 0-3 softmax (one per lane quarter, one query row per thread), 4 the MMA issuer (lane 0) and owner of
-//    the TMEM allocation, 5-6 the K copy warps, 7-8 the V copy warps.  A copy warp reads the codes of 4 keys
-//    per 16-byte load instruction (lanes 8k .. 8k+7: one key's 128-byte row), converts them and writes the
-//    128-byte-swizzled tile the MMA reads (K-major for S = Q K^T, MN-major for O += P V); the loads of tile j+1
-//    are in flight while tile j waits for its stage.  Lanes of the K warps also copy both scales of the tile's
-//    keys (cp.async) into a ring of their own that the softmax releases, so the softmax never waits for a V
-//    tile.
+//    the TMEM allocation, 5-6 the K copy warps, 7-8 the V copy warps.  A copy lane copies one 16-byte part of
+//    the rows of 16 keys per tile (lanes 8k .. 8k+7 share a key's 128-byte row) with cp.async, which lands in
+//    shared memory without passing through L1: loads into registers stalled behind the small L1 left next to
+//    ~215 KB of shared memory (64-request batch: 1,590 us with register loads and FP16 K, 996 us with cp.async
+//    and E4M3 K).
+//    Rings: K 3 x 16 KB (E4M3, read by the MMA as it lands), V codes 4 x 16 KB, V FP16 2 x 32 KB (MN-major,
+//    written by the V copy lanes from their own staged chunks), scales 6 x 1 KB.  Lanes of the K warps also
+//    copy both scales of the tile's keys into their ring, which the softmax releases, so the softmax never
+//    waits for a V tile.
 //  * TMEM: S0, S1 (128 columns each, double buffered), O (128), P0, P1 (64 columns of FP16 pairs).
 //  * The split merge: the CTA whose slice of (request, KV head) finishes last merges all slices (decode_merge.cuh).
 // Every mbarrier wait is bounded in time; on expiry the CTA flags an error, drains and exits.

@@ -6,7 +6,7 @@
 //     o   = sum_j softmax(s)_j v^_j,
 // with split-K over the keys and the split merge in the same call.  Per 16-key block, QK^T runs on the
 // FP8 tensor cores on the stored codes (the query in two exact E4M3 pieces) and PV on FP16 tensor cores on
-// the exactly converted V codes, as in decode.cu.
+// the exactly converted V codes.
 //
 // Head dimension D = 128, or 256 (the full-attention layers of FreeToken's Qwen3.6 case, PR #897 "Known
 // regression and uncertainty"): a 256-d head is two 128-d halves, each loaded, multiplied and accumulated

@@ -161,10 +161,9 @@ cudaError_t launch_store_quant(const StoreArgs& a, cudaStream_t s);
 cudaError_t launch_reconstruct(const ReconstructArgs& a, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* c, int64_t n, int num_sms, cudaStream_t s);
 cudaError_t launch_e4m3_decode(const uint8_t* c, float* x, int64_t n, int num_sms, cudaStream_t s);
-// Decode: single-row batches run the token-major kernel (decode_tok.cu), multi-row batches the kernel with
-// one KV head per CTA (decode.cu).
+// Decode (decode.cu): single-row batches run the token-major kernel (decode_tok.cu), multi-row batches the
+// tensor-memory kernel with one KV head per CTA (decode_mr.cu: max_q_rows > 1, 128-d heads).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
-// Multi-row decode on the tensor-memory path (decode_mr.cu): max_q_rows > 1, 128-d heads.
 cudaError_t launch_decode_mr(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tok(const DecodeArgs& a, cudaStream_t s);
 // Decode over a BF16 pool (bf16_pool.cu): one grid row per query row, any number of rows per request.
