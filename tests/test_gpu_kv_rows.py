@@ -149,10 +149,51 @@ def test_store_random_bit_patterns_bit_exact():
     _assert_pool_equal(gp, op, slots)
 
 
+def _mantissa_pair_rows(exps, rng):
+    """Rows that hold, for every BF16 mantissa m_a of the row's absmax (element 0) and every row exponent b in
+    `exps`, every BF16 mantissa m_x at every exponent b - k, k = 0..21, below the absmax (random signs, 127
+    elements a row, the last row of a group padded with zeros)."""
+    rows = []
+    mx = np.arange(128)
+    for b in exps:
+        for ma in range(128):
+            amax = np.float32((1 + ma / 128) * 2.0 ** b)
+            xs = [(1 + mx / 128) * 2.0 ** (b - k) for k in range(22)]
+            xs = np.concatenate(xs)
+            xs = xs[xs <= amax].astype(np.float32)
+            xs *= np.where(rng.random(xs.size) < 0.5, -1.0, 1.0).astype(np.float32)
+            pad = (-xs.size) % 127
+            xs = np.concatenate([xs, np.zeros(pad, np.float32)]).reshape(-1, 127)
+            rows.append(np.concatenate([np.full((xs.shape[0], 1), amax, np.float32), xs], axis=1))
+    return np.concatenate(rows)
+
+
+def test_store_every_bf16_mantissa_pair_bit_exact():
+    """The store's quotient x / scale, scale = RN(absmax / 448), depends on the BF16 mantissas of x and of the
+    absmax and on their exponent gap only (away from FP32 subnormals): these rows hold every such combination
+    whose quotient is in or below the E4M3 range (over row exponents from FP32-subnormal scales to 2^126): the
+    code of every quotient a BF16 row can produce, 7,592 of them exact ties at E4M3 rounding midpoints.  Codes
+    and scales bit-exact against the oracle."""
+    rng = np.random.default_rng(2024)
+    x = _mantissa_pair_rows([-120, -100, -37, 0, 11, 60, 126], rng)
+    T = (x.shape[0] + 3) // 4
+    x = np.concatenate([x, np.zeros((4 * T - x.shape[0], 128), np.float32)]).reshape(T, 4, 128)
+    bits = inputs.to_bf16_bits(x)
+    v = bits[rng.permutation(T)].copy()
+    R = T + 100
+    slots = rng.permutation(R)[:T].astype(np.int32)
+    gp = ops.KVPool.empty(R, 4)
+    ops.store_quant(gp, bits_to_cuda_bf16(bits), bits_to_cuda_bf16(v), torch.from_numpy(slots).cuda())
+    op = oracle.Pool(R, 4, 128)
+    oracle.store_quant(op, bits, v, slots)
+    _assert_pool_equal(gp, op, slots)
+    assert ops.device_errors() == 0
+
+
 def test_store_quotients_at_e4m3_midpoints_bit_exact():
     """Rows whose quotients x / scale land on or within a few ulps of E4M3 rounding midpoints, over scales
-    from 2^-40 to 2^40: the store's reciprocal fast path must fall back to the IEEE quotient exactly where
-    the code could differ.  Element 0 of every row is its absmax, so the scale is known."""
+    from 2^-40 to 2^40: any shortcut for the per-element IEEE division shows up here as a changed code.
+    Element 0 of every row is its absmax, so the scale is known."""
     rng = np.random.default_rng(123)
     T, R = 8192, 9000
     amax = (2.0 ** rng.uniform(-40, 40, size=(T, 4, 1))).astype(np.float32)
