@@ -178,10 +178,10 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
   // Few (request, head group) pairs (at most one per 8 SMs): one CTA per SM (the grid is resident at once and
   // merges cooperatively; with the single-row kernel the other CTA slot of every SM is left to the next launch
   // in the stream).
-  // Many: about 8 waves of slices, so that long requests are cut into pieces and the waves stay balanced;
-  // 13 for multi-row batches, whose CTAs balance better in finer pieces (64 requests of 1-8 rows, 4 KV heads:
-  // 8 splits 914 us, 10 splits 937 us).
-  const int64_t waves = max_q_rows > 1 ? 13 : 8;
+  // Many: about 8 waves of slices, so that long requests are cut into pieces and the waves stay balanced
+  // (multi-row, 64 requests of 1-8 rows, 4 KV heads: 4 slices 746 us, 5 slices 748 us, 8 slices 758 us,
+  // 10 slices 779 us: every multi-row CTA pays its pipeline's fill and drain).
+  const int64_t waves = 8;
   int64_t s = (8 * groups <= sms) ? sms / groups : ceil_div(waves * sms * per_sm, groups);
   // at least ~32 keys per slice for the single-row kernel (a block of 16 for each of its two key groups: short
   // requests, e.g. a sliding window, still spread over the SMs, so the split merge is spread too), ~128 for the

@@ -25,11 +25,13 @@
 //    maximum, sum, exponent and rows of O (its PV product sees P' = 0 outside its columns), and the quarters of
 //    a row are merged like split-K partials at the end of the slice.
 //  * Warps: 0-3 softmax (one per lane quarter, one query row per thread), 4 the MMA issuer (lane 0) and owner of
-//    the TMEM allocation, 5-6 the K copy warps, 7-8 the V copy warps.  A copy lane copies one 16-byte part of
-//    the rows of 16 keys per tile (lanes 8k .. 8k+7 share a key's 128-byte row) with cp.async, which lands in
-//    shared memory without passing through L1: loads into registers stalled behind the small L1 left next to
-//    ~215 KB of shared memory (64-request batch: 1,590 us with register loads and FP16 K, 996 us with cp.async
-//    and E4M3 K).
+//    the TMEM allocation, 5-8 the K copy warps, 9-12 the V copy warps (13 warps: at most 128 registers a
+//    thread).  A copy lane copies one 16-byte part of the rows of 8 keys per tile (lanes 8k .. 8k+7 share a
+//    key's 128-byte row) with cp.async, which lands in shared memory without passing through L1: loads into
+//    registers stalled behind the small L1 left next to ~215 KB of shared memory (64-request batch: 1,590 us
+//    with register loads and FP16 K, 996 us with cp.async and E4M3 K).  The gather rate follows the number of
+//    warps issuing copies: two copy warps per tensor 897 us, four 757 us, eight (80 registers a thread, the
+//    softmax spilling) 1,007 us.
 //    Rings: K 3 x 16 KB (E4M3, read by the MMA as it lands), V codes 4 x 16 KB, V FP16 2 x 32 KB (MN-major,
 //    written by the V copy lanes from their own staged chunks), scales 6 x 1 KB.  Lanes of the K warps also
 //    copy both scales of the tile's keys into their ring, which the softmax releases, so the softmax never
@@ -72,8 +74,14 @@ constexpr uint32_t MR_SMEM = MR_OFF_MISC + 16 + 1024;       // + slack for the 1
 static_assert(MR_SMEM <= 232448, "decode_mr shared memory");
 constexpr uint32_t MR_TMEM_COLS = 512;
 constexpr uint32_t MR_TMEM_O = 256, MR_TMEM_P = 384;
-constexpr int MR_THREADS = 9 * 32;
-constexpr int MR_MMA_WARP = 4, MR_KW0 = 5, MR_VW0 = 7;  // the MMA warp, the first K and the first V copy warp
+constexpr int MR_CW = 4;                            // copy warps per tensor (K, V)
+constexpr int MR_THREADS = (5 + 2 * MR_CW) * 32;
+constexpr int MR_MMA_WARP = 4, MR_KW0 = 5, MR_VW0 = 5 + MR_CW;  // the MMA warp, the first K and the first V copy warp
+constexpr int MR_CL = 32 * MR_CW;                   // copy lanes per tensor
+constexpr int MR_KPR = MR_CL / 8;                   // keys per copy round (8 lanes per 128-byte row)
+constexpr int MR_RND = MR_BN / MR_KPR;              // rounds per tile
+constexpr int MR_SPL = (MR_RND + 7) / 8;            // slots held per lane (lanes past MR_RND / MR_SPL hold none)
+static_assert(MR_RND * MR_KPR == MR_BN && (MR_RND <= 8 || MR_RND % 8 == 0), "copy lanes");
 constexpr unsigned long long MR_WAIT_NS = 2000000000ull;
 constexpr float kMrLazyMax = 8.0f;
 constexpr int kMrLazyExp = 12;
@@ -272,11 +280,11 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
   if (threadIdx.x == 0) {
     mr_bar_init(bar(MR_B_QFULL), 128);
     for (int s = 0; s < MR_NSK; s++) {
-      mr_bar_init(bar(MR_B_KFULL0 + s), 64);
+      mr_bar_init(bar(MR_B_KFULL0 + s), MR_CL);
       mr_bar_init(bar(MR_B_KEMPTY0 + s), 1);
     }
     for (int s = 0; s < MR_NSV; s++) {
-      mr_bar_init(bar(MR_B_VFULL0 + s), 64);
+      mr_bar_init(bar(MR_B_VFULL0 + s), MR_CL);
       mr_bar_init(bar(MR_B_VEMPTY0 + s), 1);
     }
     for (int s = 0; s < 2; s++) {
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
       mr_bar_init(bar(MR_B_PFULL0 + s), 4);
     }
     for (int s = 0; s < MR_NSC; s++) {
-      mr_bar_init(bar(MR_B_CFULL0 + s), 16);  // the scale lanes (when their copies land)
+      mr_bar_init(bar(MR_B_CFULL0 + s), 2 * MR_KPR);  // the scale lanes (when their copies land)
       mr_bar_init(bar(MR_B_CEMPTY0 + s), 4);
     }
     mr_bar_init(bar(MR_B_ODONE), 1);
@@ -587,37 +595,41 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
       mr_wait(bar(MR_B_DRAIN), 0, abort_flag, a.err);
     }
   } else {
-    // ---------------- copy warps: 5-6 K, 7-8 V; 64 lanes per tensor, 16 cp.async of 16 bytes a lane and tile ------
-    // Lane (kr, part) copies 16-byte part `part` of the rows of keys 8 r + kr, r = 0..15.  K codes land directly in
+    // ---------------- copy warps: MR_CW for K, then MR_CW for V; MR_RND cp.async of 16 bytes a lane and tile -------
+    // Lane (kr, part) copies 16-byte part `part` of the rows of keys KPR r + kr, r < MR_RND.  K codes land directly in
     // the 128-byte-swizzled box the MMA reads; V codes land in a plain ring and the same lane converts its own
     // chunks to FP16.  A warp keeps MR_DK (MR_DV) tiles in flight while it completes the oldest: it waits for its
     // own copies of that tile, makes them visible to the tensor cores and arrives on the tile's barrier.
     const bool is_v = warp >= MR_VW0;
     const int cl = (warp - (is_v ? MR_VW0 : MR_KW0)) * 32 + lane;
-    const int kr = cl >> 3, part = cl & 7;  // key within a round of 8, 16-byte part of the row
+    const int kr = cl >> 3, part = cl & 7;  // key within a round of MR_KPR, 16-byte part of the row
     const uint8_t* codes = is_v ? a.v_codes : a.k_codes;
     const int64_t hkv = a.num_kv_heads;
     const bool scl_lane = !is_v && part < 2;  // K lanes of part 0 / 1: the K / V scales of their keys
     const float* scales = part ? a.v_scales : a.k_scales;
     const int32_t* srow = a.req_to_slot + static_cast<int64_t>(b) * a.req_stride;
-    // slots of keys kb + 8 r + kr of tile jt, r = 2 part + i: the 8 lanes of a key group hold the 16 slots of its
-    // keys between them (loaded a tile ahead of their use; checked where used)
-    auto load_slots = [&](int jt, int32_t (&sl)[2]) {
+    // slots of keys kb + KPR r + kr of tile jt, r = SPL part + i: the 8 lanes of a key group hold the MR_RND slots
+    // of its keys between them (loaded a tile ahead of their use; checked where used)
+    auto load_slots = [&](int jt, int32_t (&sl)[MR_SPL]) {
       const int kb = j0 + jt * MR_BN;
 #pragma unroll
-      for (int i = 0; i < 2; i++) {
-        const int key = kb + 8 * (2 * part + i) + kr;
-        sl[i] = key < j1 ? __ldg(srow + key) : 0;
+      for (int i = 0; i < MR_SPL; i++) {
+        const int rd = MR_SPL * part + i;
+        const int key = kb + MR_KPR * rd + kr;
+        sl[i] = (rd < MR_RND && key < j1) ? __ldg(srow + key) : 0;
       }
     };
     // cp.async of tile jt's codes (and, on the scale lanes, its scales: stage jt % MR_NSC of the scale ring,
     // released by the softmax of tile jt - MR_NSC; its barrier is arrived on when they land); one group per tile
-    auto issue = [&](int jt, int32_t (&sl)[2]) -> bool {
+    auto issue = [&](int jt, int32_t (&sl)[MR_SPL]) -> bool {
       const int kb = j0 + jt * MR_BN;
-      const bool bad = sl[0] < 0 || sl[0] >= a.num_rows || sl[1] < 0 || sl[1] >= a.num_rows;
-      if (bad) flag_error(a.err, kDevErrBadSlot);
+      bool bad = false;
 #pragma unroll
-      for (int i = 0; i < 2; i++) sl[i] = (sl[i] < 0 || sl[i] >= a.num_rows) ? 0 : sl[i];
+      for (int i = 0; i < MR_SPL; i++) {
+        bad |= sl[i] < 0 || sl[i] >= a.num_rows;
+        sl[i] = (sl[i] < 0 || sl[i] >= a.num_rows) ? 0 : sl[i];
+      }
+      if (bad) flag_error(a.err, kDevErrBadSlot);
       bool okw = true;
       if (!is_v && jt >= MR_NSK)  // K box jt % MR_NSK: free once the QK product of tile jt - MR_NSK is done
         okw = mr_wait(bar(MR_B_KEMPTY0 + jt % MR_NSK), (jt / MR_NSK - 1) & 1, abort_flag, a.err);
@@ -627,9 +639,9 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
       const uint32_t box = is_v ? base + MR_OFF_R + (jt % MR_NSR) * MR_BOX : base + MR_OFF_K + (jt % MR_NSK) * MR_BOX;
       const uint32_t dsc = base + MR_OFF_SC + (c * MR_SC_FLOATS + part * MR_BN) * 4;
 #pragma unroll
-      for (int r = 0; r < 16; r++) {
-        const int32_t slot = __shfl_sync(0xffffffffu, sl[r & 1], (lane & ~7) | (r >> 1));
-        const int key = 8 * r + kr;
+      for (int r = 0; r < MR_RND; r++) {
+        const int32_t slot = __shfl_sync(0xffffffffu, sl[r % MR_SPL], (lane & ~7) | (r / MR_SPL));
+        const int key = MR_KPR * r + kr;
         const int64_t row = static_cast<int64_t>(slot) * hkv + h;
         const uint32_t dst = box + (is_v ? key * 128 + part * 16 : mr_chunk8(key, part));
         if (kb + key < j1) {
@@ -672,8 +684,8 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
       const uint32_t raw = base + MR_OFF_R + (t % MR_NSR) * MR_BOX;
       const uint32_t st = base + MR_OFF_V + sv * MR_TILE;
 #pragma unroll
-      for (int r = 0; r < 16; r++) {
-        const int key = 8 * r + kr;
+      for (int r = 0; r < MR_RND; r++) {
+        const int key = MR_KPR * r + kr;
         const uint4 d = (kb + key < j1) ? ld_shared_v4(raw + key * 128 + part * 16) : make_uint4(0u, 0u, 0u, 0u);
         st_shared_v4(st + mr_chunk(key, 2 * part), mr_codes_to_f16(d.x, d.y));
         st_shared_v4(st + mr_chunk(key, 2 * part + 1), mr_codes_to_f16(d.z, d.w));
@@ -683,7 +695,7 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
       return true;
     };
     const int D = is_v ? MR_DV : MR_DK;
-    int32_t slots[2];
+    int32_t slots[MR_SPL];
     load_slots(0, slots);
     for (int jt = 0; jt < T + D; jt++) {
       if (jt < T) {

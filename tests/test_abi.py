@@ -157,7 +157,7 @@ def test_decode_auto_splits_host_logic(lib):
     assert f(1, 4, 1000, 2) == 8              # at least ~128 keys per slice (multi-row kernel)
     assert f(8, 4, 32768, 1) == 19            # 8 groups: still one wave, 152 // 8
     assert f(64, 4, 40000, 1) == 38           # many groups: ~8 waves of two CTAs per SM, ceil(8 * 304 / 64)
-    assert f(64, 4, 40000, 8) == 8            # multi-row: ~13 waves, ceil(13 * 152 / 256)
+    assert f(64, 4, 40000, 8) == 5            # multi-row: ~8 waves of one CTA per SM, ceil(8 * 152 / 256)
     assert f(1, 1, 10 ** 9, 1) == 152
     assert f(0, 4, 100, 1) == 1
 
