@@ -32,7 +32,7 @@
 //    with register loads and FP16 K, 996 us with cp.async and E4M3 K).  The gather rate follows the number of
 //    warps issuing copies: two copy warps per tensor 897 us, four 757 us, eight (80 registers a thread, the
 //    softmax spilling) 1,007 us.
-//    Rings: K 3 x 16 KB (E4M3, read by the MMA as it lands), V codes 4 x 16 KB, V FP16 2 x 32 KB (MN-major,
+//    Rings: K 4 x 16 KB (E4M3, read by the MMA as it lands), V codes 3 x 16 KB, V FP16 2 x 32 KB (MN-major,
 //    written by the V copy lanes from their own staged chunks), scales 6 x 1 KB.  Lanes of the K warps also
 //    copy both scales of the tile's keys into their ring, which the softmax releases, so the softmax never
 //    waits for a V tile.
@@ -55,8 +55,8 @@ constexpr int MR_BN = 128;   // keys per tile
 constexpr uint32_t MR_BOX = 128 * 128;         // one 128-row x 128-byte swizzle box: 128 E4M3 or 64 FP16 a row
 constexpr uint32_t MR_TILE = 2 * MR_BOX;       // FP16 V tile: 128 keys x 128 FP16
 // ring stages: K (E4M3 codes, read by the MMA as they land), V codes as they land, V as FP16, scales
-constexpr int MR_NSK = 3, MR_NSR = 4, MR_NSV = 2, MR_NSC = 6;
-constexpr int MR_DK = 2, MR_DV = 3;  // tiles whose copies stay in flight while a copy warp completes the oldest
+constexpr int MR_NSK = 4, MR_NSR = 3, MR_NSV = 2, MR_NSC = 6;
+constexpr int MR_DK = 2, MR_DV = 2;  // tiles whose copies stay in flight while a copy warp completes the oldest
 constexpr uint32_t MR_OFF_Q = 0;                             // Q high and low E4M3 pieces (one box each)
 constexpr uint32_t MR_OFF_K = MR_OFF_Q + 2 * MR_BOX;
 constexpr uint32_t MR_OFF_R = MR_OFF_K + MR_NSK * MR_BOX;
