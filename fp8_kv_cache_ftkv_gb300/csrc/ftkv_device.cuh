@@ -62,7 +62,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Quantize-on-write of one 128-element BF16 row carried by a 16-lane half warp, lane l holding elements
 // 8l .. 8l+7 in `raw` (FreeToken PR #853, "What changes": each row gets its own FP32 scale).  Row
 // absmax = NaN-ignoring fmaxf from +0, scale = absmax / 448 (IEEE FP32 division), code =
-// E4M3FN_rne_satfinite(x / scale) (IEEE division); an all-zero row keeps scale 0 and divides by 1.
+// E4M3FN_rne_satfinite(x / scale) (the IEEE quotient, reached by Markstein's theorem below); an all-zero row
+// keeps scale 0 and divides by 1.
 // Every lane of the warp calls it: the max reduction shuffles within each 16-lane half.  Returns the
 // lane's 8 codes (element 8l in the lowest byte) and sets `scale`.  The store kernel and the decode
 // kernel's fused store both use this one definition.
@@ -74,15 +75,38 @@ __device__ __forceinline__ uint2 quantize_row_lane8(const uint4 raw, float& scal
   x[4] = bf16_lo(raw.z); x[5] = bf16_hi(raw.z);
   x[6] = bf16_lo(raw.w); x[7] = bf16_hi(raw.w);
   float amax = 0.0f;
+  bool nan = false;
 #pragma unroll
-  for (int i = 0; i < 8; i++) amax = fmaxf(amax, fabsf(x[i]));
+  for (int i = 0; i < 8; i++) {
+    amax = fmaxf(amax, fabsf(x[i]));
+    nan |= x[i] != x[i];
+  }
 #pragma unroll
   for (int off = 1; off < LANES; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   scale = __fdiv_rn(amax, 448.0f);
   const float div = (scale == 0.0f) ? 1.0f : scale;
+  // The IEEE quotients x / div by Markstein's division theorem (P. Markstein, "Computation of elementary
+  // functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/div) and
+  // q0 = RN(x r) (within an ulp of x / div), the remainder e = x - q0 div is exact in one FMA, and
+  // RN(q0 + e r) is the correctly rounded x / div, provided nothing overflows or underflows.  Here
+  // |x / div| <= 448 (no overflow).  A quotient that underflows FP32 is below 2^-126, far under half the
+  // smallest E4M3 subnormal (2^-10), so its code is a signed zero either way.  A row whose div or 1/div is not
+  // a normal number, or that holds a NaN, takes the IEEE division element by element.  (For x = -0 the steps
+  // give +0; a quotient here has the sign of x, so the sign is copied from x.)
+  const uint32_t de = (__float_as_uint(div) >> 23) & 0xFFu;
   float q[8];
+  if (de >= 2u && de <= 252u && !nan) {
+    const float r = __frcp_rn(div);
 #pragma unroll
-  for (int i = 0; i < 8; i++) q[i] = __fdiv_rn(x[i], div);
+    for (int i = 0; i < 8; i++) {
+      const float q0 = __fmul_rn(x[i], r);
+      const float e = __fmaf_rn(-q0, div, x[i]);
+      q[i] = copysignf(__fmaf_rn(e, r, q0), x[i]);  // the steps turn x = -0 into +0; the sign is x's anyway
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i++) q[i] = __fdiv_rn(x[i], div);
+  }
   const uint32_t w0 = e4m3x2_encode(q[0], q[1]), w1 = e4m3x2_encode(q[2], q[3]);
   const uint32_t w2 = e4m3x2_encode(q[4], q[5]), w3 = e4m3x2_encode(q[6], q[7]);
   return make_uint2(w0 | (w1 << 16), w2 | (w3 << 16));

@@ -16,11 +16,12 @@ namespace ftkv {
 // Quantize-on-write.  Half a warp carries one 128-d row (token, KV head, tensor): 16 lanes x 8 BF16
 // elements; a 256-d row takes a whole warp (32 lanes x 8), and a (token, head) pair two warps (K, V).
 // A warp handles STORE_UNITS (token, head) pairs -- K and V rows of each -- and issues all its loads
-// before any arithmetic.  One pair per warp: more warps in flight hide the division's latency better
+// before any arithmetic.  One pair per warp: more warps in flight hide the arithmetic's latency better
 // than longer load batches per warp (48-layer store: 1 pair 431 us, 2 pairs 468 us, 4 pairs 618 us).
 // Per row: NaN-ignoring absmax (fmaxf from +0), a 16-lane max reduction, scale = absmax / 448 (IEEE
-// division), then x / scale for every element (IEEE division: a reciprocal-times-correction shortcut
-// is not bit-identical to the quotient for every scale, e.g. subnormal ones).
+// division), then the IEEE quotient x / scale for every element, by one reciprocal per row and a product
+// and two FMAs per element (Markstein's theorem; rows whose scale or its reciprocal is not a normal number,
+// or that hold a NaN, divide element by element: quantize_row_lane8).
 // Bytes per (token, head): 2 x 256 B read, 2 x (128 B + 4 B) written, + the slot.
 // ---------------------------------------------------------------------------------------------
 constexpr int STORE_UNITS = 1;  // the loop form is kept so the batch size stays a one-line choice
