@@ -3,8 +3,10 @@
 // A/B"; row r of a request's R rows sees keys 0 .. n-R+r, or the last W of them with a sliding window):
 //     s_j = (q . k^_j) * sm_scale,   k^_j = decode(codeK_j) * scaleK_j,   v^_j likewise,   o = softmax(s) v^.
 //
-// One CTA = (KV head, key slice, request): its R x G query rows (R <= 8 rows, G <= 8 query heads of the KV head)
-// are the M = 128 rows of the products, the keys of the slice come in tiles of 128.
+// One CTA = (KV head, request, key slice), in that grid order (the KV heads of a slice side by side; every
+// request's first slices before the short last ones, so the last wave holds short work): its R x G query
+// rows (R <= 8 rows, G <= 8 query heads of the KV head) are the M = 128 rows of the products, the keys of the
+// slice come in tiles of 128.
 //  * QK^T on the stored codes: the K codes are copied as they are (cp.async) into the 128-byte-swizzled
 //    K-major tile that kind::f8f6f4 MMAs read.  The query row is brought to |x| < 256 by a power of two
 //    (x = q 2^(7-e), e the exponent of the row's largest element) and split into two E4M3 pieces,
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(MR_THREADS, 1) decode_mr_kernel(const DecodeAr
 
   griddep_launch_dependents();
   griddep_wait();
-  const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x, b = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
 
@@ -754,7 +756,7 @@ cudaError_t launch_decode_mr(const DecodeArgs& a, cudaStream_t s) {
   c.pps = 1;  // one partial per key slice
   c.ptrans = 0;
   c.coop = 0;
-  return launch_k(decode_mr_kernel, dim3(a.num_kv_heads, a.num_splits, a.batch), dim3(MR_THREADS), MR_SMEM, s, c);
+  return launch_k(decode_mr_kernel, dim3(a.num_kv_heads, a.batch, a.num_splits), dim3(MR_THREADS), MR_SMEM, s, c);
 }
 
 }  // namespace ftkv
