@@ -306,7 +306,7 @@ def build_decode(args, torch, ops, inputs, device, context=None, pool_rows=None,
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode_tok_kernel<4, 128> launch of the 32K
 # batch-1 step, from an ncu capture of this kernel on the same launch geometry (4 distinct pools, cold L2); to be
 # re-taken whenever the kernel changes.
-TOK_TRAFFIC_PER_LAUNCH = 34_820_864
+TOK_TRAFFIC_PER_LAUNCH = 34_821_888
 
 
 def bf16_bytes_per_layer(n):
