@@ -20,6 +20,7 @@ FTKV_ERR_WORKSPACE = -4
 FTKV_ERR_CUDA = -6
 FTKV_MAX_SPLITS = 256
 FTKV_MAX_Q_ROWS = 8
+FTKV_MAX_BATCH = 65535
 FTKV_DECODE_STABLE_HISTORY = 0x1
 FTKV_DEVERR_BAD_SLOT = 0x1
 FTKV_DEVERR_SEQ_LEN = 0x2

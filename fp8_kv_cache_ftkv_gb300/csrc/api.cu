@@ -208,6 +208,7 @@ int decode_validate_dims(int32_t num_kv_heads, int32_t head_dim, int32_t num_q_h
   if (head_dim != FTKV_HEAD_DIM && head_dim != FTKV_HEAD_DIM_256) return FTKV_ERR_UNSUPPORTED;
   if (batch < 0 || total_q_rows < 0 || max_seq_len < 0 || req_stride < 0) return FTKV_ERR_INVALID;
   if (max_q_rows < 1 || max_q_rows > FTKV_MAX_Q_ROWS) return FTKV_ERR_UNSUPPORTED;
+  if (batch > FTKV_MAX_BATCH) return FTKV_ERR_UNSUPPORTED;  // the requests are one grid dimension
   if (head_dim == FTKV_HEAD_DIM_256 && max_q_rows > 1) return FTKV_ERR_UNSUPPORTED;  // single-row kernel only
   if (num_splits < 0 || num_splits > FTKV_MAX_SPLITS) return FTKV_ERR_INVALID;
   if (flags & ~static_cast<uint32_t>(FTKV_DECODE_STABLE_HISTORY)) return FTKV_ERR_INVALID;

@@ -51,6 +51,9 @@ extern "C" {
 #define FTKV_MAX_SPLITS 256
 /* Largest number of query rows per request in multi-row decode ([#897] opening description, #900). */
 #define FTKV_MAX_Q_ROWS 8
+/* Largest batch (requests per decode call): one grid dimension of the decode kernels holds the requests.
+ * A larger batch -> FTKV_ERR_UNSUPPORTED (split it into several calls). */
+#define FTKV_MAX_BATCH 65535
 
 /* Decode flags.
  * FTKV_DECODE_STABLE_HISTORY: the caller guarantees that no work still pending on `stream` when the call is

@@ -99,6 +99,7 @@ def test_decode_validation(lib):
     assert call(hq=30) == _lib.FTKV_ERR_UNSUPPORTED          # not a multiple of Hkv
     assert call(hq=64, pool=_pool(hkv=4)) == _lib.FTKV_ERR_UNSUPPORTED  # group 16
     assert call(mq=9) == _lib.FTKV_ERR_UNSUPPORTED
+    assert call(B=65536, total=65536) == _lib.FTKV_ERR_UNSUPPORTED  # above FTKV_MAX_BATCH
     assert call(splits=_lib.FTKV_MAX_SPLITS + 1) == _lib.FTKV_ERR_INVALID
     assert call(flags=2) == _lib.FTKV_ERR_INVALID             # unknown flag bits
     assert call(flags=_lib.FTKV_DECODE_STABLE_HISTORY, q=0x1002) == _lib.FTKV_ERR_ALIGN
