@@ -165,6 +165,19 @@ def test_decode_batched_multirow_full_size():
     assert ops.device_errors() == 0
 
 
+@pytest.mark.parametrize("rows", [[8], [4], [5, 3]])
+def test_decode_multirow_long_request_full_size(rows):
+    """One or two long requests with several query rows (8 rows x 8 heads: two groups of 32 query rows per
+    KV head; 4 rows: one group repeated over the four TMEM lane quarters) at 32,768 keys: ~38 key slices of
+    ~7 tiles each, every output element against the FP64 oracle."""
+    lens = [32768] if len(rows) == 1 else [32768, 20001]
+    wl = inputs.decode_custom(lens, rows, 60000, sigma=1.0, seed=31 + sum(rows))
+    gp, op, L, dev = _setup(wl)
+    out = _run(wl, gp, dev)
+    _check(out, _ref(wl, op, L), f"long multirow rows={rows}")
+    assert ops.device_errors() == 0
+
+
 @pytest.mark.parametrize("max_q_rows", [1, 2])
 @pytest.mark.parametrize("stable", STABLE)
 def test_decode_bad_slot_and_seq_len_are_flagged_not_faulted(stable, max_q_rows):
