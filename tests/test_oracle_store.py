@@ -2,12 +2,16 @@
 
 * Byte accounting: the integers printed in FreeToken PR #853 ("Validation": 3,249,831,936 B BF16 KV,
   1,675,694,592 B FP8 codes+scales and a 67,704,832 B workspace at 33,059 rows, 46.35 % saved;
-  "Follow-up model/workload search": 98,304 vs 50,688 bytes per token).
+  "Follow-up model/workload search": 98,304 vs 50,688 bytes per token), read from
+  tests/golden/byte_accounting.txt.
 * Store: the scale against numpy's FP32 division of the row absmax by 448, the codes against torch's
   float8_e4m3fn cast of numpy's FP32 quotient, and the E4M3 error bound on the dequantized values.
 * Reconstruct: power-of-two scales (exact products) and torch's FP32 product + BF16 cast.
 """
+import os
+
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -15,20 +19,36 @@ from fp8_kv_cache_ftkv_gb300 import inputs
 
 
 # ---------------------------------------------------------------------------------------------
-def test_byte_accounting_matches_printed_integers():
-    b = oracle.pool_bytes(33059, 48, 4, 128)
-    assert b["bf16"] == 3_249_831_936
-    assert b["fp8"] == 1_675_694_592
-    assert b["workspace"] == 67_704_832
-    saved = 1.0 - (b["fp8"] + b["workspace"]) / b["bf16"]
-    assert round(100 * saved, 2) == 46.35
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "byte_accounting.txt")
 
 
-def test_bytes_per_token():
-    b = oracle.pool_bytes(1, 48, 4, 128)
-    assert b["bf16"] == 98_304
-    assert b["fp8"] == 50_688
-    assert round(100 * (1 - b["fp8"] / b["bf16"]), 1) == 48.4
+def _golden_cases():
+    cases = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            cases.append({k: float(v) if "." in v else int(v) for k, v in (f.split("=") for f in line.split())})
+    return cases
+
+
+def test_golden_byte_accounting_fixture_is_complete():
+    cases = _golden_cases()
+    assert len(cases) == 2
+    assert {"bf16", "fp8", "workspace", "saved_with_workspace_pct"} <= set(cases[0])
+    assert {"bf16", "fp8", "saved_pct"} <= set(cases[1])
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: f"rows{c['rows']}")
+def test_byte_accounting_matches_printed_integers(case):
+    b = oracle.pool_bytes(case["rows"], case["layers"], case["kv_heads"], case["head_dim"])
+    assert b["bf16"] == case["bf16"]
+    assert b["fp8"] == case["fp8"]
+    if "workspace" in case:
+        assert b["workspace"] == case["workspace"]
+        saved = 1.0 - (b["fp8"] + b["workspace"]) / b["bf16"]
+        assert round(100 * saved, 2) == case["saved_with_workspace_pct"]
+    if "saved_pct" in case:
+        assert round(100 * (1 - b["fp8"] / b["bf16"]), 1) == case["saved_pct"]
 
 
 # ---------------------------------------------------------------------------------------------
