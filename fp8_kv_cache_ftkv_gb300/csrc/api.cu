@@ -183,10 +183,10 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
   // 10 slices 779 us: every multi-row CTA pays its pipeline's fill and drain).
   const int64_t waves = 8;
   int64_t s = (8 * groups <= sms) ? sms / groups : ceil_div(waves * sms * per_sm, groups);
-  // at least ~32 keys per slice for the single-row kernel (a block of 16 for each of its two key groups: short
-  // requests, e.g. a sliding window, still spread over the SMs, so the split merge is spread too), ~128 for the
-  // multi-row kernel
-  const int64_t by_len = ceil_div(max_seq_len, max_q_rows <= 1 ? 32 : 128);
+  // at least ~8 keys per slice for the single-row kernel: short requests still spread over the SMs, and the
+  // split merge with them (512 keys, batch 1, one call: 16 slices 20.5 us, 32 slices 14.4 us, 64 or more
+  // 12.3 us); ~128 (one tile) for the multi-row kernel
+  const int64_t by_len = ceil_div(max_seq_len, max_q_rows <= 1 ? 8 : 128);
   if (s > by_len) s = by_len;
   if (s > FTKV_MAX_SPLITS) s = FTKV_MAX_SPLITS;
   if (s < 1) s = 1;

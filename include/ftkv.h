@@ -159,9 +159,9 @@ size_t ftkv_decode_workspace_bytes(int32_t num_q_heads, int32_t num_kv_heads, in
                                    int32_t batch, int64_t total_q_rows, int32_t num_splits);
 
 /* Number of key slices the automatic choice uses for this shape (what num_splits = 0 resolves to):
- * with few (request, KV head group) pairs, one CTA per SM; with many, enough for about eight waves
- * (sixteen when max_q_rows > 1), so that long requests are cut into balanced pieces; at least ~32 keys
- * per slice (~128 when max_q_rows > 1), at most FTKV_MAX_SPLITS. */
+ * with few (request, KV head group) pairs, one CTA per SM; with many, enough for about eight waves of
+ * resident CTAs (two per SM single-row, one when max_q_rows > 1), so that long requests are cut into
+ * balanced pieces; at least ~8 keys per slice (~128 when max_q_rows > 1), at most FTKV_MAX_SPLITS. */
 int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max_seq_len,
                                 int32_t max_q_rows);
 

@@ -154,7 +154,7 @@ def test_decode_auto_splits_host_logic(lib):
     f = lib.ftkv_decode_auto_splits
     assert f(1, 4, 32768, 1) == 152           # one group: one CTA per SM
     assert f(1, 8, 32768, 1) == 76            # 8 KV heads: two groups of 4
-    assert f(1, 4, 1000, 1) == 32             # at least ~32 keys per slice (single-row kernel)
+    assert f(1, 4, 1000, 1) == 125            # at least ~8 keys per slice (single-row kernel)
     assert f(1, 4, 1000, 2) == 8              # at least ~128 keys per slice (multi-row kernel)
     assert f(8, 4, 32768, 1) == 19            # 8 groups: still one wave, 152 // 8
     assert f(64, 4, 40000, 1) == 38           # many groups: ~8 waves of two CTAs per SM, ceil(8 * 304 / 64)
