@@ -4,6 +4,7 @@
 // enqueued; kernels are launched on the caller's stream and never allocate.  The per-device error
 // word (slots outside the pool, sequence lengths above the declared bound) is a 4-byte __device__
 // variable of this translation unit whose address is handed to the kernels.
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -175,14 +176,23 @@ int32_t ftkv_decode_auto_splits(int32_t batch, int32_t num_kv_heads, int64_t max
   // takes one KV head per CTA.
   const int64_t heads_per_cta = max_q_rows <= 1 ? ftkv::decode_tok_heads_per_cta(num_kv_heads) : 1;
   const int64_t groups = int64_t(batch) * (num_kv_heads / heads_per_cta);
-  // Few (request, head group) pairs (at most one per 8 SMs): one CTA per SM (the grid is resident at once and
-  // merges cooperatively; with the single-row kernel the other CTA slot of every SM is left to the next launch
-  // in the stream).
-  // Many: about 8 waves of slices, so that long requests are cut into pieces and the waves stay balanced
-  // (multi-row, 64 requests of 1-8 rows, 4 KV heads: 4 slices 746 us, 5 slices 748 us, 8 slices 758 us,
-  // 10 slices 779 us: every multi-row CTA pays its pipeline's fill and drain).
-  const int64_t waves = 8;
-  int64_t s = (8 * groups <= sms) ? sms / groups : ceil_div(waves * sms * per_sm, groups);
+  // Single-row kernel (two CTAs fit per SM):
+  //  * at most 4 (request, head group) pairs: one CTA per SM.  The grid is resident at once and merges
+  //    cooperatively, and the other CTA slot of every SM is left to the next launch in the stream (batch 1,
+  //    32K keys, 48 layers: 152 slices 675 us per step, 76-200 slices 940-1,140 us);
+  //  * more: whole waves of resident CTAs (two per SM), as few as give at least ~8 slices (8-layer chains of
+  //    16,384-key requests, per layer: 16 requests 114 us at one CTA per SM, 67 us at one wave of two;
+  //    32 requests 165 us at ~8 waves, 129 us at one or two; 64 requests 274 us at 1.7 waves, 253 us at 4;
+  //    4 requests 25.5 us either way).
+  // Multi-row kernel (one CTA per SM): few pairs (at most one per 8 SMs) one CTA per SM; many, about 8 waves
+  // (64 requests of 1-8 rows, 4 KV heads: 4 slices 746 us, 5 slices 748 us, 8 slices 758 us, 10 slices
+  // 779 us: every multi-row CTA pays its pipeline's fill and drain).
+  int64_t s;
+  if (max_q_rows <= 1)
+    s = (groups <= 4) ? sms / groups
+                      : std::max<int64_t>(1, ceil_div(8 * groups, per_sm * sms)) * per_sm * sms / groups;
+  else
+    s = (8 * groups <= sms) ? sms / groups : ceil_div(8 * sms * per_sm, groups);
   // at least ~8 keys per slice for the single-row kernel: short requests still spread over the SMs, and the
   // split merge with them (512 keys, batch 1, one call: 16 slices 20.5 us, 32 slices 14.4 us, 64 or more
   // 12.3 us); ~128 (one tile) for the multi-row kernel

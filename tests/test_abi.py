@@ -156,8 +156,12 @@ def test_decode_auto_splits_host_logic(lib):
     assert f(1, 8, 32768, 1) == 76            # 8 KV heads: two groups of 4
     assert f(1, 4, 1000, 1) == 125            # at least ~8 keys per slice (single-row kernel)
     assert f(1, 4, 1000, 2) == 8              # at least ~128 keys per slice (multi-row kernel)
-    assert f(8, 4, 32768, 1) == 19            # 8 groups: still one wave, 152 // 8
-    assert f(64, 4, 40000, 1) == 38           # many groups: ~8 waves of two CTAs per SM, ceil(8 * 304 / 64)
+    assert f(4, 4, 32768, 1) == 38            # up to 4 groups: one CTA per SM, 152 // 4
+    assert f(8, 4, 32768, 1) == 38            # more: one wave of two CTAs per SM, 304 // 8
+    assert f(16, 4, 16384, 1) == 19
+    assert f(32, 4, 16384, 1) == 9
+    assert f(64, 4, 40000, 1) == 9            # many groups: 2 whole waves for >= ~8 slices, 608 // 64
+    assert f(256, 4, 40000, 1) == 8           # 7 waves, 2128 // 256
     assert f(64, 4, 40000, 8) == 5            # multi-row: ~8 waves of one CTA per SM, ceil(8 * 152 / 256)
     assert f(1, 1, 10 ** 9, 1) == 152
     assert f(0, 4, 100, 1) == 1
